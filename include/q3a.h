@@ -1,0 +1,155 @@
+/*
+ * q3a.h — C ABI of the Qwen3 attention core for one NVIDIA GB300 (sm_103a).
+ *
+ * The library computes, from already-projected Q/K/V, the span of the Qwen3
+ * attention sublayer between the projections and o_proj:
+ *
+ *   1. QK-Norm: per-head RMSNorm over head_dim with fp32 accumulation and a
+ *      learned gamma, one gamma[d] shared by all Q heads and one by all K heads
+ *      ("Qwen3" note, llm.rainlin.net, QK-Norm section and the quoted
+ *      transformers Qwen3Attention; "7.2 Qwen3 full-scale implementation",
+ *      paper.xwysyy.cn, §7.2.1 RMSNorm).
+ *   2. Rotate-half RoPE with inv_freq_i = theta^(-2i/d), applied AFTER the norm
+ *      (§7.2.1 compute_rope_params / apply_rope; the transformers forward
+ *      quoted on the llm.rainlin.net page).
+ *   3. Causal grouped-query softmax attention, softmax(q.k / sqrt(d)) . V, where
+ *      query head h reads KV group floor(h / g), g = Hq / Hkv (§7.2.1
+ *      GroupedQueryAttention: repeat_interleave, triu mask, scale head_dim^0.5).
+ *   4. Decode: the new K is normalised and rotated at position start_pos and
+ *      appended to the cache; cached K is used as stored and never re-rotated
+ *      ("Chapter 20, Qwen3 and Qwen3.5", book.ozine.me, §20.3 KV cache).
+ *
+ * Conventions shared by every entry point
+ *   - bf16 means IEEE bfloat16 bit patterns (q3a_bf16), round-to-nearest-even.
+ *   - Every tensor pointer is a DEVICE pointer unless the comment says HOST.
+ *     All device tensors are dense, row-major in the order given, and 16-byte
+ *     aligned.
+ *   - The caller owns every buffer, including the workspace. The library never
+ *     allocates or frees memory. It launches asynchronously on `stream`
+ *     (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *   - Arguments are validated on the host BEFORE anything is launched or
+ *     written. A rejected call leaves every buffer untouched (the
+ *     validate-then-mutate rule of the context-length tests, §20.9 of the
+ *     book.ozine.me chapter).
+ *   - The library never aborts and never prints.
+ *   - head_dim d must be 128 (the fixed Qwen3 head width, §7.2.1).
+ *   - Hq % Hkv == 0 and g = Hq/Hkv in {1, 2, 4, 8, 16}.
+ *   - eps > 0 and theta > 1.
+ */
+#ifndef Q3A_H_
+#define Q3A_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t q3a_bf16;
+
+typedef enum {
+  Q3A_OK = 0,
+  Q3A_EINVAL = 1,   /* bad argument: null/misaligned pointer, shape, eps, theta, workspace too small */
+  Q3A_ERANGE = 2,   /* decode: start_pos[b] < 0 or start_pos[b] + 1 > S_max (context overflow) */
+  Q3A_ECUDA = 3,    /* a CUDA launch or runtime call failed */
+  Q3A_ETIMEOUT = 4, /* a device-side bounded wait gave up; see q3a_last_device_error */
+  Q3A_ENOTIMPL = 5  /* combination of arguments that this build does not implement */
+} q3a_status;
+
+/* Human-readable name of a status code. Static storage; never NULL. */
+const char* q3a_status_string(q3a_status s);
+
+/* ---------------------------------------------------------------------------
+ * q3a_qknorm_rope — steps 1 and 2 alone (QK-Norm then RoPE) on one tensor.
+ *
+ *   x     [B, T, H, d] bf16, projected Q or K as viewed per head.
+ *   gamma [d] bf16, the norm's learned scale (shared by all H heads).
+ *   y     [B, T, H, d] bf16, y = RoPE_pos(RMSNorm(x) * gamma), rounded once.
+ *         y may equal x (in place); any other overlap is undefined.
+ *   Row (b, t, h) is rotated at position pos0 + t.
+ *   pos0 >= 0 and pos0 + T - 1 <= 2^30.
+ *   B == 0, T == 0 or H == 0: returns Q3A_OK and launches nothing.
+ * Sources: §7.2.1 RMSNorm forward (fp32 variance, rsqrt(var + eps), times
+ * scale, cast back) and apply_rope (x*cos + cat(-x2, x1)*sin).
+ * ------------------------------------------------------------------------- */
+q3a_status q3a_qknorm_rope(const q3a_bf16* x, const q3a_bf16* gamma, q3a_bf16* y,
+                           int B, int T, int H, int d, int pos0,
+                           double theta, float eps, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * q3a_prefill — causal prefill of the whole attention core.
+ *
+ *   q       [B, T, Hq, d]  bf16 projected queries (token-major, per head).
+ *   k, v    [B, T, Hkv, d] bf16 projected keys / values.
+ *   q_gamma, k_gamma [d]   bf16 QK-Norm scales.
+ *   out     [B, T, Hq, d]  bf16 attention output, i.e. [B, T, Hq*d], the layout
+ *           that feeds o_proj (§7.2.1: context.transpose(1,2).reshape(b,T,d_out)).
+ *   Positions are 0..T-1 (prefill always starts at position 0).
+ *   Row (b, i, h) attends to keys j = 0..i of group h / (Hq/Hkv).
+ *   Softmax scale is fixed to 1/sqrt(d).
+ *   workspace: device scratch of at least q3a_prefill_workspace_size() bytes,
+ *           256-byte aligned, owned by the caller, contents need not be
+ *           initialised; it holds the normalised+rotated Q and K and an error
+ *           word. It must not be shared by two calls that run concurrently.
+ *   B == 0 or T == 0: returns Q3A_OK and launches nothing.
+ *   Limits: B*T*Hq <= 2^31 - 1 rows.
+ * ------------------------------------------------------------------------- */
+size_t q3a_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d);
+
+q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
+                       const q3a_bf16* q_gamma, const q3a_bf16* k_gamma,
+                       q3a_bf16* out,
+                       int B, int T, int Hq, int Hkv, int d,
+                       double theta, float eps,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * q3a_decode — one new token per sequence against a KV cache.
+ *
+ *   q       [B, Hq, d]  bf16 projected query of the new token.
+ *   k_new   [B, Hkv, d] bf16 projected key of the new token (NOT normalised).
+ *   v_new   [B, Hkv, d] bf16 projected value of the new token.
+ *   k_cache [B, Hkv, S_max, d] bf16, rows 0..start_pos[b]-1 hold keys that are
+ *           already normalised and rotated (as this library writes them).
+ *   v_cache [B, Hkv, S_max, d] bf16, rows 0..start_pos[b]-1 hold values.
+ *   start_pos HOST int32 [B]: position of the new token of sequence b.
+ *   out     [B, Hq, d] bf16 attention output of the new token.
+ *   Side effect: k_cache[b, :, start_pos[b], :] = bf16(RoPE(RMSNorm(k_new)))
+ *   and v_cache[b, :, start_pos[b], :] = v_new. Rows beyond start_pos[b] are
+ *   neither read nor written.
+ *   Requires 0 <= start_pos[b] and start_pos[b] + 1 <= S_max for every b,
+ *   else Q3A_ERANGE with the caches untouched. B <= 4096.
+ *   workspace: at least q3a_decode_workspace_size() bytes of device scratch,
+ *   256-byte aligned, owned by the caller; holds split partials and an
+ *   error word. Not shareable between concurrent calls.
+ *   B == 0: returns Q3A_OK and launches nothing.
+ * Source: §20.3 of the book.ozine.me chapter (the new K is rotated at
+ * start_pos and concatenated; the old K is never rotated again) and the
+ * cache update after RoPE in the quoted transformers forward.
+ * ------------------------------------------------------------------------- */
+size_t q3a_decode_workspace_size(int B, int Hq, int Hkv, int d, int S_max);
+
+q3a_status q3a_decode(const q3a_bf16* q, const q3a_bf16* k_new, const q3a_bf16* v_new,
+                      q3a_bf16* k_cache, q3a_bf16* v_cache,
+                      const int32_t* start_pos,
+                      const q3a_bf16* q_gamma, const q3a_bf16* k_gamma,
+                      q3a_bf16* out,
+                      int B, int Hq, int Hkv, int d, int S_max,
+                      double theta, float eps,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * q3a_last_device_error — reads, synchronously on `stream`, the error word
+ * that the kernels of the last call which used `workspace` left in its first
+ * bytes (prefill and decode workspaces both keep it at offset 0).
+ * Returns Q3A_OK when the word is zero, Q3A_ETIMEOUT when a bounded device
+ * wait gave up, Q3A_EINVAL for a NULL workspace, Q3A_ECUDA if the read failed.
+ * ------------------------------------------------------------------------- */
+q3a_status q3a_last_device_error(const void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q3A_H_ */

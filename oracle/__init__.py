@@ -1,0 +1,179 @@
+"""CPU oracle of the Qwen3 attention core (QK-Norm -> RoPE -> causal GQA).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers. The product library never
+imports, links or runs anything here, and this package imports nothing from it.
+
+The arithmetic lives in ``q3a_oracle.c`` (plain fp64 loops, see its header for
+the definition and the page passages each step follows). This module compiles
+it with gcc and wraps it with ctypes. Inputs are bf16 torch CPU tensors (their
+exact values are widened to fp64); outputs are fp64 torch tensors.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+against closed forms, invariants and a separately written brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q3a_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libq3a_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_u16p = ctypes.c_void_p
+_f64p = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libq3a_oracle.so`` (gcc, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-Wall", "-Wextra",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i, l, d = ctypes.c_int, ctypes.c_long, ctypes.c_double
+            lib.q3a_oracle_set_threads.argtypes = [i]
+            lib.q3a_oracle_threads.restype = i
+            lib.q3a_oracle_rmsnorm_row.argtypes = [_u16p, _u16p, i, d, _f64p]
+            lib.q3a_oracle_rope_row.argtypes = [_f64p, i, d, d]
+            lib.q3a_oracle_qknorm_rope.argtypes = [_u16p, _u16p, i, i, i, i, l, d, d, _f64p]
+            lib.q3a_oracle_qknorm_rope.restype = i
+            lib.q3a_oracle_prefill.argtypes = [_u16p] * 5 + [i] * 5 + [d, d, _f64p]
+            lib.q3a_oracle_prefill.restype = i
+            lib.q3a_oracle_prefill_rows.argtypes = ([_u16p] * 5 + [i] * 5 + [d, d, l]
+                                                    + [ctypes.c_void_p] * 3 + [_f64p])
+            lib.q3a_oracle_prefill_rows.restype = i
+            lib.q3a_oracle_decode.argtypes = ([_u16p] * 5 + [ctypes.c_void_p] + [_u16p] * 2
+                                              + [i] * 4 + [l, d, d, ctypes.c_void_p,
+                                                            _f64p, _f64p])
+            lib.q3a_oracle_decode.restype = i
+            _lib = lib
+    return _lib
+
+
+def _bf16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype != torch.bfloat16 or t.device.type != "cpu":
+        raise TypeError(f"{name}: expected a bf16 CPU tensor, got {t.dtype} on {t.device}")
+    return t.contiguous()
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+def set_threads(n: int) -> None:
+    """Number of OpenMP threads the oracle uses (0 = OpenMP default)."""
+    _load().q3a_oracle_set_threads(int(n))
+
+
+def threads() -> int:
+    """Threads the oracle's parallel loops run with."""
+    return int(_load().q3a_oracle_threads())
+
+
+def rmsnorm_row(x: torch.Tensor, gamma: torch.Tensor, eps: float) -> torch.Tensor:
+    """Step 1 on one row: x / sqrt(mean(x^2) + eps) * gamma, fp64."""
+    x, gamma = _bf16(x, "x"), _bf16(gamma, "gamma")
+    d = x.numel()
+    y = torch.empty(d, dtype=torch.float64)
+    _load().q3a_oracle_rmsnorm_row(_ptr(x), _ptr(gamma), d, float(eps), _ptr(y))
+    return y
+
+
+def rope_row(y: torch.Tensor, pos: float, theta: float) -> torch.Tensor:
+    """Step 2 on one fp64 row (returns a rotated copy)."""
+    out = y.to(torch.float64).contiguous().clone()
+    _load().q3a_oracle_rope_row(_ptr(out), out.numel(), float(pos), float(theta))
+    return out
+
+
+def qknorm_rope(x: torch.Tensor, gamma: torch.Tensor, theta: float, eps: float,
+                pos0: int = 0) -> torch.Tensor:
+    """Steps 1-2 on x [B, T, H, d]; row (b, t, h) is rotated at pos0 + t. fp64 out."""
+    x, gamma = _bf16(x, "x"), _bf16(gamma, "gamma")
+    B, T, H, d = x.shape
+    out = torch.empty((B, T, H, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_qknorm_rope(_ptr(x), _ptr(gamma), B, T, H, d, int(pos0),
+                                        float(theta), float(eps), _ptr(out))
+    if rc:
+        raise ValueError(f"oracle qknorm_rope rejected its arguments ({rc})")
+    return out
+
+
+def prefill(q, k, v, q_gamma, k_gamma, theta: float, eps: float) -> torch.Tensor:
+    """Full causal prefill; q [B,T,Hq,d], k/v [B,T,Hkv,d] -> fp64 [B,T,Hq,d]."""
+    q, k, v = _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v")
+    q_gamma, k_gamma = _bf16(q_gamma, "q_gamma"), _bf16(k_gamma, "k_gamma")
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    out = torch.empty((B, T, Hq, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(q_gamma), _ptr(k_gamma),
+                                    B, T, Hq, Hkv, d, float(theta), float(eps), _ptr(out))
+    if rc:
+        raise ValueError(f"oracle prefill failed ({rc})")
+    return out
+
+
+def prefill_rows(q, k, v, q_gamma, k_gamma, theta: float, eps: float,
+                 rows: torch.Tensor) -> torch.Tensor:
+    """Sampled causal prefill. rows: int32 [n, 3] of (b, t, h). -> fp64 [n, d]."""
+    q, k, v = _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v")
+    q_gamma, k_gamma = _bf16(q_gamma, "q_gamma"), _bf16(k_gamma, "k_gamma")
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    rows = rows.to(torch.int32)
+    rb, rt, rh = (rows[:, c].contiguous() for c in range(3))
+    n = rows.shape[0]
+    out = torch.empty((n, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_prefill_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(q_gamma),
+                                         _ptr(k_gamma), B, T, Hq, Hkv, d, float(theta),
+                                         float(eps), n, _ptr(rb), _ptr(rt), _ptr(rh),
+                                         _ptr(out))
+    if rc:
+        raise ValueError(f"oracle prefill_rows failed ({rc})")
+    return out
+
+
+def decode(q, k_new, v_new, k_cache, v_cache, start_pos, q_gamma, k_gamma,
+           theta: float, eps: float, select=None):
+    """One decode step. Returns (out fp64 [B,Hq,d], appended key row fp64 [B,Hkv,d]).
+
+    ``select``: optional bool [B]; only those sequences are computed (others
+    are left as zeros).
+    """
+    q, k_new, v_new = _bf16(q, "q"), _bf16(k_new, "k_new"), _bf16(v_new, "v_new")
+    k_cache, v_cache = _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    q_gamma, k_gamma = _bf16(q_gamma, "q_gamma"), _bf16(k_gamma, "k_gamma")
+    B, Hq, d = q.shape
+    Hkv, S_max = k_cache.shape[1], k_cache.shape[2]
+    sp = torch.as_tensor(start_pos, dtype=torch.int32).contiguous()
+    sel = None if select is None else torch.as_tensor(select, dtype=torch.uint8).contiguous()
+    out = torch.zeros((B, Hq, d), dtype=torch.float64)
+    k_row = torch.zeros((B, Hkv, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                   _ptr(v_cache), _ptr(sp), _ptr(q_gamma), _ptr(k_gamma),
+                                   B, Hq, Hkv, d, S_max, float(theta), float(eps),
+                                   None if sel is None else _ptr(sel), _ptr(out), _ptr(k_row))
+    if rc:
+        raise ValueError(f"oracle decode failed ({rc})")
+    return out, k_row
