@@ -1,0 +1,82 @@
+// q3a_internal.h — host-side interfaces between the C ABI (q3a_api.cu) and the
+// kernels of libq3a. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q3a {
+
+// ----- K1: QK-Norm + RoPE prologue ------------------------------------------
+// One tensor of head rows. Row (b, t, h) of x starts at element
+//   (b * xsb + t * xst + h * xsh) * 128
+// (strides counted in rows of 128 elements); the same for y with ys*.
+struct RopeTensor {
+  const uint16_t* x;
+  const uint16_t* gamma;
+  uint16_t* y;
+  int H;
+  long long xsb, xst, xsh;
+  long long ysb, yst, ysh;
+};
+
+struct RopeArgs {
+  RopeTensor t[2];
+  int ntensors;  // 1 or 2 (both tensors share B, T and the positions)
+  int B, T;
+  long long pos0;  // row (b, t, h) is rotated at pos0 + t
+  float eps;
+  double inv_freq[64];  // theta^(-2i/128)
+};
+
+void fill_inv_freq(double theta, double* inv_freq);
+cudaError_t launch_qknorm_rope(const RopeArgs& a, cudaStream_t stream);
+
+// ----- K2: causal GQA prefill attention (tcgen05) ---------------------------
+struct PrefillArgs {
+  CUtensorMap tm_q;  // Qhat [B, T, Hq, 128] bf16, box {64, g, 128/g, 1}
+  CUtensorMap tm_k;  // Khat [B*Hkv, T, 128] bf16, box {64, 128, 1}
+  CUtensorMap tm_v;  // V    [B, T, Hkv, 128] bf16, box {64, 1, 128, 1}
+  uint16_t* out;     // [B, T, Hq, 128] bf16
+  uint32_t* err;     // device error word
+  int B, T, Hq, Hkv, g;
+  int n_mtiles;      // ceil(T / (128 / g))
+};
+
+cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
+
+// ----- K3/K4: split-KV decode ------------------------------------------------
+constexpr int kDecodeMaxB = 2048;
+constexpr int kDecodeChunk = 1024;  // keys per split
+constexpr int kDecodePartialFloats = 2 + 128;  // m, l, acc[128] per (split, head)
+
+struct DecodeArgs {
+  CUtensorMap tm_kc;  // k_cache [B*Hkv, S_max, 128] bf16, box {64, 64, 1}
+  CUtensorMap tm_vc;  // v_cache, same
+  const uint16_t* q;      // [B, Hq, 128]
+  const uint16_t* k_new;  // [B, Hkv, 128]
+  const uint16_t* v_new;  // [B, Hkv, 128]
+  const uint16_t* q_gamma;
+  const uint16_t* k_gamma;
+  uint16_t* k_cache;  // for the append
+  uint16_t* v_cache;
+  float* partial;     // [B, Hkv, split_stride, g, kDecodePartialFloats] fp32
+  uint16_t* out;      // [B, Hq, 128]
+  uint32_t* err;
+  int B, Hq, Hkv, g, S_max, split_stride, max_splits;
+  float eps;
+  double inv_freq[64];
+  int start_pos[kDecodeMaxB];
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// ----- tensor maps -----------------------------------------------------------
+// cuTensorMapEncodeTiled (bf16, 128-byte swizzle, zero fill out of bounds),
+// obtained through the runtime's driver entry point. dims[0] is innermost;
+// strides_bytes has rank-1 entries (dims 1..rank-1).
+CUresult encode_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box);
+
+}  // namespace q3a

@@ -1,0 +1,62 @@
+// q3a_rope.cuh — device pieces of QK-Norm + rotate-half RoPE shared by the
+// prologue kernel (K1) and the decode kernel (K3).
+//
+//   y = x * rsqrt(mean(x^2) + eps) * gamma                       (fp32)
+//   y'_i = y_i cos a_i - y_{i+64} sin a_i ; y'_{i+64} = y_{i+64} cos a_i + y_i sin a_i
+//   a_i = p * theta^(-2i/128)
+// ("7.2 Qwen3 full-scale implementation", §7.2.1 RMSNorm, compute_rope_params,
+// apply_rope; norm first, then RoPE.)
+#pragma once
+
+#include "q3a_device.cuh"
+
+namespace q3a {
+
+// (cos a, sin a) for a = p * w. The product and its reduction modulo 2 pi are
+// done in fp64 (exact enough for p up to 2^30), the reduced angle in fp32.
+__device__ __forceinline__ float2 rope_cos_sin(long long p, double w) {
+  const double ang = (double)p * w;
+  const double turns = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
+  const double red = fma(-turns, 6.283185307179586, ang);
+  float s, c;
+  sincosf((float)red, &s, &c);
+  return make_float2(c, s);
+}
+
+// One head row held by a half-warp: lane L (0..15) holds x[4L..4L+3] in xl and
+// their rotate-half partners x[64+4L..64+4L+3] in xh, with the matching gamma
+// slices gl/gh and the (cos, sin) of angles 4L..4L+3 in cs[0..3]. All 32 lanes
+// of the warp must call this together (two rows per warp).
+__device__ __forceinline__ void qknorm_rope_halfwarp(const float (&xl)[4], const float (&xh)[4],
+                                                     const float (&gl)[4], const float (&gh)[4],
+                                                     const float2 (&cs)[4], float eps,
+                                                     float (&ol)[4], float (&oh)[4]) {
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) ss = fmaf(xl[j], xl[j], fmaf(xh[j], xh[j], ss));
+  ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  const float inv_rms = rsqrtf(ss * (1.0f / 128.0f) + eps);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float yl = xl[j] * inv_rms * gl[j];
+    const float yh = xh[j] * inv_rms * gh[j];
+    ol[j] = yl * cs[j].x - yh * cs[j].y;
+    oh[j] = yh * cs[j].x + yl * cs[j].y;
+  }
+}
+
+__device__ __forceinline__ void unpack4(uint2 v, float (&f)[4]) {
+  f[0] = bf16_lo(v.x);
+  f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y);
+  f[3] = bf16_hi(v.y);
+}
+
+__device__ __forceinline__ uint2 pack4(const float (&f)[4]) {
+  return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+}
+
+}  // namespace q3a
