@@ -119,7 +119,7 @@ q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
  *   and v_cache[b, :, start_pos[b], :] = v_new. Rows beyond start_pos[b] are
  *   neither read nor written.
  *   Requires 0 <= start_pos[b] and start_pos[b] + 1 <= S_max for every b,
- *   else Q3A_ERANGE with the caches untouched. B <= 4096.
+ *   else Q3A_ERANGE with the caches untouched. B <= 2048, S_max <= 2^30.
  *   workspace: at least q3a_decode_workspace_size() bytes of device scratch,
  *   256-byte aligned, owned by the caller; holds split partials and an
  *   error word. Not shareable between concurrent calls.

@@ -1,0 +1,267 @@
+// q3a_api.cu — the C ABI of include/q3a.h: argument validation (always before
+// anything is launched or written), workspace layout, TMA tensor maps, and the
+// kernel launches. The library allocates nothing and keeps no per-call state.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "q3a.h"
+#include "q3a_internal.h"
+
+namespace q3a {
+namespace {
+
+constexpr size_t kHeader = 256;  // error word and padding at the start of a workspace
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool group_ok(int Hq, int Hkv) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return false;
+  const int g = Hq / Hkv;
+  return g == 1 || g == 2 || g == 4 || g == 8 || g == 16;
+}
+
+bool scalars_ok(double theta, float eps) {
+  return isfinite(theta) && theta > 1.0 && isfinite(eps) && eps > 0.0f;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+q3a_status from_cuda(cudaError_t e) { return e == cudaSuccess ? Q3A_OK : Q3A_ECUDA; }
+
+size_t prefill_q_bytes(int B, int T, int Hq) { return (size_t)B * T * Hq * 128 * 2; }
+size_t prefill_k_bytes(int B, int T, int Hkv) { return (size_t)B * T * Hkv * 128 * 2; }
+
+int decode_split_stride(int S_max) { return (S_max + kDecodeChunk - 1) / kDecodeChunk; }
+
+}  // namespace
+
+CUresult encode_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t d[5], s[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d,
+            s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace q3a
+
+using namespace q3a;
+
+extern "C" {
+
+const char* q3a_status_string(q3a_status s) {
+  switch (s) {
+    case Q3A_OK: return "ok";
+    case Q3A_EINVAL: return "invalid argument";
+    case Q3A_ERANGE: return "start_pos out of range (context overflow)";
+    case Q3A_ECUDA: return "CUDA error";
+    case Q3A_ETIMEOUT: return "device-side wait timed out";
+    case Q3A_ENOTIMPL: return "not implemented";
+  }
+  return "unknown status";
+}
+
+q3a_status q3a_qknorm_rope(const q3a_bf16* x, const q3a_bf16* gamma, q3a_bf16* y, int B, int T,
+                           int H, int d, int pos0, double theta, float eps, void* stream) {
+  if (d != 128 || B < 0 || T < 0 || H < 0 || pos0 < 0) return Q3A_EINVAL;
+  if ((long long)pos0 + (long long)T - 1 > (1LL << 30)) return Q3A_EINVAL;
+  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
+  if (B == 0 || T == 0 || H == 0) return Q3A_OK;
+  if (!x || !gamma || !y || !aligned16(x) || !aligned16(gamma) || !aligned16(y))
+    return Q3A_EINVAL;
+  RopeArgs a;
+  memset(&a, 0, sizeof a);
+  a.t[0] = RopeTensor{x, gamma, y, H, (long long)T * H, H, 1, (long long)T * H, H, 1};
+  a.ntensors = 1;
+  a.B = B;
+  a.T = T;
+  a.pos0 = pos0;
+  a.eps = eps;
+  fill_inv_freq(theta, a.inv_freq);
+  return from_cuda(launch_qknorm_rope(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t q3a_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d) {
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || d != 128) return 0;
+  return kHeader + align256(prefill_q_bytes(B, T, Hq)) + align256(prefill_k_bytes(B, T, Hkv));
+}
+
+q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
+                       const q3a_bf16* q_gamma, const q3a_bf16* k_gamma, q3a_bf16* out, int B,
+                       int T, int Hq, int Hkv, int d, double theta, float eps, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  if (d != 128 || B < 0 || T < 0 || !group_ok(Hq, Hkv)) return Q3A_EINVAL;
+  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
+  if ((long long)B * T * Hq > 0x7fffffffLL || T > (1 << 30)) return Q3A_EINVAL;
+  if (B == 0 || T == 0) return Q3A_OK;
+  const void* ptrs[] = {q, k, v, q_gamma, k_gamma, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return Q3A_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
+  if (ws_bytes < q3a_prefill_workspace_size(B, T, Hq, Hkv, d)) return Q3A_EINVAL;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  uint16_t* qhat = reinterpret_cast<uint16_t*>(ws + kHeader);
+  uint16_t* khat =
+      reinterpret_cast<uint16_t*>(ws + kHeader + align256(prefill_q_bytes(B, T, Hq)));
+  const int g = Hq / Hkv;
+
+  // tensor maps first: a failure here launches nothing
+  PrefillArgs pa;
+  memset(&pa, 0, sizeof pa);
+  {
+    const uint64_t dq[4] = {128, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
+    const uint64_t sq[3] = {256, (uint64_t)Hq * 256, (uint64_t)T * Hq * 256};
+    const uint32_t bq[4] = {64, (uint32_t)g, (uint32_t)(128 / g), 1};
+    const uint64_t dk[3] = {128, (uint64_t)T, (uint64_t)B * Hkv};
+    const uint64_t sk[2] = {256, (uint64_t)T * 256};
+    const uint32_t bk[3] = {64, 128, 1};
+    const uint64_t dv[4] = {128, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
+    const uint64_t sv[3] = {256, (uint64_t)Hkv * 256, (uint64_t)T * Hkv * 256};
+    const uint32_t bv[4] = {64, 1, 128, 1};
+    if (encode_tensor_map(&pa.tm_q, qhat, 4, dq, sq, bq) != CUDA_SUCCESS ||
+        encode_tensor_map(&pa.tm_k, khat, 3, dk, sk, bk) != CUDA_SUCCESS ||
+        encode_tensor_map(&pa.tm_v, v, 4, dv, sv, bv) != CUDA_SUCCESS)
+      return Q3A_ECUDA;
+  }
+  pa.out = out;
+  pa.err = err;
+  pa.B = B;
+  pa.T = T;
+  pa.Hq = Hq;
+  pa.Hkv = Hkv;
+  pa.g = g;
+  pa.n_mtiles = (T + (128 / g) - 1) / (128 / g);
+
+  RopeArgs ra;
+  memset(&ra, 0, sizeof ra);
+  // Q -> Qhat, same [B, T, Hq] row order
+  ra.t[0] = RopeTensor{q, q_gamma, qhat, Hq, (long long)T * Hq, Hq, 1, (long long)T * Hq, Hq, 1};
+  // K [B, T, Hkv] -> Khat [B, Hkv, T] so that a 128-key tile of one group is contiguous
+  ra.t[1] = RopeTensor{k, k_gamma, khat, Hkv, (long long)T * Hkv, Hkv, 1, (long long)Hkv * T, 1, T};
+  ra.ntensors = 2;
+  ra.B = B;
+  ra.T = T;
+  ra.pos0 = 0;
+  ra.eps = eps;
+  fill_inv_freq(theta, ra.inv_freq);
+
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = launch_qknorm_rope(ra, st);
+  if (e == cudaSuccess) e = launch_prefill_attention(pa, st);
+  return from_cuda(e);
+}
+
+size_t q3a_decode_workspace_size(int B, int Hq, int Hkv, int d, int S_max) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || d != 128 || S_max <= 0 || Hq % Hkv) return 0;
+  const size_t parts = (size_t)B * Hkv * decode_split_stride(S_max) * (Hq / Hkv) *
+                       kDecodePartialFloats * sizeof(float);
+  return kHeader + align256(parts);
+}
+
+q3a_status q3a_decode(const q3a_bf16* q, const q3a_bf16* k_new, const q3a_bf16* v_new,
+                      q3a_bf16* k_cache, q3a_bf16* v_cache, const int32_t* start_pos,
+                      const q3a_bf16* q_gamma, const q3a_bf16* k_gamma, q3a_bf16* out, int B,
+                      int Hq, int Hkv, int d, int S_max, double theta, float eps,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  if (d != 128 || B < 0 || B > kDecodeMaxB || S_max <= 0 || !group_ok(Hq, Hkv))
+    return Q3A_EINVAL;
+  if (S_max > (1 << 30)) return Q3A_EINVAL;
+  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
+  if (B == 0) return Q3A_OK;
+  const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, q_gamma, k_gamma, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return Q3A_EINVAL;
+  if (!start_pos) return Q3A_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
+  if (ws_bytes < q3a_decode_workspace_size(B, Hq, Hkv, d, S_max)) return Q3A_EINVAL;
+  int max_splits = 0;
+  for (int b = 0; b < B; ++b) {
+    const int32_t p = start_pos[b];
+    if (p < 0 || (long long)p + 1 > S_max) return Q3A_ERANGE;  // nothing written yet
+    const int n = (p + 1 + kDecodeChunk - 1) / kDecodeChunk;
+    if (n > max_splits) max_splits = n;
+  }
+
+  static_assert(sizeof(DecodeArgs) < 32000, "kernel parameter limit");
+  DecodeArgs dargs;  // kernel parameters, staged on the host stack
+  DecodeArgs* da = &dargs;
+  memset(da, 0, sizeof *da);
+  const uint64_t dc[3] = {128, (uint64_t)S_max, (uint64_t)B * Hkv};
+  const uint64_t sc[2] = {256, (uint64_t)S_max * 256};
+  const uint32_t bc[3] = {64, 64, 1};
+  if (encode_tensor_map(&da->tm_kc, k_cache, 3, dc, sc, bc) != CUDA_SUCCESS ||
+      encode_tensor_map(&da->tm_vc, v_cache, 3, dc, sc, bc) != CUDA_SUCCESS)
+    return Q3A_ECUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  da->q = q;
+  da->k_new = k_new;
+  da->v_new = v_new;
+  da->q_gamma = q_gamma;
+  da->k_gamma = k_gamma;
+  da->k_cache = k_cache;
+  da->v_cache = v_cache;
+  da->partial = reinterpret_cast<float*>(ws + kHeader);
+  da->out = out;
+  da->err = reinterpret_cast<uint32_t*>(ws);
+  da->B = B;
+  da->Hq = Hq;
+  da->Hkv = Hkv;
+  da->g = Hq / Hkv;
+  da->S_max = S_max;
+  da->split_stride = decode_split_stride(S_max);
+  da->max_splits = max_splits;
+  da->eps = eps;
+  fill_inv_freq(theta, da->inv_freq);
+  for (int b = 0; b < B; ++b) da->start_pos[b] = start_pos[b];
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(da->err, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = launch_decode(*da, st);
+  return from_cuda(e);
+}
+
+q3a_status q3a_last_device_error(const void* workspace, void* stream) {
+  if (!workspace) return Q3A_EINVAL;
+  uint32_t word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return Q3A_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return Q3A_ECUDA;
+  return word == 0 ? Q3A_OK : Q3A_ETIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+include/q3a.h declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from qwen3_qk_norm_gb300 import binding
+from qwen3_qk_norm_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "q3a.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q3a_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert "q3a_prefill" in names and "q3a_decode" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(binding.EXPORTED) == names
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.q3a_status_string(s)
+    assert b"range" in lib.q3a_status_string(binding.Q3A_ERANGE)
+
+
+FAKE = 1 << 20  # an aligned non-null address; never dereferenced on rejected calls
+
+
+def prefill_call(lib, **kw):
+    a = dict(B=1, T=4, Hq=32, Hkv=8, d=128, theta=1e6, eps=1e-6, ws=FAKE, ws_bytes=1 << 40)
+    a.update(kw)
+    return lib.q3a_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["T"], a["Hq"], a["Hkv"],
+                           a["d"], a["theta"], a["eps"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(d=64), dict(d=256), dict(Hq=30), dict(Hq=96, Hkv=3),
+                                dict(Hq=64, Hkv=2), dict(eps=0.0), dict(eps=-1.0),
+                                dict(theta=1.0), dict(theta=float("nan")), dict(B=-1),
+                                dict(T=-2), dict(ws=FAKE + 16), dict(ws=0), dict(ws_bytes=1024)])
+def test_prefill_rejects_bad_arguments(lib, kw):
+    assert prefill_call(lib, **kw) == binding.Q3A_EINVAL
+
+
+def test_prefill_empty_shapes_launch_nothing(lib):
+    assert prefill_call(lib, B=0) == binding.Q3A_OK
+    assert prefill_call(lib, T=0) == binding.Q3A_OK
+
+
+def test_prefill_null_or_misaligned_pointer(lib):
+    args = [FAKE] * 6
+    for i in range(6):
+        for bad in (0, FAKE + 2):
+            a = list(args)
+            a[i] = bad
+            st = lib.q3a_prefill(*a, 1, 4, 32, 8, 128, 1e6, 1e-6, FAKE, 1 << 40, None)
+            assert st == binding.Q3A_EINVAL
+
+
+def decode_call(lib, start_pos, S_max=64, **kw):
+    B = len(start_pos)
+    sp = (ctypes.c_int32 * B)(*start_pos)
+    a = dict(Hq=32, Hkv=8, d=128, theta=1e6, eps=1e-6, ws=FAKE, ws_bytes=1 << 40)
+    a.update(kw)
+    return lib.q3a_decode(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.addressof(sp), FAKE, FAKE, FAKE, B,
+                          a["Hq"], a["Hkv"], a["d"], S_max, a["theta"], a["eps"], a["ws"],
+                          a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("sp", [[64], [0, 64], [-1], [5, 100, 3]])
+def test_decode_context_overflow_is_erange(lib, sp):
+    """start_pos + 1 > S_max (or negative) is refused before anything is written."""
+    assert decode_call(lib, sp, S_max=64) == binding.Q3A_ERANGE
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert decode_call(lib, [3], d=64) == binding.Q3A_EINVAL
+    assert decode_call(lib, [3], Hq=12, Hkv=8) == binding.Q3A_EINVAL
+    assert decode_call(lib, [3], ws_bytes=16) == binding.Q3A_EINVAL
+    assert decode_call(lib, [3] * 2049) == binding.Q3A_EINVAL
+    assert decode_call(lib, [], S_max=64) == binding.Q3A_OK
+
+
+def test_workspace_sizes(lib):
+    B, T, Hq, Hkv = 4, 4096, 32, 8
+    ws = binding.prefill_workspace_size(B, T, Hq, Hkv)
+    assert ws >= 256 + B * T * (Hq + Hkv) * 128 * 2
+    assert binding.prefill_workspace_size(B, T, Hq, Hkv, 64) == 0
+    dws = binding.decode_workspace_size(64, 32, 8, 32768)
+    assert dws >= 256 + 64 * 8 * 32 * 4 * 130 * 4

@@ -1,0 +1,122 @@
+"""Causal GQA prefill (K1 + K2) on the GPU against the fp64 oracle, via the C ABI."""
+import pytest
+import torch
+
+import oracle
+from qwen3_qk_norm_gb300 import binding, inputs
+from qwen3_qk_norm_gb300.inputs import WORKLOADS
+from gpu_util import assert_close_attention
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(x, theta, eps=1e-6):
+    d = {k: t.cuda() for k, t in x.items()}
+    out = binding.prefill(d["q"], d["k"], d["v"], d["q_gamma"], d["k_gamma"], theta, eps)
+    torch.cuda.synchronize()
+    return out
+
+
+# small shapes: several M tiles and KV tiles, ragged tails, every g
+@pytest.mark.parametrize("B,T,Hq,Hkv,theta", [
+    (1, 1, 16, 8, 1e6),      # a single token
+    (1, 2, 4, 4, 1e6),       # g = 1
+    (1, 127, 8, 4, 1e6),     # one KV tile minus one
+    (2, 129, 16, 8, 1e6),    # one KV tile plus one, B > 1
+    (1, 255, 8, 1, 1e7),     # g = 8
+    (1, 300, 16, 1, 1e6),    # g = 16
+    (2, 200, 2, 2, 1e6),     # g = 1, ragged
+    (3, 520, 8, 2, 1e6),     # g = 4, five KV tiles
+])
+def test_prefill_small_shapes(cuda_lib, B, T, Hq, Hkv, theta):
+    x = inputs.prefill_inputs(B, T, Hq, Hkv, seed=B * 1000 + T)
+    ref = oracle.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], theta, 1e-6)
+    assert_close_attention(run_prefill(x, theta), ref, f"prefill B{B} T{T} Hq{Hq} Hkv{Hkv}")
+
+
+def test_prefill_qwen3_06b_t128_full(cuda_lib):
+    w = WORKLOADS["qwen3-0.6b-prefill-b1-t128"]
+    x = inputs.workload_inputs(w)
+    ref = oracle.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], w.theta, w.eps)
+    assert_close_attention(run_prefill(x, w.theta), ref, w.name)
+
+
+def test_prefill_with_norm_outliers(cuda_lib):
+    x = inputs.prefill_inputs(1, 700, 32, 8, seed=5, outlier_frac=0.01, outlier_scale=30.0)
+    ref = oracle.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    assert_close_attention(run_prefill(x, 1e6), ref, "outliers")
+
+
+def test_prefill_future_tokens_leave_past_rows_bit_identical(cuda_lib):
+    B, T, Hq, Hkv, cut = 1, 400, 8, 2, 170
+    x = inputs.prefill_inputs(B, T, Hq, Hkv, seed=9)
+    a = run_prefill(x, 1e6)
+    y = dict(x)
+    y["k"] = x["k"].clone()
+    y["v"] = x["v"].clone()
+    y["k"][:, cut:] = inputs.prefill_inputs(B, T - cut, Hkv, Hkv, seed=10)["k"]
+    y["v"][:, cut:] = inputs.prefill_inputs(B, T - cut, Hkv, Hkv, seed=11)["v"]
+    b = run_prefill(y, 1e6)
+    assert torch.equal(a[:, :cut], b[:, :cut])
+    assert not torch.equal(a[:, cut:], b[:, cut:])
+
+
+def test_prefill_row0_is_v_row0(cuda_lib):
+    x = inputs.prefill_inputs(2, 64, 16, 4, seed=12)
+    out = run_prefill(x, 1e6).cpu()
+    for h in range(16):
+        assert torch.equal(out[:, 0, h], x["v"][:, 0, h // 4])
+
+
+def test_prefill_is_deterministic(cuda_lib):
+    x = inputs.prefill_inputs(1, 300, 32, 8, seed=13)
+    assert torch.equal(run_prefill(x, 1e6), run_prefill(x, 1e6))
+
+
+def test_prefill_rejects_bad_group_and_leaves_out_untouched(cuda_lib):
+    x = {k: t.cuda() for k, t in inputs.prefill_inputs(1, 8, 12, 8, seed=14).items()}
+    out = torch.full_like(x["q"], 7.0)
+    with pytest.raises(binding.Q3AError) as e:
+        binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6, out=out)
+    assert e.value.status == binding.Q3A_EINVAL
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
+
+
+def test_prefill_no_device_error_word(cuda_lib):
+    x = {k: t.cuda() for k, t in inputs.prefill_inputs(1, 130, 8, 2, seed=15).items()}
+    ws = torch.empty(binding.prefill_workspace_size(1, 130, 8, 2), dtype=torch.uint8,
+                     device="cuda")
+    binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6, workspace=ws)
+    assert binding.last_device_error(ws) == binding.Q3A_OK
+
+
+def sample_rows(B, T, Hq, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    fixed = [(0, 0, 0), (B - 1, T - 1, Hq - 1), (0, T - 1, 0), (B - 1, 127, 1 % Hq),
+             (0, 128, Hq // 2), (0, min(T - 1, 4095), Hq - 1)]
+    rnd = [(int(torch.randint(0, B, (1,), generator=g)), int(torch.randint(0, T, (1,), generator=g)),
+            int(torch.randint(0, Hq, (1,), generator=g))) for _ in range(n)]
+    return torch.tensor(fixed + rnd, dtype=torch.int32)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["qwen3-8b-prefill-b4-t4096", "qwen3-32b-prefill-b2-t8192",
+                                  "qwen3-30b-a3b-prefill-b1-t32768"])
+def test_prefill_full_size_sampled_rows(cuda_lib, name):
+    """Full-size workloads, launched as the benchmark launches them; sampled
+    output rows against the oracle computed one by one."""
+    w = WORKLOADS[name]
+    x = inputs.workload_inputs(w, device="cuda")
+    out = binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], w.theta, w.eps)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    rows = sample_rows(w.B, w.T, w.Hq, 40, seed=w.seed)
+    cpu = {k: t.cpu() for k, t in x.items()}
+    if w.outlier_frac > 0:  # include rows the x30 outliers hit
+        big = (cpu["q"].float().abs().amax(-1) > 20).nonzero()[:6].to(torch.int32)
+        rows = torch.cat([rows, big], 0)
+    ref = oracle.prefill_rows(cpu["q"], cpu["k"], cpu["v"], cpu["q_gamma"], cpu["k_gamma"],
+                              w.theta, w.eps, rows)
+    got = torch.stack([out[b, t, h] for b, t, h in rows.tolist()])
+    assert_close_attention(got, ref, name)
