@@ -105,6 +105,32 @@ q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
                        void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The two halves of q3a_prefill, for callers that schedule them separately
+ * (and for timing each kernel). q3a_prefill(...) is exactly
+ * q3a_prefill_prologue(...) followed by q3a_prefill_attention(...) on the
+ * same stream and workspace.
+ *
+ * q3a_prefill_prologue — steps 1-2: normalises and rotates q and k (positions
+ *   0..T-1) into `workspace`, and clears the workspace's error word. Same
+ *   argument rules as q3a_prefill.
+ * q3a_prefill_attention — step 3: causal GQA attention of the normalised,
+ *   rotated Q and K that the last q3a_prefill_prologue with the same B, T, Hq,
+ *   Hkv left in `workspace`, against v, into out. The workspace contents are
+ *   only read. Calling it on a workspace that no prologue of these shapes has
+ *   filled computes on whatever bytes are there (no fault, meaningless output).
+ * Sources: as q3a_prefill.
+ * ------------------------------------------------------------------------- */
+q3a_status q3a_prefill_prologue(const q3a_bf16* q, const q3a_bf16* k,
+                                const q3a_bf16* q_gamma, const q3a_bf16* k_gamma,
+                                int B, int T, int Hq, int Hkv, int d,
+                                double theta, float eps,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+q3a_status q3a_prefill_attention(const q3a_bf16* v, q3a_bf16* out,
+                                 int B, int T, int Hq, int Hkv, int d,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_decode — one new token per sequence against a KV cache.
  *
  *   q       [B, Hq, d]  bf16 projected query of the new token.

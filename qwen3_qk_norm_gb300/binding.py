@@ -19,7 +19,8 @@ Q3A_OK, Q3A_EINVAL, Q3A_ERANGE, Q3A_ECUDA, Q3A_ETIMEOUT, Q3A_ENOTIMPL = range(6)
 STATUS_NAMES = {0: "Q3A_OK", 1: "Q3A_EINVAL", 2: "Q3A_ERANGE", 3: "Q3A_ECUDA",
                 4: "Q3A_ETIMEOUT", 5: "Q3A_ENOTIMPL"}
 EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size", "q3a_prefill",
-            "q3a_decode_workspace_size", "q3a_decode", "q3a_last_device_error"]
+            "q3a_prefill_prologue", "q3a_prefill_attention", "q3a_decode_workspace_size",
+            "q3a_decode", "q3a_last_device_error"]
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +59,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_prefill_workspace_size.restype = sz
         lib.q3a_prefill.argtypes = [vp] * 6 + [i] * 5 + [d, f, vp, sz, vp]
         lib.q3a_prefill.restype = i
+        lib.q3a_prefill_prologue.argtypes = [vp] * 4 + [i] * 5 + [d, f, vp, sz, vp]
+        lib.q3a_prefill_prologue.restype = i
+        lib.q3a_prefill_attention.argtypes = [vp] * 2 + [i] * 5 + [vp, sz, vp]
+        lib.q3a_prefill_attention.restype = i
         lib.q3a_decode_workspace_size.argtypes = [i] * 5
         lib.q3a_decode_workspace_size.restype = sz
         lib.q3a_decode.argtypes = [vp] * 9 + [i] * 5 + [d, f, vp, sz, vp]
@@ -131,6 +136,35 @@ def prefill(q, k, v, q_gamma, k_gamma, theta: float, eps: float, out=None,
                             float(eps), workspace.data_ptr(), workspace.numel(),
                             _stream(q.device))
     _raise(st, "q3a_prefill")
+    return out
+
+
+def prefill_prologue(q, k, q_gamma, k_gamma, theta: float, eps: float,
+                     workspace: torch.Tensor) -> None:
+    """Steps 1-2 of prefill into ``workspace`` (see q3a_prefill_prologue)."""
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _check(q, "q")
+    _check(k, "k", (B, T, Hkv, d))
+    _check(q_gamma, "q_gamma", (d,))
+    _check(k_gamma, "k_gamma", (d,))
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_prefill_prologue(q.data_ptr(), k.data_ptr(), q_gamma.data_ptr(),
+                                     k_gamma.data_ptr(), B, T, Hq, Hkv, d, float(theta),
+                                     float(eps), workspace.data_ptr(), workspace.numel(),
+                                     _stream(q.device))
+    _raise(st, "q3a_prefill_prologue")
+
+
+def prefill_attention(v, out, Hq: int, workspace: torch.Tensor) -> torch.Tensor:
+    """Step 3 of prefill from ``workspace`` (see q3a_prefill_attention)."""
+    B, T, Hkv, d = v.shape
+    _check(v, "v")
+    _check(out, "out", (B, T, Hq, d))
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_prefill_attention(v.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, d,
+                                      workspace.data_ptr(), workspace.numel(), _stream(v.device))
+    _raise(st, "q3a_prefill_attention")
     return out
 
 

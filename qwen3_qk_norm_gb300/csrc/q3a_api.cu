@@ -117,57 +117,33 @@ size_t q3a_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d) {
   return kHeader + align256(prefill_q_bytes(B, T, Hq)) + align256(prefill_k_bytes(B, T, Hkv));
 }
 
-q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
-                       const q3a_bf16* q_gamma, const q3a_bf16* k_gamma, q3a_bf16* out, int B,
-                       int T, int Hq, int Hkv, int d, double theta, float eps, void* workspace,
-                       size_t ws_bytes, void* stream) {
+static q3a_status prefill_check(const void* const* ptrs, int nptrs, int B, int T, int Hq,
+                                int Hkv, int d, void* workspace, size_t ws_bytes, bool* empty) {
+  *empty = false;
   if (d != 128 || B < 0 || T < 0 || !group_ok(Hq, Hkv)) return Q3A_EINVAL;
-  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
   if ((long long)B * T * Hq > 0x7fffffffLL || T > (1 << 30)) return Q3A_EINVAL;
-  if (B == 0 || T == 0) return Q3A_OK;
-  const void* ptrs[] = {q, k, v, q_gamma, k_gamma, out};
-  for (const void* p : ptrs)
-    if (!p || !aligned16(p)) return Q3A_EINVAL;
+  if (B == 0 || T == 0) {
+    *empty = true;
+    return Q3A_OK;
+  }
+  for (int i = 0; i < nptrs; ++i)
+    if (!ptrs[i] || !aligned16(ptrs[i])) return Q3A_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
   if (ws_bytes < q3a_prefill_workspace_size(B, T, Hq, Hkv, d)) return Q3A_EINVAL;
+  return Q3A_OK;
+}
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
-  uint16_t* qhat = reinterpret_cast<uint16_t*>(ws + kHeader);
-  uint16_t* khat =
-      reinterpret_cast<uint16_t*>(ws + kHeader + align256(prefill_q_bytes(B, T, Hq)));
-  const int g = Hq / Hkv;
+static uint16_t* ws_qhat(void* ws) { return reinterpret_cast<uint16_t*>((uint8_t*)ws + kHeader); }
+static uint16_t* ws_khat(void* ws, int B, int T, int Hq) {
+  return reinterpret_cast<uint16_t*>((uint8_t*)ws + kHeader + align256(prefill_q_bytes(B, T, Hq)));
+}
 
-  // tensor maps first: a failure here launches nothing
-  PrefillArgs pa;
-  memset(&pa, 0, sizeof pa);
-  {
-    const uint64_t dq[4] = {128, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
-    const uint64_t sq[3] = {256, (uint64_t)Hq * 256, (uint64_t)T * Hq * 256};
-    const uint32_t bq[4] = {64, (uint32_t)g, (uint32_t)(128 / g), 1};
-    const uint64_t dk[3] = {128, (uint64_t)T, (uint64_t)B * Hkv};
-    const uint64_t sk[2] = {256, (uint64_t)T * 256};
-    const uint32_t bk[3] = {64, 128, 1};
-    const uint64_t dv[4] = {128, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
-    const uint64_t sv[3] = {256, (uint64_t)Hkv * 256, (uint64_t)T * Hkv * 256};
-    const uint32_t bv[4] = {64, 1, 128, 1};
-    if (encode_tensor_map(&pa.tm_q, qhat, 4, dq, sq, bq) != CUDA_SUCCESS ||
-        encode_tensor_map(&pa.tm_k, khat, 3, dk, sk, bk) != CUDA_SUCCESS ||
-        encode_tensor_map(&pa.tm_v, v, 4, dv, sv, bv) != CUDA_SUCCESS)
-      return Q3A_ECUDA;
-  }
-  pa.out = out;
-  pa.err = err;
-  pa.B = B;
-  pa.T = T;
-  pa.Hq = Hq;
-  pa.Hkv = Hkv;
-  pa.g = g;
-  pa.n_mtiles = (T + (128 / g) - 1) / (128 / g);
-
-  RopeArgs ra;
+static void prologue_args(RopeArgs& ra, const q3a_bf16* q, const q3a_bf16* k,
+                          const q3a_bf16* q_gamma, const q3a_bf16* k_gamma, int B, int T, int Hq,
+                          int Hkv, double theta, float eps, void* workspace) {
   memset(&ra, 0, sizeof ra);
+  uint16_t* qhat = ws_qhat(workspace);
+  uint16_t* khat = ws_khat(workspace, B, T, Hq);
   // Q -> Qhat, same [B, T, Hq] row order
   ra.t[0] = RopeTensor{q, q_gamma, qhat, Hq, (long long)T * Hq, Hq, 1, (long long)T * Hq, Hq, 1};
   // K [B, T, Hkv] -> Khat [B, Hkv, T] so that a 128-key tile of one group is contiguous
@@ -177,10 +153,81 @@ q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
   ra.T = T;
   ra.pos0 = 0;
   ra.eps = eps;
+  ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
   fill_inv_freq(theta, ra.inv_freq);
+}
 
-  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), st);
-  if (e == cudaSuccess) e = launch_qknorm_rope(ra, st);
+static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* out, int B, int T,
+                                 int Hq, int Hkv, void* workspace) {
+  memset(&pa, 0, sizeof pa);
+  const int g = Hq / Hkv;
+  const uint64_t dq[4] = {128, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
+  const uint64_t sq[3] = {256, (uint64_t)Hq * 256, (uint64_t)T * Hq * 256};
+  const uint32_t bq[4] = {64, (uint32_t)g, (uint32_t)(128 / g), 1};
+  const uint64_t dk[3] = {128, (uint64_t)T, (uint64_t)B * Hkv};
+  const uint64_t sk[2] = {256, (uint64_t)T * 256};
+  const uint32_t bk[3] = {64, 128, 1};
+  const uint64_t dv[4] = {128, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
+  const uint64_t sv[3] = {256, (uint64_t)Hkv * 256, (uint64_t)T * Hkv * 256};
+  const uint32_t bv[4] = {64, 1, 128, 1};
+  if (encode_tensor_map(&pa.tm_q, ws_qhat(workspace), 4, dq, sq, bq) != CUDA_SUCCESS ||
+      encode_tensor_map(&pa.tm_k, ws_khat(workspace, B, T, Hq), 3, dk, sk, bk) != CUDA_SUCCESS ||
+      encode_tensor_map(&pa.tm_v, v, 4, dv, sv, bv) != CUDA_SUCCESS)
+    return Q3A_ECUDA;
+  pa.out = out;
+  pa.err = reinterpret_cast<uint32_t*>(workspace);
+  pa.B = B;
+  pa.T = T;
+  pa.Hq = Hq;
+  pa.Hkv = Hkv;
+  pa.g = g;
+  pa.n_mtiles = (T + (128 / g) - 1) / (128 / g);
+  return Q3A_OK;
+}
+
+q3a_status q3a_prefill_prologue(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* q_gamma,
+                                const q3a_bf16* k_gamma, int B, int T, int Hq, int Hkv, int d,
+                                double theta, float eps, void* workspace, size_t ws_bytes,
+                                void* stream) {
+  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
+  const void* ptrs[] = {q, k, q_gamma, k_gamma};
+  bool empty;
+  q3a_status s = prefill_check(ptrs, 4, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
+  if (s != Q3A_OK || empty) return s;
+  RopeArgs ra;
+  prologue_args(ra, q, k, q_gamma, k_gamma, B, T, Hq, Hkv, theta, eps, workspace);
+  return from_cuda(launch_qknorm_rope(ra, static_cast<cudaStream_t>(stream)));
+}
+
+q3a_status q3a_prefill_attention(const q3a_bf16* v, q3a_bf16* out, int B, int T, int Hq, int Hkv,
+                                 int d, void* workspace, size_t ws_bytes, void* stream) {
+  const void* ptrs[] = {v, out};
+  bool empty;
+  q3a_status s = prefill_check(ptrs, 2, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
+  if (s != Q3A_OK || empty) return s;
+  PrefillArgs pa;
+  s = attention_args(pa, v, out, B, T, Hq, Hkv, workspace);
+  if (s != Q3A_OK) return s;
+  return from_cuda(launch_prefill_attention(pa, static_cast<cudaStream_t>(stream)));
+}
+
+q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
+                       const q3a_bf16* q_gamma, const q3a_bf16* k_gamma, q3a_bf16* out, int B,
+                       int T, int Hq, int Hkv, int d, double theta, float eps, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
+  const void* ptrs[] = {q, k, v, q_gamma, k_gamma, out};
+  bool empty;
+  q3a_status s = prefill_check(ptrs, 6, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
+  if (s != Q3A_OK || empty) return s;
+  // tensor maps first: a failure there launches nothing
+  PrefillArgs pa;
+  s = attention_args(pa, v, out, B, T, Hq, Hkv, workspace);
+  if (s != Q3A_OK) return s;
+  RopeArgs ra;
+  prologue_args(ra, q, k, q_gamma, k_gamma, B, T, Hq, Hkv, theta, eps, workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_qknorm_rope(ra, st);
   if (e == cudaSuccess) e = launch_prefill_attention(pa, st);
   return from_cuda(e);
 }

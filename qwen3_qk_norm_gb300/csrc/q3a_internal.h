@@ -27,6 +27,7 @@ struct RopeArgs {
   int B, T;
   long long pos0;  // row (b, t, h) is rotated at pos0 + t
   float eps;
+  uint32_t* err_clear;  // if non-null, block 0 zeroes this error word
   double inv_freq[64];  // theta^(-2i/128)
 };
 

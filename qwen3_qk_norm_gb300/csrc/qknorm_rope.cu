@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
   const long long n_tok = (long long)a.B * a.T;
   const long long tok0 = (long long)blockIdx.x * kTokPerCta;
 
+  if (a.err_clear && blockIdx.x == 0 && tid == 0) *a.err_clear = 0u;
+
   {  // rotation table of this CTA's tokens
     const int tt = tid >> 6, i = tid & 63;
     const long long tok = tok0 + tt;
