@@ -1,0 +1,499 @@
+"""Benchmark of the Qwen3 attention core on GB300: causal prefill TFLOP/s and
+decode GB/s, each against the measured roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0. A step is one q3a_prefill (QK-Norm + RoPE prologue,
+then causal GQA attention) over the Qwen3-8B-shaped prefill workload (B=4,
+T=4096, Hq=32, Hkv=8), inputs resident in HBM; ``value`` is its algorithmic
+TFLOP/s (unmasked causal pairs only). The same run times the Qwen3-8B-shaped
+decode workload (batch 64, start_pos in [1024, 32768)) in GB/s under "decode".
+With N > 1 (torchrun) every rank runs its own copy of the workload (weak
+scaling, no data-path collective); the time is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on bounded samples of the same
+workload (the only reference this method has: the pages give no code to run).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from qwen3_qk_norm_gb300 import accounting, inputs  # noqa: E402
+from qwen3_qk_norm_gb300.inputs import WORKLOADS  # noqa: E402
+
+METRIC = "causal prefill attention TFLOP/s and decode GB/s at 1 GB300, % of roofline"
+PREFILL_WORKLOAD = "qwen3-8b-prefill-b4-t4096"
+DECODE_WORKLOAD = "qwen3-8b-decode-b64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 2 ** 20
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (host logic; covered by the gloo tests)
+# ----------------------------------------------------------------------------
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        if device is not None and device.type == "cuda":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's value (times are reported as the max over ranks)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Weak scaling: every rank processes the same units; the job's rate is the
+    sum of the units over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# ----------------------------------------------------------------------------
+# measurement helpers
+# ----------------------------------------------------------------------------
+def measured_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: torch.device, period_ms: int = 50):
+        self.proc = None
+        self.lines: list[str] = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:  # noqa: BLE001
+            sel = ["-i", str(device.index or 0)]
+        self.cmd = ["nvidia-smi"] + sel + ["--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                           f"-lms={period_ms}"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [s for s in sm if s > 0.5 * max(sm)]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, source: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since that capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("source_sha") != source_sha(source):
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+def synchronize_all(device):
+    torch.cuda.synchronize(device)
+
+
+# ----------------------------------------------------------------------------
+# our implementation
+# ----------------------------------------------------------------------------
+def bench_prefill(binding, device, steps: int, warmup: int, world: int):
+    w = WORKLOADS[PREFILL_WORKLOAD]
+    x = inputs.workload_inputs(w, device=device)
+    out = torch.empty_like(x["q"])
+    ws = torch.empty(binding.prefill_workspace_size(w.B, w.T, w.Hq, w.Hkv), dtype=torch.uint8,
+                     device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        binding.prefill_prologue(x["q"], x["k"], x["q_gamma"], x["k_gamma"], w.theta, w.eps, ws)
+        if ev is not None:
+            ev[1].record(stream)
+        binding.prefill_attention(x["v"], out, w.Hq, ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(world, device)
+    synchronize_all(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t1.record(stream)
+    synchronize_all(device)
+    barrier(world, device)
+    total_ms = t0.elapsed_time(t1)
+    k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    status = binding.last_device_error(ws)
+    if status != 0:
+        raise RuntimeError(f"prefill device error word: {status}")
+    return w, x, total_ms / steps, statistics.mean(k1_ms), statistics.mean(k2_ms)
+
+
+def bench_prefill_e2e(binding, device, w, steps: int):
+    """Same step through q3a_prefill with host buffers: pinned host -> device
+    copies of the step's inputs and device -> host copy of its output inside
+    the timed region."""
+    xc = inputs.workload_inputs(w, device=device)
+    host = {k: t.to("cpu").pin_memory() for k, t in xc.items()}
+    dev = {k: torch.empty_like(t) for k, t in xc.items()}
+    out = torch.empty_like(xc["q"])
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    ws = torch.empty(binding.prefill_workspace_size(w.B, w.T, w.Hq, w.Hkv), dtype=torch.uint8,
+                     device=device)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out.numel() * out.element_size()
+
+    def step():
+        for k in dev:
+            dev[k].copy_(host[k], non_blocking=True)
+        binding.prefill(dev["q"], dev["k"], dev["v"], dev["q_gamma"], dev["k_gamma"], w.theta,
+                        w.eps, out=out, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    step()
+    synchronize_all(device)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    synchronize_all(device)
+    dt = (time.perf_counter() - t0) / steps
+    return dt, h2d, d2h
+
+
+def bench_decode(binding, device, steps: int, warmup: int, world: int):
+    w = WORKLOADS[DECODE_WORKLOAD]
+    x = inputs.workload_inputs(w, device=device)
+    out = torch.empty_like(x["q"])
+    ws = torch.empty(binding.decode_workspace_size(w.B, w.Hq, w.Hkv, w.S_max), dtype=torch.uint8,
+                     device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        binding.decode(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                       x["start_pos"], x["q_gamma"], x["k_gamma"], w.theta, w.eps, out=out,
+                       workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    barrier(world, device)
+    synchronize_all(device)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    synchronize_all(device)
+    barrier(world, device)
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    status = binding.last_device_error(ws)
+    if status != 0:
+        raise RuntimeError(f"decode device error word: {status}")
+    return w, x["start_pos"], ms
+
+
+def cpu_baseline_prefill(w, x_cpu: dict, budget_s: float = 12.0, seed: int = 0) -> dict:
+    """The fp64 oracle on a bounded sample of the prefill workload's query rows
+    (random (b, t, h)), on all host cores, for about ``budget_s`` seconds."""
+    import oracle
+
+    oracle.build()
+    g = torch.Generator().manual_seed(seed)
+    rows_done, flops = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        n = 16
+        rows = torch.stack([torch.randint(0, w.B, (n,), generator=g),
+                            torch.randint(0, w.T, (n,), generator=g),
+                            torch.randint(0, w.Hq, (n,), generator=g)], 1).to(torch.int32)
+        oracle.prefill_rows(x_cpu["q"], x_cpu["k"], x_cpu["v"], x_cpu["q_gamma"],
+                            x_cpu["k_gamma"], w.theta, w.eps, rows)
+        rows_done += n
+        flops += sum(4 * w.d * (int(t) + 1) for t in rows[:, 1].tolist())
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{rows_done} random query rows (b,t,h) of {w.name}, each computed from "
+                      f"scratch in fp64 (its keys normalised and rotated again); {dt:.1f} s wall"}
+
+
+def run_profile_case(which: str) -> None:
+    """A few launches of one kernel on a case sized for an ncu capture
+    (inputs larger than L2, a few GB on the device at most)."""
+    from qwen3_qk_norm_gb300 import binding
+    from qwen3_qk_norm_gb300.build import build
+    build()
+    device = torch.device("cuda", 0)
+    if which == "prefill":
+        w = WORKLOADS[PREFILL_WORKLOAD]
+        x = inputs.workload_inputs(w, device=device)
+        for _ in range(3):
+            binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], w.theta, w.eps)
+    else:
+        w = WORKLOADS[DECODE_WORKLOAD]
+        B = 16  # a quarter of the batch: 2 GiB of cache instead of 8
+        x = inputs.decode_inputs(B, w.Hq, w.Hkv, w.S_max, w.sp_lo, w.sp_hi, w.d, w.seed,
+                                 device=device)
+        for _ in range(3):
+            binding.decode(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                           x["start_pos"], x["q_gamma"], x["k_gamma"], w.theta, w.eps)
+        print(json.dumps({"decode_bytes_per_step": accounting.decode_bytes(
+            x["start_pos"].tolist(), w.Hq, w.Hkv, w.d), "B": B}))
+    torch.cuda.synchronize(device)
+
+
+def run_ours(args) -> None:
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    from qwen3_qk_norm_gb300 import binding
+    from qwen3_qk_norm_gb300.build import build
+    build()
+    binding.load()
+    peaks, peak_src = measured_peaks()
+
+    with ClockSampler(device) as clk:
+        w, x, step_ms, k1_ms, k2_ms = bench_prefill(binding, device, args.steps, args.warmup, world)
+        dw, start_pos, dec_ms = (None, None, None)
+        if not args.no_decode:
+            dw, start_pos, dec_ms = bench_decode(binding, device, args.steps, args.warmup, world)
+    clocks = clk.summary()
+
+    flops = accounting.prefill_flops(w.B, w.T, w.Hq, w.d)
+    step_ms_max = max_over_ranks(step_ms, world, device)
+    k2_ms_max = max_over_ranks(k2_ms, world, device)
+    k1_ms_max = max_over_ranks(k1_ms, world, device)
+    value = whole_job_rate(flops, world, step_ms_max / 1e3) / 1e12
+    k2_tflops = flops / (k2_ms_max / 1e3) / 1e12
+    k1_bytes = (w.B * w.T * (w.Hq + w.Hkv) * w.d * 2) * 2 + 2 * w.d * 2
+    src_k2 = os.path.join(ROOT, "qwen3_qk_norm_gb300", "csrc", "prefill_attention.cu")
+    traffic = ncu_traffic("prefill_attention_kernel", src_k2)
+
+    e2e_steps = max(1, min(args.steps, 10))
+    e2e_dt, h2d, d2h = bench_prefill_e2e(binding, device, w, e2e_steps)
+    e2e_dt = max_over_ranks(e2e_dt, world, device)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "theta": w.theta, "eps": w.eps, "outliers": "1% of Q/K rows x30",
+                   "causal": True, "parallelism": f"replicas x{world} (weak, no collective)",
+                   "l2": "inputs larger than L2: q,k,v,Qhat,Khat,out = "
+                         f"{(w.B * w.T * (2 * w.Hq + 3 * w.Hkv) * w.d * 2 + w.B * w.T * w.Hq * w.d * 2) / 2**20:.0f} MiB per step"},
+        "roofline": {"bound": "tensor", "kernel": "prefill_attention_kernel",
+                     "achieved": round(k2_tflops, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(k2_tflops / peaks["bf16_tflops"], 4),
+                     "peak_source": f"{peak_src} bf16 dense burst",
+                     "frac_of_sustained": round(k2_tflops / peaks.get(
+                         "bf16_tflops_sustained", peaks["bf16_tflops"]), 4),
+                     "traffic": traffic, "flops_per_launch": flops,
+                     "ms_per_launch": round(k2_ms_max, 4)},
+        "prologue": {"kernel": "qknorm_rope_kernel", "ms_per_launch": round(k1_ms_max, 4),
+                     "bytes_per_launch": k1_bytes,
+                     "achieved_gbs": round(k1_bytes / (k1_ms_max / 1e3) / 1e9, 1),
+                     "frac_of_hbm": round(k1_bytes / (k1_ms_max / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "e2e": {"value": round(whole_job_rate(flops, world, e2e_dt) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "q3a_prefill with pinned host inputs copied in and the output copied out "
+                       "every step"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if dec_ms is not None:
+        dbytes = accounting.decode_bytes(start_pos.tolist(), dw.Hq, dw.Hkv, dw.d)
+        dec_ms_max = max_over_ranks(dec_ms, world, device)
+        gbs = whole_job_rate(dbytes, world, dec_ms_max / 1e3) / 1e9
+        per_gpu = dbytes / (dec_ms_max / 1e3) / 1e9
+        line["decode"] = {
+            "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(dec_ms_max, 4),
+            "config": {"workload": dw.name, "B": dw.B, "Hq": dw.Hq, "Hkv": dw.Hkv,
+                       "S_max": dw.S_max, "start_pos": f"U[{dw.sp_lo}, {dw.sp_hi}) seed {dw.seed}",
+                       "bytes_per_step": dbytes},
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_combine_kernel",
+                         "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(per_gpu / peaks["hbm_gbs"], 4),
+                         "peak_source": f"{peak_src} copy bandwidth",
+                         "traffic": ncu_traffic("decode_split_kernel", os.path.join(
+                             ROOT, "qwen3_qk_norm_gb300", "csrc", "decode_attention.cu"))},
+            "gpu_launches": 2 * args.steps,
+        }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x_cpu = {k: t.cpu() for k, t in x.items()}
+        line["cpu_baseline"] = cpu_baseline_prefill(w, x_cpu)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle on bounded samples of the same workload
+# ----------------------------------------------------------------------------
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    w = WORKLOADS[PREFILL_WORKLOAD]
+    x = inputs.workload_inputs(w, device="cpu")
+    g = torch.Generator().manual_seed(1234)
+    n_rows = 8
+
+    def one_step():
+        rows = torch.stack([torch.randint(0, w.B, (n_rows,), generator=g),
+                            torch.randint(0, w.T, (n_rows,), generator=g),
+                            torch.randint(0, w.Hq, (n_rows,), generator=g)], 1).to(torch.int32)
+        t0 = time.perf_counter()
+        oracle.prefill_rows(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], w.theta, w.eps,
+                            rows)
+        return time.perf_counter() - t0, sum(4 * w.d * (int(t) + 1) for t in rows[:, 1].tolist())
+
+    for _ in range(args.warmup):
+        one_step()
+    secs, flops = 0.0, 0
+    for _ in range(args.steps):
+        s, f = one_step()
+        secs += s
+        flops += f
+    value = flops / secs / 1e12
+    sample = f"{n_rows} random query rows of {w.name} per step, fp64, each row from scratch"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["prefill", "decode"],
+                    help="run a few launches of one kernel for an ncu capture, print no JSON")
+    args = ap.parse_args(argv)
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
+    if args.warmup < 3:
+        args.warmup = 3  # never time cold kernels
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
