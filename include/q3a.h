@@ -166,6 +166,43 @@ q3a_status q3a_decode(const q3a_bf16* q, const q3a_bf16* k_new, const q3a_bf16* 
                       void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * q3a_decode_noalloc — q3a_decode for callers that cannot allocate device
+ * memory for a workspace: a plugin whose host framework owns every device
+ * allocation and hands it none, or a latency-critical loop that must not call
+ * cudaMalloc because cudaMalloc can synchronise the device. The scratch that
+ * q3a_decode keeps in the caller's workspace (split partials and the error
+ * word) lives instead in one static device array of
+ * Q3A_DECODE_NOALLOC_SCRATCH_BYTES bytes inside the library; every GPU that
+ * loads the library holds that array until the process exits. The pages have
+ * no counterpart of this entry point: it exists for callers of this library.
+ *
+ *   Arguments, results, the cache append and the error rules are those of
+ *   q3a_decode, without workspace and ws_bytes.
+ *   Size limit: it needs 256 + 4 * 130 * B * Hkv * g * S bytes, where
+ *   S = max over b of ceil((start_pos[b] + 1) / 1024) and g = Hq / Hkv; a
+ *   call that needs more than Q3A_DECODE_NOALLOC_SCRATCH_BYTES returns
+ *   Q3A_EINVAL before anything is launched or written.
+ *   No allocation: it calls no cudaMalloc, cudaFree or allocating routine.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *   first call before any stream capture on the device.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents (the error word is cleared at the start of each call).
+ *   Calls whose executions overlap on the GPU (different streams, or several
+ *   host threads) race on the array and may return wrong results; order them
+ *   on one stream or serialise them.
+ * ------------------------------------------------------------------------- */
+#define Q3A_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+q3a_status q3a_decode_noalloc(const q3a_bf16* q, const q3a_bf16* k_new, const q3a_bf16* v_new,
+                              q3a_bf16* k_cache, q3a_bf16* v_cache,
+                              const int32_t* start_pos,
+                              const q3a_bf16* q_gamma, const q3a_bf16* k_gamma,
+                              q3a_bf16* out,
+                              int B, int Hq, int Hkv, int d, int S_max,
+                              double theta, float eps, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_last_device_error — reads, synchronously on `stream`, the error word
  * that the kernels of the last call which used `workspace` left in its first
  * bytes (prefill and decode workspaces both keep it at offset 0).

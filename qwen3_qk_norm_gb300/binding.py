@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "Q3A_OK", 1: "Q3A_EINVAL", 2: "Q3A_ERANGE", 3: "Q3A_ECUDA",
                 4: "Q3A_ETIMEOUT", 5: "Q3A_ENOTIMPL"}
 EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size", "q3a_prefill",
             "q3a_prefill_prologue", "q3a_prefill_attention", "q3a_decode_workspace_size",
-            "q3a_decode", "q3a_last_device_error"]
+            "q3a_decode", "q3a_decode_noalloc", "q3a_last_device_error"]
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +67,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_decode_workspace_size.restype = sz
         lib.q3a_decode.argtypes = [vp] * 9 + [i] * 5 + [d, f, vp, sz, vp]
         lib.q3a_decode.restype = i
+        lib.q3a_decode_noalloc.argtypes = [vp] * 9 + [i] * 5 + [d, f, vp]
+        lib.q3a_decode_noalloc.restype = i
         lib.q3a_last_device_error.argtypes = [vp, vp]
         lib.q3a_last_device_error.restype = i
         _lib = lib
