@@ -181,7 +181,8 @@ static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* o
   pa.Hq = Hq;
   pa.Hkv = Hkv;
   pa.g = g;
-  pa.n_mtiles = (T + (128 / g) - 1) / (128 / g);
+  const int rows_tok = prefill_tokens_per_cta(g);
+  pa.n_mtiles = (T + rows_tok - 1) / rows_tok;
   return Q3A_OK;
 }
 

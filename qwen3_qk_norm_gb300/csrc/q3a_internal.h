@@ -42,10 +42,12 @@ struct PrefillArgs {
   uint16_t* out;     // [B, T, Hq, 128] bf16
   uint32_t* err;     // device error word
   int B, T, Hq, Hkv, g;
-  int n_mtiles;      // ceil(T / (128 / g))
+  int n_mtiles;      // ceil(T / prefill_tokens_per_cta(g))
 };
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
+// tokens of one KV group that one attention CTA covers (n_mtiles = ceil(T / this))
+int prefill_tokens_per_cta(int g);
 
 // ----- K3/K4: split-KV decode ------------------------------------------------
 constexpr int kDecodeMaxB = 2048;
