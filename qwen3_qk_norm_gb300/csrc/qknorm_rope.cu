@@ -23,9 +23,10 @@ namespace q3a {
 
 namespace {
 
-constexpr int kTokPerCta = 4;
+constexpr int kTokPerCta = 4;  // 64 angle-table entries per token
 constexpr int kThreads = 256;
 constexpr int kHalfWarps = kThreads / 16;
+constexpr int kUnroll = 4;  // rows per half-warp per pass
 
 __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
   __shared__ float2 cs[kTokPerCta][64];
@@ -65,37 +66,53 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
   // rows are taken by whole warps (two per warp) so the shuffles stay converged
   const int rows_even = (rows + 1) & ~1;
 
-  for (int r = hw; r < rows_even; r += kHalfWarps) {
-    const bool live = r < rows;
-    const int rr = live ? r : rows - 1;
-    const int tt = rr / rows_per_tok;
-    int h = rr - tt * rows_per_tok;
-    const int s = (h < H0) ? 0 : 1;
-    if (s) h -= H0;
-    const long long tok = tok0 + tt;
-    const long long b = tok / a.T, t = tok - b * a.T;
-    // field-wise selects keep the parameter struct out of local memory
-    const uint16_t* xr = (s ? a.t[1].x : a.t[0].x) +
-                         (b * (s ? a.t[1].xsb : a.t[0].xsb) + t * (s ? a.t[1].xst : a.t[0].xst) +
-                          (long long)h * (s ? a.t[1].xsh : a.t[0].xsh)) * 128;
-    uint16_t* yr = (s ? a.t[1].y : a.t[0].y) +
-                   (b * (s ? a.t[1].ysb : a.t[0].ysb) + t * (s ? a.t[1].yst : a.t[0].yst) +
-                    (long long)h * (s ? a.t[1].ysh : a.t[0].ysh)) * 128;
-    float xl[4], xh[4], ol[4], oh[4];
-    unpack4(reinterpret_cast<const uint2*>(xr)[lane16], xl);
-    unpack4(reinterpret_cast<const uint2*>(xr + 64)[lane16], xh);
-    float2 c_s[4];
-    float gls[4], ghs[4];
+  // Each half-warp handles kUnroll rows per pass, all loads first, so that
+  // kUnroll x 256 bytes per half-warp are in flight at once.
+  for (int r0 = hw; r0 < rows_even; r0 += kHalfWarps * kUnroll) {
+    float xl[kUnroll][4], xh[kUnroll][4];
+    uint16_t* yr[kUnroll];
+    int sel[kUnroll], tts[kUnroll];
+    bool live[kUnroll];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      c_s[j] = cs[tt][4 * lane16 + j];
-      gls[j] = s ? gl[1][j] : gl[0][j];
-      ghs[j] = s ? gh[1][j] : gh[0][j];
+    for (int u = 0; u < kUnroll; ++u) {
+      const int r = r0 + u * kHalfWarps;
+      live[u] = r < rows;
+      const int rr = live[u] ? r : rows - 1;
+      const int tt = rr / rows_per_tok;
+      int h = rr - tt * rows_per_tok;
+      const int s = (h < H0) ? 0 : 1;
+      if (s) h -= H0;
+      const long long tok = tok0 + tt;
+      const long long b = tok / a.T, t = tok - b * a.T;
+      // field-wise selects keep the parameter struct out of local memory
+      const uint16_t* xr =
+          (s ? a.t[1].x : a.t[0].x) +
+          (b * (s ? a.t[1].xsb : a.t[0].xsb) + t * (s ? a.t[1].xst : a.t[0].xst) +
+           (long long)h * (s ? a.t[1].xsh : a.t[0].xsh)) * 128;
+      yr[u] = (s ? a.t[1].y : a.t[0].y) +
+              (b * (s ? a.t[1].ysb : a.t[0].ysb) + t * (s ? a.t[1].yst : a.t[0].yst) +
+               (long long)h * (s ? a.t[1].ysh : a.t[0].ysh)) * 128;
+      sel[u] = s;
+      tts[u] = tt;
+      unpack4(reinterpret_cast<const uint2*>(xr)[lane16], xl[u]);
+      unpack4(reinterpret_cast<const uint2*>(xr + 64)[lane16], xh[u]);
     }
-    qknorm_rope_halfwarp(xl, xh, gls, ghs, c_s, a.eps, ol, oh);
-    if (live) {
-      reinterpret_cast<uint2*>(yr)[lane16] = pack4(ol);
-      reinterpret_cast<uint2*>(yr + 64)[lane16] = pack4(oh);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (r0 + u * kHalfWarps >= rows_even) break;  // uniform across the warp
+      float2 c_s[4];
+      float gls[4], ghs[4], ol[4], oh[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        c_s[j] = cs[tts[u]][4 * lane16 + j];
+        gls[j] = sel[u] ? gl[1][j] : gl[0][j];
+        ghs[j] = sel[u] ? gh[1][j] : gh[0][j];
+      }
+      qknorm_rope_halfwarp(xl[u], xh[u], gls, ghs, c_s, a.eps, ol, oh);
+      if (live[u]) {
+        reinterpret_cast<uint2*>(yr[u])[lane16] = pack4(ol);
+        reinterpret_cast<uint2*>(yr[u] + 64)[lane16] = pack4(oh);
+      }
     }
   }
 }
