@@ -261,17 +261,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 128; ++e)
           if (key0 + e > tok) s[e] = -INFINITY;
       }
-      float mt = s[0];
+      // row max as a tree: eight independent chains, then a 3-level fold
+      float mx[8];
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mt = fmaxf(mt, s[e]);
-      const float m_tile = mt * kScaleLog2;
+      for (int e = 0; e < 8; ++e) mx[e] = s[e];
+#pragma unroll
+      for (int e = 8; e < 128; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
+#pragma unroll
+      for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+      const float m_tile = mx[0] * kScaleLog2;
       const bool move = m_tile > m + kRescaleThreshold;
       const float m_new = move ? m_tile : m;
       const float alpha = move ? ex2(m - m_new) : 1.0f;
       m = m_new;
       l *= alpha;
 
-      float sum = 0.f;
+      float sums[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pw[32];
@@ -279,11 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; ++e) {
           const float p0 = ex2(fmaf(s[c * 64 + 2 * e], kScaleLog2, -m));
           const float p1 = ex2(fmaf(s[c * 64 + 2 * e + 1], kScaleLog2, -m));
-          sum += p0 + p1;
+          sums[e & 3] += p0 + p1;
           pw[e] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tmem_s + c * 32, pw);
       }
+      const float sum = (sums[0] + sums[1]) + (sums[2] + sums[3]);
       // O_t holds every PV up to j-1 here (the S_t,j commit covers them);
       // rescale it before PV_t,j adds terms relative to the new max
       if (j > 0 && __any_sync(kFull, move)) {

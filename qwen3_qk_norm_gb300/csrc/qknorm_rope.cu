@@ -8,14 +8,16 @@
 // implementation" (§7.2.1 GroupedQueryAttention.forward: q_norm/k_norm, then
 // apply_rope) and the transformers Qwen3Attention quoted on the "Qwen3" note.
 //
-// Layout of the work: one CTA per 4 tokens. The 4 x 64 rotation angles of its
+// Layout of the work: one CTA per 8 tokens. The 8 x 64 rotation angles of its
 // tokens are formed once per CTA in fp64 (p * w_i, reduced modulo 2 pi) and
 // turned into fp32 (cos, sin) pairs in shared memory; every head row of those
 // tokens (Q and K rows in the same launch) reuses them. A half-warp owns one
 // row: lane L holds elements 4L..4L+3 and their rotate-half partners
 // 64+4L..64+4L+3, so the rotation needs no data exchange and the RMS needs a
 // 4-step shuffle reduction inside the half-warp. Loads and stores are 8-byte
-// vectors, 128 contiguous bytes per half-warp per instruction.
+// vectors, 128 contiguous bytes per half-warp per instruction. Row addresses
+// come from per-token offsets computed once per CTA, so the row loop has no
+// integer division.
 #include "q3a_internal.h"
 #include "q3a_rope.cuh"
 
@@ -23,23 +25,39 @@ namespace q3a {
 
 namespace {
 
-constexpr int kTokPerCta = 4;  // 64 angle-table entries per token
+constexpr int kTokPerCta = 8;
 constexpr int kThreads = 256;
 constexpr int kHalfWarps = kThreads / 16;
-constexpr int kUnroll = 4;  // rows per half-warp per pass
 
 __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
-  __shared__ float2 cs[kTokPerCta][64];
+  __shared__ __align__(16) float cos_s[kTokPerCta][64];
+  __shared__ __align__(16) float sin_s[kTokPerCta][64];
+  __shared__ long long xbase[kTokPerCta][2], ybase[kTokPerCta][2];  // in rows of 128
   const int tid = threadIdx.x;
   const long long n_tok = (long long)a.B * a.T;
   const long long tok0 = (long long)blockIdx.x * kTokPerCta;
+  const int tok_here = (int)min((long long)kTokPerCta, n_tok - tok0);
 
   if (a.err_clear && blockIdx.x == 0 && tid == 0) *a.err_clear = 0u;
 
-  {  // rotation table of this CTA's tokens
-    const int tt = tid >> 6, i = tid & 63;
-    const long long tok = tok0 + tt;
-    if (tok < n_tok) cs[tt][i] = rope_cos_sin(a.pos0 + tok % a.T, a.inv_freq[i]);
+  // rotation table of this CTA's tokens (two entries per thread)
+  for (int e = tid; e < kTokPerCta * 64; e += kThreads) {
+    const int tt = e >> 6, i = e & 63;
+    if (tt < tok_here) {
+      const float2 c_s = rope_cos_sin(a.pos0 + (tok0 + tt) % a.T, a.inv_freq[i]);
+      cos_s[tt][i] = c_s.x;
+      sin_s[tt][i] = c_s.y;
+    }
+  }
+  // per-token row offsets of both tensors: the only divisions of the kernel
+  if (tid < kTokPerCta * 2) {
+    const int tt = tid >> 1, s = tid & 1;
+    if (tt < tok_here && s < a.ntensors) {
+      const long long tok = tok0 + tt;
+      const long long b = tok / a.T, t = tok - b * a.T;
+      xbase[tt][s] = b * (s ? a.t[1].xsb : a.t[0].xsb) + t * (s ? a.t[1].xst : a.t[0].xst);
+      ybase[tt][s] = b * (s ? a.t[1].ysb : a.t[0].ysb) + t * (s ? a.t[1].yst : a.t[0].yst);
+    }
   }
 
   const int lane16 = tid & 15;
@@ -61,58 +79,50 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
 
   const int H0 = a.t[0].H;
   const int rows_per_tok = H0 + (a.ntensors > 1 ? a.t[1].H : 0);
-  const long long tok_here = min((long long)kTokPerCta, n_tok - tok0);
-  const int rows = (int)tok_here * rows_per_tok;
-  // rows are taken by whole warps (two per warp) so the shuffles stay converged
-  const int rows_even = (rows + 1) & ~1;
+  const int rows = tok_here * rows_per_tok;
+  const int rows_even = (rows + 1) & ~1;  // whole warps, so the shuffles stay converged
+  const uint16_t* x0 = a.t[0].x;
+  const uint16_t* x1 = a.t[1].x;
+  uint16_t* y0 = a.t[0].y;
+  uint16_t* y1 = a.t[1].y;
+  const long long xsh0 = a.t[0].xsh, xsh1 = a.t[1].xsh, ysh0 = a.t[0].ysh, ysh1 = a.t[1].ysh;
 
-  // Each half-warp handles kUnroll rows per pass, all loads first, so that
-  // kUnroll x 256 bytes per half-warp are in flight at once.
-  for (int r0 = hw; r0 < rows_even; r0 += kHalfWarps * kUnroll) {
-    float xl[kUnroll][4], xh[kUnroll][4];
-    uint16_t* yr[kUnroll];
-    int sel[kUnroll], tts[kUnroll];
-    bool live[kUnroll];
+  // (tt, h) of row r = hw, advanced by kHalfWarps rows per pass without division
+  int tt = 0, h = hw;
+  while (h >= rows_per_tok) {
+    h -= rows_per_tok;
+    ++tt;
+  }
+  for (int r = hw; r < rows_even; r += kHalfWarps) {
+    const bool live = r < rows;
+    const int ttl = live ? tt : tok_here - 1;
+    const int hl = live ? h : rows_per_tok - 1;
+    const int s = hl < H0 ? 0 : 1;
+    const int hs = s ? hl - H0 : hl;
+    const uint16_t* xr = (s ? x1 : x0) + (xbase[ttl][s] + (long long)hs * (s ? xsh1 : xsh0)) * 128;
+    uint16_t* yr = (s ? y1 : y0) + (ybase[ttl][s] + (long long)hs * (s ? ysh1 : ysh0)) * 128;
+    float xl[4], xh[4], ol[4], oh[4];
+    unpack4(reinterpret_cast<const uint2*>(xr)[lane16], xl);
+    unpack4(reinterpret_cast<const uint2*>(xr + 64)[lane16], xh);
+    const float4 c4 = reinterpret_cast<const float4*>(cos_s[ttl])[lane16];
+    const float4 s4 = reinterpret_cast<const float4*>(sin_s[ttl])[lane16];
+    const float2 c_s[4] = {make_float2(c4.x, s4.x), make_float2(c4.y, s4.y),
+                           make_float2(c4.z, s4.z), make_float2(c4.w, s4.w)};
+    float gls[4], ghs[4];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int r = r0 + u * kHalfWarps;
-      live[u] = r < rows;
-      const int rr = live[u] ? r : rows - 1;
-      const int tt = rr / rows_per_tok;
-      int h = rr - tt * rows_per_tok;
-      const int s = (h < H0) ? 0 : 1;
-      if (s) h -= H0;
-      const long long tok = tok0 + tt;
-      const long long b = tok / a.T, t = tok - b * a.T;
-      // field-wise selects keep the parameter struct out of local memory
-      const uint16_t* xr =
-          (s ? a.t[1].x : a.t[0].x) +
-          (b * (s ? a.t[1].xsb : a.t[0].xsb) + t * (s ? a.t[1].xst : a.t[0].xst) +
-           (long long)h * (s ? a.t[1].xsh : a.t[0].xsh)) * 128;
-      yr[u] = (s ? a.t[1].y : a.t[0].y) +
-              (b * (s ? a.t[1].ysb : a.t[0].ysb) + t * (s ? a.t[1].yst : a.t[0].yst) +
-               (long long)h * (s ? a.t[1].ysh : a.t[0].ysh)) * 128;
-      sel[u] = s;
-      tts[u] = tt;
-      unpack4(reinterpret_cast<const uint2*>(xr)[lane16], xl[u]);
-      unpack4(reinterpret_cast<const uint2*>(xr + 64)[lane16], xh[u]);
+    for (int j = 0; j < 4; ++j) {
+      gls[j] = s ? gl[1][j] : gl[0][j];
+      ghs[j] = s ? gh[1][j] : gh[0][j];
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (r0 + u * kHalfWarps >= rows_even) break;  // uniform across the warp
-      float2 c_s[4];
-      float gls[4], ghs[4], ol[4], oh[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        c_s[j] = cs[tts[u]][4 * lane16 + j];
-        gls[j] = sel[u] ? gl[1][j] : gl[0][j];
-        ghs[j] = sel[u] ? gh[1][j] : gh[0][j];
-      }
-      qknorm_rope_halfwarp(xl[u], xh[u], gls, ghs, c_s, a.eps, ol, oh);
-      if (live[u]) {
-        reinterpret_cast<uint2*>(yr[u])[lane16] = pack4(ol);
-        reinterpret_cast<uint2*>(yr[u] + 64)[lane16] = pack4(oh);
-      }
+    qknorm_rope_halfwarp(xl, xh, gls, ghs, c_s, a.eps, ol, oh);
+    if (live) {
+      reinterpret_cast<uint2*>(yr)[lane16] = pack4(ol);
+      reinterpret_cast<uint2*>(yr + 64)[lane16] = pack4(oh);
+    }
+    h += kHalfWarps;
+    while (h >= rows_per_tok) {
+      h -= rows_per_tok;
+      ++tt;
     }
   }
 }
