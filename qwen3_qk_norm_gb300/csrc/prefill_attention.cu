@@ -34,10 +34,15 @@
 // thread, so when a softmax warpgroup sees S_t,j, O_t already holds every
 // PV up to j-1 and can be rescaled in place.
 //
-// Online softmax in the exp2 domain with a lazy rescale: the running row max m
-// only moves (and O_t, l are rescaled by 2^(m_old - m_new)) when a tile's max
-// exceeds it by more than 8, so P stays below 2^8 and most tiles skip the
-// TMEM read-modify-write of O.
+// Softmax in the exp2 domain. QK-Norm bounds every logit: |qhat| <=
+// sqrt(128) max|gamma_q| and |khat| <= sqrt(128) max|gamma_k|, so
+// |qhat . khat| / sqrt(128) <= sqrt(128) max|gamma_q| max|gamma_k| (the
+// prologue writes this bound to the workspace). While the bound is moderate,
+// p = 2^(s - bound) never underflows for the terms that matter, and the
+// softmax needs neither a row max nor any rescaling of O: it is then a pure
+// elementwise map plus a running sum. For large gammas the kernel falls back
+// to the online max with a lazy rescale (the max only moves, and O_t, l are
+// rescaled by 2^(m_old - m_new), when a tile's max exceeds it by more than 8).
 //
 // Registers: the softmax warpgroups raise their budget to 208 per thread
 // (setmaxnreg) and warpgroup 2 lowers its to 88; the host checks that the
@@ -69,6 +74,9 @@ constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr float kScaleLog2 = 0.12751743074380046f;  // log2(e) / sqrt(128)
 constexpr float kRescaleThreshold = 8.0f;
+// largest logit bound (log2 units) for which 2^(-2 bound), the smallest
+// dominant term, is still a normal float after the fixed shift
+constexpr float kFixedMaxLimit = 60.0f;
 constexpr unsigned kFull = 0xffffffffu;
 
 static_assert(kQTiles * 128 * kRegsSoftmax + (kThreads - kQTiles * 128) * kRegsOther <=
@@ -238,7 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_s = tmem + t * 128 + lane_off;
     const uint32_t tmem_o = tmem + 256 + t * 128 + lane_off;
     const int tok = t0 + t * tile_tok + r / g;
-    float m = -INFINITY, l = 0.f;
+    // QK-Norm bounds every logit (in the exp2 domain) by `bound`. When
+    // 2^(-2 bound) is still a normal float, subtracting this fixed bound
+    // instead of the running row max gives the same softmax with no
+    // reduction and no rescaling; otherwise fall back to the online max.
+    const float bound = *a.logit_bound;
+    const bool fixed_max = bound >= 0.f && bound <= kFixedMaxLimit;
+    float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
+    float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       ok = __all_sync(kFull,
@@ -261,40 +276,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 128; ++e)
           if (key0 + e > tok) s[e] = -INFINITY;
       }
-      // row max as a tree: eight independent chains, then a 3-level fold
-      float mx[8];
+      bool move = false;
+      float alpha = 1.0f;
+      if (!fixed_max) {
+        // row max as a tree: eight independent chains, then a 3-level fold
+        float mx[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = s[e];
+        for (int e = 0; e < 8; ++e) mx[e] = s[e];
 #pragma unroll
-      for (int e = 8; e < 128; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
+        for (int e = 8; e < 128; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
 #pragma unroll
-      for (int w = 4; w >= 1; w >>= 1)
+        for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
-        for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-      const float m_tile = mx[0] * kScaleLog2;
-      const bool move = m_tile > m + kRescaleThreshold;
-      const float m_new = move ? m_tile : m;
-      const float alpha = move ? ex2(m - m_new) : 1.0f;
-      m = m_new;
-      l *= alpha;
+          for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+        const float m_tile = mx[0] * kScaleLog2;
+        move = m_tile > m + kRescaleThreshold;
+        const float m_new = move ? m_tile : m;
+        alpha = move ? ex2(m - m_new) : 1.0f;
+        m = m_new;
+        l *= alpha;
+      }
 
-      float sums[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      // p = 2^(s * scale - m), two at a time on the f32x2 pipes
+      const uint64_t scale2 = f2_pack(kScaleLog2, kScaleLog2);
+      const uint64_t negm2 = f2_pack(-m, -m);
+      uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pw[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2(fmaf(s[c * 64 + 2 * e], kScaleLog2, -m));
-          const float p1 = ex2(fmaf(s[c * 64 + 2 * e + 1], kScaleLog2, -m));
-          sums[e & 3] += p0 + p1;
+          const uint64_t x = f2_fma(f2_pack(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]), scale2, negm2);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
           pw[e] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tmem_s + c * 32, pw);
       }
-      const float sum = (sums[0] + sums[1]) + (sums[2] + sums[3]);
       // O_t holds every PV up to j-1 here (the S_t,j commit covers them);
       // rescale it before PV_t,j adds terms relative to the new max
-      if (j > 0 && __any_sync(kFull, move)) {
+      if (!fixed_max && j > 0 && __any_sync(kFull, move)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -306,7 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tmem_wait_st();
-      l += sum;
+      float a0, a1, b0, b1;
+      f2_unpack(sum2[0], a0, a1);
+      f2_unpack(sum2[1], b0, b1);
+      l += (a0 + a1) + (b0 + b1);
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);
     }

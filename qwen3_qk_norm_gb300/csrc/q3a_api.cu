@@ -154,6 +154,7 @@ static void prologue_args(RopeArgs& ra, const q3a_bf16* q, const q3a_bf16* k,
   ra.pos0 = 0;
   ra.eps = eps;
   ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
+  ra.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
   fill_inv_freq(theta, ra.inv_freq);
 }
 
@@ -176,6 +177,7 @@ static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* o
     return Q3A_ECUDA;
   pa.out = out;
   pa.err = reinterpret_cast<uint32_t*>(workspace);
+  pa.logit_bound = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + 8);
   pa.B = B;
   pa.T = T;
   pa.Hq = Hq;

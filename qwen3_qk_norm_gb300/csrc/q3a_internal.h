@@ -28,6 +28,10 @@ struct RopeArgs {
   long long pos0;  // row (b, t, h) is rotated at pos0 + t
   float eps;
   uint32_t* err_clear;  // if non-null, block 0 zeroes this error word
+  // if non-null, block 0 writes here the bound on |q.k| / sqrt(128) * log2(e)
+  // that QK-Norm guarantees: sqrt(128) * max|gamma_q| * max|gamma_k| * log2(e)
+  // (tensor 0 is Q, tensor 1 is K)
+  float* logit_bound;
   double inv_freq[64];  // theta^(-2i/128)
 };
 
@@ -41,6 +45,7 @@ struct PrefillArgs {
   CUtensorMap tm_v;  // V    [B, T, Hkv, 128] bf16, box {64, 1, 128, 1}
   uint16_t* out;     // [B, T, Hq, 128] bf16
   uint32_t* err;     // device error word
+  const float* logit_bound;  // written by the prologue (see RopeArgs)
   int B, T, Hq, Hkv, g;
   int n_mtiles;      // ceil(T / prefill_tokens_per_cta(g))
 };

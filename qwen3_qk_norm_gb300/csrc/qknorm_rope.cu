@@ -28,6 +28,7 @@ namespace {
 constexpr int kTokPerCta = 8;
 constexpr int kThreads = 256;
 constexpr int kHalfWarps = kThreads / 16;
+constexpr int kUnroll = 2;  // rows in flight per half-warp
 
 __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
   __shared__ __align__(16) float cos_s[kTokPerCta][64];
@@ -38,7 +39,24 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
   const long long tok0 = (long long)blockIdx.x * kTokPerCta;
   const int tok_here = (int)min((long long)kTokPerCta, n_tok - tok0);
 
-  if (a.err_clear && blockIdx.x == 0 && tid == 0) *a.err_clear = 0u;
+  if (blockIdx.x == 0 && tid < 32) {
+    if (a.err_clear && tid == 0) *a.err_clear = 0u;
+    if (a.logit_bound && a.ntensors == 2) {
+      // QK-Norm bounds every logit: |qhat| <= sqrt(128) max|gamma_q| and the
+      // same for khat, so |qhat . khat| / sqrt(128) <= sqrt(128) gq gk
+      float gq = 0.f, gk = 0.f;
+      for (int i = tid; i < 128; i += 32) {
+        gq = fmaxf(gq, fabsf(__uint_as_float((uint32_t)a.t[0].gamma[i] << 16)));
+        gk = fmaxf(gk, fabsf(__uint_as_float((uint32_t)a.t[1].gamma[i] << 16)));
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        gq = fmaxf(gq, __shfl_xor_sync(0xffffffffu, gq, o));
+        gk = fmaxf(gk, __shfl_xor_sync(0xffffffffu, gk, o));
+      }
+      if (tid == 0) *a.logit_bound = 11.313708498984761f * gq * gk * 1.4426950408889634f;
+    }
+  }
 
   // rotation table of this CTA's tokens (two entries per thread)
   for (int e = tid; e < kTokPerCta * 64; e += kThreads) {
@@ -87,42 +105,56 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
   uint16_t* y1 = a.t[1].y;
   const long long xsh0 = a.t[0].xsh, xsh1 = a.t[1].xsh, ysh0 = a.t[0].ysh, ysh1 = a.t[1].ysh;
 
-  // (tt, h) of row r = hw, advanced by kHalfWarps rows per pass without division
+  // (tt, h) of row r = hw, advanced by kHalfWarps rows at a time without
+  // division; kUnroll rows per half-warp are loaded before any is used
   int tt = 0, h = hw;
   while (h >= rows_per_tok) {
     h -= rows_per_tok;
     ++tt;
   }
-  for (int r = hw; r < rows_even; r += kHalfWarps) {
-    const bool live = r < rows;
-    const int ttl = live ? tt : tok_here - 1;
-    const int hl = live ? h : rows_per_tok - 1;
-    const int s = hl < H0 ? 0 : 1;
-    const int hs = s ? hl - H0 : hl;
-    const uint16_t* xr = (s ? x1 : x0) + (xbase[ttl][s] + (long long)hs * (s ? xsh1 : xsh0)) * 128;
-    uint16_t* yr = (s ? y1 : y0) + (ybase[ttl][s] + (long long)hs * (s ? ysh1 : ysh0)) * 128;
-    float xl[4], xh[4], ol[4], oh[4];
-    unpack4(reinterpret_cast<const uint2*>(xr)[lane16], xl);
-    unpack4(reinterpret_cast<const uint2*>(xr + 64)[lane16], xh);
-    const float4 c4 = reinterpret_cast<const float4*>(cos_s[ttl])[lane16];
-    const float4 s4 = reinterpret_cast<const float4*>(sin_s[ttl])[lane16];
-    const float2 c_s[4] = {make_float2(c4.x, s4.x), make_float2(c4.y, s4.y),
-                           make_float2(c4.z, s4.z), make_float2(c4.w, s4.w)};
-    float gls[4], ghs[4];
+  for (int r = hw; r < rows_even; r += kHalfWarps * kUnroll) {
+    float xl[kUnroll][4], xh[kUnroll][4];
+    uint16_t* yr[kUnroll];
+    int tsel[kUnroll], ssel[kUnroll];
+    bool live[kUnroll];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      gls[j] = s ? gl[1][j] : gl[0][j];
-      ghs[j] = s ? gh[1][j] : gh[0][j];
+    for (int u = 0; u < kUnroll; ++u) {
+      live[u] = r + u * kHalfWarps < rows;
+      const int ttl = live[u] ? tt : tok_here - 1;
+      const int hl = live[u] ? h : rows_per_tok - 1;
+      const int sl = hl < H0 ? 0 : 1;
+      const int hs = sl ? hl - H0 : hl;
+      const uint16_t* xr =
+          (sl ? x1 : x0) + (xbase[ttl][sl] + (long long)hs * (sl ? xsh1 : xsh0)) * 128;
+      yr[u] = (sl ? y1 : y0) + (ybase[ttl][sl] + (long long)hs * (sl ? ysh1 : ysh0)) * 128;
+      tsel[u] = ttl;
+      ssel[u] = sl;
+      unpack4(reinterpret_cast<const uint2*>(xr)[lane16], xl[u]);
+      unpack4(reinterpret_cast<const uint2*>(xr + 64)[lane16], xh[u]);
+      h += kHalfWarps;
+      while (h >= rows_per_tok) {
+        h -= rows_per_tok;
+        ++tt;
+      }
     }
-    qknorm_rope_halfwarp(xl, xh, gls, ghs, c_s, a.eps, ol, oh);
-    if (live) {
-      reinterpret_cast<uint2*>(yr)[lane16] = pack4(ol);
-      reinterpret_cast<uint2*>(yr + 64)[lane16] = pack4(oh);
-    }
-    h += kHalfWarps;
-    while (h >= rows_per_tok) {
-      h -= rows_per_tok;
-      ++tt;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (r + u * kHalfWarps >= rows_even) break;  // same for both halves of a warp
+      const float4 c4 = reinterpret_cast<const float4*>(cos_s[tsel[u]])[lane16];
+      const float4 s4 = reinterpret_cast<const float4*>(sin_s[tsel[u]])[lane16];
+      const float2 c_s[4] = {make_float2(c4.x, s4.x), make_float2(c4.y, s4.y),
+                             make_float2(c4.z, s4.z), make_float2(c4.w, s4.w)};
+      float gls[4], ghs[4], ol[4], oh[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gls[j] = ssel[u] ? gl[1][j] : gl[0][j];
+        ghs[j] = ssel[u] ? gh[1][j] : gh[0][j];
+      }
+      qknorm_rope_halfwarp(xl[u], xh[u], gls, ghs, c_s, a.eps, ol, oh);
+      if (live[u]) {
+        reinterpret_cast<uint2*>(yr[u])[lane16] = pack4(ol);
+        reinterpret_cast<uint2*>(yr[u] + 64)[lane16] = pack4(oh);
+      }
     }
   }
 }

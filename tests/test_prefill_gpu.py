@@ -47,6 +47,19 @@ def test_prefill_with_norm_outliers(cuda_lib):
     assert_close_attention(run_prefill(x, 1e6), ref, "outliers")
 
 
+@pytest.mark.parametrize("gmax", [1.0, 1.9, 2.1, 6.0])  # bound 16, 59 | 72, 586 (log2 units)
+def test_prefill_both_softmax_paths(cuda_lib, gmax):
+    """QK-Norm bounds the logits by sqrt(128) max|gamma_q| max|gamma_k|. Small
+    gammas take the fixed-shift softmax; large ones (bound above the kernel's
+    limit) take the online-max path. Both must match the oracle."""
+    x = inputs.prefill_inputs(1, 300, 16, 4, seed=int(gmax * 10))
+    g = torch.Generator().manual_seed(77)
+    x["q_gamma"] = (torch.rand(128, generator=g) * gmax).to(torch.bfloat16)
+    x["k_gamma"] = (torch.rand(128, generator=g) * gmax).to(torch.bfloat16)
+    ref = oracle.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    assert_close_attention(run_prefill(x, 1e6), ref, f"gamma max {gmax}")
+
+
 def test_prefill_future_tokens_leave_past_rows_bit_identical(cuda_lib):
     B, T, Hq, Hkv, cut = 1, 400, 8, 2, 170
     x = inputs.prefill_inputs(B, T, Hq, Hkv, seed=9)
