@@ -47,7 +47,7 @@ def test_prefill_with_norm_outliers(cuda_lib):
     assert_close_attention(run_prefill(x, 1e6), ref, "outliers")
 
 
-@pytest.mark.parametrize("gmax", [1.0, 1.9, 2.1, 2.5])  # bound 16, 59 | 72, 102 (log2 units)
+@pytest.mark.parametrize("gmax", [1.0, 1.9, 2.1, 2.3])  # bound 16, 59 | 72, 86 (log2 units)
 def test_prefill_both_softmax_paths(cuda_lib, gmax):
     """QK-Norm bounds the logits by sqrt(128) max|gamma_q| max|gamma_k|. Small
     gammas take the fixed-shift softmax; large ones (bound above the kernel's
