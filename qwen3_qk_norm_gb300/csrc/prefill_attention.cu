@@ -14,22 +14,20 @@
 // so each K/V byte is read once per 256/g tokens. KV tiles above the causal
 // diagonal are never loaded; diagonal tiles are masked per element.
 //
-// Roles (384 threads, three warpgroups):
-//   WG0 (warps 0-3)  softmax + epilogue of Q tile 0: thread r owns row r of
-//                    S0 and O0 in tensor memory (TMEM lane r);
-//   WG1 (warps 4-7)  the same for Q tile 1;
-//   WG2 warp 8       TMA producer: Q0, Q1 once, then K_j, V_j through a ring
-//                    of four 32 KB slots;
-//   WG2 warp 9       MMA issuer (one thread).
-// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each. The softmax
-// writes P_t (bf16, two per column) over the first 64 columns of S_t, and
-// O_t += P_t V_j reads it from there (tcgen05.mma with A in tensor memory), so
-// P never touches shared memory.
+// Roles (640 threads, five warpgroups):
+//   WG 0..3   softmax + epilogue. WG w serves Q tile t = w/2 and the column
+//             half c = w%2 of its rows: thread r of the warpgroup owns TMEM
+//             lane r (row r) and columns 64c..64c+63 of S_t and O_t;
+//   WG 4      warp 16: TMA producer (Q0, Q1 once, then K_j, V_j through a
+//             ring of four 32 KB slots); warp 17: MMA issuer (one thread).
+// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each. A softmax
+// thread writes its 64 probabilities as bf16 pairs (32 columns) over the first
+// half of its own S columns, and O_t += P_t V_j reads them from there
+// (tcgen05.mma with A in tensor memory), so P never touches shared memory.
 // MMA stream: S0_0, S1_0, then per KV tile j: PV0_j, S0_{j+1}, PV1_j,
 // S1_{j+1}. tcgen05.mma ops of one thread execute in issue order, so S_t,j+1
 // overwrites S_t/P_t only after PV_t,j has read P_t. While the tensor core
-// runs one tile's PV and next QK^T, the other tile's softmax computes, so the
-// two softmax warpgroups take turns keeping the tensor core busy.
+// runs one tile's PV and next QK^T, the other tile's softmax computes.
 // The commit that signals "S_t,j ready" also covers every earlier MMA of the
 // thread, so when a softmax warpgroup sees S_t,j, O_t already holds every
 // PV up to j-1 and can be rescaled in place.
@@ -40,13 +38,12 @@
 // prologue writes this bound to the workspace). While the bound is moderate,
 // p = 2^(s - bound) never underflows for the terms that matter, and the
 // softmax needs neither a row max nor any rescaling of O: it is then a pure
-// elementwise map plus a running sum. For large gammas the kernel falls back
-// to the online max with a lazy rescale (the max only moves, and O_t, l are
-// rescaled by 2^(m_old - m_new), when a tile's max exceeds it by more than 8).
-//
-// Registers: the softmax warpgroups raise their budget to 208 per thread
-// (setmaxnreg) and warpgroup 2 lowers its to 88; the host checks that the
-// launch's register allocation covers that split before launching.
+// elementwise map plus a running sum, and the two threads of a row never talk
+// until the epilogue adds their partial sums. For large gammas the kernel
+// falls back to an online max with a lazy rescale (the two halves of a row
+// exchange their tile maxima through shared memory and an mbarrier; the max only moves, and
+// O_t, l are rescaled by 2^(m_old - m_new), when a tile's max exceeds it by
+// more than 8).
 //
 // Every mbarrier wait is bounded (q3a_device.cuh); a timeout sets the error
 // word, all roles unwind, in-flight copies and MMAs are drained and TMEM is
@@ -61,32 +58,31 @@ namespace {
 constexpr int BM = 128;  // query rows per Q tile
 constexpr int BN = 128;  // keys per KV tile
 constexpr int kQTiles = 2;
-constexpr int kSlots = 4;  // K/V ring slots
-constexpr int kThreads = 384;
-constexpr uint32_t kRegsSoftmax = 208;
-constexpr uint32_t kRegsOther = 88;
+constexpr int kSoftmaxWGs = 4;  // two column halves per Q tile
+constexpr int kSlots = 4;       // K/V ring slots
+constexpr int kThreads = (kSoftmaxWGs + 1) * 128;
 constexpr uint32_t kHalf = 16384;      // 128 rows x 128 bytes
 constexpr uint32_t kTile = 2 * kHalf;  // 128 rows x 128 bf16
 constexpr uint32_t OFF_Q = 0;          // two Q tiles
 constexpr uint32_t OFF_RING = OFF_Q + kQTiles * kTile;
 constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kTile;
-constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
+// row-half exchange: tile maxima [2 tiles][2 halves][2 parities][128] fp32,
+// then partial sums [2 tiles][2 halves][128] fp32
+constexpr uint32_t OFF_XCHG = OFF_BAR + 256;
+constexpr uint32_t kSmemBytes = OFF_XCHG + (kQTiles * 2 * 2 * 128 + kQTiles * 2 * 128) * 4 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kScaleLog2 = 0.12751743074380046f;  // log2(e) / sqrt(128)
 constexpr float kRescaleThreshold = 8.0f;
 // largest logit bound (log2 units) for which 2^(-2 bound), the smallest
-// dominant term, is still a normal float after the fixed shift
+// possible term after the fixed shift, is still a normal float
 constexpr float kFixedMaxLimit = 60.0f;
 constexpr unsigned kFull = 0xffffffffu;
-
-static_assert(kQTiles * 128 * kRegsSoftmax + (kThreads - kQTiles * 128) * kRegsOther <=
-                  kThreads * 168,
-              "register split exceeds a 168-register launch");
 
 struct Bars {
   uint64_t q_full;
   uint64_t slot_full[kSlots], slot_empty[kSlots];
   uint64_t s_full[kQTiles], p_full[kQTiles], o_final[kQTiles];
+  uint64_t xmax_full[kQTiles];  // fallback path: both row halves posted their tile max
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -103,14 +99,16 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint3
   }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_s, uint32_t v_addr,
                                          bool accumulate) {
-  // A = P (TMEM, 16 keys = 8 columns per step), B = V (MN-major: 64-wide d
-  // blocks 16 KB apart, 8-key groups 1 KB apart; 16 keys = 2 KB per step)
+  // A = P in TMEM: keys 0..63 as bf16 pairs in S columns 0..31, keys 64..127
+  // in S columns 64..95 (16 keys = 8 columns per step). B = V, MN-major: 64-wide
+  // d blocks 16 KB apart, 8-key groups 1 KB apart; 16 keys = 2 KB per step.
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_bf16_ts(tmem_o, tmem_p + kk * 8, smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024), idesc,
+    mma_bf16_ts(tmem_o, tmem_s + (kk >> 2) * 64 + (kk & 3) * 8,
+                smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024), idesc,
                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
@@ -120,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  float* xchg = reinterpret_cast<float*>(smem + OFF_XCHG);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item: longest CTAs first ---------------------------------------
@@ -141,8 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->p_full[t], 256);
       mbar_init(&bars->o_final[t], 1);
+      mbar_init(&bars->xmax_full[t], 256);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -155,9 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort_flag;
 
-  if (warp >= 8) {
-    regs_decrease<kRegsOther>();
-    if (warp == 8 && lane == 0) {
+  if (warp >= kSoftmaxWGs * 4) {
+    if (warp == kSoftmaxWGs * 4 && lane == 0) {
       // ---------------------------------------------------------- producer
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_k);
@@ -193,30 +192,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = max(0, issued - kSlots); i < issued; ++i)
           mbar_wait(&bars->slot_full[i % kSlots], (i / kSlots) & 1, nullptr, 0, nullptr);
       }
-    } else if (warp == 9 && lane == 0) {
+    } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t q_addr = smem_u32(smem + OFF_Q);
       const uint32_t ring = smem_u32(smem + OFF_RING);
-      auto slot_addr = [&](int i) { return ring + (uint32_t)(i % kSlots) * kTile; };
       bool ok = mbar_wait(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) &&
                 mbar_wait(&bars->slot_full[0], 0, a.err, kDevTimeoutMma, abort);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < kQTiles; ++t) {
-          issue_qk(tmem + t * 128, q_addr + t * kTile, slot_addr(0));
+          issue_qk(tmem + t * 128, q_addr + t * kTile, ring);
           mma_commit(&bars->s_full[t]);
         }
         mma_commit(&bars->slot_empty[0]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;  // loads holding V_j and K_{j+1}
+        const uint32_t v_addr = ring + (uint32_t)(iv % kSlots) * kTile;
+        const uint32_t k_addr = ring + (uint32_t)(ik % kSlots) * kTile;
         ok = mbar_wait(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, a.err, kDevTimeoutMma,
                        abort);
         for (int t = 0; ok && t < kQTiles; ++t) {
           ok = mbar_wait(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(tmem + 256 + t * 128, tmem + t * 128, slot_addr(iv), j > 0);
+          issue_pv(tmem + 256 + t * 128, tmem + t * 128, v_addr, j > 0);
           if (j + 1 == n_tiles) mma_commit(&bars->o_final[t]);
           if (j + 1 < n_tiles) {
             if (t == 0) {
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
-            issue_qk(tmem + t * 128, q_addr + t * kTile, slot_addr(ik));
+            issue_qk(tmem + t * 128, q_addr + t * kTile, k_addr);
             mma_commit(&bars->s_full[t]);
           }
         }
@@ -239,17 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    regs_increase<kRegsSoftmax>();
-    const int t = warp >> 2;            // Q tile of this warpgroup
+    const int wg = warp >> 2;
+    const int t = wg >> 1;              // Q tile
+    const int hc = wg & 1;              // column half: keys / O columns 64hc..64hc+63
     const int r = threadIdx.x & 127;    // row of S_t / O_t, TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tmem_s = tmem + t * 128 + lane_off;
-    const uint32_t tmem_o = tmem + 256 + t * 128 + lane_off;
+    const uint32_t tmem_s = tmem + t * 128 + hc * 64 + lane_off;
+    const uint32_t tmem_o = tmem + 256 + t * 128 + hc * 64 + lane_off;
+    const uint32_t bar_id = 1 + t;      // named barrier of the two halves of tile t (epilogue)
+    float* xmax = xchg + (t * 2) * 2 * 128;  // [half][parity][128]
     const int tok = t0 + t * tile_tok + r / g;
-    // QK-Norm bounds every logit (in the exp2 domain) by `bound`. When
-    // 2^(-2 bound) is still a normal float, subtracting this fixed bound
-    // instead of the running row max gives the same softmax with no
-    // reduction and no rescaling; otherwise fall back to the online max.
     const float bound = *a.logit_bound;
     const bool fixed_max = bound >= 0.f && bound <= kFixedMaxLimit;
     float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
@@ -260,36 +259,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                       mbar_wait(&bars->s_full[t], j & 1, a.err, kDevTimeoutSoftmax, abort));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem_s + c * 32, sr[c]);
+      uint32_t sr[2][32];
+      tmem_ld32(tmem_s, sr[0]);
+      tmem_ld32(tmem_s + 32, sr[1]);
       tmem_wait_ld();
 
-      float s[128];
+      float s[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
-      const int key0 = j * BN;
-      if (key0 + BN - 1 > tok) {
+      const int key0 = j * BN + hc * 64;
+      if (key0 + 63 > tok) {
 #pragma unroll
-        for (int e = 0; e < 128; ++e)
+        for (int e = 0; e < 64; ++e)
           if (key0 + e > tok) s[e] = -INFINITY;
       }
       bool move = false;
       float alpha = 1.0f;
       if (!fixed_max) {
-        // row max as a tree: eight independent chains, then a 3-level fold
         float mx[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx[e] = s[e];
 #pragma unroll
-        for (int e = 8; e < 128; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
+        for (int e = 8; e < 64; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
 #pragma unroll
         for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-        const float m_tile = mx[0] * kScaleLog2;
+        // the other half of the row: exchange tile maxima (two parity slots)
+        xmax[(hc * 2 + (j & 1)) * 128 + r] = mx[0];
+        mbar_arrive(&bars->xmax_full[t]);
+        ok = __all_sync(kFull, mbar_wait(&bars->xmax_full[t], j & 1, a.err, kDevTimeoutSoftmax,
+                                         abort));
+        if (!ok) break;
+        const float mrow = fmaxf(mx[0], xmax[((hc ^ 1) * 2 + (j & 1)) * 128 + r]);
+        const float m_tile = mrow * kScaleLog2;
         move = m_tile > m + kRescaleThreshold;
         const float m_new = move ? m_tile : m;
         alpha = move ? ex2(m - m_new) : 1.0f;
@@ -301,25 +306,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t scale2 = f2_pack(kScaleLog2, kScaleLog2);
       const uint64_t negm2 = f2_pack(-m, -m);
       uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+      uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pw[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const uint64_t x = f2_fma(f2_pack(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]), scale2, negm2);
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
-          pw[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tmem_s + c * 32, pw);
+      for (int e = 0; e < 32; ++e) {
+        const uint64_t x = f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
+        pw[e] = pack_bf16x2(p0, p1);
       }
+      tmem_st32(tmem_s, pw);  // P over the first 32 of this thread's S columns
       // O_t holds every PV up to j-1 here (the S_t,j commit covers them);
-      // rescale it before PV_t,j adds terms relative to the new max
+      // rescale this thread's O columns before PV_t,j adds terms relative to
+      // the new max
       if (!fixed_max && j > 0 && __any_sync(kFull, move)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
           tmem_ld32(tmem_o + c * 32, o);
           tmem_wait_ld();
@@ -336,18 +339,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);
     }
-    // ---- epilogue: O / l -> bf16 -> out
+    // ---- epilogue: the row's two partial sums, then O / l -> bf16 -> out
+    ok = __all_sync(kFull, ok && !*abort);
+    // the partial sums go to a slot the loop never uses; every thread of both
+    // halves reaches this barrier exactly once (aborted or not)
+    float* lsum = xchg + kQTiles * 2 * 2 * 128 + t * 2 * 128;  // [tile][half][128]
+    lsum[hc * 128 + r] = l;
+    named_barrier_sync(bar_id, 256);
     if (ok) {
+      l += lsum[(hc ^ 1) * 128 + r];
       ok = __all_sync(kFull, mbar_wait(&bars->o_final[t], 0, a.err, kDevTimeoutEpilogue, abort));
     }
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const bool store = tok < a.T;
-      uint16_t* orow =
-          a.out + (((long long)b * a.T + tok) * a.Hq + (long long)kv * g + (r % g)) * 128;
+      uint16_t* orow = a.out +
+                       (((long long)b * a.T + tok) * a.Hq + (long long)kv * g + (r % g)) * 128 +
+                       hc * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
         tmem_ld32(tmem_o + c * 32, o);
         tmem_wait_ld();
@@ -383,25 +394,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 int prefill_tokens_per_cta(int g) { return kQTiles * (BM / g); }
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream) {
-  // per-device set-up: the dynamic shared memory limit, and a check that the
-  // launch's register allocation covers the setmaxnreg split (otherwise the
-  // softmax warpgroups would wait forever for registers)
-  static unsigned long long checked_mask = 0;
+  // per-device set-up: the dynamic shared memory limit is a per-device
+  // attribute of the function
+  static unsigned long long done_mask = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(checked_mask & (1ull << dev))) {
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, prefill_attention_kernel);
-    if (e != cudaSuccess) return e;
-    const long long launch_regs = (long long)fa.numRegs * kThreads;
-    const long long split = (long long)kQTiles * 128 * kRegsSoftmax +
-                            (long long)(kThreads - kQTiles * 128) * kRegsOther;
-    if (split > launch_regs) return cudaErrorInvalidConfiguration;
+  if (dev >= 64 || !(done_mask & (1ull << dev))) {
     e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev < 64) checked_mask |= 1ull << dev;
+    if (dev < 64) done_mask |= 1ull << dev;
   }
   const long long grid = (long long)a.n_mtiles * a.B * a.Hkv;
   if (grid == 0) return cudaSuccess;
