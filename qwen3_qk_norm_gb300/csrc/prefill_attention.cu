@@ -89,27 +89,30 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+// Descriptors of 128-byte-swizzled tiles whose bases are 1024-byte aligned:
+// moving the start address by `off` bytes adds off >> 4 to the low field, so
+// each MMA step costs one 64-bit add.
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+  mma_ss<0>(tmem_s, q_desc, k_desc, idesc);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-    mma_bf16_ss(tmem_s, smem_desc_sw128(q_addr + off, 16, 1024),
-                smem_desc_sw128(k_addr + off, 16, 1024), idesc, kk > 0);
+  for (int kk = 1; kk < 8; ++kk) {
+    const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+    mma_ss<1>(tmem_s, q_desc + off, k_desc + off, idesc);
   }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_s, uint32_t v_addr,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_s, uint64_t v_desc,
+                                         uint32_t accumulate) {
   // A = P in TMEM: keys 0..63 as bf16 pairs in S columns 0..31, keys 64..127
   // in S columns 64..95 (16 keys = 8 columns per step). B = V, MN-major: 64-wide
   // d blocks 16 KB apart, 8-key groups 1 KB apart; 16 keys = 2 KB per step.
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+  mma_bf16_ts(tmem_o, tmem_s, v_desc, idesc, accumulate);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    mma_bf16_ts(tmem_o, tmem_s + (kk >> 2) * 64 + (kk & 3) * 8,
-                smem_desc_sw128(v_addr + kk * 2048, kHalf, 1024), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 1; kk < 8; ++kk)
+    mma_bf16_ts(tmem_o, tmem_s + (kk >> 2) * 64 + (kk & 3) * 8, v_desc + (uint64_t)(kk * 2048 >> 4),
+                idesc, 1u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -196,27 +199,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       const uint32_t q_addr = smem_u32(smem + OFF_Q);
       const uint32_t ring = smem_u32(smem + OFF_RING);
+      // base descriptors, built once: Q tiles (K-major), ring slots as K
+      // (K-major) and as V (MN-major)
+      const uint64_t q_desc0 = smem_desc_sw128(q_addr, 16, 1024);
+      const uint64_t q_desc1 = smem_desc_sw128(q_addr + kTile, 16, 1024);
+      const uint64_t slot_k0 = smem_desc_sw128(ring, 16, 1024);
+      const uint64_t slot_v0 = smem_desc_sw128(ring, kHalf, 1024);
+      constexpr uint64_t kSlotStep = kTile >> 4;  // descriptor units per slot
       bool ok = mbar_wait(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) &&
                 mbar_wait(&bars->slot_full[0], 0, a.err, kDevTimeoutMma, abort);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < kQTiles; ++t) {
-          issue_qk(tmem + t * 128, q_addr + t * kTile, ring);
-          mma_commit(&bars->s_full[t]);
-        }
+        issue_qk(tmem, q_desc0, slot_k0);
+        mma_commit(&bars->s_full[0]);
+        issue_qk(tmem + 128, q_desc1, slot_k0);
+        mma_commit(&bars->s_full[1]);
         mma_commit(&bars->slot_empty[0]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;  // loads holding V_j and K_{j+1}
-        const uint32_t v_addr = ring + (uint32_t)(iv % kSlots) * kTile;
-        const uint32_t k_addr = ring + (uint32_t)(ik % kSlots) * kTile;
+        const uint64_t v_desc = slot_v0 + (uint64_t)(iv % kSlots) * kSlotStep;
+        const uint64_t k_desc = slot_k0 + (uint64_t)(ik % kSlots) * kSlotStep;
         ok = mbar_wait(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, a.err, kDevTimeoutMma,
                        abort);
         for (int t = 0; ok && t < kQTiles; ++t) {
           ok = mbar_wait(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(tmem + 256 + t * 128, tmem + t * 128, v_addr, j > 0);
+          issue_pv(tmem + 256 + t * 128, tmem + t * 128, v_desc, j > 0 ? 1u : 0u);
           if (j + 1 == n_tiles) mma_commit(&bars->o_final[t]);
           if (j + 1 < n_tiles) {
             if (t == 0) {
@@ -225,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
-            issue_qk(tmem + t * 128, q_addr + t * kTile, k_addr);
+            issue_qk(tmem + t * 128, t ? q_desc1 : q_desc0, k_desc);
             mma_commit(&bars->s_full[t]);
           }
         }
