@@ -19,18 +19,15 @@
 //             half c = w%2 of its rows: thread r of the warpgroup owns TMEM
 //             lane r (row r) and columns 64c..64c+63 of S_t and O_t;
 //   WG 4      warp 16: TMA producer (Q0, Q1 once, then K_j, V_j through a
-//             ring of four 32 KB slots); warps 17 and 18: one MMA-issuing
-//             thread per Q tile.
+//             ring of four 32 KB slots); warp 17: MMA issuer (one thread).
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each. A softmax
 // thread writes its 64 probabilities as bf16 pairs (32 columns) over the first
 // half of its own S columns, and O_t += P_t V_j reads them from there
 // (tcgen05.mma with A in tensor memory), so P never touches shared memory.
-// MMA stream of tile t (its own issuing thread): S_t,0, then per KV tile j:
-// PV_t,j, S_t,j+1. tcgen05.mma ops of one thread execute in issue order, so
-// S_t,j+1 overwrites S_t/P_t only after PV_t,j has read P_t. While the tensor
-// core runs one tile's PV and next QK^T, the other tile's softmax computes;
-// with one issuer per tile, one issuer's barrier checks overlap the other's
-// MMAs.
+// MMA stream: S0_0, S1_0, then per KV tile j: PV0_j, S0_{j+1}, PV1_j,
+// S1_{j+1}. tcgen05.mma ops of one thread execute in issue order, so S_t,j+1
+// overwrites S_t/P_t only after PV_t,j has read P_t. While the tensor core
+// runs one tile's PV and next QK^T, the other tile's softmax computes.
 // The commit that signals "S_t,j ready" also covers every earlier MMA of the
 // thread, so when a softmax warpgroup sees S_t,j, O_t already holds every
 // PV up to j-1 and can be rescaled in place.
@@ -86,7 +83,7 @@ struct Bars {
   uint64_t slot_full[kSlots], slot_empty[kSlots];
   uint64_t s_full[kQTiles], p_full[kQTiles], o_final[kQTiles];
   uint64_t xmax_full[kQTiles];  // fallback path: both row halves posted their tile max
-  uint64_t drain[kQTiles];
+  uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -142,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->slot_full[s], 1);
-      mbar_init(&bars->slot_empty[s], kQTiles);  // one commit per MMA issuer
+      mbar_init(&bars->slot_empty[s], 1);
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -150,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_final[t], 1);
       mbar_init(&bars->xmax_full[t], 256);
     }
-    for (int t = 0; t < kQTiles; ++t) mbar_init(&bars->drain[t], 1);
+    mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -198,18 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = max(0, issued - kSlots); i < issued; ++i)
           mbar_wait(&bars->slot_full[i % kSlots], (i / kSlots) & 1, nullptr, 0, nullptr);
       }
-    } else if ((warp == kSoftmaxWGs * 4 + 1 || warp == kSoftmaxWGs * 4 + 2) && lane == 0) {
-      // ---------------------------------------------------------- MMA issuers
-      // One issuing thread per Q tile (in different warps), so that one
-      // thread's barrier checks and commits overlap the other's MMAs. Order
-      // only matters within a tile (PV_t,j before S_t,j+1, which reuses the
-      // TMEM columns of P_t); commits track the issuing thread's own MMAs.
-      const int t = warp - (kSoftmaxWGs * 4 + 1);
-      const uint32_t tmem_s = tmem + t * 128, tmem_o = tmem + 256 + t * 128;
+    } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t q_addr = smem_u32(smem + OFF_Q);
       const uint32_t ring = smem_u32(smem + OFF_RING);
-      // base descriptors, built once: this thread's Q tile (K-major), ring
-      // slots as K (K-major) and as V (MN-major)
-      const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + OFF_Q) + t * kTile, 16, 1024);
+      // base descriptors, built once: Q tiles (K-major), ring slots as K
+      // (K-major) and as V (MN-major)
+      const uint64_t q_desc0 = smem_desc_sw128(q_addr, 16, 1024);
+      const uint64_t q_desc1 = smem_desc_sw128(q_addr + kTile, 16, 1024);
       const uint64_t slot_k0 = smem_desc_sw128(ring, 16, 1024);
       const uint64_t slot_v0 = smem_desc_sw128(ring, kHalf, 1024);
       constexpr uint64_t kSlotStep = kTile >> 4;  // descriptor units per slot
@@ -217,33 +210,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&bars->slot_full[0], 0, a.err, kDevTimeoutMma, abort);
       if (ok) {
         tc_fence_after();
-        issue_qk(tmem_s, q_desc, slot_k0);
-        mma_commit(&bars->s_full[t]);
+        issue_qk(tmem, q_desc0, slot_k0);
+        mma_commit(&bars->s_full[0]);
+        issue_qk(tmem + 128, q_desc1, slot_k0);
+        mma_commit(&bars->s_full[1]);
         mma_commit(&bars->slot_empty[0]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;  // loads holding V_j and K_{j+1}
-        const bool more = j + 1 < n_tiles;
+        const uint64_t v_desc = slot_v0 + (uint64_t)(iv % kSlots) * kSlotStep;
+        const uint64_t k_desc = slot_k0 + (uint64_t)(ik % kSlots) * kSlotStep;
         ok = mbar_wait(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, a.err, kDevTimeoutMma,
-                       abort) &&
-             (!more || mbar_wait(&bars->slot_full[ik % kSlots], (ik / kSlots) & 1, a.err,
-                                 kDevTimeoutMma, abort)) &&
-             mbar_wait(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(tmem_o, tmem_s, slot_v0 + (uint64_t)(iv % kSlots) * kSlotStep, j > 0 ? 1u : 0u);
-        mma_commit(&bars->slot_empty[iv % kSlots]);
-        if (more) {
-          issue_qk(tmem_s, q_desc, slot_k0 + (uint64_t)(ik % kSlots) * kSlotStep);
-          mma_commit(&bars->s_full[t]);
-          mma_commit(&bars->slot_empty[ik % kSlots]);
-        } else {
-          mma_commit(&bars->o_final[t]);
+                       abort);
+        for (int t = 0; ok && t < kQTiles; ++t) {
+          ok = mbar_wait(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(tmem + 256 + t * 128, tmem + t * 128, v_desc, j > 0 ? 1u : 0u);
+          if (j + 1 == n_tiles) mma_commit(&bars->o_final[t]);
+          if (j + 1 < n_tiles) {
+            if (t == 0) {
+              ok = mbar_wait(&bars->slot_full[ik % kSlots], (ik / kSlots) & 1, a.err,
+                             kDevTimeoutMma, abort);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_qk(tmem + t * 128, t ? q_desc1 : q_desc0, k_desc);
+            mma_commit(&bars->s_full[t]);
+          }
         }
+        if (!ok) break;
+        mma_commit(&bars->slot_empty[iv % kSlots]);
+        if (j + 1 < n_tiles) mma_commit(&bars->slot_empty[ik % kSlots]);
       }
-      // drain: every MMA this thread issued has completed once this phase completes
-      mma_commit(&bars->drain[t]);
-      mbar_wait(&bars->drain[t], 0, nullptr, 0, nullptr);
+      // drain: every MMA issued above has completed once this phase completes
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, nullptr, 0, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax
