@@ -218,30 +218,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;  // loads holding V_j and K_{j+1}
+        const bool more = j + 1 < n_tiles;
         const uint64_t v_desc = slot_v0 + (uint64_t)(iv % kSlots) * kSlotStep;
         const uint64_t k_desc = slot_k0 + (uint64_t)(ik % kSlots) * kSlotStep;
-        ok = mbar_wait(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, a.err, kDevTimeoutMma,
-                       abort);
+        // tile 0: V_j, K_{j+1} and P0_j in one poll, then PV0_j and S0_{j+1}
+        // as one contiguous group; tile 1: P1_j, then PV1_j and S1_{j+1}
+        const int kload = more ? ik : iv;
+        ok = mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1,
+                        &bars->slot_full[kload % kSlots], (kload / kSlots) & 1, &bars->p_full[0],
+                        j & 1, a.err, kDevTimeoutMma, abort);
         for (int t = 0; ok && t < kQTiles; ++t) {
-          ok = mbar_wait(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
-          if (!ok) break;
+          if (t > 0) {
+            ok = mbar_wait(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
+            if (!ok) break;
+          }
           tc_fence_after();
           issue_pv(tmem + 256 + t * 128, tmem + t * 128, v_desc, j > 0 ? 1u : 0u);
-          if (j + 1 == n_tiles) mma_commit(&bars->o_final[t]);
-          if (j + 1 < n_tiles) {
-            if (t == 0) {
-              ok = mbar_wait(&bars->slot_full[ik % kSlots], (ik / kSlots) & 1, a.err,
-                             kDevTimeoutMma, abort);
-              if (!ok) break;
-              tc_fence_after();
-            }
+          if (more) {
             issue_qk(tmem + t * 128, t ? q_desc1 : q_desc0, k_desc);
             mma_commit(&bars->s_full[t]);
+          } else {
+            mma_commit(&bars->o_final[t]);
           }
         }
         if (!ok) break;
         mma_commit(&bars->slot_empty[iv % kSlots]);
-        if (j + 1 < n_tiles) mma_commit(&bars->slot_empty[ik % kSlots]);
+        if (more) mma_commit(&bars->slot_empty[ik % kSlots]);
       }
       // drain: every MMA issued above has completed once this phase completes
       mma_commit(&bars->drain);

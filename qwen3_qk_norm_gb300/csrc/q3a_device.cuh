@@ -110,6 +110,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// Up to three barriers at once: the three try_waits are issued back to back,
+// so an already-complete set costs one round trip instead of three. Falls
+// back to waiting on each in turn (bounded) for any that was not complete.
+__device__ __forceinline__ bool mbar_wait3(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
+                                           uint64_t* b2, uint32_t p2, uint32_t* err,
+                                           uint32_t code, volatile int* abort) {
+  uint32_t ok0, ok1, ok2;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q0, [%3], %4;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q1, [%5], %6;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q2, [%7], %8;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\tselp.u32 %1, 1, 0, q1;\n\tselp.u32 %2, 1, 0, q2;\n\t}"
+      : "=r"(ok0), "=r"(ok1), "=r"(ok2)
+      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2)
+      : "memory");
+  if (ok0 && ok1 && ok2) return true;
+  return (ok0 || mbar_wait(b0, p0, err, code, abort)) &&
+         (ok1 || mbar_wait(b1, p1, err, code, abort)) &&
+         (ok2 || mbar_wait(b2, p2, err, code, abort));
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------
