@@ -30,7 +30,9 @@
 // runs one tile's PV and next QK^T, the other tile's softmax computes.
 // The commit that signals "S_t,j ready" also covers every earlier MMA of the
 // thread, so when a softmax warpgroup sees S_t,j, O_t already holds every
-// PV up to j-1 and can be rescaled in place.
+// PV up to j-1 and can be rescaled in place, and K_j and V_{j-1} are no longer
+// read by tile t: the softmax warpgroups, not the MMA thread, hand the ring
+// slots back to the producer, which keeps commits off the MMA issue path.
 //
 // Softmax in the exp2 domain. QK-Norm bounds every logit: |qhat| <=
 // sqrt(128) max|gamma_q| and |khat| <= sqrt(128) max|gamma_k|, so
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->slot_full[s], 1);
-      mbar_init(&bars->slot_empty[s], 1);
+      mbar_init(&bars->slot_empty[s], kQTiles);  // one arrive per Q tile's softmax
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -214,7 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars->s_full[0]);
         issue_qk(tmem + 128, q_desc1, slot_k0);
         mma_commit(&bars->s_full[1]);
-        mma_commit(&bars->slot_empty[0]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;  // loads holding V_j and K_{j+1}
@@ -242,8 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(&bars->slot_empty[iv % kSlots]);
-        if (more) mma_commit(&bars->slot_empty[ik % kSlots]);
       }
       // drain: every MMA issued above has completed once this phase completes
       mma_commit(&bars->drain);
@@ -270,6 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(kFull,
                       mbar_wait(&bars->s_full[t], j & 1, a.err, kDevTimeoutSoftmax, abort));
       if (!ok) break;
+      // S_t,j is complete, and so is every earlier MMA of the issuing thread:
+      // K_j is no longer read by tile t, nor V_{j-1} (read by PV_t,j-1)
+      if (hc == 0 && r == 0) {
+        mbar_arrive(&bars->slot_empty[(2 * j) % kSlots]);
+        if (j > 0) mbar_arrive(&bars->slot_empty[(2 * j - 1) % kSlots]);
+      }
       tc_fence_after();
       uint32_t sr[2][32];
       tmem_ld32(tmem_s, sr[0]);
