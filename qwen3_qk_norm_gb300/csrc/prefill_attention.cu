@@ -62,7 +62,6 @@ constexpr int BN = 128;  // keys per KV tile
 constexpr int kQTiles = 2;
 constexpr int kSoftmaxWGs = 4;  // two column halves per Q tile
 constexpr int kSlots = 4;       // K/V ring slots
-constexpr int kPrefetchLoads = 4;  // L2 prefetch distance beyond the ring, in loads
 constexpr int kThreads = (kSoftmaxWGs + 1) * 128;
 constexpr uint32_t kHalf = 16384;      // 128 rows x 128 bytes
 constexpr uint32_t kTile = 2 * kHalf;  // 128 rows x 128 bf16
@@ -175,23 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(qd + kHalf, &a.tm_q, &bars->q_full, 64, kv * g, tq, b);
       }
       const int n_loads = 2 * n_tiles;  // K_0, V_0, K_1, V_1, ...
-      // The ring holds two K/V tile pairs, about one load round trip ahead of
-      // the MMAs; L2 prefetches of the next tiles (no shared memory needed)
-      // make the TMA loads that follow hit L2.
-      auto prefetch = [&](int i) {
-        const int j = i >> 1;
-        if ((i & 1) == 0) {
-          tma_prefetch_l2_3d(&a.tm_k, 0, j * BN, b * a.Hkv + kv);
-          tma_prefetch_l2_3d(&a.tm_k, 64, j * BN, b * a.Hkv + kv);
-        } else {
-          tma_prefetch_l2_4d(&a.tm_v, 0, kv, j * BN, b);
-          tma_prefetch_l2_4d(&a.tm_v, 64, kv, j * BN, b);
-        }
-      };
-      for (int i = 0; i < min(n_loads, kSlots + kPrefetchLoads); ++i) prefetch(i);
       int issued = 0;
       for (int i = 0; i < n_loads; ++i) {
-        if (i + kSlots + kPrefetchLoads < n_loads) prefetch(i + kSlots + kPrefetchLoads);
         const int s = i % kSlots;
         if (!mbar_wait(&bars->slot_empty[s], ((i / kSlots) & 1) ^ 1, a.err, kDevTimeoutTma, abort))
           break;
@@ -246,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         j & 1, a.err, kDevTimeoutMma, abort);
         for (int t = 0; ok && t < kQTiles; ++t) {
           if (t > 0) {
-            ok = mbar_wait<false>(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
+            ok = mbar_wait(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
             if (!ok) break;
           }
           tc_fence_after();

@@ -94,18 +94,13 @@ constexpr uint32_t kSuspendHintNs = 20000;
 
 // Wait until the phase with the given parity has completed. Returns false
 // (and records `code`) if it did not complete within kWaitLimitCycles, or if
-// another thread of the CTA already gave up (*abort set). kSleep: the thread
-// sleeps in hardware between checks (for warps that share a scheduler with
-// busy ones); otherwise it polls, which reacts faster (for a latency-critical
-// single thread such as an MMA issuer).
-template <bool kSleep = true>
+// another thread of the CTA already gave up (*abort set).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           uint32_t code, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (kSleep ? mbar_try_wait_sleep(bar, parity, kSuspendHintNs) : mbar_try_wait(bar, parity))
-      return true;
+    if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
     if (abort && *abort) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       record_error(err, code);
@@ -117,7 +112,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 
 // Up to three barriers at once: the three try_waits are issued back to back,
 // so an already-complete set costs one round trip instead of three. Falls
-// back to polling each in turn (bounded) for any that was not complete.
+// back to waiting on each in turn (bounded) for any that was not complete.
 __device__ __forceinline__ bool mbar_wait3(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
                                            uint64_t* b2, uint32_t p2, uint32_t* err,
                                            uint32_t code, volatile int* abort) {
@@ -132,9 +127,9 @@ __device__ __forceinline__ bool mbar_wait3(uint64_t* b0, uint32_t p0, uint64_t* 
       : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2)
       : "memory");
   if (ok0 && ok1 && ok2) return true;
-  return (ok0 || mbar_wait<false>(b0, p0, err, code, abort)) &&
-         (ok1 || mbar_wait<false>(b1, p1, err, code, abort)) &&
-         (ok2 || mbar_wait<false>(b2, p2, err, code, abort));
+  return (ok0 || mbar_wait(b0, p0, err, code, abort)) &&
+         (ok1 || mbar_wait(b1, p1, err, code, abort)) &&
+         (ok2 || mbar_wait(b2, p2, err, code, abort));
 }
 
 // ---------------------------------------------------------------------------
@@ -161,22 +156,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, uint64_
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
       "r"(smem_u32(bar))
       : "memory");
-}
-
-// L2 prefetch of a tensor tile (no shared memory, no completion to wait for):
-// a later TMA load of the same box then hits L2.
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2,
-                                                   int c3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
 }
 
 // Generic-proxy writes to shared memory become visible to the async proxy
