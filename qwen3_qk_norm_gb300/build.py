@@ -21,7 +21,8 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libq3a.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                     "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
+                     "--expt-relaxed-constexpr", "-Xcudafe", "--diag_error=174",
+                     "-I" + INCLUDE, "-I" + CSRC]
 
 
 def _nvcc() -> str:

@@ -208,6 +208,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t slot_k0 = smem_desc_sw128(ring, 16, 1024);
       const uint64_t slot_v0 = smem_desc_sw128(ring, kHalf, 1024);
       constexpr uint64_t kSlotStep = kTile >> 4;  // descriptor units per slot
+      // An mbarrier wait issued by this thread after a tcgen05.commit stalls
+      // until that commit resolves, i.e. until every earlier MMA has finished.
+      // So each commit below is followed by a full MMA group before the next
+      // wait, by which time it has resolved: the waits for a group's inputs
+      // are placed before the commit of the previous group.
+      auto wait_inputs = [&](int j) {  // V_j, K_{j+1} (if any) and P0_j
+        const int iv = 2 * j + 1, ik = 2 * j + 2;
+        const int kload = j + 1 < n_tiles ? ik : iv;
+        return mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1,
+                          &bars->slot_full[kload % kSlots], (kload / kSlots) & 1,
+                          &bars->p_full[0], j & 1, a.err, kDevTimeoutMma, abort);
+      };
       bool ok = mbar_wait(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) &&
                 mbar_wait(&bars->slot_full[0], 0, a.err, kDevTimeoutMma, abort);
       if (ok) {
@@ -215,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_qk(tmem, q_desc0, slot_k0);
         mma_commit(&bars->s_full[0]);
         issue_qk(tmem + 128, q_desc1, slot_k0);
+        ok = wait_inputs(0);
         mma_commit(&bars->s_full[1]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
@@ -222,27 +235,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = j + 1 < n_tiles;
         const uint64_t v_desc = slot_v0 + (uint64_t)(iv % kSlots) * kSlotStep;
         const uint64_t k_desc = slot_k0 + (uint64_t)(ik % kSlots) * kSlotStep;
-        // tile 0: V_j, K_{j+1} and P0_j in one poll, then PV0_j and S0_{j+1}
-        // as one contiguous group; tile 1: P1_j, then PV1_j and S1_{j+1}
-        const int kload = more ? ik : iv;
-        ok = mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1,
-                        &bars->slot_full[kload % kSlots], (kload / kSlots) & 1, &bars->p_full[0],
-                        j & 1, a.err, kDevTimeoutMma, abort);
-        for (int t = 0; ok && t < kQTiles; ++t) {
-          if (t > 0) {
-            ok = mbar_wait(&bars->p_full[t], j & 1, a.err, kDevTimeoutMma, abort);
-            if (!ok) break;
-          }
-          tc_fence_after();
-          issue_pv(tmem + 256 + t * 128, tmem + t * 128, v_desc, j > 0 ? 1u : 0u);
-          if (more) {
-            issue_qk(tmem + t * 128, t ? q_desc1 : q_desc0, k_desc);
-            mma_commit(&bars->s_full[t]);
-          } else {
-            mma_commit(&bars->o_final[t]);
-          }
-        }
+        // tile 0: PV0_j, S0_{j+1} (inputs waited for above)
+        tc_fence_after();
+        issue_pv(tmem + 256, tmem, v_desc, j > 0 ? 1u : 0u);
+        if (more) issue_qk(tmem, q_desc0, k_desc);
+        ok = mbar_poll(&bars->p_full[1], j & 1, a.err, kDevTimeoutMma, abort);
+        mma_commit(more ? &bars->s_full[0] : &bars->o_final[0]);
         if (!ok) break;
+        // tile 1: PV1_j, S1_{j+1}
+        tc_fence_after();
+        issue_pv(tmem + 256 + 128, tmem + 128, v_desc, j > 0 ? 1u : 0u);
+        if (more) {
+          issue_qk(tmem + 128, q_desc1, k_desc);
+          ok = wait_inputs(j + 1);
+          mma_commit(&bars->s_full[1]);
+        } else {
+          mma_commit(&bars->o_final[1]);
+        }
       }
       // drain: every MMA issued above has completed once this phase completes
       mma_commit(&bars->drain);

@@ -94,13 +94,18 @@ constexpr uint32_t kSuspendHintNs = 20000;
 
 // Wait until the phase with the given parity has completed. Returns false
 // (and records `code`) if it did not complete within kWaitLimitCycles, or if
-// another thread of the CTA already gave up (*abort set).
+// another thread of the CTA already gave up (*abort set). kSleep: the thread
+// sleeps in hardware between checks (for warps that share a scheduler with
+// busy ones); otherwise it polls, which reacts faster (for a latency-critical
+// single thread such as an MMA issuer).
+template <bool kSleep = true>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           uint32_t code, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
+    if (kSleep ? mbar_try_wait_sleep(bar, parity, kSuspendHintNs) : mbar_try_wait(bar, parity))
+      return true;
     if (abort && *abort) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       record_error(err, code);
@@ -110,9 +115,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// mbar_wait that polls instead of sleeping (for a latency-critical thread).
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          uint32_t code, volatile int* abort) {
+  return mbar_wait<false>(bar, parity, err, code, abort);
+}
+
 // Up to three barriers at once: the three try_waits are issued back to back,
 // so an already-complete set costs one round trip instead of three. Falls
-// back to waiting on each in turn (bounded) for any that was not complete.
+// back to polling each in turn (bounded) for any that was not complete.
 __device__ __forceinline__ bool mbar_wait3(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
                                            uint64_t* b2, uint32_t p2, uint32_t* err,
                                            uint32_t code, volatile int* abort) {
@@ -127,9 +138,9 @@ __device__ __forceinline__ bool mbar_wait3(uint64_t* b0, uint32_t p0, uint64_t* 
       : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2)
       : "memory");
   if (ok0 && ok1 && ok2) return true;
-  return (ok0 || mbar_wait(b0, p0, err, code, abort)) &&
-         (ok1 || mbar_wait(b1, p1, err, code, abort)) &&
-         (ok2 || mbar_wait(b2, p2, err, code, abort));
+  return (ok0 || mbar_poll(b0, p0, err, code, abort)) &&
+         (ok1 || mbar_poll(b1, p1, err, code, abort)) &&
+         (ok2 || mbar_poll(b2, p2, err, code, abort));
 }
 
 // ---------------------------------------------------------------------------
