@@ -68,7 +68,7 @@ const char* q3a_status_string(q3a_status s);
  *   y     [B, T, H, d] bf16, y = RoPE_pos(RMSNorm(x) * gamma), rounded once.
  *         y may equal x (in place); any other overlap is undefined.
  *   Row (b, t, h) is rotated at position pos0 + t.
- *   pos0 >= 0 and pos0 + T - 1 <= 2^30.
+ *   pos0 >= 0 and pos0 + T - 1 <= 2^30; H <= 512.
  *   B == 0, T == 0 or H == 0: returns Q3A_OK and launches nothing.
  * Sources: §7.2.1 RMSNorm forward (fp32 variance, rsqrt(var + eps), times
  * scale, cast back) and apply_rope (x*cos + cat(-x2, x1)*sin).
@@ -93,7 +93,7 @@ q3a_status q3a_qknorm_rope(const q3a_bf16* x, const q3a_bf16* gamma, q3a_bf16* y
  *           initialised; it holds the normalised+rotated Q and K and an error
  *           word. It must not be shared by two calls that run concurrently.
  *   B == 0 or T == 0: returns Q3A_OK and launches nothing.
- *   Limits: B*T*Hq <= 2^31 - 1 rows.
+ *   Limits: B*T*Hq <= 2^31 - 1 rows; Hq + Hkv <= 512.
  * ------------------------------------------------------------------------- */
 size_t q3a_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d);
 

@@ -95,6 +95,7 @@ const char* q3a_status_string(q3a_status s) {
 q3a_status q3a_qknorm_rope(const q3a_bf16* x, const q3a_bf16* gamma, q3a_bf16* y, int B, int T,
                            int H, int d, int pos0, double theta, float eps, void* stream) {
   if (d != 128 || B < 0 || T < 0 || H < 0 || pos0 < 0) return Q3A_EINVAL;
+  if (H > qknorm_rope_max_heads()) return Q3A_EINVAL;
   if ((long long)pos0 + (long long)T - 1 > (1LL << 30)) return Q3A_EINVAL;
   if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
   if (B == 0 || T == 0 || H == 0) return Q3A_OK;
@@ -122,6 +123,7 @@ static q3a_status prefill_check(const void* const* ptrs, int nptrs, int B, int T
   *empty = false;
   if (d != 128 || B < 0 || T < 0 || !group_ok(Hq, Hkv)) return Q3A_EINVAL;
   if ((long long)B * T * Hq > 0x7fffffffLL || T > (1 << 30)) return Q3A_EINVAL;
+  if (Hq + Hkv > qknorm_rope_max_heads()) return Q3A_EINVAL;
   if (B == 0 || T == 0) {
     *empty = true;
     return Q3A_OK;

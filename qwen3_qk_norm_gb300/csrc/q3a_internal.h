@@ -9,9 +9,11 @@
 namespace q3a {
 
 // ----- K1: QK-Norm + RoPE prologue ------------------------------------------
-// One tensor of head rows. Row (b, t, h) of x starts at element
-//   (b * xsb + t * xst + h * xsh) * 128
-// (strides counted in rows of 128 elements); the same for y with ys*.
+// One tensor of head rows. The input x is token-contiguous: row (b, t, h) at
+// element ((b * T + t) * H + h) * 128, i.e. xsb = T*H, xst = H, xsh = 1 (the
+// kernel stages whole token blocks with bulk copies). Output row (b, t, h) of
+// y starts at element (b * ysb + t * yst + h * ysh) * 128 (strides counted in
+// rows of 128 elements).
 struct RopeTensor {
   const uint16_t* x;
   const uint16_t* gamma;
@@ -27,6 +29,7 @@ struct RopeArgs {
   int B, T;
   long long pos0;  // row (b, t, h) is rotated at pos0 + t
   float eps;
+  int tok_per_cta;      // set by launch_qknorm_rope
   uint32_t* err_clear;  // if non-null, block 0 zeroes this error word
   // if non-null, block 0 writes here the bound on |q.k| / sqrt(128) * log2(e)
   // that QK-Norm guarantees: sqrt(128) * max|gamma_q| * max|gamma_k| * log2(e)
@@ -36,6 +39,7 @@ struct RopeArgs {
 };
 
 void fill_inv_freq(double theta, double* inv_freq);
+int qknorm_rope_max_heads();  // largest H0 + H1 one launch accepts
 cudaError_t launch_qknorm_rope(const RopeArgs& a, cudaStream_t stream);
 
 // ----- K2: causal GQA prefill attention (tcgen05) ---------------------------

@@ -8,16 +8,18 @@
 // implementation" (§7.2.1 GroupedQueryAttention.forward: q_norm/k_norm, then
 // apply_rope) and the transformers Qwen3Attention quoted on the "Qwen3" note.
 //
-// Layout of the work: one CTA per 8 tokens. The 8 x 64 rotation angles of its
-// tokens are formed once per CTA in fp64 (p * w_i, reduced modulo 2 pi) and
-// turned into fp32 (cos, sin) pairs in shared memory; every head row of those
-// tokens (Q and K rows in the same launch) reuses them. A half-warp owns one
-// row: lane L holds elements 4L..4L+3 and their rotate-half partners
-// 64+4L..64+4L+3, so the rotation needs no data exchange and the RMS needs a
-// 4-step shuffle reduction inside the half-warp. Loads and stores are 8-byte
-// vectors, 128 contiguous bytes per half-warp per instruction. Row addresses
-// come from per-token offsets computed once per CTA, so the row loop has no
-// integer division.
+// Layout of the work. The kernel is a pure stream (HBM-bound), so it is built
+// around keeping many bytes in flight: a CTA owns a few consecutive tokens,
+// and the head rows of those tokens are contiguous in the [tokens, H, 128]
+// inputs, so one bulk copy per tensor (cp.async.bulk, completion on an
+// mbarrier) brings them all into shared memory. While that copy is in flight
+// the CTA forms the rotation angles of its tokens (p * w_i and its reduction
+// modulo 2 pi in fp64, then fp32 cos/sin). A half-warp then owns one row:
+// lane L holds elements 4L..4L+3 and their rotate-half partners 64+4L..,
+// so the rotation needs no data exchange and the RMS needs a 4-step shuffle
+// reduction. Results overwrite the staged rows, and bulk stores write them
+// out: one store per tensor when the output has the input's layout, one per
+// row otherwise (the head-major K layout of the prefill workspace).
 #include "q3a_internal.h"
 #include "q3a_rope.cuh"
 
@@ -25,27 +27,60 @@ namespace q3a {
 
 namespace {
 
-constexpr int kTokPerCta = 8;
 constexpr int kThreads = 256;
 constexpr int kHalfWarps = kThreads / 16;
-constexpr int kUnroll = 2;  // rows in flight per half-warp
+constexpr int kMaxTok = 8;
 
-__global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
-  __shared__ __align__(16) float cos_s[kTokPerCta][64];
-  __shared__ __align__(16) float sin_s[kTokPerCta][64];
-  __shared__ long long xbase[kTokPerCta][2], ybase[kTokPerCta][2];  // in rows of 128
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_constant__ RopeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(16) float cos_s[kMaxTok][64];
+  __shared__ __align__(16) float sin_s[kMaxTok][64];
+  __shared__ uint64_t bar;
   const int tid = threadIdx.x;
+  const int tok_per_cta = a.tok_per_cta;
   const long long n_tok = (long long)a.B * a.T;
-  const long long tok0 = (long long)blockIdx.x * kTokPerCta;
-  const int tok_here = (int)min((long long)kTokPerCta, n_tok - tok0);
+  const long long tok0 = (long long)blockIdx.x * tok_per_cta;
+  const int tok_here = (int)min((long long)tok_per_cta, n_tok - tok0);
+  const int H0 = a.t[0].H, H1 = a.ntensors > 1 ? a.t[1].H : 0;
+  const uint32_t bytes0 = (uint32_t)tok_here * H0 * 256, bytes1 = (uint32_t)tok_here * H1 * 256;
+  uint16_t* rows0 = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* rows1 = reinterpret_cast<uint16_t*>(smem + (size_t)tok_per_cta * H0 * 256);
 
-  if (blockIdx.x == 0 && tid < 32) {
-    if (a.err_clear && tid == 0) *a.err_clear = 0u;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, bytes0 + bytes1);
+    if (bytes0) bulk_load(rows0, a.t[0].x + tok0 * H0 * 128, bytes0, &bar);
+    if (bytes1) bulk_load(rows1, a.t[1].x + tok0 * H1 * 128, bytes1, &bar);
+  }
+  if (blockIdx.x == 0 && tid >= 32 && tid < 64) {
+    const int l = tid - 32;
+    if (a.err_clear && l == 0) *a.err_clear = 0u;
     if (a.logit_bound && a.ntensors == 2) {
       // QK-Norm bounds every logit: |qhat| <= sqrt(128) max|gamma_q| and the
       // same for khat, so |qhat . khat| / sqrt(128) <= sqrt(128) gq gk
       float gq = 0.f, gk = 0.f;
-      for (int i = tid; i < 128; i += 32) {
+      for (int i = l; i < 128; i += 32) {
         gq = fmaxf(gq, fabsf(__uint_as_float((uint32_t)a.t[0].gamma[i] << 16)));
         gk = fmaxf(gk, fabsf(__uint_as_float((uint32_t)a.t[1].gamma[i] << 16)));
       }
@@ -54,33 +89,18 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
         gq = fmaxf(gq, __shfl_xor_sync(0xffffffffu, gq, o));
         gk = fmaxf(gk, __shfl_xor_sync(0xffffffffu, gk, o));
       }
-      if (tid == 0) *a.logit_bound = 11.313708498984761f * gq * gk * 1.4426950408889634f;
+      if (l == 0) *a.logit_bound = 11.313708498984761f * gq * gk * 1.4426950408889634f;
     }
   }
-
-  // rotation table of this CTA's tokens (two entries per thread)
-  for (int e = tid; e < kTokPerCta * 64; e += kThreads) {
+  // rotation table of this CTA's tokens while the rows are in flight
+  for (int e = tid; e < tok_here * 64; e += kThreads) {
     const int tt = e >> 6, i = e & 63;
-    if (tt < tok_here) {
-      const float2 c_s = rope_cos_sin(a.pos0 + (tok0 + tt) % a.T, a.inv_freq[i]);
-      cos_s[tt][i] = c_s.x;
-      sin_s[tt][i] = c_s.y;
-    }
+    const float2 c_s = rope_cos_sin(a.pos0 + (tok0 + tt) % a.T, a.inv_freq[i]);
+    cos_s[tt][i] = c_s.x;
+    sin_s[tt][i] = c_s.y;
   }
-  // per-token row offsets of both tensors: the only divisions of the kernel
-  if (tid < kTokPerCta * 2) {
-    const int tt = tid >> 1, s = tid & 1;
-    if (tt < tok_here && s < a.ntensors) {
-      const long long tok = tok0 + tt;
-      const long long b = tok / a.T, t = tok - b * a.T;
-      xbase[tt][s] = b * (s ? a.t[1].xsb : a.t[0].xsb) + t * (s ? a.t[1].xst : a.t[0].xst);
-      ybase[tt][s] = b * (s ? a.t[1].ysb : a.t[0].ysb) + t * (s ? a.t[1].yst : a.t[0].yst);
-    }
-  }
-
   const int lane16 = tid & 15;
   const int hw = tid >> 4;
-  // gamma slices of both tensors, reused for every row
   float gl[2][4], gh[2][4];
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
@@ -93,70 +113,69 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(RopeArgs a) {
       for (int j = 0; j < 4; ++j) gl[s][j] = gh[s][j] = 0.f;
     }
   }
+  __syncthreads();  // barrier initialised, table written
+  mbar_wait(&bar, 0, nullptr, 0, nullptr);
+
+  const int R0 = tok_here * H0, R1 = tok_here * H1;
+  const int rows = R0 + R1;
+  const int rows_even = (rows + 1) & ~1;  // whole warps, so the shuffles stay converged
+  for (int q = hw; q < rows_even; q += kHalfWarps) {
+    const bool live = q < rows;
+    const int qq = live ? q : rows - 1;
+    const int s = qq < R0 ? 0 : 1;
+    const int rr = s ? qq - R0 : qq;
+    const int tt = rr / (s ? H1 : H0);
+    uint16_t* row = (s ? rows1 : rows0) + (size_t)rr * 128;
+    float xl[4], xh[4], ol[4], oh[4];
+    unpack4(reinterpret_cast<const uint2*>(row)[lane16], xl);
+    unpack4(reinterpret_cast<const uint2*>(row + 64)[lane16], xh);
+    const float4 c4 = reinterpret_cast<const float4*>(cos_s[tt])[lane16];
+    const float4 s4 = reinterpret_cast<const float4*>(sin_s[tt])[lane16];
+    const float2 c_s[4] = {make_float2(c4.x, s4.x), make_float2(c4.y, s4.y),
+                           make_float2(c4.z, s4.z), make_float2(c4.w, s4.w)};
+    float gls[4], ghs[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      gls[j] = s ? gl[1][j] : gl[0][j];
+      ghs[j] = s ? gh[1][j] : gh[0][j];
+    }
+    qknorm_rope_halfwarp(xl, xh, gls, ghs, c_s, a.eps, ol, oh);
+    if (live) {
+      reinterpret_cast<uint2*>(row)[lane16] = pack4(ol);
+      reinterpret_cast<uint2*>(row + 64)[lane16] = pack4(oh);
+    }
+  }
+  fence_proxy_async_smem();  // the bulk stores below read what was just written
   __syncthreads();
 
-  const int H0 = a.t[0].H;
-  const int rows_per_tok = H0 + (a.ntensors > 1 ? a.t[1].H : 0);
-  const int rows = tok_here * rows_per_tok;
-  const int rows_even = (rows + 1) & ~1;  // whole warps, so the shuffles stay converged
-  const uint16_t* x0 = a.t[0].x;
-  const uint16_t* x1 = a.t[1].x;
-  uint16_t* y0 = a.t[0].y;
-  uint16_t* y1 = a.t[1].y;
-  const long long xsh0 = a.t[0].xsh, xsh1 = a.t[1].xsh, ysh0 = a.t[0].ysh, ysh1 = a.t[1].ysh;
-
-  // (tt, h) of row r = hw, advanced by kHalfWarps rows at a time without
-  // division; kUnroll rows per half-warp are loaded before any is used
-  int tt = 0, h = hw;
-  while (h >= rows_per_tok) {
-    h -= rows_per_tok;
-    ++tt;
-  }
-  for (int r = hw; r < rows_even; r += kHalfWarps * kUnroll) {
-    float xl[kUnroll][4], xh[kUnroll][4];
-    uint16_t* yr[kUnroll];
-    int tsel[kUnroll], ssel[kUnroll];
-    bool live[kUnroll];
+  // bulk stores: a tensor whose output has the input's layout goes out as one
+  // block; otherwise one 256-byte row per store, spread over the threads
+  bool issued = false;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      live[u] = r + u * kHalfWarps < rows;
-      const int ttl = live[u] ? tt : tok_here - 1;
-      const int hl = live[u] ? h : rows_per_tok - 1;
-      const int sl = hl < H0 ? 0 : 1;
-      const int hs = sl ? hl - H0 : hl;
-      const uint16_t* xr =
-          (sl ? x1 : x0) + (xbase[ttl][sl] + (long long)hs * (sl ? xsh1 : xsh0)) * 128;
-      yr[u] = (sl ? y1 : y0) + (ybase[ttl][sl] + (long long)hs * (sl ? ysh1 : ysh0)) * 128;
-      tsel[u] = ttl;
-      ssel[u] = sl;
-      unpack4(reinterpret_cast<const uint2*>(xr)[lane16], xl[u]);
-      unpack4(reinterpret_cast<const uint2*>(xr + 64)[lane16], xh[u]);
-      h += kHalfWarps;
-      while (h >= rows_per_tok) {
-        h -= rows_per_tok;
-        ++tt;
+  for (int s = 0; s < 2; ++s) {
+    if (s >= a.ntensors) break;
+    const int H = s ? H1 : H0;
+    const uint16_t* src = s ? rows1 : rows0;
+    uint16_t* y = s ? a.t[1].y : a.t[0].y;
+    const long long ysb = s ? a.t[1].ysb : a.t[0].ysb, yst = s ? a.t[1].yst : a.t[0].yst,
+                    ysh = s ? a.t[1].ysh : a.t[0].ysh;
+    const bool contiguous = ysh == 1 && yst == H && ysb == (long long)a.T * H;
+    if (contiguous) {
+      if (tid == 0 && (s ? bytes1 : bytes0)) {
+        bulk_store(y + tok0 * H * 128, src, s ? bytes1 : bytes0);
+        issued = true;
       }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (r + u * kHalfWarps >= rows_even) break;  // same for both halves of a warp
-      const float4 c4 = reinterpret_cast<const float4*>(cos_s[tsel[u]])[lane16];
-      const float4 s4 = reinterpret_cast<const float4*>(sin_s[tsel[u]])[lane16];
-      const float2 c_s[4] = {make_float2(c4.x, s4.x), make_float2(c4.y, s4.y),
-                             make_float2(c4.z, s4.z), make_float2(c4.w, s4.w)};
-      float gls[4], ghs[4], ol[4], oh[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        gls[j] = ssel[u] ? gl[1][j] : gl[0][j];
-        ghs[j] = ssel[u] ? gh[1][j] : gh[0][j];
-      }
-      qknorm_rope_halfwarp(xl[u], xh[u], gls, ghs, c_s, a.eps, ol, oh);
-      if (live[u]) {
-        reinterpret_cast<uint2*>(yr[u])[lane16] = pack4(ol);
-        reinterpret_cast<uint2*>(yr[u] + 64)[lane16] = pack4(oh);
+    } else {
+      for (int rr = tid; rr < tok_here * H; rr += kThreads) {
+        const int tt = rr / H, h = rr - tt * H;
+        const long long tok = tok0 + tt;
+        const long long b = tok / a.T, t = tok - b * a.T;
+        bulk_store(y + (b * ysb + t * yst + (long long)h * ysh) * 128, src + (size_t)rr * 128, 256);
+        issued = true;
       }
     }
   }
+  if (issued) bulk_commit_and_wait_read();  // shared memory stays valid until read
 }
 
 }  // namespace
@@ -165,12 +184,33 @@ void fill_inv_freq(double theta, double* inv_freq) {
   for (int i = 0; i < 64; ++i) inv_freq[i] = pow(theta, -(2.0 * i) / 128.0);
 }
 
-cudaError_t launch_qknorm_rope(const RopeArgs& a, cudaStream_t stream) {
-  const long long n_tok = (long long)a.B * a.T;
+int qknorm_rope_max_heads() { return 512; }
+
+cudaError_t launch_qknorm_rope(const RopeArgs& a_in, cudaStream_t stream) {
+  const long long n_tok = (long long)a_in.B * a_in.T;
   if (n_tok == 0) return cudaSuccess;
-  const long long grid = (n_tok + kTokPerCta - 1) / kTokPerCta;
+  RopeArgs a = a_in;
+  const int rows_per_tok = a.t[0].H + (a.ntensors > 1 ? a.t[1].H : 0);
+  if (rows_per_tok <= 0 || rows_per_tok > qknorm_rope_max_heads()) return cudaErrorInvalidValue;
+  // 32-40 KB of staged rows per CTA: several CTAs per SM keep ~150+ KB of
+  // loads in flight
+  int tok = (40 * 1024) / (rows_per_tok * 256);
+  tok = tok < 1 ? 1 : (tok > kMaxTok ? kMaxTok : tok);
+  a.tok_per_cta = tok;
+  const size_t smem = (size_t)tok * rows_per_tok * 256;
+  static unsigned long long attr_mask = 0;  // per-device dynamic smem opt-in
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(attr_mask & (1ull << dev))) {
+    e = cudaFuncSetAttribute(qknorm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             512 * 256);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_mask |= 1ull << dev;
+  }
+  const long long grid = (n_tok + tok - 1) / tok;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  qknorm_rope_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(a);
+  qknorm_rope_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
