@@ -67,6 +67,9 @@ def _load():
                                               + [i] * 4 + [l, d, d, ctypes.c_void_p,
                                                             _f64p, _f64p])
             lib.q3a_oracle_decode.restype = i
+            lib.q3a_oracle_prefill_chunk.argtypes = ([_u16p] * 5 + [ctypes.c_void_p] + [_u16p] * 2
+                                                     + [i] * 5 + [l, d, d, _f64p, _f64p])
+            lib.q3a_oracle_prefill_chunk.restype = i
             _lib = lib
     return _lib
 
@@ -177,3 +180,26 @@ def decode(q, k_new, v_new, k_cache, v_cache, start_pos, q_gamma, k_gamma,
     if rc:
         raise ValueError(f"oracle decode failed ({rc})")
     return out, k_row
+
+
+def prefill_chunk(q, k, v, k_cache, v_cache, start_pos, q_gamma, k_gamma, theta: float,
+                  eps: float):
+    """Chunked prefill. q [B,Tq,Hq,d], k/v [B,Tq,Hkv,d]; caches [B,Hkv,S_max,d].
+
+    Returns (out fp64 [B,Tq,Hq,d], appended key rows fp64 [B,Tq,Hkv,d]).
+    """
+    q, k, v = _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v")
+    k_cache, v_cache = _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    q_gamma, k_gamma = _bf16(q_gamma, "q_gamma"), _bf16(k_gamma, "k_gamma")
+    B, Tq, Hq, d = q.shape
+    Hkv, S_max = k_cache.shape[1], k_cache.shape[2]
+    sp = torch.as_tensor(start_pos, dtype=torch.int32).contiguous()
+    out = torch.zeros((B, Tq, Hq, d), dtype=torch.float64)
+    k_rows = torch.zeros((B, Tq, Hkv, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_prefill_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache),
+                                          _ptr(v_cache), _ptr(sp), _ptr(q_gamma), _ptr(k_gamma),
+                                          B, Tq, Hq, Hkv, d, S_max, float(theta), float(eps),
+                                          _ptr(out), _ptr(k_rows))
+    if rc:
+        raise ValueError(f"oracle prefill_chunk failed ({rc})")
+    return out, k_rows

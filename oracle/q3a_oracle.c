@@ -30,6 +30,11 @@
  *           exp(s_j - max s) / sum exp(s_k - max s).
  *           Source: §7.2.1 GroupedQueryAttention.forward (masked_fill with -inf,
  *           softmax(scores / head_dim**0.5), @ values).
+ *   chunk   a chunk of Tq new tokens of sequence b at positions start_pos[b]+t:
+ *           cached rows 0..start_pos[b]-1 as stored, then the chunk's own keys
+ *           (steps 1-2 at their positions) under the causal mask; the same
+ *           section of the book.ozine.me chapter (rectangular causal mask from
+ *           pos_start).
  *   decode  the new token at p = start_pos: qhat and khat_new from steps 1-2 at
  *           p; keys = cached rows 0..p-1 exactly as stored (never re-normalised
  *           or re-rotated), then khat_new; values = cached rows 0..p-1, then
@@ -316,6 +321,77 @@ int q3a_oracle_decode(const uint16_t* q, const uint16_t* k_new, const uint16_t* 
         q3a_oracle_rope_row(qhat, d, (double)p, theta);
         attend_row(qhat, keys, vals, nk, d, scores, out + (b * Hq + h) * d);
       }
+    }
+    free(keys);
+    free(vals);
+    free(scores);
+    free(qhat);
+  }
+  return failed ? -2 : 0;
+}
+
+/* Chunked prefill against a KV cache ("Chapter 20, Qwen3 and Qwen3.5", §20.3:
+ * the model keeps a position counter and builds a rectangular causal mask
+ * starting at pos_start; the new keys are rotated at their own positions and
+ * concatenated to the cached ones, which are not rotated again).
+ *   q [B,Tq,Hq,d], k/v [B,Tq,Hkv,d] bf16: the chunk's projected rows;
+ *   caches [B,Hkv,S_max,d] bf16: rows 0..start_pos[b]-1 read as stored;
+ *   token t of sequence b sits at position p = start_pos[b] + t and attends
+ *   to the cached rows 0..start_pos[b]-1 and the chunk's keys 0..t.
+ *   out fp64 [B,Tq,Hq,d]; k_rows fp64 [B,Tq,Hkv,d] = the normalised, rotated
+ *   chunk keys (the rows a call appends to the cache, before rounding). */
+int q3a_oracle_prefill_chunk(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             const uint16_t* k_cache, const uint16_t* v_cache,
+                             const int32_t* start_pos, const uint16_t* q_gamma,
+                             const uint16_t* k_gamma, int B, int Tq, int Hq, int Hkv, int d,
+                             long S_max, double theta, double eps, double* out, double* k_rows) {
+  if (check_shape(B, Tq, Hq, Hkv, d) || S_max <= 0 || !out || !k_rows) return -1;
+  for (int b = 0; b < B; ++b)
+    if (start_pos[b] < 0 || (long)start_pos[b] + Tq > S_max) return -1;
+  int g = Hq / Hkv;
+  long units = (long)B * Hkv;
+  int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(OMP_THREADS)
+#endif
+  for (long u = 0; u < units; ++u) {
+    long b = u / Hkv, kv = u % Hkv;
+    long p0 = start_pos[b];
+    long n_all = p0 + Tq;
+    double* keys = (double*)malloc(sizeof(double) * (size_t)(n_all > 0 ? n_all : 1) * d);
+    double* vals = (double*)malloc(sizeof(double) * (size_t)(n_all > 0 ? n_all : 1) * d);
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(n_all > 0 ? n_all : 1));
+    double* qhat = (double*)malloc(sizeof(double) * d);
+    if (!keys || !vals || !scores || !qhat) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      failed = 1;
+    } else {
+      const uint16_t* kc = k_cache + (b * Hkv + kv) * S_max * d;
+      const uint16_t* vc = v_cache + (b * Hkv + kv) * S_max * d;
+      for (long j = 0; j < p0; ++j)
+        for (int c = 0; c < d; ++c) {
+          keys[j * d + c] = widen_bf16(kc[j * d + c]);
+          vals[j * d + c] = widen_bf16(vc[j * d + c]);
+        }
+      for (long t = 0; t < Tq; ++t) {
+        long r = ((b * Tq + t) * Hkv + kv) * d;
+        double* kn = keys + (p0 + t) * d;
+        q3a_oracle_rmsnorm_row(k + r, k_gamma, d, eps, kn);
+        q3a_oracle_rope_row(kn, d, (double)(p0 + t), theta);
+        for (int c = 0; c < d; ++c) {
+          k_rows[r + c] = kn[c];
+          vals[(p0 + t) * d + c] = widen_bf16(v[r + c]);
+        }
+      }
+      for (long t = 0; t < Tq; ++t)
+        for (long h = kv * g; h < (kv + 1) * g; ++h) {
+          long rq = ((b * Tq + t) * Hq + h) * d;
+          q3a_oracle_rmsnorm_row(q + rq, q_gamma, d, eps, qhat);
+          q3a_oracle_rope_row(qhat, d, (double)(p0 + t), theta);
+          attend_row(qhat, keys, vals, p0 + t + 1, d, scores, out + rq);
+        }
     }
     free(keys);
     free(vals);

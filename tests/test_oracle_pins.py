@@ -399,3 +399,112 @@ def test_kv_bytes_per_token_match_the_pages():
     # "about 4.5 GiB" for 32K tokens of Qwen3-8B
     q3 = kv_cache_bytes_per_token(36, 8) * 32768 / 2 ** 30
     assert q3 == pytest.approx(gold["context_32k_tokens_gib"]["Qwen3-8B"], abs=0.05)
+
+
+# ----------------------------------------------------------------------------
+# Chunked prefill against a cache (§20.3: rectangular causal mask from
+# pos_start; new keys rotated at their own positions, cached keys as stored)
+# ----------------------------------------------------------------------------
+
+def _brute_force_chunk(x, k_cache, v_cache, start_pos, theta, eps):
+    q, k, v = (x[n].to(torch.float64).tolist() for n in ("q", "k", "v"))
+    kc, vc = k_cache.to(torch.float64), v_cache.to(torch.float64)
+    gq = x["q_gamma"].to(torch.float64).tolist()
+    gk = x["k_gamma"].to(torch.float64).tolist()
+    B, Tq, Hq, Hkv = len(q), len(q[0]), len(q[0][0]), len(k[0][0])
+    g = Hq // Hkv
+
+    def norm(row, gamma):
+        inv = 1.0 / math.sqrt(math.fsum(e * e for e in row) / D + eps)
+        return [row[c] * inv * gamma[c] for c in range(D)]
+
+    def rotate(row, p):
+        res = [0.0] * D
+        for i in range(HALF):
+            ang = p * theta ** (-2.0 * i / D)
+            c, s = math.cos(ang), math.sin(ang)
+            res[i] = c * row[i] - s * row[i + HALF]
+            res[i + HALF] = s * row[i] + c * row[i + HALF]
+        return res
+
+    out = torch.zeros((B, Tq, Hq, D), dtype=torch.float64)
+    for b in range(B):
+        p0 = int(start_pos[b])
+        for h in range(Hq):
+            kv = ((h + 1) - 1) // g
+            keys = [kc[b, kv, j].tolist() for j in range(p0)]
+            vals = [vc[b, kv, j].tolist() for j in range(p0)]
+            keys += [rotate(norm(k[b][t][kv], gk), p0 + t) for t in range(Tq)]
+            vals += [v[b][t][kv] for t in range(Tq)]
+            for t in range(Tq):
+                qh = rotate(norm(q[b][t][h], gq), p0 + t)
+                n = p0 + t + 1
+                w = [math.exp(math.fsum(qh[c] * keys[j][c] for c in range(D)) / math.sqrt(D))
+                     for j in range(n)]
+                z = math.fsum(w)
+                for c in range(D):
+                    out[b, t, h, c] = math.fsum(w[j] * vals[j][c] for j in range(n)) / z
+    return out
+
+
+def test_chunk_matches_brute_force():
+    B, Tq, Hq, Hkv, S = 2, 3, 4, 2, 12
+    x = inputs.prefill_inputs(B, Tq, Hq, Hkv, seed=31)
+    cache = inputs.decode_inputs(B, Hq, Hkv, S, 0, 1, seed=32, start_pos=[4, 7])
+    out, _ = oracle.prefill_chunk(x["q"], x["k"], x["v"], cache["k_cache"], cache["v_cache"],
+                                  [4, 7], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    ref = _brute_force_chunk(x, cache["k_cache"], cache["v_cache"], [4, 7], 1e6, 1e-6)
+    assert (out - ref).abs().max() < 1e-12
+
+
+def test_chunk_at_position_zero_is_prefill():
+    B, T, Hq, Hkv, S = 2, 9, 8, 2, 16
+    x = inputs.prefill_inputs(B, T, Hq, Hkv, seed=33)
+    nan_cache = torch.full((B, Hkv, S, D), float("nan"), dtype=torch.bfloat16)
+    out, k_rows = oracle.prefill_chunk(x["q"], x["k"], x["v"], nan_cache, nan_cache, [0, 0],
+                                       x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    full = oracle.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    assert torch.equal(out, full)           # no cached row is read
+    assert torch.equal(k_rows, oracle.qknorm_rope(x["k"], x["k_gamma"], 1e6, 1e-6))
+
+
+def test_chunk_of_one_token_is_decode():
+    B, Hq, Hkv, S = 3, 8, 4, 20
+    y = inputs.decode_inputs(B, Hq, Hkv, S, 2, 19, seed=34)
+    out, k_rows = oracle.prefill_chunk(y["q"][:, None], y["k_new"][:, None], y["v_new"][:, None],
+                                       y["k_cache"], y["v_cache"], y["start_pos"], y["q_gamma"],
+                                       y["k_gamma"], 1e6, 1e-6)
+    dec, k_row = oracle.decode(y["q"], y["k_new"], y["v_new"], y["k_cache"], y["v_cache"],
+                               y["start_pos"], y["q_gamma"], y["k_gamma"], 1e6, 1e-6)
+    assert torch.equal(out[:, 0], dec)
+    assert torch.equal(k_rows[:, 0], k_row)
+
+
+def test_chunks_0_2_5_6_equal_one_prefill():
+    """§20.9's chunked-cache check: chunks [0:2], [2:5], [5:6] through the cache
+    give the full forward's outputs (to the bf16 rounding of cached keys)."""
+    T, Hq, Hkv, S = 6, 4, 2, 8
+    x = inputs.prefill_inputs(1, T, Hq, Hkv, seed=35)
+    full = oracle.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    k_cache = torch.full((1, Hkv, S, D), float("nan"), dtype=torch.bfloat16)
+    v_cache = torch.full((1, Hkv, S, D), float("nan"), dtype=torch.bfloat16)
+    outs = []
+    for lo, hi in [(0, 2), (2, 5), (5, 6)]:
+        out, k_rows = oracle.prefill_chunk(x["q"][:, lo:hi], x["k"][:, lo:hi], x["v"][:, lo:hi],
+                                           k_cache, v_cache, [lo], x["q_gamma"], x["k_gamma"],
+                                           1e6, 1e-6)
+        k_cache[0, :, lo:hi] = k_rows[0].transpose(0, 1).to(torch.bfloat16)
+        v_cache[0, :, lo:hi] = x["v"][0, lo:hi].transpose(0, 1)
+        outs.append(out)
+    got = torch.cat(outs, dim=1)
+    assert (got - full).abs().max() < 1e-2
+    # the first chunk reads no cached row: exact
+    assert torch.equal(outs[0], full[:, :2])
+
+
+def test_chunk_rejects_overflow():
+    x = inputs.prefill_inputs(1, 3, 2, 1, seed=36)
+    cache = torch.zeros((1, 1, 4, D), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        oracle.prefill_chunk(x["q"], x["k"], x["v"], cache, cache, [2], x["q_gamma"],
+                             x["k_gamma"], 1e6, 1e-6)
