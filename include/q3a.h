@@ -131,6 +131,46 @@ q3a_status q3a_prefill_attention(const q3a_bf16* v, q3a_bf16* out,
                                  void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * q3a_prefill_chunk — prefill of a chunk of Tq new tokens per sequence
+ * against a KV cache, appending the chunk to the cache.
+ *
+ *   q       [B, Tq, Hq, d]  bf16 projected queries of the chunk.
+ *   k, v    [B, Tq, Hkv, d] bf16 projected keys / values of the chunk.
+ *   k_cache, v_cache [B, Hkv, S_max, d] bf16: rows 0..start_pos[b]-1 hold the
+ *           sequence's earlier keys (normalised and rotated, as this library
+ *           writes them, with the same k_gamma) and values.
+ *   start_pos HOST int32 [B]: position of the chunk's first token in
+ *           sequence b; token t is at position start_pos[b] + t.
+ *   out     [B, Tq, Hq, d] bf16: token t of sequence b attends to cache rows
+ *           0..start_pos[b]-1 and the chunk's keys 0..t (causal).
+ *   Side effect: k_cache[b, :, start_pos[b] + t] = bf16(RoPE(RMSNorm(k)))
+ *   and v_cache[b, :, start_pos[b] + t] = v for t < Tq; other rows are
+ *   neither read nor written.
+ *   With start_pos[b] = 0 for all b this is q3a_prefill that also fills the
+ *   cache; with Tq = 1 it computes what q3a_decode computes.
+ *   Requires 0 <= start_pos[b] and start_pos[b] + Tq <= S_max for every b,
+ *   else Q3A_ERANGE with the caches untouched. B <= 2048, S_max <= 2^30,
+ *   Hq + 2 Hkv <= 512.
+ *   workspace: at least q3a_prefill_chunk_workspace_size() bytes, 256-byte
+ *   aligned, owned by the caller (normalised queries and an error word).
+ *   B == 0 or Tq == 0: returns Q3A_OK and launches nothing.
+ * Source: "Chapter 20, Qwen3 and Qwen3.5" (book.ozine.me), §20.3: a position
+ * counter and a rectangular causal mask starting at pos_start; new keys are
+ * rotated at their positions and concatenated to the cached ones; §20.9: the
+ * chunked-cache check (chunks [0:2], [2:5], [5:6] against one forward).
+ * ------------------------------------------------------------------------- */
+size_t q3a_prefill_chunk_workspace_size(int B, int Tq, int Hq, int Hkv, int d);
+
+q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
+                             q3a_bf16* k_cache, q3a_bf16* v_cache,
+                             const int32_t* start_pos,
+                             const q3a_bf16* q_gamma, const q3a_bf16* k_gamma,
+                             q3a_bf16* out,
+                             int B, int Tq, int Hq, int Hkv, int d, int S_max,
+                             double theta, float eps,
+                             void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_decode — one new token per sequence against a KV cache.
  *
  *   q       [B, Hq, d]  bf16 projected query of the new token.

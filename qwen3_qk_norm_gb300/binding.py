@@ -19,7 +19,8 @@ Q3A_OK, Q3A_EINVAL, Q3A_ERANGE, Q3A_ECUDA, Q3A_ETIMEOUT, Q3A_ENOTIMPL = range(6)
 STATUS_NAMES = {0: "Q3A_OK", 1: "Q3A_EINVAL", 2: "Q3A_ERANGE", 3: "Q3A_ECUDA",
                 4: "Q3A_ETIMEOUT", 5: "Q3A_ENOTIMPL"}
 EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size", "q3a_prefill",
-            "q3a_prefill_prologue", "q3a_prefill_attention", "q3a_decode_workspace_size",
+            "q3a_prefill_prologue", "q3a_prefill_attention", "q3a_prefill_chunk_workspace_size",
+            "q3a_prefill_chunk", "q3a_decode_workspace_size",
             "q3a_decode", "q3a_decode_noalloc", "q3a_last_device_error"]
 
 _lock = threading.Lock()
@@ -63,6 +64,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_prefill_prologue.restype = i
         lib.q3a_prefill_attention.argtypes = [vp] * 2 + [i] * 5 + [vp, sz, vp]
         lib.q3a_prefill_attention.restype = i
+        lib.q3a_prefill_chunk_workspace_size.argtypes = [i] * 5
+        lib.q3a_prefill_chunk_workspace_size.restype = sz
+        lib.q3a_prefill_chunk.argtypes = [vp] * 9 + [i] * 6 + [d, f, vp, sz, vp]
+        lib.q3a_prefill_chunk.restype = i
         lib.q3a_decode_workspace_size.argtypes = [i] * 5
         lib.q3a_decode_workspace_size.restype = sz
         lib.q3a_decode.argtypes = [vp] * 9 + [i] * 5 + [d, f, vp, sz, vp]
@@ -170,6 +175,51 @@ def prefill_attention(v, out, Hq: int, workspace: torch.Tensor) -> torch.Tensor:
     return out
 
 
+def prefill_chunk_workspace_size(B: int, Tq: int, Hq: int, Hkv: int, d: int = 128) -> int:
+    return int(load().q3a_prefill_chunk_workspace_size(B, Tq, Hq, Hkv, d))
+
+
+def _host_positions(start_pos, B: int) -> torch.Tensor:
+    sp = torch.as_tensor(start_pos, dtype=torch.int32).contiguous()
+    if sp.device.type != "cpu" or sp.numel() != B:
+        raise ValueError("start_pos: expected a host array of B int32")
+    return sp
+
+
+def prefill_chunk(q, k, v, k_cache, v_cache, start_pos, q_gamma, k_gamma, theta: float,
+                  eps: float, out=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Prefill of a chunk of Tq tokens per sequence against the caches, which
+    it extends by the chunk's normalised, rotated keys and its values.
+
+    q [B,Tq,Hq,128], k/v [B,Tq,Hkv,128] bf16; caches [B,Hkv,S_max,128] bf16;
+    start_pos: host int32 [B], position of each sequence's first chunk token.
+    """
+    B, Tq, Hq, d = q.shape
+    Hkv, S_max = k_cache.shape[1], k_cache.shape[2]
+    _check(q, "q")
+    _check(k, "k", (B, Tq, Hkv, d))
+    _check(v, "v", (B, Tq, Hkv, d))
+    _check(k_cache, "k_cache", (B, Hkv, S_max, d))
+    _check(v_cache, "v_cache", (B, Hkv, S_max, d))
+    _check(q_gamma, "q_gamma", (d,))
+    _check(k_gamma, "k_gamma", (d,))
+    sp = _host_positions(start_pos, B)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", q.shape)
+    need = prefill_chunk_workspace_size(B, Tq, Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_prefill_chunk(q.data_ptr(), k.data_ptr(), v.data_ptr(), k_cache.data_ptr(),
+                                  v_cache.data_ptr(), sp.data_ptr(), q_gamma.data_ptr(),
+                                  k_gamma.data_ptr(), out.data_ptr(), B, Tq, Hq, Hkv, d, S_max,
+                                  float(theta), float(eps), workspace.data_ptr(),
+                                  workspace.numel(), _stream(q.device))
+    _raise(st, "q3a_prefill_chunk")
+    return out
+
+
 def decode_workspace_size(B: int, Hq: int, Hkv: int, S_max: int, d: int = 128) -> int:
     return int(load().q3a_decode_workspace_size(B, Hq, Hkv, d, S_max))
 
@@ -190,9 +240,7 @@ def decode(q, k_new, v_new, k_cache, v_cache, start_pos, q_gamma, k_gamma, theta
     _check(v_cache, "v_cache", (B, Hkv, S_max, d))
     _check(q_gamma, "q_gamma", (d,))
     _check(k_gamma, "k_gamma", (d,))
-    sp = torch.as_tensor(start_pos, dtype=torch.int32).contiguous()
-    if sp.device.type != "cpu" or sp.numel() != B:
-        raise ValueError("start_pos: expected a host array of B int32")
+    sp = _host_positions(start_pos, B)
     if out is None:
         out = torch.empty_like(q)
     _check(out, "out", q.shape)

@@ -85,6 +85,7 @@ struct Bars {
   uint64_t slot_full[kSlots], slot_empty[kSlots];
   uint64_t s_full[kQTiles], p_full[kQTiles], o_final[kQTiles];
   uint64_t xmax_full[kQTiles];  // fallback path: both row halves posted their tile max
+  uint64_t vtail;               // cache V: rows past the valid keys cleared in the last tile
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -135,7 +136,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tile_tok = BM / g;  // tokens per Q tile
   const int t0 = mt * kQTiles * tile_tok;
   const int t_last = min(t0 + kQTiles * tile_tok, a.T) - 1;
-  const int n_tiles = t_last / BN + 1;
+  // token t of this sequence sits at position p0 + t (p0 = 0 for a plain
+  // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
+  const int p0 = a.chunk ? a.pos_b[b] : 0;
+  const int n_tiles = (p0 + t_last) / BN + 1;
+  const int n_keys = p0 + a.T;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -150,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->xmax_full[t], 256);
     }
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->vtail, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -160,8 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort_flag;
 
+  // Cache V (chunked prefill): the last V tile holds rows past the valid keys
+  // (whatever the cache holds there). Their weights are 0, but 0 x NaN is NaN
+  // in the PV product, so the producer warp clears them before PV reads them.
+  const bool v_tail = a.v_headmajor && n_tiles * BN > n_keys;
   if (warp >= kSoftmaxWGs * 4) {
-    if (warp == kSoftmaxWGs * 4 && lane == 0) {
+    if (warp == kSoftmaxWGs * 4) {
+     if (lane == 0) {
       // ---------------------------------------------------------- producer
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_k);
@@ -185,6 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((i & 1) == 0) {
           tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 0, j * BN, b * a.Hkv + kv);
           tma_load_3d(dst + kHalf, &a.tm_k, &bars->slot_full[s], 64, j * BN, b * a.Hkv + kv);
+        } else if (a.v_headmajor) {
+          tma_load_3d(dst, &a.tm_v, &bars->slot_full[s], 0, j * BN, b * a.Hkv + kv);
+          tma_load_3d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, j * BN, b * a.Hkv + kv);
         } else {
           tma_load_4d(dst, &a.tm_v, &bars->slot_full[s], 0, kv, j * BN, b);
           tma_load_4d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, kv, j * BN, b);
@@ -196,6 +210,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bars->q_full, 0, nullptr, 0, nullptr);
         for (int i = max(0, issued - kSlots); i < issued; ++i)
           mbar_wait(&bars->slot_full[i % kSlots], (i / kSlots) & 1, nullptr, 0, nullptr);
+      }
+     }
+      if (v_tail) {
+        __syncwarp();
+        const int iv = 2 * n_tiles - 1;  // load index of the last V tile
+        const bool ok = __all_sync(kFull, mbar_wait(&bars->slot_full[iv % kSlots],
+                                                    (iv / kSlots) & 1, a.err, kDevTimeoutTma,
+                                                    abort));
+        if (ok) {
+          uint8_t* vt = smem + OFF_RING + (iv % kSlots) * kTile;
+          const int first = n_keys - (n_tiles - 1) * BN;  // first row to clear
+          const int chunks = (BN - first) * 16;           // 16-byte chunks, both halves
+          for (int c = lane; c < chunks; c += 32) {
+            const int row = first + (c >> 4), half = (c >> 3) & 1, q16 = c & 7;
+            *reinterpret_cast<uint4*>(vt + half * kHalf + row * 128 + q16 * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->vtail);
+        }
       }
     } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -213,11 +248,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // So each commit below is followed by a full MMA group before the next
       // wait, by which time it has resolved: the waits for a group's inputs
       // are placed before the commit of the previous group.
-      auto wait_inputs = [&](int j) {  // V_j, K_{j+1} (if any) and P0_j
+      auto wait_inputs = [&](int j) {  // V_j, K_{j+1} (or the cleared V tail) and P0_j
         const int iv = 2 * j + 1, ik = 2 * j + 2;
-        const int kload = j + 1 < n_tiles ? ik : iv;
-        return mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1,
-                          &bars->slot_full[kload % kSlots], (kload / kSlots) & 1,
+        const bool last = j + 1 == n_tiles;
+        uint64_t* second = last ? (v_tail ? &bars->vtail : &bars->slot_full[iv % kSlots])
+                                : &bars->slot_full[ik % kSlots];
+        const uint32_t second_par = last ? (v_tail ? 0u : (uint32_t)((iv / kSlots) & 1))
+                                         : (uint32_t)((ik / kSlots) & 1);
+        return mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, second, second_par,
                           &bars->p_full[0], j & 1, a.err, kDevTimeoutMma, abort);
       };
       bool ok = mbar_wait(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) &&
@@ -269,8 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_id = 1 + t;      // named barrier of the two halves of tile t (epilogue)
     float* xmax = xchg + (t * 2) * 2 * 128;  // [half][parity][128]
     const int tok = t0 + t * tile_tok + r / g;
+    const int tok_pos = p0 + tok;  // position of this row's token
     const float bound = *a.logit_bound;
-    const bool fixed_max = bound >= 0.f && bound <= kFixedMaxLimit;
+    const bool fixed_max = a.fixed_shift_ok && bound >= 0.f && bound <= kFixedMaxLimit;
     float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -296,10 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
       const int key0 = j * BN + hc * 64;
-      if (key0 + 63 > tok) {
+      if (key0 + 63 > tok_pos) {
 #pragma unroll
         for (int e = 0; e < 64; ++e)
-          if (key0 + e > tok) s[e] = -INFINITY;
+          if (key0 + e > tok_pos) s[e] = -INFINITY;
       }
       bool move = false;
       float alpha = 1.0f;
@@ -379,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const bool store = tok < a.T;
+      const bool store = tok < a.T;  // rows of tokens past the chunk are padding
       uint16_t* orow = a.out +
                        (((long long)b * a.T + tok) * a.Hq + (long long)kv * g + (r % g)) * 128 +
                        hc * 64;

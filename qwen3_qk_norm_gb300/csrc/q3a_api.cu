@@ -163,6 +163,7 @@ static void prologue_args(RopeArgs& ra, const q3a_bf16* q, const q3a_bf16* k,
 static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* out, int B, int T,
                                  int Hq, int Hkv, void* workspace) {
   memset(&pa, 0, sizeof pa);
+  pa.fixed_shift_ok = 1;  // every key is normalised in this call with k_gamma
   const int g = Hq / Hkv;
   const uint64_t dq[4] = {128, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
   const uint64_t sq[3] = {256, (uint64_t)Hq * 256, (uint64_t)T * Hq * 256};
@@ -231,6 +232,96 @@ q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
   if (s != Q3A_OK) return s;
   RopeArgs ra;
   prologue_args(ra, q, k, q_gamma, k_gamma, B, T, Hq, Hkv, theta, eps, workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_qknorm_rope(ra, st);
+  if (e == cudaSuccess) e = launch_prefill_attention(pa, st);
+  return from_cuda(e);
+}
+
+size_t q3a_prefill_chunk_workspace_size(int B, int Tq, int Hq, int Hkv, int d) {
+  if (B < 0 || Tq < 0 || Hq <= 0 || Hkv <= 0 || d != 128) return 0;
+  return kHeader + align256(prefill_q_bytes(B, Tq, Hq));
+}
+
+q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
+                             q3a_bf16* k_cache, q3a_bf16* v_cache, const int32_t* start_pos,
+                             const q3a_bf16* q_gamma, const q3a_bf16* k_gamma, q3a_bf16* out,
+                             int B, int Tq, int Hq, int Hkv, int d, int S_max, double theta,
+                             float eps, void* workspace, size_t ws_bytes, void* stream) {
+  if (d != 128 || B < 0 || Tq < 0 || B > kMaxBatch || !group_ok(Hq, Hkv)) return Q3A_EINVAL;
+  if (S_max <= 0 || S_max > (1 << 30)) return Q3A_EINVAL;
+  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
+  if ((long long)B * Tq * Hq > 0x7fffffffLL) return Q3A_EINVAL;
+  if (Hq + 2 * Hkv > qknorm_rope_max_heads()) return Q3A_EINVAL;
+  if (B == 0 || Tq == 0) return Q3A_OK;
+  const void* ptrs[] = {q, k, v, k_cache, v_cache, q_gamma, k_gamma, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return Q3A_EINVAL;
+  if (!start_pos) return Q3A_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
+  if (ws_bytes < q3a_prefill_chunk_workspace_size(B, Tq, Hq, Hkv, d)) return Q3A_EINVAL;
+  bool all_at_zero = true;
+  for (int b = 0; b < B; ++b) {
+    const int32_t p = start_pos[b];
+    if (p < 0 || (long long)p + Tq > S_max) return Q3A_ERANGE;  // nothing written yet
+    all_at_zero = all_at_zero && p == 0;
+  }
+  const int g = Hq / Hkv;
+  uint16_t* qhat = ws_qhat(workspace);
+
+  // tensor maps first: a failure there launches nothing
+  PrefillArgs pa;
+  memset(&pa, 0, sizeof pa);
+  {
+    const uint64_t dq[4] = {128, (uint64_t)Hq, (uint64_t)Tq, (uint64_t)B};
+    const uint64_t sq[3] = {256, (uint64_t)Hq * 256, (uint64_t)Tq * Hq * 256};
+    const uint32_t bq[4] = {64, (uint32_t)g, (uint32_t)(128 / g), 1};
+    const uint64_t dc[3] = {128, (uint64_t)S_max, (uint64_t)B * Hkv};
+    const uint64_t sc[2] = {256, (uint64_t)S_max * 256};
+    const uint32_t bc[3] = {64, 128, 1};
+    if (encode_tensor_map(&pa.tm_q, qhat, 4, dq, sq, bq) != CUDA_SUCCESS ||
+        encode_tensor_map(&pa.tm_k, k_cache, 3, dc, sc, bc) != CUDA_SUCCESS ||
+        encode_tensor_map(&pa.tm_v, v_cache, 3, dc, sc, bc) != CUDA_SUCCESS)
+      return Q3A_ECUDA;
+  }
+  pa.out = out;
+  pa.err = reinterpret_cast<uint32_t*>(workspace);
+  pa.logit_bound = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + 8);
+  pa.B = B;
+  pa.T = Tq;
+  pa.Hq = Hq;
+  pa.Hkv = Hkv;
+  pa.g = g;
+  const int rows_tok = prefill_tokens_per_cta(g);
+  pa.n_mtiles = (Tq + rows_tok - 1) / rows_tok;
+  pa.v_headmajor = 1;
+  pa.chunk = 1;
+  // cached keys come from earlier calls: only a chunk with no cached keys
+  // may use the logit bound of this call's gammas
+  pa.fixed_shift_ok = all_at_zero ? 1 : 0;
+  for (int b = 0; b < B; ++b) pa.pos_b[b] = start_pos[b];
+
+  RopeArgs ra;
+  memset(&ra, 0, sizeof ra);
+  const long long S = S_max;
+  // Q -> Qhat [B, Tq, Hq]; K -> k_cache rows start_pos[b] + t (normalised,
+  // rotated); V -> v_cache rows start_pos[b] + t (copied)
+  ra.t[0] = RopeTensor{q, q_gamma, qhat, Hq, (long long)Tq * Hq, Hq, 1, (long long)Tq * Hq, Hq, 1,
+                       0, 0};
+  ra.t[1] = RopeTensor{k, k_gamma, k_cache, Hkv, (long long)Tq * Hkv, Hkv, 1,
+                       (long long)Hkv * S, 1, S, 0, 1};
+  ra.t[2] = RopeTensor{v, nullptr, v_cache, Hkv, (long long)Tq * Hkv, Hkv, 1,
+                       (long long)Hkv * S, 1, S, 1, 1};
+  ra.ntensors = 3;
+  ra.B = B;
+  ra.T = Tq;
+  ra.per_b_pos = 1;
+  for (int b = 0; b < B; ++b) ra.pos_b[b] = start_pos[b];
+  ra.eps = eps;
+  ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
+  ra.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
+  fill_inv_freq(theta, ra.inv_freq);
+
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_qknorm_rope(ra, st);
   if (e == cudaSuccess) e = launch_prefill_attention(pa, st);

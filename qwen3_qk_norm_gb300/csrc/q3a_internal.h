@@ -16,18 +16,25 @@ namespace q3a {
 // rows of 128 elements).
 struct RopeTensor {
   const uint16_t* x;
-  const uint16_t* gamma;
+  const uint16_t* gamma;  // unused when copy_only
   uint16_t* y;
   int H;
   long long xsb, xst, xsh;
   long long ysb, yst, ysh;
+  int copy_only;     // 1: rows are copied unchanged (values into a cache)
+  int y_at_position; // 1: output row t of sequence b goes to row pos_b[b] + t
 };
 
+constexpr int kMaxBatch = 2048;  // sequences per call of the position-aware paths
+
 struct RopeArgs {
-  RopeTensor t[2];
-  int ntensors;  // 1 or 2 (both tensors share B, T and the positions)
+  RopeTensor t[3];
+  int ntensors;  // 1..3 (all tensors share B, T and the positions); tensors
+                 // that normalise come first
   int B, T;
-  long long pos0;  // row (b, t, h) is rotated at pos0 + t
+  long long pos0;  // row (b, t, h) is rotated at pos0 + t ...
+  int per_b_pos;   // ... or, if set, at pos_b[b] + t
+  int pos_b[kMaxBatch];
   float eps;
   int tok_per_cta;      // set by launch_qknorm_rope
   uint32_t* err_clear;  // if non-null, block 0 zeroes this error word
@@ -45,13 +52,18 @@ cudaError_t launch_qknorm_rope(const RopeArgs& a, cudaStream_t stream);
 // ----- K2: causal GQA prefill attention (tcgen05) ---------------------------
 struct PrefillArgs {
   CUtensorMap tm_q;  // Qhat [B, T, Hq, 128] bf16, box {64, g, 128/g, 1}
-  CUtensorMap tm_k;  // Khat [B*Hkv, T, 128] bf16, box {64, 128, 1}
-  CUtensorMap tm_v;  // V    [B, T, Hkv, 128] bf16, box {64, 1, 128, 1}
+  CUtensorMap tm_k;  // Khat [B*Hkv, rows, 128] bf16, box {64, 128, 1} (workspace or cache)
+  CUtensorMap tm_v;  // V [B, T, Hkv, 128], box {64, 1, 128, 1}; or, with v_headmajor,
+                     // [B*Hkv, rows, 128] (the cache), box {64, 128, 1}
   uint16_t* out;     // [B, T, Hq, 128] bf16
   uint32_t* err;     // device error word
   const float* logit_bound;  // written by the prologue (see RopeArgs)
   int B, T, Hq, Hkv, g;
   int n_mtiles;      // ceil(T / prefill_tokens_per_cta(g))
+  int v_headmajor;   // V read from a [B, Hkv, S_max, 128] cache
+  int fixed_shift_ok;  // 0: always use the online max (cached keys present)
+  int chunk;         // positions and key counts come from pos_b (else pos_b = 0)
+  int pos_b[kMaxBatch];  // chunk: token t of sequence b is at position pos_b[b] + t
 };
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
@@ -59,7 +71,7 @@ cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
 int prefill_tokens_per_cta(int g);
 
 // ----- K3/K4: split-KV decode ------------------------------------------------
-constexpr int kDecodeMaxB = 2048;
+constexpr int kDecodeMaxB = kMaxBatch;
 constexpr int kDecodeChunk = 1024;  // keys per split
 constexpr int kDecodePartialFloats = 2 + 128;  // m, l, acc[128] per (split, head)
 

@@ -62,21 +62,25 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
   const long long tok0 = (long long)blockIdx.x * tok_per_cta;
   const int tok_here = (int)min((long long)tok_per_cta, n_tok - tok0);
   const int H0 = a.t[0].H, H1 = a.ntensors > 1 ? a.t[1].H : 0;
+  const int H2 = a.ntensors > 2 ? a.t[2].H : 0;
   const uint32_t bytes0 = (uint32_t)tok_here * H0 * 256, bytes1 = (uint32_t)tok_here * H1 * 256;
+  const uint32_t bytes2 = (uint32_t)tok_here * H2 * 256;
   uint16_t* rows0 = reinterpret_cast<uint16_t*>(smem);
   uint16_t* rows1 = reinterpret_cast<uint16_t*>(smem + (size_t)tok_per_cta * H0 * 256);
+  uint16_t* rows2 = reinterpret_cast<uint16_t*>(smem + (size_t)tok_per_cta * (H0 + H1) * 256);
 
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar, bytes0 + bytes1);
+    mbar_arrive_expect_tx(&bar, bytes0 + bytes1 + bytes2);
     if (bytes0) bulk_load(rows0, a.t[0].x + tok0 * H0 * 128, bytes0, &bar);
     if (bytes1) bulk_load(rows1, a.t[1].x + tok0 * H1 * 128, bytes1, &bar);
+    if (bytes2) bulk_load(rows2, a.t[2].x + tok0 * H2 * 128, bytes2, &bar);
   }
   if (blockIdx.x == 0 && tid >= 32 && tid < 64) {
     const int l = tid - 32;
     if (a.err_clear && l == 0) *a.err_clear = 0u;
-    if (a.logit_bound && a.ntensors == 2) {
+    if (a.logit_bound && a.ntensors >= 2) {
       // QK-Norm bounds every logit: |qhat| <= sqrt(128) max|gamma_q| and the
       // same for khat, so |qhat . khat| / sqrt(128) <= sqrt(128) gq gk
       float gq = 0.f, gk = 0.f;
@@ -95,7 +99,10 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
   // rotation table of this CTA's tokens while the rows are in flight
   for (int e = tid; e < tok_here * 64; e += kThreads) {
     const int tt = e >> 6, i = e & 63;
-    const float2 c_s = rope_cos_sin(a.pos0 + (tok0 + tt) % a.T, a.inv_freq[i]);
+    const long long tok = tok0 + tt;
+    const long long b = tok / a.T, t = tok - b * a.T;
+    const long long pos = (a.per_b_pos ? (long long)a.pos_b[b] : a.pos0) + t;
+    const float2 c_s = rope_cos_sin(pos, a.inv_freq[i]);
     cos_s[tt][i] = c_s.x;
     sin_s[tt][i] = c_s.y;
   }
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const uint16_t* gp = s ? a.t[1].gamma : a.t[0].gamma;
-    if (s < a.ntensors) {
+    if (s < a.ntensors && !a.t[s].copy_only) {
       unpack4(reinterpret_cast<const uint2*>(gp)[lane16], gl[s]);
       unpack4(reinterpret_cast<const uint2*>(gp + 64)[lane16], gh[s]);
     } else {
@@ -116,7 +123,8 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
   __syncthreads();  // barrier initialised, table written
   mbar_wait(&bar, 0, nullptr, 0, nullptr);
 
-  const int R0 = tok_here * H0, R1 = tok_here * H1;
+  const int R0 = a.t[0].copy_only ? 0 : tok_here * H0;
+  const int R1 = (a.ntensors > 1 && !a.t[1].copy_only) ? tok_here * H1 : 0;
   const int rows = R0 + R1;
   const int rows_even = (rows + 1) & ~1;  // whole warps, so the shuffles stay converged
   for (int q = hw; q < rows_even; q += kHalfWarps) {
@@ -152,24 +160,27 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
   // block; otherwise one 256-byte row per store, spread over the threads
   bool issued = false;
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {
+  for (int s = 0; s < 3; ++s) {
     if (s >= a.ntensors) break;
-    const int H = s ? H1 : H0;
-    const uint16_t* src = s ? rows1 : rows0;
-    uint16_t* y = s ? a.t[1].y : a.t[0].y;
-    const long long ysb = s ? a.t[1].ysb : a.t[0].ysb, yst = s ? a.t[1].yst : a.t[0].yst,
-                    ysh = s ? a.t[1].ysh : a.t[0].ysh;
-    const bool contiguous = ysh == 1 && yst == H && ysb == (long long)a.T * H;
+    const int H = s == 2 ? H2 : (s ? H1 : H0);
+    const uint16_t* src = s == 2 ? rows2 : (s ? rows1 : rows0);
+    const RopeTensor& ts = a.t[s];  // s is a compile-time index after unrolling
+    uint16_t* y = ts.y;
+    const long long ysb = ts.ysb, yst = ts.yst, ysh = ts.ysh;
+    const int at_pos = ts.y_at_position;
+    const bool contiguous = !at_pos && ysh == 1 && yst == H && ysb == (long long)a.T * H;
     if (contiguous) {
-      if (tid == 0 && (s ? bytes1 : bytes0)) {
-        bulk_store(y + tok0 * H * 128, src, s ? bytes1 : bytes0);
+      const uint32_t bytes = s == 2 ? bytes2 : (s ? bytes1 : bytes0);
+      if (tid == 0 && bytes) {
+        bulk_store(y + tok0 * H * 128, src, bytes);
         issued = true;
       }
     } else {
       for (int rr = tid; rr < tok_here * H; rr += kThreads) {
         const int tt = rr / H, h = rr - tt * H;
         const long long tok = tok0 + tt;
-        const long long b = tok / a.T, t = tok - b * a.T;
+        const long long b = tok / a.T;
+        const long long t = tok - b * a.T + (at_pos ? (long long)a.pos_b[b] : 0);
         bulk_store(y + (b * ysb + t * yst + (long long)h * ysh) * 128, src + (size_t)rr * 128, 256);
         issued = true;
       }
@@ -190,8 +201,12 @@ cudaError_t launch_qknorm_rope(const RopeArgs& a_in, cudaStream_t stream) {
   const long long n_tok = (long long)a_in.B * a_in.T;
   if (n_tok == 0) return cudaSuccess;
   RopeArgs a = a_in;
-  const int rows_per_tok = a.t[0].H + (a.ntensors > 1 ? a.t[1].H : 0);
+  const int rows_per_tok =
+      a.t[0].H + (a.ntensors > 1 ? a.t[1].H : 0) + (a.ntensors > 2 ? a.t[2].H : 0);
   if (rows_per_tok <= 0 || rows_per_tok > qknorm_rope_max_heads()) return cudaErrorInvalidValue;
+  if (a.ntensors < 1 || a.ntensors > 3 || (a.ntensors == 3 && !a.t[2].copy_only))
+    return cudaErrorInvalidValue;  // only the first two tensors normalise
+  if (a.per_b_pos && a.B > kMaxBatch) return cudaErrorInvalidValue;
   // 32-40 KB of staged rows per CTA: several CTAs per SM keep ~150+ KB of
   // loads in flight
   int tok = (40 * 1024) / (rows_per_tok * 256);

@@ -102,3 +102,52 @@ def test_workspace_sizes(lib):
     assert binding.prefill_workspace_size(B, T, Hq, Hkv, 64) == 0
     dws = binding.decode_workspace_size(64, 32, 8, 32768)
     assert dws >= 256 + 64 * 8 * 32 * 4 * 130 * 4
+
+
+def chunk_call(lib, start_pos, Tq=4, S_max=64, **kw):
+    B = len(start_pos)
+    sp = (ctypes.c_int32 * B)(*start_pos)
+    a = dict(Hq=32, Hkv=8, d=128, theta=1e6, eps=1e-6, ws=FAKE, ws_bytes=1 << 40)
+    a.update(kw)
+    return lib.q3a_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.addressof(sp), FAKE, FAKE,
+                                 FAKE, B, Tq, a["Hq"], a["Hkv"], a["d"], S_max, a["theta"],
+                                 a["eps"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("sp,Tq", [([61], 4), ([0, 61], 4), ([-1], 1), ([0], 65), ([63], 2)])
+def test_chunk_context_overflow_is_erange(lib, sp, Tq):
+    """start_pos + Tq > S_max (or a negative position) is refused before any write."""
+    assert chunk_call(lib, sp, Tq=Tq, S_max=64) == binding.Q3A_ERANGE
+
+
+def test_chunk_rejects_bad_arguments(lib):
+    assert chunk_call(lib, [3], d=64) == binding.Q3A_EINVAL
+    assert chunk_call(lib, [3], Hq=12, Hkv=8) == binding.Q3A_EINVAL
+    assert chunk_call(lib, [3], ws_bytes=16) == binding.Q3A_EINVAL
+    assert chunk_call(lib, [3], ws=FAKE + 16) == binding.Q3A_EINVAL
+    assert chunk_call(lib, [3], S_max=0) == binding.Q3A_EINVAL
+    assert chunk_call(lib, [3] * 2049, S_max=64) == binding.Q3A_EINVAL
+    assert chunk_call(lib, [3], Hq=256, Hkv=256) == binding.Q3A_EINVAL  # Hq + 2 Hkv > 512
+    assert chunk_call(lib, [], S_max=64) == binding.Q3A_OK
+    assert chunk_call(lib, [3], Tq=0) == binding.Q3A_OK
+
+
+def test_chunk_null_or_misaligned_pointer(lib):
+    sp = (ctypes.c_int32 * 1)(3)
+    args = [FAKE] * 9
+    args[5] = ctypes.addressof(sp)
+    for i in [0, 1, 2, 3, 4, 6, 7, 8]:
+        for bad in (0, FAKE + 2):
+            a = list(args)
+            a[i] = bad
+            st = lib.q3a_prefill_chunk(*a, 1, 4, 32, 8, 128, 64, 1e6, 1e-6, FAKE, 1 << 40, None)
+            assert st == binding.Q3A_EINVAL
+    a = list(args)
+    a[5] = 0
+    assert lib.q3a_prefill_chunk(*a, 1, 4, 32, 8, 128, 64, 1e6, 1e-6, FAKE, 1 << 40,
+                                 None) == binding.Q3A_EINVAL
+
+
+def test_chunk_workspace_size(lib):
+    assert binding.prefill_chunk_workspace_size(2, 100, 32, 8) >= 256 + 2 * 100 * 32 * 256
+    assert binding.prefill_chunk_workspace_size(2, 100, 32, 8, 64) == 0
