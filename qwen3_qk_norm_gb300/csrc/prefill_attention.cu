@@ -118,8 +118,24 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_s, uint6
                 idesc, 1u);
 }
 
+// The plain prefill and the chunk against the caches are two instantiations,
+// so the plain one carries none of the chunk's bookkeeping.
+__device__ __forceinline__ const PrefillArgs& base_args(const PrefillArgs& a) { return a; }
+__device__ __forceinline__ const PrefillArgs& base_args(const PrefillChunkArgs& a) {
+  return a.base;
+}
+__device__ __forceinline__ int chunk_start(const PrefillArgs&, int) { return 0; }
+__device__ __forceinline__ int chunk_start(const PrefillChunkArgs& a, int b) { return a.pos_b[b]; }
+__device__ __forceinline__ bool fixed_shift_allowed(const PrefillArgs&) { return true; }
+__device__ __forceinline__ bool fixed_shift_allowed(const PrefillChunkArgs& a) {
+  return a.fixed_shift_ok != 0;
+}
+
+template <class Args>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_attention_kernel(const __grid_constant__ PrefillArgs a) {
+    prefill_attention_kernel(const __grid_constant__ Args args) {
+  constexpr bool kChunk = sizeof(Args) != sizeof(PrefillArgs);
+  const PrefillArgs& a = base_args(args);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -138,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_last = min(t0 + kQTiles * tile_tok, a.T) - 1;
   // token t of this sequence sits at position p0 + t (p0 = 0 for a plain
   // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
-  const int p0 = a.chunk ? a.pos_b[b] : 0;
+  const int p0 = chunk_start(args, b);
   const int n_tiles = (p0 + t_last) / BN + 1;
   const int n_keys = p0 + a.T;
 
@@ -169,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Cache V (chunked prefill): the last V tile holds rows past the valid keys
   // (whatever the cache holds there). Their weights are 0, but 0 x NaN is NaN
   // in the PV product, so the producer warp clears them before PV reads them.
-  const bool v_tail = a.v_headmajor && n_tiles * BN > n_keys;
+  const bool v_tail = kChunk && n_tiles * BN > n_keys;
   if (warp >= kSoftmaxWGs * 4) {
     if (warp == kSoftmaxWGs * 4) {
      if (lane == 0) {
@@ -196,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((i & 1) == 0) {
           tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 0, j * BN, b * a.Hkv + kv);
           tma_load_3d(dst + kHalf, &a.tm_k, &bars->slot_full[s], 64, j * BN, b * a.Hkv + kv);
-        } else if (a.v_headmajor) {
+        } else if (kChunk) {
           tma_load_3d(dst, &a.tm_v, &bars->slot_full[s], 0, j * BN, b * a.Hkv + kv);
           tma_load_3d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, j * BN, b * a.Hkv + kv);
         } else {
@@ -309,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tok = t0 + t * tile_tok + r / g;
     const int tok_pos = p0 + tok;  // position of this row's token
     const float bound = *a.logit_bound;
-    const bool fixed_max = a.fixed_shift_ok && bound >= 0.f && bound <= kFixedMaxLimit;
+    const bool fixed_max = fixed_shift_allowed(args) && bound >= 0.f && bound <= kFixedMaxLimit;
     float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -458,24 +474,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int prefill_tokens_per_cta(int g) { return kQTiles * (BM / g); }
 
-cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream) {
+static const PrefillArgs& base_args_host(const PrefillArgs& a) { return a; }
+static const PrefillArgs& base_args_host(const PrefillChunkArgs& a) { return a.base; }
+
+template <class Args>
+static cudaError_t launch(const Args& args, cudaStream_t stream) {
   // per-device set-up: the dynamic shared memory limit is a per-device
-  // attribute of the function
+  // attribute of each instantiation
   static unsigned long long done_mask = 0;
+  const PrefillArgs& a = base_args_host(args);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(done_mask & (1ull << dev))) {
-    e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_attention_kernel<Args>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) done_mask |= 1ull << dev;
   }
   const long long grid = (long long)a.n_mtiles * a.B * a.Hkv;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  prefill_attention_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(a);
+  prefill_attention_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream) {
+  return launch(a, stream);
+}
+
+cudaError_t launch_prefill_attention(const PrefillChunkArgs& a, cudaStream_t stream) {
+  if (a.base.B > kMaxBatch) return cudaErrorInvalidValue;
+  return launch(a, stream);
 }
 
 }  // namespace q3a

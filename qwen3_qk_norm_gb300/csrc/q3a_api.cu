@@ -163,7 +163,6 @@ static void prologue_args(RopeArgs& ra, const q3a_bf16* q, const q3a_bf16* k,
 static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* out, int B, int T,
                                  int Hq, int Hkv, void* workspace) {
   memset(&pa, 0, sizeof pa);
-  pa.fixed_shift_ok = 1;  // every key is normalised in this call with k_gamma
   const int g = Hq / Hkv;
   const uint64_t dq[4] = {128, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
   const uint64_t sq[3] = {256, (uint64_t)Hq * 256, (uint64_t)T * Hq * 256};
@@ -270,8 +269,9 @@ q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf1
   uint16_t* qhat = ws_qhat(workspace);
 
   // tensor maps first: a failure there launches nothing
-  PrefillArgs pa;
-  memset(&pa, 0, sizeof pa);
+  PrefillChunkArgs ca;
+  memset(&ca, 0, sizeof ca);
+  PrefillArgs& pa = ca.base;
   {
     const uint64_t dq[4] = {128, (uint64_t)Hq, (uint64_t)Tq, (uint64_t)B};
     const uint64_t sq[3] = {256, (uint64_t)Hq * 256, (uint64_t)Tq * Hq * 256};
@@ -294,12 +294,10 @@ q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf1
   pa.g = g;
   const int rows_tok = prefill_tokens_per_cta(g);
   pa.n_mtiles = (Tq + rows_tok - 1) / rows_tok;
-  pa.v_headmajor = 1;
-  pa.chunk = 1;
   // cached keys come from earlier calls: only a chunk with no cached keys
   // may use the logit bound of this call's gammas
-  pa.fixed_shift_ok = all_at_zero ? 1 : 0;
-  for (int b = 0; b < B; ++b) pa.pos_b[b] = start_pos[b];
+  ca.fixed_shift_ok = all_at_zero ? 1 : 0;
+  for (int b = 0; b < B; ++b) ca.pos_b[b] = start_pos[b];
 
   RopeArgs ra;
   memset(&ra, 0, sizeof ra);
@@ -324,7 +322,7 @@ q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf1
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_qknorm_rope(ra, st);
-  if (e == cudaSuccess) e = launch_prefill_attention(pa, st);
+  if (e == cudaSuccess) e = launch_prefill_attention(ca, st);
   return from_cuda(e);
 }
 

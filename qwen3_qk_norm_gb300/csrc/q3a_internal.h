@@ -53,20 +53,25 @@ cudaError_t launch_qknorm_rope(const RopeArgs& a, cudaStream_t stream);
 struct PrefillArgs {
   CUtensorMap tm_q;  // Qhat [B, T, Hq, 128] bf16, box {64, g, 128/g, 1}
   CUtensorMap tm_k;  // Khat [B*Hkv, rows, 128] bf16, box {64, 128, 1} (workspace or cache)
-  CUtensorMap tm_v;  // V [B, T, Hkv, 128], box {64, 1, 128, 1}; or, with v_headmajor,
-                     // [B*Hkv, rows, 128] (the cache), box {64, 128, 1}
+  CUtensorMap tm_v;  // V [B, T, Hkv, 128], box {64, 1, 128, 1}; or, for a chunk,
+                     // [B*Hkv, S_max, 128] (the cache), box {64, 128, 1}
   uint16_t* out;     // [B, T, Hq, 128] bf16
   uint32_t* err;     // device error word
   const float* logit_bound;  // written by the prologue (see RopeArgs)
   int B, T, Hq, Hkv, g;
   int n_mtiles;      // ceil(T / prefill_tokens_per_cta(g))
-  int v_headmajor;   // V read from a [B, Hkv, S_max, 128] cache
-  int fixed_shift_ok;  // 0: always use the online max (cached keys present)
-  int chunk;         // positions and key counts come from pos_b (else pos_b = 0)
-  int pos_b[kMaxBatch];  // chunk: token t of sequence b is at position pos_b[b] + t
+};
+
+// A chunk against the caches: keys and values are read from the head-major
+// caches, and token t of sequence b sits at position pos_b[b] + t.
+struct PrefillChunkArgs {
+  PrefillArgs base;
+  int fixed_shift_ok;  // 0: cached keys present, always use the online max
+  int pos_b[kMaxBatch];
 };
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_attention(const PrefillChunkArgs& a, cudaStream_t stream);
 // tokens of one KV group that one attention CTA covers (n_mtiles = ceil(T / this))
 int prefill_tokens_per_cta(int g);
 
