@@ -37,6 +37,7 @@ from qwen3_qk_norm_gb300.inputs import WORKLOADS  # noqa: E402
 METRIC = "causal prefill attention TFLOP/s and decode GB/s at 1 GB300, % of roofline"
 PREFILL_WORKLOAD = "qwen3-8b-prefill-b4-t4096"
 DECODE_WORKLOAD = "qwen3-8b-decode-b64"
+CHUNK_WORKLOAD = "qwen3-8b-chunk-b4-t1024-at3072"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2 ** 20
 
@@ -277,6 +278,48 @@ def bench_decode(binding, device, steps: int, warmup: int, world: int):
     return w, x["start_pos"], ms
 
 
+def bench_chunk(binding, device, steps: int, warmup: int, world: int):
+    """Chunked prefill: the caches hold each prompt's first sp_lo tokens
+    (written by an untimed chunk from position 0); the timed step is the
+    prompt's last T tokens as one chunk. Every step rewrites the same rows."""
+    w = WORKLOADS[CHUNK_WORKLOAD]
+    x = inputs.workload_inputs(w, device=device)
+    p0 = w.sp_lo
+    kc = torch.full((w.B, w.Hkv, w.S_max, w.d), float("nan"), dtype=torch.bfloat16, device=device)
+    vc = torch.full_like(kc, float("nan"))
+    head = {k: x[k][:, :p0].contiguous() for k in ("q", "k", "v")}
+    tail = {k: x[k][:, p0:].contiguous() for k in ("q", "k", "v")}
+    binding.prefill_chunk(head["q"], head["k"], head["v"], kc, vc, [0] * w.B, x["q_gamma"],
+                          x["k_gamma"], w.theta, w.eps)
+    del head
+    out = torch.empty_like(tail["q"])
+    ws = torch.empty(binding.prefill_chunk_workspace_size(w.B, w.T, w.Hq, w.Hkv),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    start = [p0] * w.B
+
+    def step():
+        binding.prefill_chunk(tail["q"], tail["k"], tail["v"], kc, vc, start, x["q_gamma"],
+                              x["k_gamma"], w.theta, w.eps, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    barrier(world, device)
+    synchronize_all(device)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    synchronize_all(device)
+    barrier(world, device)
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    status = binding.last_device_error(ws)
+    if status != 0:
+        raise RuntimeError(f"chunk device error word: {status}")
+    return w, start, ms
+
+
 def cpu_baseline_prefill(w, x_cpu: dict, budget_s: float = 12.0, seed: int = 0) -> dict:
     """The fp64 oracle on a bounded sample of the prefill workload's query rows
     (random (b, t, h)), on all host cores, for about ``budget_s`` seconds."""
@@ -314,6 +357,8 @@ def run_profile_case(which: str) -> None:
         x = inputs.workload_inputs(w, device=device)
         for _ in range(3):
             binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], w.theta, w.eps)
+    elif which == "chunk":
+        bench_chunk(binding, device, 3, 0, 1)
     else:
         w = WORKLOADS[DECODE_WORKLOAD]
         B = 16  # a quarter of the batch: 2 GiB of cache instead of 8
@@ -345,6 +390,9 @@ def run_ours(args) -> None:
         dw, start_pos, dec_ms = (None, None, None)
         if not args.no_decode:
             dw, start_pos, dec_ms = bench_decode(binding, device, args.steps, args.warmup, world)
+        cw, c_start, ch_ms = (None, None, None)
+        if not args.no_chunk:
+            cw, c_start, ch_ms = bench_chunk(binding, device, args.steps, args.warmup, world)
     clocks = clk.summary()
 
     flops = accounting.prefill_flops(w.B, w.T, w.Hq, w.d)
@@ -416,6 +464,24 @@ def run_ours(args) -> None:
                              ROOT, "qwen3_qk_norm_gb300", "csrc", "decode_attention.cu"))},
             "gpu_launches": 2 * args.steps,
         }
+    if ch_ms is not None:
+        cflops = accounting.chunk_flops(c_start, cw.T, cw.Hq, cw.d)
+        ch_ms_max = max_over_ranks(ch_ms, world, device)
+        per_gpu = cflops / (ch_ms_max / 1e3) / 1e12
+        line["chunk"] = {
+            "value": round(whole_job_rate(cflops, world, ch_ms_max / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s", "ms_per_step": round(ch_ms_max, 4),
+            "config": {"workload": cw.name, "B": cw.B, "Tq": cw.T, "start_pos": cw.sp_lo,
+                       "Hq": cw.Hq, "Hkv": cw.Hkv, "S_max": cw.S_max, "flops_per_step": cflops,
+                       "api": "q3a_prefill_chunk (prologue writes the chunk into the caches, "
+                              "attention reads them)"},
+            "roofline": {"bound": "tensor", "kernel": "qknorm_rope_kernel + "
+                         "prefill_attention_kernel<PrefillChunkArgs>",
+                         "achieved": round(per_gpu, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(per_gpu / peaks["bf16_tflops"], 4),
+                         "peak_source": f"{peak_src} bf16 dense burst", "traffic": None},
+            "gpu_launches": 2 * args.steps,
+        }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x_cpu = {k: t.cpu() for k, t in x.items()}
         line["cpu_baseline"] = cpu_baseline_prefill(w, x_cpu)
@@ -481,7 +547,8 @@ def main(argv=None) -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill", "decode"],
+    ap.add_argument("--no-chunk", action="store_true")
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "chunk"],
                     help="run a few launches of one kernel for an ncu capture, print no JSON")
     args = ap.parse_args(argv)
     if args.profile_case:

@@ -11,6 +11,13 @@ def prefill_flops(B: int, T: int, Hq: int, d: int = 128) -> int:
     return 4 * d * Hq * B * T * (T + 1) // 2
 
 
+def chunk_flops(start_pos, Tq: int, Hq: int, d: int = 128) -> int:
+    """Algorithmic flops of a chunk of Tq tokens per sequence after start_pos[b]
+    cached tokens: token t sees start_pos[b] + t + 1 keys, 4d flops per pair."""
+    pairs = sum(Tq * int(p) + Tq * (Tq + 1) // 2 for p in start_pos)
+    return 4 * d * Hq * pairs
+
+
 def decode_bytes(start_pos, Hq: int, Hkv: int, d: int = 128) -> int:
     """Algorithmic HBM bytes of one decode step.
 

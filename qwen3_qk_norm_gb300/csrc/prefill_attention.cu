@@ -47,6 +47,18 @@
 // O_t, l are rescaled by 2^(m_old - m_new), when a tile's max exceeds it by
 // more than 8).
 //
+// Chunk against a KV cache ("Chapter 20, Qwen3 and Qwen3.5", §20.3: a
+// position counter, new keys rotated at their positions and appended to the
+// cached ones, a causal mask that starts at the chunk's first position). The
+// second instantiation reads K and V from the head-major caches, into which
+// the prologue has already written the chunk's rows; token t of sequence b
+// sits at position pos_b[b] + t and sees keys 0..pos_b[b] + t. Rows of the
+// last V tile past the valid keys hold whatever the cache holds there (a
+// probability of 0 times a NaN is NaN), so the producer warp clears them in
+// shared memory before the MMA issuer is allowed to read that tile. Cached
+// keys were normalised by earlier calls, so the fixed shift (which relies on
+// this call's gammas) is used only when no sequence has cached keys.
+//
 // Every mbarrier wait is bounded (q3a_device.cuh); a timeout sets the error
 // word, all roles unwind, in-flight copies and MMAs are drained and TMEM is
 // freed before the CTA exits.

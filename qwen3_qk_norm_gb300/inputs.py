@@ -16,6 +16,9 @@ Recipe (all draws from a ``torch.Generator`` seeded with the workload's seed):
            [B,Hkv,d] ~ N(0,1); then gamma_q, gamma_k ~ U(0.5, 1.5). Cache rows
            start_pos[b] and later are set to NaN, so that a read of a row that
            the step may not read shows up in the output.
+  chunk:   the prefill draws for whole prompts of sp_lo + T tokens (seeded as
+           above); the first sp_lo tokens go into the caches through an earlier
+           chunk, the last T are the timed chunk. Caches start as NaN.
 
 Large workloads are drawn on the GPU (``device="cuda"``) with torch's CUDA
 generator; small ones on the CPU. Either way the draws are deterministic for a
@@ -31,14 +34,14 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "prefill" or "decode"
+    kind: str  # "prefill", "decode" or "chunk"
     B: int
     Hq: int
     Hkv: int
     d: int = 128
-    T: int = 0          # prefill tokens per sequence
-    S_max: int = 0      # decode cache capacity
-    sp_lo: int = 0      # decode start_pos range [sp_lo, sp_hi)
+    T: int = 0          # prefill (or chunk) tokens per sequence
+    S_max: int = 0      # decode / chunk cache capacity
+    sp_lo: int = 0      # decode start_pos range [sp_lo, sp_hi); chunk: its start position
     sp_hi: int = 0
     theta: float = 1e6
     eps: float = 1e-6
@@ -62,6 +65,10 @@ WORKLOADS = {
         Workload("qwen3-8b-decode-b64", "decode", B=64, Hq=32, Hkv=8, S_max=32768,
                  sp_lo=1024, sp_hi=32768, theta=1e6, seed=3,
                  note="Qwen3-8B-shaped decode, start_pos ~ U[1024, 32768)"),
+        Workload("qwen3-8b-chunk-b4-t1024-at3072", "chunk", B=4, T=1024, Hq=32, Hkv=8,
+                 S_max=4096, sp_lo=3072, sp_hi=3073, theta=1e6, seed=5,
+                 note="Qwen3-8B-shaped chunked prefill: the last 1024 tokens of 4096-token "
+                      "prompts whose first 3072 tokens are already in the cache"),
         Workload("qwen3-30b-a3b-prefill-b1-t32768", "prefill", B=1, T=32768, Hq=32, Hkv=4,
                  theta=1e7, seed=4, note="Qwen3-30B-A3B-shaped long-context prefill"),
     ]
@@ -125,6 +132,8 @@ def decode_inputs(B: int, Hq: int, Hkv: int, S_max: int, sp_lo: int, sp_hi: int,
 
 
 def workload_inputs(w: Workload, device="cpu") -> dict:
+    if w.kind == "chunk":  # whole prompts; the caller splits them
+        return prefill_inputs(w.B, w.sp_lo + w.T, w.Hq, w.Hkv, w.d, w.seed, device=device)
     if w.kind == "prefill":
         return prefill_inputs(w.B, w.T, w.Hq, w.Hkv, w.d, w.seed, w.outlier_frac,
                               w.outlier_scale, device=device)

@@ -191,3 +191,36 @@ def test_chunk_qwen3_8b_shape(cuda_lib):
     for i, b in enumerate(sel):
         p = start_pos[b]
         assert_within_one_ulp(kc[b, :, p:p + Tq].transpose(0, 1), k_rows[i], "appended keys")
+
+
+@pytest.mark.slow
+def test_chunk_workload_sampled_rows(cuda_lib):
+    """The chunked-prefill workload as the benchmark launches it (the prompts'
+    first tokens written by a chunk from position 0, then the last chunk);
+    sampled rows of the last chunk against the oracle's prefill rows of the
+    whole prompt computed one by one."""
+    from qwen3_qk_norm_gb300.inputs import WORKLOADS
+    w = WORKLOADS["qwen3-8b-chunk-b4-t1024-at3072"]
+    x = inputs.workload_inputs(w, device="cuda")
+    p0 = w.sp_lo
+    kc = torch.full((w.B, w.Hkv, w.S_max, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    sl = lambda t, a, b: t[:, a:b].contiguous()  # noqa: E731
+    binding.prefill_chunk(sl(x["q"], 0, p0), sl(x["k"], 0, p0), sl(x["v"], 0, p0), kc, vc,
+                          [0] * w.B, x["q_gamma"], x["k_gamma"], w.theta, w.eps)
+    out = binding.prefill_chunk(sl(x["q"], p0, None), sl(x["k"], p0, None),
+                                sl(x["v"], p0, None), kc, vc, [p0] * w.B, x["q_gamma"],
+                                x["k_gamma"], w.theta, w.eps)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    g = torch.Generator().manual_seed(w.seed)
+    rows = [(b, t, h) for b, t, h in [(0, 0, 0), (w.B - 1, w.T - 1, w.Hq - 1)]]
+    rows += [(int(torch.randint(0, w.B, (1,), generator=g)),
+              int(torch.randint(0, w.T, (1,), generator=g)),
+              int(torch.randint(0, w.Hq, (1,), generator=g))) for _ in range(30)]
+    cpu = {k: t.cpu() for k, t in x.items()}
+    ref = oracle.prefill_rows(cpu["q"], cpu["k"], cpu["v"], cpu["q_gamma"], cpu["k_gamma"],
+                              w.theta, w.eps,
+                              torch.tensor([(b, p0 + t, h) for b, t, h in rows], dtype=torch.int32))
+    got = torch.stack([out[b, t, h] for b, t, h in rows])
+    assert_close_attention(got, ref, w.name)
