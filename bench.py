@@ -151,20 +151,32 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def source_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+CSRC = os.path.join(ROOT, "qwen3_qk_norm_gb300", "csrc")
+KERNEL_SOURCES = {  # the kernel's file and every header it includes
+    "prefill_attention_kernel": ["prefill_attention.cu", "q3a_device.cuh", "q3a_internal.h"],
+    "qknorm_rope_kernel": ["qknorm_rope.cu", "q3a_rope.cuh", "q3a_device.cuh", "q3a_internal.h"],
+    "decode_split_kernel": ["decode_attention.cu", "q3a_rope.cuh", "q3a_device.cuh",
+                            "q3a_internal.h"],
+}
 
 
-def ncu_traffic(kernel: str, source: str) -> float | None:
+def source_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str) -> float | None:
     """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    source is unchanged since that capture."""
+    sources are unchanged since that capture."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f).get(kernel)
-    if not rec or rec.get("source_sha") != source_sha(source):
+    if not rec or rec.get("source_sha") != source_sha(kernel):
         return None
     return float(rec["dram_bytes_per_launch"])
 
@@ -176,8 +188,9 @@ def synchronize_all(device):
 # ----------------------------------------------------------------------------
 # our implementation
 # ----------------------------------------------------------------------------
-def bench_prefill(binding, device, steps: int, warmup: int, world: int):
-    w = WORKLOADS[PREFILL_WORKLOAD]
+def bench_prefill(binding, device, steps: int, warmup: int, world: int,
+                  name: str = PREFILL_WORKLOAD):
+    w = WORKLOADS[name]
     x = inputs.workload_inputs(w, device=device)
     out = torch.empty_like(x["q"])
     ws = torch.empty(binding.prefill_workspace_size(w.B, w.T, w.Hq, w.Hkv), dtype=torch.uint8,
@@ -386,7 +399,8 @@ def run_ours(args) -> None:
     peaks, peak_src = measured_peaks()
 
     with ClockSampler(device) as clk:
-        w, x, step_ms, k1_ms, k2_ms = bench_prefill(binding, device, args.steps, args.warmup, world)
+        w, x, step_ms, k1_ms, k2_ms = bench_prefill(binding, device, args.steps, args.warmup, world,
+                                                    args.prefill_workload)
         dw, start_pos, dec_ms = (None, None, None)
         if not args.no_decode:
             dw, start_pos, dec_ms = bench_decode(binding, device, args.steps, args.warmup, world)
@@ -402,13 +416,13 @@ def run_ours(args) -> None:
     value = whole_job_rate(flops, world, step_ms_max / 1e3) / 1e12
     k2_tflops = flops / (k2_ms_max / 1e3) / 1e12
     k1_bytes = (w.B * w.T * (w.Hq + w.Hkv) * w.d * 2) * 2 + 2 * w.d * 2
-    src_k2 = os.path.join(ROOT, "qwen3_qk_norm_gb300", "csrc", "prefill_attention.cu")
-    traffic = ncu_traffic("prefill_attention_kernel", src_k2)
+    traffic = ncu_traffic("prefill_attention_kernel")
 
     e2e_steps = max(1, min(args.steps, 10))
     e2e_dt, h2d, d2h = bench_prefill_e2e(binding, device, w, e2e_steps)
     e2e_dt = max_over_ranks(e2e_dt, world, device)
 
+    step_bytes = w.B * w.T * (3 * w.Hq + 3 * w.Hkv) * w.d * 2
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -423,10 +437,12 @@ def run_ours(args) -> None:
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
-                   "theta": w.theta, "eps": w.eps, "outliers": "1% of Q/K rows x30",
+                   "theta": w.theta, "eps": w.eps, "outliers": (f"{w.outlier_frac:.0%} of Q/K rows x{w.outlier_scale:g}"
+                                 if w.outlier_frac > 0 else "none"),
                    "causal": True, "parallelism": f"replicas x{world} (weak, no collective)",
-                   "l2": "inputs larger than L2: q,k,v,Qhat,Khat,out = "
-                         f"{(w.B * w.T * (2 * w.Hq + 3 * w.Hkv) * w.d * 2 + w.B * w.T * w.Hq * w.d * 2) / 2**20:.0f} MiB per step"},
+                   "l2": (f"inputs {'larger' if step_bytes > L2_BYTES else 'SMALLER'} than L2 "
+                          f"(no flush): q,k,v,Qhat,Khat,out = {step_bytes / 2**20:.0f} MiB "
+                          "per step")},
         "roofline": {"bound": "tensor", "kernel": "prefill_attention_kernel",
                      "achieved": round(k2_tflops, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(k2_tflops / peaks["bf16_tflops"], 4),
@@ -438,7 +454,8 @@ def run_ours(args) -> None:
         "prologue": {"kernel": "qknorm_rope_kernel", "ms_per_launch": round(k1_ms_max, 4),
                      "bytes_per_launch": k1_bytes,
                      "achieved_gbs": round(k1_bytes / (k1_ms_max / 1e3) / 1e9, 1),
-                     "frac_of_hbm": round(k1_bytes / (k1_ms_max / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+                     "frac_of_hbm": round(k1_bytes / (k1_ms_max / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                     "traffic": ncu_traffic("qknorm_rope_kernel")},
         "e2e": {"value": round(whole_job_rate(flops, world, e2e_dt) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "q3a_prefill with pinned host inputs copied in and the output copied out "
@@ -460,8 +477,7 @@ def run_ours(args) -> None:
                          "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(per_gpu / peaks["hbm_gbs"], 4),
                          "peak_source": f"{peak_src} copy bandwidth",
-                         "traffic": ncu_traffic("decode_split_kernel", os.path.join(
-                             ROOT, "qwen3_qk_norm_gb300", "csrc", "decode_attention.cu"))},
+                         "traffic": ncu_traffic("decode_split_kernel")},
             "gpu_launches": 2 * args.steps,
         }
     if ch_ms is not None:
@@ -548,6 +564,9 @@ def main(argv=None) -> None:
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunk", action="store_true")
+    ap.add_argument("--prefill-workload", default=PREFILL_WORKLOAD,
+                    choices=[n for n, w in WORKLOADS.items() if w.kind == "prefill"],
+                    help="prefill workload of the step (the default is the headline one)")
     ap.add_argument("--profile-case", choices=["prefill", "decode", "chunk"],
                     help="run a few launches of one kernel for an ncu capture, print no JSON")
     args = ap.parse_args(argv)
