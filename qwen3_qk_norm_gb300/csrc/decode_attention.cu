@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < 64) cs[threadIdx.x] = rope_cos_sin(p, a.inv_freq[threadIdx.x]);
+  if (threadIdx.x < 64) cs[threadIdx.x] = rope_cos_sin(p, a.turn_freq[threadIdx.x]);
   __syncthreads();
   volatile int* abort = &bars->abort_flag;
 

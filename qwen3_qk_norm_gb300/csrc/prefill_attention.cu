@@ -352,16 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j > 0) mbar_arrive(&bars->slot_empty[(2 * j - 1) % kSlots]);
       }
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(tmem_s, sr[0]);
-      tmem_ld32(tmem_s + 32, sr[1]);
-      tmem_wait_ld();
+      uint32_t sr[64];
+      tmem_ld64_wait(tmem_s, sr);
 
       float s[64];
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c * 32 + e]);
       const int key0 = j * BN + hc * 64;
       if (key0 + 63 > tok_pos) {
 #pragma unroll
@@ -409,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
         pw[e] = pack_bf16x2(p0, p1);
       }
-      tmem_st32(tmem_s, pw);  // P over the first 32 of this thread's S columns
+      tmem_st32_wait(tmem_s, pw);  // P over the first 32 of this thread's S columns
       // O_t holds every PV up to j-1 here (the S_t,j commit covers them);
       // rescale this thread's O columns before PV_t,j adds terms relative to
       // the new max
@@ -417,14 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          tmem_ld32(tmem_o + c * 32, o);
-          tmem_wait_ld();
+          tmem_ld32_wait(tmem_o + c * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tmem_o + c * 32, o);
+          tmem_st32_wait(tmem_o + c * 32, o);
         }
       }
-      tmem_wait_st();
       float a0, a1, b0, b1;
       f2_unpack(sum2[0], a0, a1);
       f2_unpack(sum2[1], b0, b1);
@@ -453,8 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem_o + c * 32, o);
-        tmem_wait_ld();
+        tmem_ld32_wait(tmem_o + c * 32, o);
         if (store) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {

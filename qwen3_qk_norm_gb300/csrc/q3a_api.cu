@@ -109,7 +109,7 @@ q3a_status q3a_qknorm_rope(const q3a_bf16* x, const q3a_bf16* gamma, q3a_bf16* y
   a.T = T;
   a.pos0 = pos0;
   a.eps = eps;
-  fill_inv_freq(theta, a.inv_freq);
+  fill_turn_freq(theta, a.turn_freq);
   return from_cuda(launch_qknorm_rope(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -157,7 +157,7 @@ static void prologue_args(RopeArgs& ra, const q3a_bf16* q, const q3a_bf16* k,
   ra.eps = eps;
   ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
   ra.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
-  fill_inv_freq(theta, ra.inv_freq);
+  fill_turn_freq(theta, ra.turn_freq);
 }
 
 static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* out, int B, int T,
@@ -318,7 +318,7 @@ q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf1
   ra.eps = eps;
   ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
   ra.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
-  fill_inv_freq(theta, ra.inv_freq);
+  fill_turn_freq(theta, ra.turn_freq);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_qknorm_rope(ra, st);
@@ -386,7 +386,7 @@ q3a_status q3a_decode(const q3a_bf16* q, const q3a_bf16* k_new, const q3a_bf16* 
   da->split_stride = decode_split_stride(S_max);
   da->max_splits = max_splits;
   da->eps = eps;
-  fill_inv_freq(theta, da->inv_freq);
+  fill_turn_freq(theta, da->turn_freq);
   for (int b = 0; b < B; ++b) da->start_pos[b] = start_pos[b];
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -42,10 +42,12 @@ struct RopeArgs {
   // that QK-Norm guarantees: sqrt(128) * max|gamma_q| * max|gamma_k| * log2(e)
   // (tensor 0 is Q, tensor 1 is K)
   float* logit_bound;
-  double inv_freq[64];  // theta^(-2i/128)
+  unsigned long long turn_freq[64];  // theta^(-2i/128) / (2 pi), 0.64 fixed point
 };
 
-void fill_inv_freq(double theta, double* inv_freq);
+// RoPE frequencies as fractions of a turn in 0.64 fixed point, so that the
+// angle of position p is p * turn_freq[i] modulo 2^64 (exact wrap-around)
+void fill_turn_freq(double theta, unsigned long long* turn_freq);
 int qknorm_rope_max_heads();  // largest H0 + H1 one launch accepts
 cudaError_t launch_qknorm_rope(const RopeArgs& a, cudaStream_t stream);
 
@@ -95,7 +97,7 @@ struct DecodeArgs {
   uint32_t* err;
   int B, Hq, Hkv, g, S_max, split_stride, max_splits;
   float eps;
-  double inv_freq[64];
+  unsigned long long turn_freq[64];
   int start_pos[kDecodeMaxB];
 };
 

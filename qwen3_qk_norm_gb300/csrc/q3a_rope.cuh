@@ -12,14 +12,16 @@
 
 namespace q3a {
 
-// (cos a, sin a) for a = p * w. The product and its reduction modulo 2 pi are
-// done in fp64 (exact enough for p up to 2^30), the reduced angle in fp32.
-__device__ __forceinline__ float2 rope_cos_sin(long long p, double w) {
-  const double ang = (double)p * w;
-  const double turns = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
-  const double red = fma(-turns, 6.283185307179586, ang);
+// (cos a, sin a) for a = p * w with w = 2 pi * turn / 2^64. p * turn modulo
+// 2^64 is the angle in turns, exactly (integer wrap-around); its top 32 bits,
+// as a signed fraction x of half a turn, give a = pi * x with |x| < 1, and
+// sincospif evaluates it without a range reduction. The error of the 64-bit
+// frequency (below 2^-64 turn) times p stays under 2^-34 turn for p < 2^30.
+__device__ __forceinline__ float2 rope_cos_sin(long long p, unsigned long long turn) {
+  const unsigned long long f = (unsigned long long)p * turn;
+  const float x = (float)(int)(f >> 32) * 4.656612873077393e-10f;  // 2^-31
   float s, c;
-  sincosf((float)red, &s, &c);
+  sincospif(x, &s, &c);
   return make_float2(c, s);
 }
 

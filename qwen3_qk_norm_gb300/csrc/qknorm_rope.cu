@@ -20,6 +20,11 @@
 // reduction. Results overwrite the staged rows, and bulk stores write them
 // out: one store per tensor when the output has the input's layout, one per
 // row otherwise (the head-major K layout of the prefill workspace).
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
 #include "q3a_internal.h"
 #include "q3a_rope.cuh"
 
@@ -102,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
     const long long tok = tok0 + tt;
     const long long b = tok / a.T, t = tok - b * a.T;
     const long long pos = (a.per_b_pos ? (long long)a.pos_b[b] : a.pos0) + t;
-    const float2 c_s = rope_cos_sin(pos, a.inv_freq[i]);
+    const float2 c_s = rope_cos_sin(pos, a.turn_freq[i]);
     cos_s[tt][i] = c_s.x;
     sin_s[tt][i] = c_s.y;
   }
@@ -191,8 +196,33 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
 
 }  // namespace
 
-void fill_inv_freq(double theta, double* inv_freq) {
-  for (int i = 0; i < 64; ++i) inv_freq[i] = pow(theta, -(2.0 * i) / 128.0);
+void fill_turn_freq(double theta, unsigned long long* turn_freq) {
+  // w_i / (2 pi) in long double (64 or more mantissa bits), scaled to 2^64.
+  // long double arithmetic can be slow (software quad precision on some
+  // hosts), so the last few thetas are remembered.
+  struct Entry {
+    double theta;
+    unsigned long long f[64];
+  };
+  static Entry cache[4];
+  static int n_cached = 0, next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int c = 0; c < n_cached; ++c)
+    if (cache[c].theta == theta) {
+      memcpy(turn_freq, cache[c].f, sizeof cache[c].f);
+      return;
+    }
+  const long double two_pi = 6.283185307179586476925286766559L;
+  Entry& e = cache[next];
+  e.theta = theta;
+  for (int i = 0; i < 64; ++i) {
+    const long double w = powl((long double)theta, -(long double)(2 * i) / 128.0L);
+    e.f[i] = (unsigned long long)llroundl(w / two_pi * 18446744073709551616.0L);
+  }
+  memcpy(turn_freq, e.f, sizeof e.f);
+  next = (next + 1) % 4;
+  if (n_cached < 4) ++n_cached;
 }
 
 int qknorm_rope_max_heads() { return 512; }
