@@ -206,6 +206,36 @@ q3a_status q3a_decode(const q3a_bf16* q, const q3a_bf16* k_new, const q3a_bf16* 
                       void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * q3a_decode_device_pos — q3a_decode with the positions in DEVICE memory,
+ * for decode loops captured into a CUDA graph (the positions change between
+ * replays; the parameters of the captured launches do not).
+ *
+ *   Arguments as q3a_decode, except:
+ *   start_pos DEVICE int32 [B], 4-byte aligned, read by the kernels when they
+ *           run (the call never reads it on the host and never synchronises).
+ *   Range check on the device: a one-block kernel checks
+ *   0 <= start_pos[b] < S_max for every b before the decode kernels run; if
+ *   any position is out of range, nothing is written (caches and out are
+ *   left as they were) and the workspace's error word records it:
+ *   q3a_last_device_error() then returns Q3A_ERANGE. Host-checkable argument
+ *   errors return Q3A_EINVAL at the call as for q3a_decode.
+ *   Work: every split a sequence could need at S_max is launched; splits past
+ *   a sequence's length exit at once.
+ *   workspace: q3a_decode_workspace_size() bytes (the same as q3a_decode).
+ * Source: as q3a_decode; the pages have no counterpart for graph capture or
+ * device-resident positions (a serving-loop concern).
+ * ------------------------------------------------------------------------- */
+q3a_status q3a_decode_device_pos(const q3a_bf16* q, const q3a_bf16* k_new,
+                                 const q3a_bf16* v_new,
+                                 q3a_bf16* k_cache, q3a_bf16* v_cache,
+                                 const int32_t* start_pos,
+                                 const q3a_bf16* q_gamma, const q3a_bf16* k_gamma,
+                                 q3a_bf16* out,
+                                 int B, int Hq, int Hkv, int d, int S_max,
+                                 double theta, float eps,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_decode_noalloc — q3a_decode for callers that cannot allocate device
  * memory for a workspace: a plugin whose host framework owns every device
  * allocation and hands it none, or a latency-critical loop that must not call
@@ -246,8 +276,10 @@ q3a_status q3a_decode_noalloc(const q3a_bf16* q, const q3a_bf16* k_new, const q3
  * q3a_last_device_error — reads, synchronously on `stream`, the error word
  * that the kernels of the last call which used `workspace` left in its first
  * bytes (prefill and decode workspaces both keep it at offset 0).
- * Returns Q3A_OK when the word is zero, Q3A_ETIMEOUT when a bounded device
- * wait gave up, Q3A_EINVAL for a NULL workspace, Q3A_ECUDA if the read failed.
+ * Returns Q3A_OK when the word is zero, Q3A_ERANGE when the device-side
+ * position check of q3a_decode_device_pos failed, Q3A_ETIMEOUT when a bounded
+ * device wait gave up, Q3A_EINVAL for a NULL workspace, Q3A_ECUDA if the read
+ * failed.
  * ------------------------------------------------------------------------- */
 q3a_status q3a_last_device_error(const void* workspace, void* stream);
 

@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "Q3A_OK", 1: "Q3A_EINVAL", 2: "Q3A_ERANGE", 3: "Q3A_ECUDA",
 EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size", "q3a_prefill",
             "q3a_prefill_prologue", "q3a_prefill_attention", "q3a_prefill_chunk_workspace_size",
             "q3a_prefill_chunk", "q3a_decode_workspace_size",
-            "q3a_decode", "q3a_decode_noalloc", "q3a_last_device_error"]
+            "q3a_decode", "q3a_decode_device_pos", "q3a_decode_noalloc",
+            "q3a_last_device_error"]
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_decode_workspace_size.restype = sz
         lib.q3a_decode.argtypes = [vp] * 9 + [i] * 5 + [d, f, vp, sz, vp]
         lib.q3a_decode.restype = i
+        lib.q3a_decode_device_pos.argtypes = [vp] * 9 + [i] * 5 + [d, f, vp, sz, vp]
+        lib.q3a_decode_device_pos.restype = i
         lib.q3a_decode_noalloc.argtypes = [vp] * 9 + [i] * 5 + [d, f, vp]
         lib.q3a_decode_noalloc.restype = i
         lib.q3a_last_device_error.argtypes = [vp, vp]
@@ -254,6 +257,39 @@ def decode(q, k_new, v_new, k_cache, v_cache, start_pos, q_gamma, k_gamma, theta
                            float(theta), float(eps), workspace.data_ptr(), workspace.numel(),
                            _stream(q.device))
     _raise(st, "q3a_decode")
+    return out
+
+
+def decode_device_pos(q, k_new, v_new, k_cache, v_cache, start_pos, q_gamma, k_gamma,
+                      theta: float, eps: float, out=None,
+                      workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """One decode step with the positions in device memory (start_pos: CUDA
+    int32 [B]); capturable into a CUDA graph. An out-of-range position makes
+    the step write nothing and last_device_error() return Q3A_ERANGE."""
+    B, Hq, d = q.shape
+    Hkv, S_max = k_cache.shape[1], k_cache.shape[2]
+    _check(q, "q")
+    _check(k_new, "k_new", (B, Hkv, d))
+    _check(v_new, "v_new", (B, Hkv, d))
+    _check(k_cache, "k_cache", (B, Hkv, S_max, d))
+    _check(v_cache, "v_cache", (B, Hkv, S_max, d))
+    _check(q_gamma, "q_gamma", (d,))
+    _check(k_gamma, "k_gamma", (d,))
+    _check(start_pos, "start_pos", (B,), dtype=torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", q.shape)
+    need = decode_workspace_size(B, Hq, Hkv, S_max, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_decode_device_pos(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                      k_cache.data_ptr(), v_cache.data_ptr(),
+                                      start_pos.data_ptr(), q_gamma.data_ptr(),
+                                      k_gamma.data_ptr(), out.data_ptr(), B, Hq, Hkv, d, S_max,
+                                      float(theta), float(eps), workspace.data_ptr(),
+                                      workspace.numel(), _stream(q.device))
+    _raise(st, "q3a_decode_device_pos")
     return out
 
 

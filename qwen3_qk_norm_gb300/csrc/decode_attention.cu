@@ -95,10 +95,19 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// Position of sequence b: from the parameters, or from device memory after
+// the device-side check (kDevPos).
+template <bool kDevPos>
+__device__ __forceinline__ int decode_pos(const DecodeArgs& a, int b) {
+  return kDevPos ? a.pos_dev[b] : a.start_pos[b];
+}
+
+template <bool kDevPos>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   const int c = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
-  const int p = a.start_pos[b];
+  if (kDevPos && *a.pos_valid == 0) return;  // some position out of range: write nothing
+  const int p = decode_pos<kDevPos>(a, b);
   const int L = p + 1;  // keys of this sequence, the new one included
   const int n_splits = (L + kDecodeChunk - 1) / kDecodeChunk;
   if (c >= n_splits) return;
@@ -380,10 +389,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+template <bool kDevPos>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  if (kDevPos && *a.pos_valid == 0) return;
   const int g = a.g, kv = h / g, j = h % g;
-  const int L = a.start_pos[b] + 1;
+  const int L = decode_pos<kDevPos>(a, b) + 1;
   const int n_splits = (L + kDecodeChunk - 1) / kDecodeChunk;
   const float* base =
       a.partial + ((((long long)b * a.Hkv + kv) * a.split_stride) * g + j) * kDecodePartialFloats;
@@ -401,6 +412,23 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   a.out[((long long)b * a.Hq + h) * 128 + d] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
 }
 
+// Device-side validation of positions that live in device memory: every
+// start_pos[b] must satisfy 0 <= p < S_max. One block; writes the verdict and
+// the error word (0, or kErrWordRange) before any decode kernel runs.
+__global__ void __launch_bounds__(256) decode_pos_check_kernel(const int32_t* pos, int B, int S_max,
+                                                               uint32_t* err, uint32_t* valid) {
+  int bad = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int p = pos[b];
+    bad |= (p < 0 || p >= S_max) ? 1 : 0;
+  }
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    *valid = bad ? 0u : 1u;
+    *err = bad ? kErrWordRange : 0u;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -408,19 +436,34 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !(attr_done_mask & (1ull << dev))) {
-    e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
+  if (dev >= 64 || !(attr_done_mask & (1ull << dev))) {
+    e = cudaFuncSetAttribute(decode_split_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done_mask |= 1ull << dev;
+    e = cudaFuncSetAttribute(decode_split_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_done_mask |= 1ull << dev;
   }
   if (a.B == 0) return cudaSuccess;
   dim3 grid1(a.max_splits, a.Hkv, a.B);
-  decode_split_kernel<<<grid1, kThreads, kSmemBytes, stream>>>(a);
+  dim3 grid2(a.Hq, a.B);
+  if (a.pos_dev) {
+    // positions unknown on the host: the check decides, and every split a
+    // sequence may need is launched (the ones past its length exit at once)
+    decode_pos_check_kernel<<<1, 256, 0, stream>>>(a.pos_dev, a.B, a.S_max, a.err, a.pos_valid);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_split_kernel<true><<<grid1, kThreads, kSmemBytes, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<true><<<grid2, 128, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
+  decode_split_kernel<false><<<grid1, kThreads, kSmemBytes, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 grid2(a.Hq, a.B);
-  decode_combine_kernel<<<grid2, 128, 0, stream>>>(a);
+  decode_combine_kernel<false><<<grid2, 128, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -395,6 +395,60 @@ q3a_status q3a_decode(const q3a_bf16* q, const q3a_bf16* k_new, const q3a_bf16* 
   return from_cuda(e);
 }
 
+q3a_status q3a_decode_device_pos(const q3a_bf16* q, const q3a_bf16* k_new,
+                                 const q3a_bf16* v_new, q3a_bf16* k_cache, q3a_bf16* v_cache,
+                                 const int32_t* start_pos, const q3a_bf16* q_gamma,
+                                 const q3a_bf16* k_gamma, q3a_bf16* out, int B, int Hq, int Hkv,
+                                 int d, int S_max, double theta, float eps, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+  if (d != 128 || B < 0 || B > kDecodeMaxB || S_max <= 0 || !group_ok(Hq, Hkv))
+    return Q3A_EINVAL;
+  if (S_max > (1 << 30)) return Q3A_EINVAL;
+  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
+  if (B == 0) return Q3A_OK;
+  const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, q_gamma, k_gamma, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return Q3A_EINVAL;
+  if (!start_pos || (reinterpret_cast<uintptr_t>(start_pos) & 3u)) return Q3A_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
+  if (ws_bytes < q3a_decode_workspace_size(B, Hq, Hkv, d, S_max)) return Q3A_EINVAL;
+
+  DecodeArgs dargs;  // kernel parameters, staged on the host stack
+  DecodeArgs* da = &dargs;
+  memset(da, 0, sizeof *da);
+  const uint64_t dc[3] = {128, (uint64_t)S_max, (uint64_t)B * Hkv};
+  const uint64_t sc[2] = {256, (uint64_t)S_max * 256};
+  const uint32_t bc[3] = {64, 64, 1};
+  if (encode_tensor_map(&da->tm_kc, k_cache, 3, dc, sc, bc) != CUDA_SUCCESS ||
+      encode_tensor_map(&da->tm_vc, v_cache, 3, dc, sc, bc) != CUDA_SUCCESS)
+    return Q3A_ECUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  da->q = q;
+  da->k_new = k_new;
+  da->v_new = v_new;
+  da->q_gamma = q_gamma;
+  da->k_gamma = k_gamma;
+  da->k_cache = k_cache;
+  da->v_cache = v_cache;
+  da->partial = reinterpret_cast<float*>(ws + kHeader);
+  da->out = out;
+  da->err = reinterpret_cast<uint32_t*>(ws);
+  da->B = B;
+  da->Hq = Hq;
+  da->Hkv = Hkv;
+  da->g = Hq / Hkv;
+  da->S_max = S_max;
+  da->split_stride = decode_split_stride(S_max);
+  da->max_splits = da->split_stride;  // positions are not known here
+  da->eps = eps;
+  fill_turn_freq(theta, da->turn_freq);
+  da->pos_dev = start_pos;
+  da->pos_valid = reinterpret_cast<uint32_t*>(ws + 16);
+  // no host synchronisation and no host-side reads of device memory: the
+  // call can be captured into a CUDA graph and replayed with new positions
+  return from_cuda(launch_decode(*da, static_cast<cudaStream_t>(stream)));
+}
+
 q3a_status q3a_last_device_error(const void* workspace, void* stream) {
   if (!workspace) return Q3A_EINVAL;
   uint32_t word = 0;
@@ -402,7 +456,8 @@ q3a_status q3a_last_device_error(const void* workspace, void* stream) {
   if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return Q3A_ECUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return Q3A_ECUDA;
-  return word == 0 ? Q3A_OK : Q3A_ETIMEOUT;
+  if (word == 0) return Q3A_OK;
+  return word == kErrWordRange ? Q3A_ERANGE : Q3A_ETIMEOUT;
 }
 
 }  // extern "C"

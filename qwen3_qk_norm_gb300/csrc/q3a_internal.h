@@ -98,8 +98,16 @@ struct DecodeArgs {
   int B, Hq, Hkv, g, S_max, split_stride, max_splits;
   float eps;
   unsigned long long turn_freq[64];
-  int start_pos[kDecodeMaxB];
+  int start_pos[kDecodeMaxB];  // host positions, copied into the parameters ...
+  // ... or, when pos_dev is set, positions read on the device: a one-block
+  // check writes *pos_valid (1: every position in range) and the error word
+  // before the decode kernels run; with *pos_valid == 0 they write nothing
+  const int32_t* pos_dev;
+  uint32_t* pos_valid;
 };
+
+// error word value of a device-side position check that failed
+constexpr uint32_t kErrWordRange = 0x201;
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

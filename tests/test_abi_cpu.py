@@ -151,3 +151,23 @@ def test_chunk_null_or_misaligned_pointer(lib):
 def test_chunk_workspace_size(lib):
     assert binding.prefill_chunk_workspace_size(2, 100, 32, 8) >= 256 + 2 * 100 * 32 * 256
     assert binding.prefill_chunk_workspace_size(2, 100, 32, 8, 64) == 0
+
+
+def test_device_pos_decode_host_checks(lib):
+    """Argument errors the host can see are refused before any launch; the
+    positions themselves are on the device and are not read here."""
+    def call(**kw):
+        a = dict(B=2, Hq=32, Hkv=8, d=128, S_max=64, theta=1e6, eps=1e-6, ws=FAKE,
+                 ws_bytes=1 << 40, pos=FAKE)
+        a.update(kw)
+        return lib.q3a_decode_device_pos(FAKE, FAKE, FAKE, FAKE, FAKE, a["pos"], FAKE, FAKE, FAKE,
+                                         a["B"], a["Hq"], a["Hkv"], a["d"], a["S_max"],
+                                         a["theta"], a["eps"], a["ws"], a["ws_bytes"], None)
+    assert call(d=64) == binding.Q3A_EINVAL
+    assert call(Hq=12) == binding.Q3A_EINVAL
+    assert call(pos=0) == binding.Q3A_EINVAL
+    assert call(pos=FAKE + 2) == binding.Q3A_EINVAL
+    assert call(ws_bytes=16) == binding.Q3A_EINVAL
+    assert call(S_max=0) == binding.Q3A_EINVAL
+    assert call(B=2049) == binding.Q3A_EINVAL
+    assert call(B=0) == binding.Q3A_OK
