@@ -288,7 +288,29 @@ def bench_decode(binding, device, steps: int, warmup: int, world: int):
     status = binding.last_device_error(ws)
     if status != 0:
         raise RuntimeError(f"decode device error word: {status}")
-    return w, x["start_pos"], ms
+
+    # the same step from a captured CUDA graph (positions in device memory)
+    pos = x["start_pos"].to(device)
+    graph = torch.cuda.CUDAGraph()
+    synchronize_all(device)
+    with torch.cuda.graph(graph):
+        binding.decode_device_pos(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                                  pos, x["q_gamma"], x["k_gamma"], w.theta, w.eps, out=out,
+                                  workspace=ws)
+    for _ in range(warmup):
+        graph.replay()
+    gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    synchronize_all(device)
+    for i in range(steps):
+        gev[i][0].record(stream)
+        graph.replay()
+        gev[i][1].record(stream)
+    synchronize_all(device)
+    graph_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in gev)
+    status = binding.last_device_error(ws)
+    if status != 0:
+        raise RuntimeError(f"graph decode device error word: {status}")
+    return w, x["start_pos"], ms, graph_ms
 
 
 def bench_chunk(binding, device, steps: int, warmup: int, world: int):
@@ -401,9 +423,10 @@ def run_ours(args) -> None:
     with ClockSampler(device) as clk:
         w, x, step_ms, k1_ms, k2_ms = bench_prefill(binding, device, args.steps, args.warmup, world,
                                                     args.prefill_workload)
-        dw, start_pos, dec_ms = (None, None, None)
+        dw, start_pos, dec_ms, dec_graph_ms = (None, None, None, None)
         if not args.no_decode:
-            dw, start_pos, dec_ms = bench_decode(binding, device, args.steps, args.warmup, world)
+            dw, start_pos, dec_ms, dec_graph_ms = bench_decode(binding, device, args.steps,
+                                                               args.warmup, world)
         cw, c_start, ch_ms = (None, None, None)
         if not args.no_chunk:
             cw, c_start, ch_ms = bench_chunk(binding, device, args.steps, args.warmup, world)
@@ -479,6 +502,10 @@ def run_ours(args) -> None:
                          "peak_source": f"{peak_src} copy bandwidth",
                          "traffic": ncu_traffic("decode_split_kernel")},
             "gpu_launches": 2 * args.steps,
+            "graph": {"api": "q3a_decode_device_pos captured in a CUDA graph, replayed",
+                      "ms_per_step": round(dec_graph_ms, 4),
+                      "value": round(dbytes / (dec_graph_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+                      "gpu_launches": 3 * args.steps},
         }
     if ch_ms is not None:
         cflops = accounting.chunk_flops(c_start, cw.T, cw.Hq, cw.d)
