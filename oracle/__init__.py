@@ -1,4 +1,5 @@
-"""CPU oracle of the Qwen3 attention core (QK-Norm -> RoPE -> causal GQA).
+"""CPU oracle of the Qwen3 attention core (QK-Norm -> RoPE -> causal GQA),
+and of the gated global-attention layer of Qwen3-Next / Qwen3.5.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg are the only callers. The product library never
@@ -70,6 +71,14 @@ def _load():
             lib.q3a_oracle_prefill_chunk.argtypes = ([_u16p] * 5 + [ctypes.c_void_p] + [_u16p] * 2
                                                      + [i] * 5 + [l, d, d, _f64p, _f64p])
             lib.q3a_oracle_prefill_chunk.restype = i
+            lib.q3a_oracle_zc_rmsnorm_row.argtypes = [_u16p, _u16p, i, d, _f64p]
+            lib.q3a_oracle_partial_rope_row.argtypes = [_f64p, i, i, d, d]
+            lib.q3a_oracle_partial_rope_row.restype = i
+            lib.q3a_oracle_gated_prefill.argtypes = [_u16p] * 5 + [i] * 6 + [d, d, _f64p]
+            lib.q3a_oracle_gated_prefill.restype = i
+            lib.q3a_oracle_gated_prefill_rows.argtypes = ([_u16p] * 5 + [i] * 6 + [d, d, l]
+                                                          + [ctypes.c_void_p] * 3 + [_f64p])
+            lib.q3a_oracle_gated_prefill_rows.restype = i
             _lib = lib
     return _lib
 
@@ -203,3 +212,68 @@ def prefill_chunk(q, k, v, k_cache, v_cache, start_pos, q_gamma, k_gamma, theta:
     if rc:
         raise ValueError(f"oracle prefill_chunk failed ({rc})")
     return out, k_rows
+
+
+# ---------------------------------------------------------------------------
+# The gated global-attention layer of Qwen3-Next / Qwen3.5 (steps g1-g5 of
+# q3a_oracle.c): per-head query/gate split, zero-centred norm (1 + w), partial
+# rotary on the first d_r coordinates, causal GQA attention, sigmoid gate.
+# ---------------------------------------------------------------------------
+
+def zc_rmsnorm_row(x: torch.Tensor, w: torch.Tensor, eps: float) -> torch.Tensor:
+    """g2 on one row: x / sqrt(mean(x^2) + eps) * (1 + w), fp64."""
+    x, w = _bf16(x, "x"), _bf16(w, "w")
+    d = x.numel()
+    y = torch.empty(d, dtype=torch.float64)
+    _load().q3a_oracle_zc_rmsnorm_row(_ptr(x), _ptr(w), d, float(eps), _ptr(y))
+    return y
+
+
+def partial_rope_row(y: torch.Tensor, d_r: int, pos: float, theta: float) -> torch.Tensor:
+    """g3 on one fp64 row: rotate-half RoPE of the first d_r coordinates only."""
+    out = y.to(torch.float64).contiguous().clone()
+    rc = _load().q3a_oracle_partial_rope_row(_ptr(out), out.numel(), int(d_r), float(pos),
+                                             float(theta))
+    if rc:
+        raise ValueError(f"oracle partial_rope_row rejected d_r={d_r}")
+    return out
+
+
+def gated_prefill(qg, k, v, q_w, k_w, d_r: int, theta: float, eps: float) -> torch.Tensor:
+    """Gated causal prefill. qg [B,T,Hq,2d] (per head: query, then gate),
+    k/v [B,T,Hkv,d], q_w/k_w [d] zero-centred weights -> fp64 [B,T,Hq,d]."""
+    qg, k, v = _bf16(qg, "qg"), _bf16(k, "k"), _bf16(v, "v")
+    q_w, k_w = _bf16(q_w, "q_w"), _bf16(k_w, "k_w")
+    B, T, Hq, d2 = qg.shape
+    Hkv, d = k.shape[2], k.shape[3]
+    if d2 != 2 * d:
+        raise ValueError(f"qg last dim {d2} != 2 * {d}")
+    out = torch.empty((B, T, Hq, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_gated_prefill(_ptr(qg), _ptr(k), _ptr(v), _ptr(q_w), _ptr(k_w),
+                                          B, T, Hq, Hkv, d, int(d_r), float(theta), float(eps),
+                                          _ptr(out))
+    if rc:
+        raise ValueError(f"oracle gated_prefill failed ({rc})")
+    return out
+
+
+def gated_prefill_rows(qg, k, v, q_w, k_w, d_r: int, theta: float, eps: float,
+                       rows: torch.Tensor) -> torch.Tensor:
+    """Sampled gated prefill. rows: int32 [n, 3] of (b, t, h) -> fp64 [n, d]."""
+    qg, k, v = _bf16(qg, "qg"), _bf16(k, "k"), _bf16(v, "v")
+    q_w, k_w = _bf16(q_w, "q_w"), _bf16(k_w, "k_w")
+    B, T, Hq, d2 = qg.shape
+    Hkv, d = k.shape[2], k.shape[3]
+    if d2 != 2 * d:
+        raise ValueError(f"qg last dim {d2} != 2 * {d}")
+    rows = rows.to(torch.int32)
+    rb, rt, rh = (rows[:, c].contiguous() for c in range(3))
+    n = rows.shape[0]
+    out = torch.empty((n, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_gated_prefill_rows(_ptr(qg), _ptr(k), _ptr(v), _ptr(q_w),
+                                               _ptr(k_w), B, T, Hq, Hkv, d, int(d_r),
+                                               float(theta), float(eps), n, _ptr(rb),
+                                               _ptr(rt), _ptr(rh), _ptr(out))
+    if rc:
+        raise ValueError(f"oracle gated_prefill_rows failed ({rc})")
+    return out

@@ -400,3 +400,175 @@ int q3a_oracle_prefill_chunk(const uint16_t* q, const uint16_t* k, const uint16_
   }
   return failed ? -2 : 0;
 }
+
+/* ==========================================================================
+ * The gated global-attention layer of Qwen3-Next / Qwen3.5.
+ * Sources: "Chapter 20, Qwen3 and Qwen3.5" (book.ozine.me) §20.4 (zero-
+ * initialised norm weight used as 1 + w; W_query emitting 2*H*d values that
+ * are split into query and gate inside each head; z = Attn(Q,K,V) * sigmoid
+ * (gate); Q/K normalised per head, then rotated; partial_rotary_factor:
+ * only the first d_r coordinates rotate, with d_r as the denominator of the
+ * frequency exponent), and "14. The Qwen family" (niuwancheng.cn), the
+ * Qwen3-Next section (q_proj output doubled, half query and half gate;
+ * head_dim 256 with RoPE on 64 dims; x_hat * (1 + weight)).
+ *
+ *   g1  per head h of a token, qg[h*2d .. h*2d+d-1] is the query row and
+ *       qg[h*2d+d .. h*2d+2d-1] the gate row;
+ *   g2  zero-centred RMSNorm: y_i = x_i / sqrt(mean x^2 + eps) * (1 + w_i);
+ *   g3  rotate-half RoPE on y_0..y_{d_r-1} alone (steps 2 with d := d_r, so
+ *       w_i = theta^(-2i/d_r) and pairs (i, i + d_r/2)); y_{d_r}.. pass through;
+ *   g4  steps 3-5 (GQA map h -> h/g, causal mask, softmax of q.k/sqrt(d), P.V);
+ *   g5  z_c = o_c * sigmoid(gate_c), sigmoid(x) = 1 / (1 + exp(-x)).
+ * ========================================================================== */
+
+/* g2 on one row; y may not alias x. */
+void q3a_oracle_zc_rmsnorm_row(const uint16_t* x, const uint16_t* w, int d, double eps,
+                               double* y) {
+  double sum_sq = 0.0;
+  for (int i = 0; i < d; ++i) {
+    double xi = widen_bf16(x[i]);
+    sum_sq += xi * xi;
+  }
+  double inv_rms = 1.0 / sqrt(sum_sq / (double)d + eps);
+  for (int i = 0; i < d; ++i) y[i] = widen_bf16(x[i]) * inv_rms * (1.0 + widen_bf16(w[i]));
+}
+
+/* g3 on one fp64 row of length d, in place (d is only checked against d_r). */
+int q3a_oracle_partial_rope_row(double* y, int d, int d_r, double pos, double theta) {
+  if (d_r < 0 || (d_r & 1) || d_r > d) return -1;
+  if (d_r > 0) q3a_oracle_rope_row(y, d_r, pos, theta);
+  return 0;
+}
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+static int check_gated(int B, int T, int Hq, int Hkv, int d, int d_r) {
+  if (check_shape(B, T, Hq, Hkv, d)) return -1;
+  if (d_r < 0 || (d_r & 1) || d_r > d) return -1;
+  return 0;
+}
+
+/* The output row of query head h of token i of sequence b (g1-g5), with the
+ * keys 0..i normalised and rotated here. out[d]. */
+static int gated_row(const uint16_t* qg, const uint16_t* k, const uint16_t* v,
+                     const uint16_t* q_w, const uint16_t* k_w, int T, int Hq, int Hkv, int d,
+                     int d_r, double theta, double eps, long b, long i, long h, double* out) {
+  long kv = h / (Hq / Hkv);
+  long nk = i + 1;
+  double* keys = (double*)malloc(sizeof(double) * (size_t)nk * d);
+  double* vals = (double*)malloc(sizeof(double) * (size_t)nk * d);
+  double* scores = (double*)malloc(sizeof(double) * (size_t)nk);
+  double* qhat = (double*)malloc(sizeof(double) * d);
+  int rc = 0;
+  if (!keys || !vals || !scores || !qhat) {
+    rc = -2;
+  } else {
+    for (long j = 0; j < nk; ++j) {
+      long r = ((b * T + j) * Hkv + kv) * d;
+      q3a_oracle_zc_rmsnorm_row(k + r, k_w, d, eps, keys + j * d);
+      q3a_oracle_partial_rope_row(keys + j * d, d, d_r, (double)j, theta);
+      for (int c = 0; c < d; ++c) vals[j * d + c] = widen_bf16(v[r + c]);
+    }
+    const uint16_t* qrow = qg + ((b * T + i) * Hq + h) * 2L * d; /* g1: query half */
+    const uint16_t* grow = qrow + d;                              /* g1: gate half */
+    q3a_oracle_zc_rmsnorm_row(qrow, q_w, d, eps, qhat);
+    q3a_oracle_partial_rope_row(qhat, d, d_r, (double)i, theta);
+    attend_row(qhat, keys, vals, nk, d, scores, out);
+    for (int c = 0; c < d; ++c) out[c] *= sigmoid(widen_bf16(grow[c]));
+  }
+  free(keys);
+  free(vals);
+  free(scores);
+  free(qhat);
+  return rc;
+}
+
+/* Full gated causal prefill. qg [B,T,Hq,2d], k/v [B,T,Hkv,d] bf16, q_w/k_w [d]
+ * bf16 (zero-centred weights); out fp64 [B,T,Hq,d]. Keys are normalised and
+ * rotated once per (b, t, kv) and shared by the rows that read them. */
+int q3a_oracle_gated_prefill(const uint16_t* qg, const uint16_t* k, const uint16_t* v,
+                             const uint16_t* q_w, const uint16_t* k_w, int B, int T, int Hq,
+                             int Hkv, int d, int d_r, double theta, double eps, double* out) {
+  if (check_gated(B, T, Hq, Hkv, d, d_r) || !qg || !k || !v || !q_w || !k_w || !out) return -1;
+  int g = Hq / Hkv;
+  long krows = (long)B * T * Hkv;
+  double* khat = (double*)malloc(sizeof(double) * (size_t)(krows > 0 ? krows : 1) * d);
+  double* vals = (double*)malloc(sizeof(double) * (size_t)(krows > 0 ? krows : 1) * d);
+  if (!khat || !vals) {
+    free(khat);
+    free(vals);
+    return -2;
+  }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(OMP_THREADS)
+#endif
+  for (long r = 0; r < krows; ++r) {
+    long b = r / ((long)T * Hkv), t = (r / Hkv) % T, kv = r % Hkv;
+    double* kd = khat + (((b * Hkv + kv) * T) + t) * d;
+    double* vd = vals + (((b * Hkv + kv) * T) + t) * d;
+    q3a_oracle_zc_rmsnorm_row(k + r * d, k_w, d, eps, kd);
+    q3a_oracle_partial_rope_row(kd, d, d_r, (double)t, theta);
+    for (int c = 0; c < d; ++c) vd[c] = widen_bf16(v[r * d + c]);
+  }
+  long qrows = (long)B * T * Hq;
+  int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(OMP_THREADS)
+#endif
+  {
+    double* qhat = (double*)malloc(sizeof(double) * d);
+    double* scores = (double*)malloc(sizeof(double) * (T > 0 ? T : 1));
+    if (!qhat || !scores) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      failed = 1;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 16)
+#endif
+      for (long r = 0; r < qrows; ++r) {
+        long b = r / ((long)T * Hq), i = (r / Hq) % T, h = r % Hq;
+        long kv = h / g;
+        const uint16_t* qrow = qg + r * 2L * d; /* g1: query half, then gate half */
+        const uint16_t* grow = qrow + d;
+        q3a_oracle_zc_rmsnorm_row(qrow, q_w, d, eps, qhat);
+        q3a_oracle_partial_rope_row(qhat, d, d_r, (double)i, theta);
+        attend_row(qhat, khat + (b * Hkv + kv) * (long)T * d,
+                   vals + (b * Hkv + kv) * (long)T * d, i + 1, d, scores, out + r * d);
+        for (int c = 0; c < d; ++c) out[r * d + c] *= sigmoid(widen_bf16(grow[c]));
+      }
+    }
+    free(qhat);
+    free(scores);
+  }
+  free(khat);
+  free(vals);
+  return failed ? -2 : 0;
+}
+
+/* Sampled gated prefill: n rows (rb[s], rt[s], rh[s]); out fp64 [n, d]. */
+int q3a_oracle_gated_prefill_rows(const uint16_t* qg, const uint16_t* k, const uint16_t* v,
+                                  const uint16_t* q_w, const uint16_t* k_w, int B, int T,
+                                  int Hq, int Hkv, int d, int d_r, double theta, double eps,
+                                  long n, const int32_t* rb, const int32_t* rt,
+                                  const int32_t* rh, double* out) {
+  if (check_gated(B, T, Hq, Hkv, d, d_r) || n < 0 || !out) return -1;
+  for (long s = 0; s < n; ++s)
+    if (rb[s] < 0 || rb[s] >= B || rt[s] < 0 || rt[s] >= T || rh[s] < 0 || rh[s] >= Hq)
+      return -1;
+  int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(OMP_THREADS)
+#endif
+  for (long s = 0; s < n; ++s) {
+    if (gated_row(qg, k, v, q_w, k_w, T, Hq, Hkv, d, d_r, theta, eps, rb[s], rt[s], rh[s],
+                  out + s * d)) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      failed = 1;
+    }
+  }
+  return failed ? -2 : 0;
+}

@@ -19,6 +19,11 @@ Recipe (all draws from a ``torch.Generator`` seeded with the workload's seed):
   chunk:   the prefill draws for whole prompts of sp_lo + T tokens (seeded as
            above); the first sp_lo tokens go into the caches through an earlier
            chunk, the last T are the timed chunk. Caches start as NaN.
+  gated:   (Qwen3-Next / Qwen3.5 global attention) the query projection
+           QG [B,T,Hq,2d] (per head: query, then gate), K [B,T,Hkv,d],
+           V [B,T,Hkv,d] ~ N(0,1) in fp32, in that order; then the zero-centred
+           norm weights w_q, w_k ~ U(-0.5, 0.5) [d] (scales 1 + w in [0.5, 1.5],
+           the range of the gammas above); rounded to bf16 at the end.
 
 Large workloads are drawn on the GPU (``device="cuda"``) with torch's CUDA
 generator; small ones on the CPU. Either way the draws are deterministic for a
@@ -34,7 +39,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "prefill", "decode" or "chunk"
+    kind: str  # "prefill", "decode", "chunk" or "gated"
     B: int
     Hq: int
     Hkv: int
@@ -48,6 +53,7 @@ class Workload:
     seed: int = 0
     outlier_frac: float = 0.0
     outlier_scale: float = 1.0
+    d_r: int = 0        # gated: rotated leading coordinates per head
     note: str = field(default="", compare=False)
 
 
@@ -71,6 +77,15 @@ WORKLOADS = {
                       "prompts whose first 3072 tokens are already in the cache"),
         Workload("qwen3-30b-a3b-prefill-b1-t32768", "prefill", B=1, T=32768, Hq=32, Hkv=4,
                  theta=1e7, seed=4, note="Qwen3-30B-A3B-shaped long-context prefill"),
+        Workload("qwen3.5-0.8b-gated-b1-t300", "gated", B=1, T=300, Hq=8, Hkv=2, d=256,
+                 d_r=64, theta=1e7, seed=6,
+                 note="Qwen3.5-0.8B-shaped gated global attention, small (full parity)"),
+        Workload("qwen3-next-80b-gated-b4-t4096", "gated", B=4, T=4096, Hq=16, Hkv=2, d=256,
+                 d_r=64, theta=1e7, seed=7,
+                 note="Qwen3-Next-80B-A3B-shaped gated global attention prefill"),
+        Workload("qwen3.5-397b-gated-b1-t8192", "gated", B=1, T=8192, Hq=32, Hkv=2, d=256,
+                 d_r=64, theta=1e7, seed=8,
+                 note="Qwen3.5-397B-A17B-shaped gated global attention prefill (g = 16)"),
     ]
 }
 
@@ -131,7 +146,24 @@ def decode_inputs(B: int, Hq: int, Hkv: int, S_max: int, sp_lo: int, sp_hi: int,
                 k_gamma=k_gamma.to(bf))
 
 
+def gated_inputs(B: int, T: int, Hq: int, Hkv: int, d: int = 256, seed: int = 0,
+                 device="cpu") -> dict:
+    """QG (query|gate per head), K, V, w_q, w_k as bf16 tensors on ``device``."""
+    dev = torch.device(device)
+    g = _gen(dev, seed)
+    f32 = torch.float32
+    qg = torch.randn((B, T, Hq, 2 * d), generator=g, device=dev, dtype=f32)
+    k = torch.randn((B, T, Hkv, d), generator=g, device=dev, dtype=f32)
+    v = torch.randn((B, T, Hkv, d), generator=g, device=dev, dtype=f32)
+    q_w = torch.rand((d,), generator=g, device=dev, dtype=f32) - 0.5
+    k_w = torch.rand((d,), generator=g, device=dev, dtype=f32) - 0.5
+    bf = torch.bfloat16
+    return dict(qg=qg.to(bf), k=k.to(bf), v=v.to(bf), q_w=q_w.to(bf), k_w=k_w.to(bf))
+
+
 def workload_inputs(w: Workload, device="cpu") -> dict:
+    if w.kind == "gated":
+        return gated_inputs(w.B, w.T, w.Hq, w.Hkv, w.d, w.seed, device=device)
     if w.kind == "chunk":  # whole prompts; the caller splits them
         return prefill_inputs(w.B, w.sp_lo + w.T, w.Hq, w.Hkv, w.d, w.seed, device=device)
     if w.kind == "prefill":
