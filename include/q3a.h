@@ -273,6 +273,51 @@ q3a_status q3a_decode_noalloc(const q3a_bf16* q, const q3a_bf16* k_new, const q3
                               double theta, float eps, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * q3a_gated_prefill — causal prefill of the gated global-attention layer of
+ * Qwen3-Next / Qwen3.5 ("Chapter 20, Qwen3 and Qwen3.5" §20.4; "14. The Qwen
+ * family", Qwen3-Next section).
+ *
+ *   qg      [B, T, Hq, 2d] bf16, the query projection viewed per head: for head
+ *           h, qg[b, t, h, 0 .. d-1] is the query and qg[b, t, h, d .. 2d-1]
+ *           the output gate (the split is inside each head's 2d block).
+ *   k, v    [B, T, Hkv, d] bf16 projected keys / values.
+ *   q_w, k_w [d] bf16 zero-centred norm weights: the norm scales by 1 + w.
+ *   out     [B, T, Hq, d] bf16, z = sigmoid(gate) * softmax(q k^T / sqrt(d)) v
+ *           (the input of the output projection), one rounding.
+ *   Per head, Q and K are RMS-normalised (fp32) and scaled by 1 + w, then the
+ *   first d_rot coordinates are rotated (rotate-half pairs (i, i + d_rot/2),
+ *   frequencies theta^(-2i/d_rot), positions 0..T-1); the others pass through.
+ *   d must be 256; d_rot a multiple of 16 in 0..256 (Qwen3-Next / Qwen3.5: 64).
+ *   Hq / Hkv in {1, 2, 4, 8, 16}; Hq + Hkv <= 192; B*T*Hq <= 2^31 - 1.
+ *   workspace: device scratch of at least q3a_gated_prefill_workspace_size()
+ *           bytes, 256-byte aligned, caller-owned, not shared by concurrent
+ *           calls; it holds the normalised+rotated Q and K and the error word.
+ *   B == 0 or T == 0: returns Q3A_OK and launches nothing. Every argument is
+ *   checked before anything is launched.
+ * q3a_gated_prefill_prologue / q3a_gated_prefill_attention — the two kernels
+ *   of q3a_gated_prefill separately (same arguments and workspace; the
+ *   attention half reads what the last prologue of the same shapes wrote, and
+ *   reads the gate from qg).
+ * ------------------------------------------------------------------------- */
+size_t q3a_gated_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d);
+
+q3a_status q3a_gated_prefill(const q3a_bf16* qg, const q3a_bf16* k, const q3a_bf16* v,
+                             const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out,
+                             int B, int T, int Hq, int Hkv, int d, int d_rot,
+                             double theta, float eps,
+                             void* workspace, size_t ws_bytes, void* stream);
+
+q3a_status q3a_gated_prefill_prologue(const q3a_bf16* qg, const q3a_bf16* k,
+                                      const q3a_bf16* q_w, const q3a_bf16* k_w,
+                                      int B, int T, int Hq, int Hkv, int d, int d_rot,
+                                      double theta, float eps,
+                                      void* workspace, size_t ws_bytes, void* stream);
+
+q3a_status q3a_gated_prefill_attention(const q3a_bf16* qg, const q3a_bf16* v, q3a_bf16* out,
+                                       int B, int T, int Hq, int Hkv, int d,
+                                       void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_last_device_error — reads, synchronously on `stream`, the error word
  * that the kernels of the last call which used `workspace` left in its first
  * bytes (prefill and decode workspaces both keep it at offset 0).

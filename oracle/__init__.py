@@ -79,6 +79,9 @@ def _load():
             lib.q3a_oracle_gated_prefill_rows.argtypes = ([_u16p] * 5 + [i] * 6 + [d, d, l]
                                                           + [ctypes.c_void_p] * 3 + [_f64p])
             lib.q3a_oracle_gated_prefill_rows.restype = i
+            lib.q3a_oracle_gated_qknorm_rope.argtypes = [_u16p, l, _u16p, i, i, i, i, i, l, d,
+                                                         d, _f64p]
+            lib.q3a_oracle_gated_qknorm_rope.restype = i
             _lib = lib
     return _lib
 
@@ -276,4 +279,19 @@ def gated_prefill_rows(qg, k, v, q_w, k_w, d_r: int, theta: float, eps: float,
                                                _ptr(rt), _ptr(rh), _ptr(out))
     if rc:
         raise ValueError(f"oracle gated_prefill_rows failed ({rc})")
+    return out
+
+
+def gated_qknorm_rope(x, w, d: int, d_r: int, theta: float, eps: float,
+                      pos0: int = 0) -> torch.Tensor:
+    """g2 then g3 on the first d elements of every row of x [B, T, H, S] (S = 2d
+    for the query halves of the query/gate projection, d for keys); row
+    (b, t, h) at position pos0 + t. -> fp64 [B, T, H, d]."""
+    x, w = _bf16(x, "x"), _bf16(w, "w")
+    B, T, H, S = x.shape
+    out = torch.empty((B, T, H, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_gated_qknorm_rope(_ptr(x), S, _ptr(w), B, T, H, d, int(d_r),
+                                              int(pos0), float(theta), float(eps), _ptr(out))
+    if rc:
+        raise ValueError(f"oracle gated_qknorm_rope rejected its arguments ({rc})")
     return out

@@ -572,3 +572,25 @@ int q3a_oracle_gated_prefill_rows(const uint16_t* qg, const uint16_t* k, const u
   }
   return failed ? -2 : 0;
 }
+
+/* g2 then g3 on every row of a [B, T, H, stride] bf16 array (the first d
+ * elements of each row are the head row; stride = 2d for the query halves of
+ * the query/gate projection, d for keys). Row (b, t, h) at position pos0 + t.
+ * out fp64 [B, T, H, d]. */
+int q3a_oracle_gated_qknorm_rope(const uint16_t* x, long stride, const uint16_t* w, int B, int T,
+                                 int H, int d, int d_r, long pos0, double theta, double eps,
+                                 double* out) {
+  if (B < 0 || T < 0 || H < 0 || d <= 0 || stride < d || d_r < 0 || (d_r & 1) || d_r > d ||
+      !x || !w || !out)
+    return -1;
+  long rows = (long)B * T * H;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(OMP_THREADS)
+#endif
+  for (long r = 0; r < rows; ++r) {
+    long t = (r / H) % T;
+    q3a_oracle_zc_rmsnorm_row(x + r * stride, w, d, eps, out + r * d);
+    q3a_oracle_partial_rope_row(out + r * d, d, d_r, (double)(pos0 + t), theta);
+  }
+  return 0;
+}

@@ -22,7 +22,8 @@ EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size"
             "q3a_prefill_prologue", "q3a_prefill_attention", "q3a_prefill_chunk_workspace_size",
             "q3a_prefill_chunk", "q3a_decode_workspace_size",
             "q3a_decode", "q3a_decode_device_pos", "q3a_decode_noalloc",
-            "q3a_last_device_error"]
+            "q3a_last_device_error", "q3a_gated_prefill_workspace_size", "q3a_gated_prefill",
+            "q3a_gated_prefill_prologue", "q3a_gated_prefill_attention"]
 
 _lock = threading.Lock()
 _lib = None
@@ -79,6 +80,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_decode_noalloc.restype = i
         lib.q3a_last_device_error.argtypes = [vp, vp]
         lib.q3a_last_device_error.restype = i
+        lib.q3a_gated_prefill_workspace_size.argtypes = [i] * 5
+        lib.q3a_gated_prefill_workspace_size.restype = sz
+        lib.q3a_gated_prefill.argtypes = [vp] * 6 + [i] * 6 + [d, f, vp, sz, vp]
+        lib.q3a_gated_prefill.restype = i
+        lib.q3a_gated_prefill_prologue.argtypes = [vp] * 4 + [i] * 6 + [d, f, vp, sz, vp]
+        lib.q3a_gated_prefill_prologue.restype = i
+        lib.q3a_gated_prefill_attention.argtypes = [vp] * 3 + [i] * 5 + [vp, sz, vp]
+        lib.q3a_gated_prefill_attention.restype = i
         _lib = lib
         return lib
 
@@ -296,3 +305,74 @@ def decode_device_pos(q, k_new, v_new, k_cache, v_cache, start_pos, q_gamma, k_g
 def last_device_error(workspace: torch.Tensor) -> int:
     """Status from the error word a call left in its workspace (synchronises)."""
     return int(load().q3a_last_device_error(workspace.data_ptr(), _stream(workspace.device)))
+
+
+# ---------------------------------------------------------------------------
+# gated global attention of Qwen3-Next / Qwen3.5 (include/q3a.h q3a_gated_*)
+# ---------------------------------------------------------------------------
+
+def gated_prefill_workspace_size(B: int, T: int, Hq: int, Hkv: int, d: int = 256) -> int:
+    return int(load().q3a_gated_prefill_workspace_size(B, T, Hq, Hkv, d))
+
+
+def _gated_shapes(qg, k):
+    B, T, Hq, d2 = qg.shape
+    d = d2 // 2
+    Hkv = k.shape[2]
+    return B, T, Hq, Hkv, d
+
+
+def gated_prefill(qg, k, v, q_w, k_w, d_rot: int, theta: float, eps: float, out=None,
+                  workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Gated causal prefill: qg [B,T,Hq,512] (per head: query, then gate),
+    k/v [B,T,Hkv,256], q_w/k_w [256] zero-centred weights -> out [B,T,Hq,256]."""
+    B, T, Hq, Hkv, d = _gated_shapes(qg, k)
+    _check(qg, "qg")
+    _check(k, "k", (B, T, Hkv, d))
+    _check(v, "v", (B, T, Hkv, d))
+    _check(q_w, "q_w", (d,))
+    _check(k_w, "k_w", (d,))
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=torch.bfloat16, device=qg.device)
+    _check(out, "out", (B, T, Hq, d))
+    need = gated_prefill_workspace_size(B, T, Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=qg.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_gated_prefill(qg.data_ptr(), k.data_ptr(), v.data_ptr(), q_w.data_ptr(),
+                                  k_w.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, d, int(d_rot),
+                                  float(theta), float(eps), workspace.data_ptr(),
+                                  workspace.numel(), _stream(qg.device))
+    _raise(st, "q3a_gated_prefill")
+    return out
+
+
+def gated_prefill_prologue(qg, k, q_w, k_w, d_rot: int, theta: float, eps: float,
+                           workspace: torch.Tensor) -> None:
+    """The norm + partial-RoPE kernel of gated_prefill into ``workspace``."""
+    B, T, Hq, Hkv, d = _gated_shapes(qg, k)
+    _check(qg, "qg")
+    _check(k, "k", (B, T, Hkv, d))
+    _check(q_w, "q_w", (d,))
+    _check(k_w, "k_w", (d,))
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_gated_prefill_prologue(qg.data_ptr(), k.data_ptr(), q_w.data_ptr(),
+                                           k_w.data_ptr(), B, T, Hq, Hkv, d, int(d_rot),
+                                           float(theta), float(eps), workspace.data_ptr(),
+                                           workspace.numel(), _stream(qg.device))
+    _raise(st, "q3a_gated_prefill_prologue")
+
+
+def gated_prefill_attention(qg, v, out, workspace: torch.Tensor) -> torch.Tensor:
+    """The gated attention kernel of gated_prefill, from ``workspace``."""
+    B, T, Hq, d2 = qg.shape
+    Hkv, d = v.shape[2], v.shape[3]
+    _check(qg, "qg")
+    _check(v, "v", (B, T, Hkv, d))
+    _check(out, "out", (B, T, Hq, d))
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_gated_prefill_attention(qg.data_ptr(), v.data_ptr(), out.data_ptr(), B, T,
+                                            Hq, Hkv, d, workspace.data_ptr(), workspace.numel(),
+                                            _stream(v.device))
+    _raise(st, "q3a_gated_prefill_attention")
+    return out

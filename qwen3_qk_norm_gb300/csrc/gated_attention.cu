@@ -1,0 +1,430 @@
+// gated_attention.cu — K6, causal grouped-query attention with the sigmoid
+// output gate of the Qwen3-Next / Qwen3.5 global-attention layer (head_dim
+// 256), on tcgen05.
+//
+// For every query row (b, i, h), with the normalised, partially rotated qhat
+// and keys khat_j of group h / g:
+//   z = sigmoid(gate[b, i, h, :]) * sum_{j <= i} softmax_j(qhat . khat_j / 16) v_j
+// ("Chapter 20, Qwen3 and Qwen3.5" §20.4: the attention output is multiplied
+// elementwise by the sigmoid of the gate half of the query projection before
+// the output projection; "14. The Qwen family", Qwen3-Next section.)
+//
+// Tiling. A CTA owns one M tile of 128 query rows: the g heads of one KV
+// group for 128/g consecutive tokens, packed row r = (token r/g, head
+// kv*g + r%g) by a 4-D TMA box, so every K/V byte a CTA loads serves 128
+// query rows. With d = 256 a 128-row Q tile is 64 KB of shared memory and its
+// fp32 O tile 256 TMEM columns, so one Q tile per CTA is what fits; KV tiles
+// are 64 keys, in 8 KB blocks (64 rows x 64 dims) through an 18-block ring,
+// so that two KV tiles ahead of the MMAs are in flight.
+//
+// Roles (640 threads):
+//   WG 0..3  softmax + epilogue. Warp w serves TMEM lanes 32(w%4).. (its rows)
+//            and the key quarter c = w/4 of every S tile (16 keys), and O
+//            columns 64c..64c+63 in the epilogue;
+//   warp 16  TMA producer (Q once, then K_0, K_1, V_0, K_2, V_1, ... in the
+//            order the MMAs consume them);
+//   warp 17  MMA issuer (one thread).
+// TMEM: S0 | S1 (64 fp32 columns each, double-buffered) ... O (256 columns at
+// 256). A softmax thread writes its 16 probabilities as 8 bf16-pair columns
+// over the first half of its own S columns; PV reads them from there
+// (tcgen05.mma with A in tensor memory). MMA stream: S_0, S_1, then per KV tile
+// j: PV_j, S_{j+2} — the tensor core computes the next scores while the
+// softmax works on S_j, and S_{j+2} overwrites S_j/P_j only after PV_j has
+// read it (one thread's tcgen05.mma execute in issue order).
+// The commit that marks S_j complete also covers every earlier MMA (K_j and
+// V_{j-2} are no longer read), so one softmax thread hands those ring blocks
+// back to the producer when it sees S_j.
+//
+// Softmax: the fixed shift of the Qwen3 kernel applies (the zero-centred norm
+// bounds |qhat| by 16 max|1 + w_q| and |khat| by 16 max|1 + w_k|; the
+// prologue writes the bound); above its limit, an online max exchanged
+// between the four key quarters of a row through shared memory, with O
+// rescaled in TMEM after the previous PV has completed.
+//
+// Every mbarrier wait is bounded; a timeout sets the error word, all roles
+// unwind, in-flight copies and MMAs are drained and TMEM is freed.
+#include "q3a_device.cuh"
+#include "q3a_internal.h"
+
+namespace q3a {
+
+namespace {
+
+constexpr int BM = 128;  // query rows per CTA
+constexpr int BN = 64;   // keys per KV tile
+constexpr int D = kGatedD;
+constexpr int kSoftmaxWGs = 4;
+constexpr int kThreads = (kSoftmaxWGs + 1) * 128;
+constexpr int kSlots = 18;            // ring blocks
+constexpr uint32_t kQBlock = 16384;   // 128 rows x 128 bytes (64 dims of the Q tile)
+constexpr uint32_t kBlock = 8192;     // 64 rows x 128 bytes (64 dims of a K or V tile)
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_RING = OFF_Q + 4 * kQBlock;
+constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kBlock;
+// tile maxima [2 parities][4 quarters][128] fp32, then partial sums [4][128]
+constexpr uint32_t OFF_XCHG = OFF_BAR + 512;
+constexpr uint32_t kSmemBytes = OFF_XCHG + (2 * 4 * 128 + 4 * 128) * 4 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 256;
+constexpr float kScaleLog2 = 0.09016844005556021f;  // log2(e) / sqrt(256)
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kFixedMaxLimit = 60.0f;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t slot_full[kSlots], slot_empty[kSlots];
+  uint64_t s_full[2], p_full[2];
+  uint64_t pv_done;    // fallback path: PV_j complete (one phase per KV tile)
+  uint64_t xmax_full;  // fallback path: all four quarters posted their tile max
+  uint64_t o_final;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 512, "barrier block");
+
+// Blocks are consumed (and loaded) in the order K_0, K_1, V_0, K_2, V_1, ...;
+// block n of that sequence sits in ring slot n % kSlots.
+__device__ __forceinline__ uint32_t slot_of(uint32_t n) { return n % kSlots; }
+__device__ __forceinline__ uint32_t use_of(uint32_t n) { return (n / kSlots) & 1u; }
+
+// S = Q K_j^T: 16 steps of 16 dims. Q block c = dims 64c..64c+63 (16 KB
+// apart); K block c of the tile is ring block first + c.
+__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64_t ring_k,
+                                        uint32_t first) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) {
+    const int c = kk >> 2;
+    const uint64_t a = q_desc + (uint64_t)((c * kQBlock + (kk & 3) * 32) >> 4);
+    const uint64_t b =
+        ring_k + (uint64_t)((slot_of(first + c) * kBlock + (kk & 3) * 32) >> 4);
+    if (kk == 0)
+      mma_ss<0>(tmem_s, a, b, idesc);
+    else
+      mma_ss<1>(tmem_s, a, b, idesc);
+  }
+}
+
+// O += P_j V_j: 4 steps of 16 keys (P columns 16kk.. of the S buffer, written
+// by key quarter kk); each step is four N = 64 MMAs, one per 64-dim V block
+// (MN-major, 8-key groups 1 KB apart, 16 keys = 2 KB per step).
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t ring_v,
+                                         uint32_t first, bool accumulate_first) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint64_t b = ring_v + (uint64_t)((slot_of(first + c) * kBlock + kk * 2048) >> 4);
+      mma_bf16_ts(tmem_o + 64 * c, tmem_p + 16 * kk, b, idesc,
+                  (accumulate_first || kk > 0) ? 1u : 0u);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gated_attention_kernel(const __grid_constant__ GatedAttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  float* xchg = reinterpret_cast<float*>(smem + OFF_XCHG);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: longest CTAs first ---------------------------------------
+  const int bk_count = a.B * a.Hkv;
+  const int mt = a.n_mtiles - 1 - (int)(blockIdx.x / bk_count);
+  const int bk = (int)(blockIdx.x % bk_count);
+  const int b = bk / a.Hkv, kv = bk % a.Hkv;
+  const int g = a.g;
+  const int t0 = mt * (BM / g);
+  const int t_last = min(t0 + BM / g, a.T) - 1;
+  const int n_tiles = t_last / BN + 1;
+  const float bound = *a.logit_bound;
+  const bool fixed_max = bound >= 0.f && bound <= kFixedMaxLimit;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bars->slot_full[s], 1);
+      mbar_init(&bars->slot_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], kSoftmaxWGs * 128);
+    }
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->xmax_full, kSoftmaxWGs * 128);
+    mbar_init(&bars->o_final, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc<kTmemCols>(&bars->tmem_base);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort = &bars->abort_flag;
+
+  if (warp >= kSoftmaxWGs * 4) {
+    if (warp == kSoftmaxWGs * 4 && lane == 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
+      mbar_arrive_expect_tx(&bars->q_full, 4 * kQBlock);
+      for (int c = 0; c < 4; ++c)
+        tma_load_4d(smem + OFF_Q + c * kQBlock, &a.tm_q, &bars->q_full, 64 * c, kv * g, t0, b);
+      uint32_t n = 0;  // blocks issued
+      bool ok = true;
+      auto load_tile = [&](bool is_k, int j) {
+        for (int c = 0; c < 4 && ok; ++c) {
+          const uint32_t s = slot_of(n);
+          if (!mbar_wait(&bars->slot_empty[s], use_of(n) ^ 1u, a.err, kDevTimeoutTma, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->slot_full[s], kBlock);
+          uint8_t* dst = smem + OFF_RING + s * kBlock;
+          if (is_k)
+            tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 64 * c, j * BN, b * a.Hkv + kv);
+          else
+            tma_load_4d(dst, &a.tm_v, &bars->slot_full[s], 64 * c, kv, j * BN, b);
+          ++n;
+        }
+      };
+      load_tile(true, 0);
+      if (n_tiles > 1) load_tile(true, 1);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        load_tile(false, j);
+        if (j + 2 < n_tiles) load_tile(true, j + 2);
+      }
+      if (*abort) {
+        // let every copy that was issued land before the CTA goes away
+        mbar_wait(&bars->q_full, 0, nullptr, 0, nullptr);
+        for (uint32_t i = n > (uint32_t)kSlots ? n - kSlots : 0u; i < n; ++i)
+          mbar_wait(&bars->slot_full[slot_of(i)], use_of(i), nullptr, 0, nullptr);
+      }
+    } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t q_addr = smem_u32(smem + OFF_Q);
+      const uint32_t ring = smem_u32(smem + OFF_RING);
+      const uint64_t q_desc = smem_desc_sw128(q_addr, 16, 1024);
+      const uint64_t ring_k = smem_desc_sw128(ring, 16, 1024);     // K-major K blocks
+      const uint64_t ring_v = smem_desc_sw128(ring, kBlock, 1024);  // MN-major V blocks
+      auto wait_tile = [&](uint32_t first) {
+        for (uint32_t c = 0; c < 4; ++c)
+          if (!mbar_poll(&bars->slot_full[slot_of(first + c)], use_of(first + c), a.err,
+                         kDevTimeoutMma, abort))
+            return false;
+        return true;
+      };
+      uint32_t n = 0;  // blocks consumed
+      bool ok = mbar_poll(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) && wait_tile(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(tmem, q_desc, ring_k, 0);
+        mma_commit(&bars->s_full[0]);
+        n = 4;
+      }
+      if (ok && n_tiles > 1) {
+        ok = wait_tile(4);
+        if (ok) {
+          tc_fence_after();
+          issue_s(tmem + BN, q_desc, ring_k, 4);
+          mma_commit(&bars->s_full[1]);
+          n = 8;
+        }
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        ok = mbar_poll(&bars->p_full[j & 1], (j >> 1) & 1, a.err, kDevTimeoutMma, abort) &&
+             wait_tile(n);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(tmem + kTmemO, tmem + (j & 1) * BN, ring_v, n, j > 0);
+        n += 4;
+        if (!fixed_max) mma_commit(&bars->pv_done);
+        if (j + 2 < n_tiles) {
+          ok = wait_tile(n);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(tmem + (j & 1) * BN, q_desc, ring_k, n);
+          n += 4;
+          mma_commit(&bars->s_full[j & 1]);
+        }
+      }
+      if (ok) mma_commit(&bars->o_final);
+      // drain: every MMA issued above has completed once this phase completes
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, nullptr, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int lq = warp & 3;   // TMEM lane quarter: rows 32 lq ..
+    const int cq = warp >> 2;  // key quarter of each S tile; O columns 64 cq ..
+    const int r = lq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(lq * 32) << 16;
+    const int tok = t0 + r / g;
+    const int h = kv * g + (r % g);
+    float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    uint32_t released = 0;  // ring blocks handed back (thread 0)
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = __all_sync(kFull, mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, a.err,
+                                       kDevTimeoutSoftmax, abort));
+      if (!ok) break;
+      // S_j is complete and so is every earlier MMA: K_0..K_j and V_0..V_{j-2}
+      // (blocks 0 .. 8j-1; 0..3 for j = 0) are no longer read
+      if (threadIdx.x == 0) {
+        const uint32_t upto = j == 0 ? 4u : 8u * (uint32_t)j;
+        for (; released < upto; ++released) mbar_arrive(&bars->slot_empty[slot_of(released)]);
+      }
+      tc_fence_after();
+      const uint32_t tmem_s = tmem + (j & 1) * BN + cq * 16 + lane_off;
+      uint32_t sr[16];
+      tmem_ld16_wait(tmem_s, sr);
+      float s[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s[e] = __uint_as_float(sr[e]);
+      const int key0 = j * BN + cq * 16;
+      if (key0 + 15 > tok) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (key0 + e > tok) s[e] = -INFINITY;
+      }
+      bool move = false;
+      float alpha = 1.0f;
+      if (!fixed_max) {
+        float mx = s[0];
+#pragma unroll
+        for (int e = 1; e < 16; ++e) mx = fmaxf(mx, s[e]);
+        float* xm = xchg + (j & 1) * 4 * 128;  // [quarter][128]
+        xm[cq * 128 + r] = mx;
+        mbar_arrive(&bars->xmax_full);
+        ok = __all_sync(kFull, mbar_wait(&bars->xmax_full, j & 1, a.err, kDevTimeoutSoftmax,
+                                         abort));
+        if (!ok) break;
+        const float mrow = fmaxf(fmaxf(xm[r], xm[128 + r]), fmaxf(xm[256 + r], xm[384 + r]));
+        const float m_tile = mrow * kScaleLog2;
+        move = m_tile > m + kRescaleThreshold;
+        const float m_new = move ? m_tile : m;
+        alpha = move ? ex2(m - m_new) : 1.0f;
+        m = m_new;
+        l *= alpha;
+      }
+      // p = 2^(s * scale - m), two at a time on the f32x2 pipes
+      const uint64_t scale2 = f2_pack(kScaleLog2, kScaleLog2);
+      const uint64_t negm2 = f2_pack(-m, -m);
+      uint64_t sum2 = f2_pack(0.f, 0.f);
+      uint32_t pw[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint64_t x = f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        sum2 = f2_add(sum2, f2_pack(p0, p1));
+        pw[e] = pack_bf16x2(p0, p1);
+      }
+      tmem_st8_wait(tmem_s, pw);  // P over the first 8 of this thread's S columns
+      if (!fixed_max && j > 0 && __any_sync(kFull, move)) {
+        // rescale this thread's O columns once PV_{j-1} has completed, before
+        // PV_j adds terms relative to the new max
+        ok = __all_sync(kFull, mbar_wait(&bars->pv_done, (j - 1) & 1, a.err, kDevTimeoutSoftmax,
+                                         abort));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o[32];
+          const uint32_t to = tmem + kTmemO + cq * 64 + c * 32 + lane_off;
+          tmem_ld32_wait(to, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32_wait(to, o);
+        }
+      }
+      float s0, s1;
+      f2_unpack(sum2, s0, s1);
+      l += s0 + s1;
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[j & 1]);
+    }
+    // ---- epilogue: the row's four partial sums, then O / l * sigmoid(gate)
+    ok = __all_sync(kFull, ok && !*abort);
+    // every thread of the four warpgroups reaches this barrier exactly once
+    float* lsum = xchg + 2 * 4 * 128;  // [quarter][128]
+    lsum[cq * 128 + r] = l;
+    named_barrier_sync(1, kSoftmaxWGs * 128);
+    if (ok) {
+      l = (lsum[r] + lsum[128 + r]) + (lsum[256 + r] + lsum[384 + r]);
+      ok = __all_sync(kFull, mbar_wait(&bars->o_final, 0, a.err, kDevTimeoutEpilogue, abort));
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const bool store = tok < a.T;  // rows past the sequence are padding
+      const long long row = ((long long)b * a.T + tok) * a.Hq + h;
+      const uint16_t* grow = a.qg + row * (2 * D) + D + cq * 64;
+      uint16_t* orow = a.out + row * D + cq * 64;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(tmem + kTmemO + cq * 64 + c * 32 + lane_off, o);
+        if (store) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 gv = reinterpret_cast<const uint4*>(grow + c * 32)[q4];
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            uint32_t zw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              // sigmoid(x) = 1 / (1 + 2^(-x log2 e))
+              const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
+              const float sg0 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g0));
+              const float sg1 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g1));
+              zw[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l * sg0,
+                                  __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l * sg1);
+            }
+            reinterpret_cast<uint4*>(orow + c * 32)[q4] = make_uint4(zw[0], zw[1], zw[2], zw[3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc<kTmemCols>(tmem);
+  }
+}
+
+}  // namespace
+
+int gated_tokens_per_cta(int g) { return BM / g; }
+
+cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream) {
+  static unsigned long long done_mask = 0;  // per-device dynamic smem opt-in
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(done_mask & (1ull << dev))) {
+    e = cudaFuncSetAttribute(gated_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) done_mask |= 1ull << dev;
+  }
+  const long long grid = (long long)a.n_mtiles * a.B * a.Hkv;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  gated_attention_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace q3a

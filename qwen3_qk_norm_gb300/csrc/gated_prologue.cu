@@ -1,0 +1,206 @@
+// gated_prologue.cu — K5, the prologue of the gated global-attention layer of
+// Qwen3-Next / Qwen3.5 (head_dim 256).
+//
+// Per head row x (d = 256 bf16):
+//   y_i = x_i * rsqrt(mean(x^2) + eps) * (1 + w_i)              (fp32)
+//   for i < d_r/2, with a_i = p * theta^(-2i/d_r):
+//     y'_i         = y_i cos a_i - y_{i+d_r/2} sin a_i
+//     y'_{i+d_r/2} = y_{i+d_r/2} cos a_i + y_i sin a_i
+//   coordinates d_r .. 255 pass through; one rounding to bf16 at the end.
+// Sources: "Chapter 20, Qwen3 and Qwen3.5" §20.4 (norm weight initialised to
+// 0 and applied as 1 + w; per-head norm of Q and K, then RoPE; partial rotary
+// over the first d_r coordinates with d_r as the frequency denominator) and
+// "14. The Qwen family", Qwen3-Next section (head_dim 256, RoPE on 64 dims).
+// The query of head h is the first half of the 512-element block that the
+// query projection emits for that head; the second half (the gate) is left for
+// the attention kernel's epilogue and never read here.
+//
+// Layout of the work (HBM-bound stream, as in the Qwen3 prologue): a CTA owns
+// a few consecutive tokens. Their key rows are contiguous and come in with one
+// bulk copy; each query row is a 512-byte bulk copy out of the interleaved
+// query/gate projection. A warp owns a row, lane L holding elements
+// 8L..8L+7; the rotated pairs (i, i + d_r/2) sit in lanes L and L + d_r/16,
+// so one shuffle per element brings the partner. Q rows go back out as one
+// block per CTA ([B, T, Hq, 256] keeps the token order), K rows one 512-byte
+// store each into the head-major [B, Hkv, T, 256] layout.
+#include "q3a_internal.h"
+#include "q3a_rope.cuh"
+
+namespace q3a {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxTok = 8;
+constexpr int kRowBytes = kGatedD * 2;
+constexpr int kMaxRows = 192;  // (Hq + Hkv) rows of one token must fit the staging buffer
+
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x);
+  f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y);
+  f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z);
+  f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w);
+  f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__global__ void __launch_bounds__(kThreads)
+    gated_prologue_kernel(const __grid_constant__ GatedPrologueArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(16) float cos_s[kMaxTok][128];
+  __shared__ __align__(16) float sin_s[kMaxTok][128];
+  __shared__ uint64_t bar;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hq = a.Hq, Hkv = a.Hkv;
+  const long long n_tok = (long long)a.B * a.T;
+  const long long tok0 = (long long)blockIdx.x * a.tok_per_cta;
+  const int tok_here = (int)min((long long)a.tok_per_cta, n_tok - tok0);
+  uint16_t* rows_q = reinterpret_cast<uint16_t*>(smem);  // [tok][Hq][256]
+  uint16_t* rows_k = rows_q + (size_t)a.tok_per_cta * Hq * kGatedD;  // [tok][Hkv][256]
+  const uint32_t q_bytes = (uint32_t)tok_here * Hq * kRowBytes;
+  const uint32_t k_bytes = (uint32_t)tok_here * Hkv * kRowBytes;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&bar, q_bytes + k_bytes);
+      bulk_load(rows_k, a.k + tok0 * Hkv * kGatedD, k_bytes, &bar);
+    }
+    __syncwarp();
+    for (int r = lane; r < tok_here * Hq; r += 32)  // query halves of the q|gate blocks
+      bulk_load(rows_q + (size_t)r * kGatedD, a.qg + (tok0 * Hq + r) * (2 * kGatedD), kRowBytes,
+                &bar);
+  }
+  if (blockIdx.x == 0 && warp == 1) {
+    if (a.err_clear && lane == 0) *a.err_clear = 0u;
+    if (a.logit_bound) {
+      float gq = 0.f, gk = 0.f;
+      for (int i = lane; i < kGatedD; i += 32) {
+        gq = fmaxf(gq, fabsf(1.0f + __uint_as_float((uint32_t)a.q_w[i] << 16)));
+        gk = fmaxf(gk, fabsf(1.0f + __uint_as_float((uint32_t)a.k_w[i] << 16)));
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        gq = fmaxf(gq, __shfl_xor_sync(0xffffffffu, gq, o));
+        gk = fmaxf(gk, __shfl_xor_sync(0xffffffffu, gk, o));
+      }
+      if (lane == 0) *a.logit_bound = 16.0f * gq * gk * 1.4426950408889634f;
+    }
+  }
+  // rotation table of this CTA's tokens while the rows are in flight
+  const int n_ang = a.d_r >> 1;
+  for (int e = tid; e < tok_here * n_ang; e += kThreads) {
+    const int tt = e / n_ang, i = e - tt * n_ang;
+    const long long tok = tok0 + tt;
+    const long long t = tok - (tok / a.T) * a.T;
+    const float2 c_s = rope_cos_sin(t, a.turn_freq[i]);
+    cos_s[tt][i] = c_s.x;
+    sin_s[tt][i] = c_s.y;
+  }
+  // this lane's scales 1 + w for elements 8L .. 8L+7
+  float sq[8], sk[8];
+  unpack8(reinterpret_cast<const uint4*>(a.q_w)[lane], sq);
+  unpack8(reinterpret_cast<const uint4*>(a.k_w)[lane], sk);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sq[e] += 1.0f;
+    sk[e] += 1.0f;
+  }
+  // rotated lanes: L < d_r/8; partner lane L +- d_r/16
+  const int hl = a.d_r >> 4;
+  const bool rotated = lane < 2 * hl;
+  const bool lower = lane < hl;
+  const int partner = rotated ? (lower ? lane + hl : lane - hl) : lane;
+  const int ang0 = rotated ? 8 * (lower ? lane : lane - hl) : 0;
+  __syncthreads();  // barrier initialised, table written
+  mbar_wait(&bar, 0, nullptr, 0, nullptr);
+
+  const int RQ = tok_here * Hq;
+  const int rows = RQ + tok_here * Hkv;
+  for (int q = warp; q < rows; q += kWarps) {
+    const bool is_q = q < RQ;
+    const int rr = is_q ? q : q - RQ;
+    const int tt = is_q ? rr / Hq : rr / Hkv;
+    uint16_t* row = (is_q ? rows_q : rows_k) + (size_t)rr * kGatedD;
+    float x[8], y[8], o[8];
+    unpack8(reinterpret_cast<const uint4*>(row)[lane], x);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float inv_rms = rsqrtf(ss * (1.0f / kGatedD) + a.eps);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = x[e] * inv_rms * (is_q ? sq[e] : sk[e]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float yp = __shfl_sync(0xffffffffu, y[e], partner);
+      if (rotated) {
+        const float c = cos_s[tt][ang0 + e], s = sin_s[tt][ang0 + e];
+        o[e] = lower ? y[e] * c - yp * s : y[e] * c + yp * s;
+      } else {
+        o[e] = y[e];
+      }
+    }
+    reinterpret_cast<uint4*>(row)[lane] = pack8(o);
+  }
+  fence_proxy_async_smem();  // the bulk stores below read what was just written
+  __syncthreads();
+
+  bool issued = false;
+  if (tid == 0) {
+    bulk_store(a.qhat + tok0 * Hq * kGatedD, rows_q, q_bytes);
+    issued = true;
+  }
+  for (int rr = tid; rr < tok_here * Hkv; rr += kThreads) {
+    const int tt = rr / Hkv, kv = rr - tt * Hkv;
+    const long long tok = tok0 + tt;
+    const long long b = tok / a.T, t = tok - b * a.T;
+    bulk_store(a.khat + ((b * Hkv + kv) * a.T + t) * kGatedD, rows_k + (size_t)rr * kGatedD,
+               kRowBytes);
+    issued = true;
+  }
+  if (issued) bulk_commit_and_wait_read();  // shared memory stays valid until read
+}
+
+}  // namespace
+
+int gated_prologue_max_heads() { return kMaxRows; }
+
+cudaError_t launch_gated_prologue(const GatedPrologueArgs& a_in, cudaStream_t stream) {
+  const long long n_tok = (long long)a_in.B * a_in.T;
+  if (n_tok == 0) return cudaSuccess;
+  GatedPrologueArgs a = a_in;
+  const int rows_per_tok = a.Hq + a.Hkv;
+  if (a.Hq <= 0 || a.Hkv <= 0 || rows_per_tok > kMaxRows) return cudaErrorInvalidValue;
+  if (a.d_r < 0 || a.d_r > kGatedD || (a.d_r & 15)) return cudaErrorInvalidValue;
+  int tok = (40 * 1024) / (rows_per_tok * kRowBytes);
+  tok = tok < 1 ? 1 : (tok > kMaxTok ? kMaxTok : tok);
+  a.tok_per_cta = tok;
+  const size_t smem = (size_t)tok * rows_per_tok * kRowBytes;
+  static unsigned long long attr_mask = 0;  // per-device dynamic smem opt-in
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(attr_mask & (1ull << dev))) {
+    e = cudaFuncSetAttribute(gated_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxRows * kRowBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_mask |= 1ull << dev;
+  }
+  const long long grid = (n_tok + tok - 1) / tok;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  gated_prologue_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace q3a

@@ -109,7 +109,7 @@ q3a_status q3a_qknorm_rope(const q3a_bf16* x, const q3a_bf16* gamma, q3a_bf16* y
   a.T = T;
   a.pos0 = pos0;
   a.eps = eps;
-  fill_turn_freq(theta, a.turn_freq);
+  fill_turn_freq(theta, 128, a.turn_freq);
   return from_cuda(launch_qknorm_rope(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -157,7 +157,7 @@ static void prologue_args(RopeArgs& ra, const q3a_bf16* q, const q3a_bf16* k,
   ra.eps = eps;
   ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
   ra.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
-  fill_turn_freq(theta, ra.turn_freq);
+  fill_turn_freq(theta, 128, ra.turn_freq);
 }
 
 static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* out, int B, int T,
@@ -318,7 +318,7 @@ q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf1
   ra.eps = eps;
   ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
   ra.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
-  fill_turn_freq(theta, ra.turn_freq);
+  fill_turn_freq(theta, 128, ra.turn_freq);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_qknorm_rope(ra, st);
@@ -386,7 +386,7 @@ q3a_status q3a_decode(const q3a_bf16* q, const q3a_bf16* k_new, const q3a_bf16* 
   da->split_stride = decode_split_stride(S_max);
   da->max_splits = max_splits;
   da->eps = eps;
-  fill_turn_freq(theta, da->turn_freq);
+  fill_turn_freq(theta, 128, da->turn_freq);
   for (int b = 0; b < B; ++b) da->start_pos[b] = start_pos[b];
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -441,12 +441,148 @@ q3a_status q3a_decode_device_pos(const q3a_bf16* q, const q3a_bf16* k_new,
   da->split_stride = decode_split_stride(S_max);
   da->max_splits = da->split_stride;  // positions are not known here
   da->eps = eps;
-  fill_turn_freq(theta, da->turn_freq);
+  fill_turn_freq(theta, 128, da->turn_freq);
   da->pos_dev = start_pos;
   da->pos_valid = reinterpret_cast<uint32_t*>(ws + 16);
   // no host synchronisation and no host-side reads of device memory: the
   // call can be captured into a CUDA graph and replayed with new positions
   return from_cuda(launch_decode(*da, static_cast<cudaStream_t>(stream)));
+}
+
+// ----- gated global attention (Qwen3-Next / Qwen3.5) -------------------------
+
+static size_t gated_q_bytes(int B, int T, int Hq) { return (size_t)B * T * Hq * kGatedD * 2; }
+static size_t gated_k_bytes(int B, int T, int Hkv) { return (size_t)B * T * Hkv * kGatedD * 2; }
+
+size_t q3a_gated_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d) {
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || d != kGatedD) return 0;
+  return kHeader + align256(gated_q_bytes(B, T, Hq)) + align256(gated_k_bytes(B, T, Hkv));
+}
+
+static q3a_status gated_check(const void* const* ptrs, int nptrs, int B, int T, int Hq, int Hkv,
+                              int d, void* workspace, size_t ws_bytes, bool* empty) {
+  *empty = false;
+  if (d != kGatedD || B < 0 || T < 0 || !group_ok(Hq, Hkv)) return Q3A_EINVAL;
+  if ((long long)B * T * Hq > 0x7fffffffLL || T > (1 << 30)) return Q3A_EINVAL;
+  if (Hq + Hkv > gated_prologue_max_heads()) return Q3A_EINVAL;
+  if (B == 0 || T == 0) {
+    *empty = true;
+    return Q3A_OK;
+  }
+  for (int i = 0; i < nptrs; ++i)
+    if (!ptrs[i] || !aligned16(ptrs[i])) return Q3A_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
+  if (ws_bytes < q3a_gated_prefill_workspace_size(B, T, Hq, Hkv, d)) return Q3A_EINVAL;
+  return Q3A_OK;
+}
+
+static uint16_t* gated_ws_q(void* ws) { return reinterpret_cast<uint16_t*>((uint8_t*)ws + kHeader); }
+static uint16_t* gated_ws_k(void* ws, int B, int T, int Hq) {
+  return reinterpret_cast<uint16_t*>((uint8_t*)ws + kHeader + align256(gated_q_bytes(B, T, Hq)));
+}
+
+static void gated_prologue_args(GatedPrologueArgs& ga, const q3a_bf16* qg, const q3a_bf16* k,
+                                const q3a_bf16* q_w, const q3a_bf16* k_w, int B, int T, int Hq,
+                                int Hkv, int d_rot, double theta, float eps, void* workspace) {
+  memset(&ga, 0, sizeof ga);
+  ga.qg = qg;
+  ga.k = k;
+  ga.q_w = q_w;
+  ga.k_w = k_w;
+  ga.qhat = gated_ws_q(workspace);
+  ga.khat = gated_ws_k(workspace, B, T, Hq);
+  ga.err_clear = reinterpret_cast<uint32_t*>(workspace);
+  ga.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
+  ga.B = B;
+  ga.T = T;
+  ga.Hq = Hq;
+  ga.Hkv = Hkv;
+  ga.d_r = d_rot;
+  ga.eps = eps;
+  if (d_rot > 0) fill_turn_freq(theta, d_rot, ga.turn_freq);
+}
+
+static q3a_status gated_attention_args(GatedAttnArgs& ga, const q3a_bf16* qg, const q3a_bf16* v,
+                                       q3a_bf16* out, int B, int T, int Hq, int Hkv,
+                                       void* workspace) {
+  memset(&ga, 0, sizeof ga);
+  const int g = Hq / Hkv;
+  const uint64_t row = kGatedD * 2;  // bytes of one head row
+  const uint64_t dq[4] = {kGatedD, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
+  const uint64_t sq[3] = {row, (uint64_t)Hq * row, (uint64_t)T * Hq * row};
+  const uint32_t bq[4] = {64, (uint32_t)g, (uint32_t)(128 / g), 1};
+  const uint64_t dk[3] = {kGatedD, (uint64_t)T, (uint64_t)B * Hkv};
+  const uint64_t sk[2] = {row, (uint64_t)T * row};
+  const uint32_t bk[3] = {64, 64, 1};
+  const uint64_t dv[4] = {kGatedD, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
+  const uint64_t sv[3] = {row, (uint64_t)Hkv * row, (uint64_t)T * Hkv * row};
+  const uint32_t bv[4] = {64, 1, 64, 1};
+  if (encode_tensor_map(&ga.tm_q, gated_ws_q(workspace), 4, dq, sq, bq) != CUDA_SUCCESS ||
+      encode_tensor_map(&ga.tm_k, gated_ws_k(workspace, B, T, Hq), 3, dk, sk, bk) !=
+          CUDA_SUCCESS ||
+      encode_tensor_map(&ga.tm_v, v, 4, dv, sv, bv) != CUDA_SUCCESS)
+    return Q3A_ECUDA;
+  ga.qg = qg;
+  ga.out = out;
+  ga.err = reinterpret_cast<uint32_t*>(workspace);
+  ga.logit_bound = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + 8);
+  ga.B = B;
+  ga.T = T;
+  ga.Hq = Hq;
+  ga.Hkv = Hkv;
+  ga.g = g;
+  const int tok = gated_tokens_per_cta(g);
+  ga.n_mtiles = (T + tok - 1) / tok;
+  return Q3A_OK;
+}
+
+static bool d_rot_ok(int d_rot) { return d_rot >= 0 && d_rot <= kGatedD && (d_rot & 15) == 0; }
+
+q3a_status q3a_gated_prefill(const q3a_bf16* qg, const q3a_bf16* k, const q3a_bf16* v,
+                             const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out, int B,
+                             int T, int Hq, int Hkv, int d, int d_rot, double theta, float eps,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  if (!scalars_ok(theta, eps) || !d_rot_ok(d_rot)) return Q3A_EINVAL;
+  const void* ptrs[] = {qg, k, v, q_w, k_w, out};
+  bool empty;
+  q3a_status s = gated_check(ptrs, 6, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
+  if (s != Q3A_OK || empty) return s;
+  GatedAttnArgs aa;  // tensor maps first: a failure there launches nothing
+  s = gated_attention_args(aa, qg, v, out, B, T, Hq, Hkv, workspace);
+  if (s != Q3A_OK) return s;
+  GatedPrologueArgs pa;
+  gated_prologue_args(pa, qg, k, q_w, k_w, B, T, Hq, Hkv, d_rot, theta, eps, workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_gated_prologue(pa, st);
+  if (e == cudaSuccess) e = launch_gated_attention(aa, st);
+  return from_cuda(e);
+}
+
+q3a_status q3a_gated_prefill_prologue(const q3a_bf16* qg, const q3a_bf16* k,
+                                      const q3a_bf16* q_w, const q3a_bf16* k_w, int B, int T,
+                                      int Hq, int Hkv, int d, int d_rot, double theta, float eps,
+                                      void* workspace, size_t ws_bytes, void* stream) {
+  if (!scalars_ok(theta, eps) || !d_rot_ok(d_rot)) return Q3A_EINVAL;
+  const void* ptrs[] = {qg, k, q_w, k_w};
+  bool empty;
+  q3a_status s = gated_check(ptrs, 4, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
+  if (s != Q3A_OK || empty) return s;
+  GatedPrologueArgs pa;
+  gated_prologue_args(pa, qg, k, q_w, k_w, B, T, Hq, Hkv, d_rot, theta, eps, workspace);
+  return from_cuda(launch_gated_prologue(pa, static_cast<cudaStream_t>(stream)));
+}
+
+q3a_status q3a_gated_prefill_attention(const q3a_bf16* qg, const q3a_bf16* v, q3a_bf16* out,
+                                       int B, int T, int Hq, int Hkv, int d, void* workspace,
+                                       size_t ws_bytes, void* stream) {
+  const void* ptrs[] = {qg, v, out};
+  bool empty;
+  q3a_status s = gated_check(ptrs, 3, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
+  if (s != Q3A_OK || empty) return s;
+  GatedAttnArgs aa;
+  s = gated_attention_args(aa, qg, v, out, B, T, Hq, Hkv, workspace);
+  if (s != Q3A_OK) return s;
+  return from_cuda(launch_gated_attention(aa, static_cast<cudaStream_t>(stream)));
 }
 
 q3a_status q3a_last_device_error(const void* workspace, void* stream) {

@@ -45,9 +45,10 @@ struct RopeArgs {
   unsigned long long turn_freq[64];  // theta^(-2i/128) / (2 pi), 0.64 fixed point
 };
 
-// RoPE frequencies as fractions of a turn in 0.64 fixed point, so that the
-// angle of position p is p * turn_freq[i] modulo 2^64 (exact wrap-around)
-void fill_turn_freq(double theta, unsigned long long* turn_freq);
+// RoPE frequencies theta^(-2i/d_rot), i < d_rot/2, as fractions of a turn in
+// 0.64 fixed point, so that the angle of position p is p * turn_freq[i] modulo
+// 2^64 (exact wrap-around). Writes d_rot/2 entries (d_rot even, <= 256).
+void fill_turn_freq(double theta, int d_rot, unsigned long long* turn_freq);
 int qknorm_rope_max_heads();  // largest H0 + H1 one launch accepts
 cudaError_t launch_qknorm_rope(const RopeArgs& a, cudaStream_t stream);
 
@@ -110,6 +111,45 @@ struct DecodeArgs {
 constexpr uint32_t kErrWordRange = 0x201;
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// ----- K5/K6: gated global attention of Qwen3-Next / Qwen3.5 (d = 256) ------
+constexpr int kGatedD = 256;
+// K5: zero-centred QK-Norm + partial RoPE. The query rows are the first 256
+// elements of each 512-element head block of qg [B, T, Hq, 512] (the last 256
+// are the gate, read by K6); k is [B, T, Hkv, 256].
+struct GatedPrologueArgs {
+  const uint16_t* qg;
+  const uint16_t* k;
+  const uint16_t* q_w;  // [256] zero-centred weights: the scale is 1 + w
+  const uint16_t* k_w;
+  uint16_t* qhat;       // [B, T, Hq, 256]
+  uint16_t* khat;       // [B, Hkv, T, 256] (head-major)
+  uint32_t* err_clear;  // block 0 zeroes this error word
+  // block 0 writes here sqrt(256) * max|1 + w_q| * max|1 + w_k| * log2(e), the
+  // bound on |qhat . khat| / sqrt(256) * log2(e) that the norm guarantees
+  float* logit_bound;
+  int B, T, Hq, Hkv, d_r;
+  float eps;
+  int tok_per_cta;  // set by launch_gated_prologue
+  unsigned long long turn_freq[128];  // theta^(-2i/d_r) / (2 pi), i < d_r/2
+};
+int gated_prologue_max_heads();
+cudaError_t launch_gated_prologue(const GatedPrologueArgs& a, cudaStream_t stream);
+
+// K6: causal GQA attention over Qhat/Khat with the sigmoid output gate.
+struct GatedAttnArgs {
+  CUtensorMap tm_q;  // Qhat [B, T, Hq, 256], box {64, g, 128/g, 1}
+  CUtensorMap tm_k;  // Khat [B*Hkv, T, 256], box {64, 128, 1}
+  CUtensorMap tm_v;  // V [B, T, Hkv, 256], box {64, 1, 128, 1}
+  const uint16_t* qg;  // gate = qg[b, t, h, 256 .. 511]
+  uint16_t* out;       // [B, T, Hq, 256] bf16
+  uint32_t* err;
+  const float* logit_bound;
+  int B, T, Hq, Hkv, g;
+  int n_mtiles;  // ceil(T / gated_tokens_per_cta(g))
+};
+cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream);
+int gated_tokens_per_cta(int g);
 
 // ----- tensor maps -----------------------------------------------------------
 // cuTensorMapEncodeTiled (bf16, 128-byte swizzle, zero fill out of bounds),

@@ -118,7 +118,7 @@ extern "C" q3a_status q3a_decode_noalloc(const q3a_bf16* q, const q3a_bf16* k_ne
   da.split_stride = max_splits;
   da.max_splits = max_splits;
   da.eps = eps;
-  fill_turn_freq(theta, da.turn_freq);
+  fill_turn_freq(theta, 128, da.turn_freq);
   for (int b = 0; b < B; ++b) da.start_pos[b] = start_pos[b];
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -36,26 +36,6 @@ constexpr int kThreads = 256;
 constexpr int kHalfWarps = kThreads / 16;
 constexpr int kMaxTok = 8;
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-               "r"(smem_u32(src)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_and_wait_read() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_constant__ RopeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) float cos_s[kMaxTok][64];
@@ -196,31 +176,34 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
 
 }  // namespace
 
-void fill_turn_freq(double theta, unsigned long long* turn_freq) {
+void fill_turn_freq(double theta, int d_rot, unsigned long long* turn_freq) {
   // w_i / (2 pi) in long double (64 or more mantissa bits), scaled to 2^64.
   // long double arithmetic can be slow (software quad precision on some
-  // hosts), so the last few thetas are remembered.
+  // hosts), so the last few (theta, d_rot) pairs are remembered.
   struct Entry {
     double theta;
-    unsigned long long f[64];
+    int d_rot;
+    unsigned long long f[128];
   };
   static Entry cache[4];
   static int n_cached = 0, next = 0;
   static std::mutex mu;
+  const int n = d_rot / 2;
   std::lock_guard<std::mutex> lock(mu);
   for (int c = 0; c < n_cached; ++c)
-    if (cache[c].theta == theta) {
-      memcpy(turn_freq, cache[c].f, sizeof cache[c].f);
+    if (cache[c].theta == theta && cache[c].d_rot == d_rot) {
+      memcpy(turn_freq, cache[c].f, sizeof(unsigned long long) * n);
       return;
     }
   const long double two_pi = 6.283185307179586476925286766559L;
   Entry& e = cache[next];
   e.theta = theta;
-  for (int i = 0; i < 64; ++i) {
-    const long double w = powl((long double)theta, -(long double)(2 * i) / 128.0L);
+  e.d_rot = d_rot;
+  for (int i = 0; i < n; ++i) {
+    const long double w = powl((long double)theta, -(long double)(2 * i) / (long double)d_rot);
     e.f[i] = (unsigned long long)llroundl(w / two_pi * 18446744073709551616.0L);
   }
-  memcpy(turn_freq, e.f, sizeof e.f);
+  memcpy(turn_freq, e.f, sizeof(unsigned long long) * n);
   next = (next + 1) % 4;
   if (n_cached < 4) ++n_cached;
 }

@@ -171,3 +171,44 @@ def test_device_pos_decode_host_checks(lib):
     assert call(S_max=0) == binding.Q3A_EINVAL
     assert call(B=2049) == binding.Q3A_EINVAL
     assert call(B=0) == binding.Q3A_OK
+
+
+def gated_call(lib, **kw):
+    a = dict(B=1, T=4, Hq=16, Hkv=2, d=256, d_rot=64, theta=1e7, eps=1e-6, ws=FAKE,
+             ws_bytes=1 << 40)
+    a.update(kw)
+    return lib.q3a_gated_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["T"], a["Hq"],
+                                 a["Hkv"], a["d"], a["d_rot"], a["theta"], a["eps"], a["ws"],
+                                 a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(d=128), dict(d_rot=8), dict(d_rot=-16), dict(d_rot=272),
+                                dict(d_rot=65), dict(Hq=12, Hkv=2), dict(Hq=64, Hkv=1),
+                                dict(Hq=190, Hkv=10), dict(eps=0.0), dict(theta=0.5),
+                                dict(B=-1), dict(ws=FAKE + 16), dict(ws=0),
+                                dict(ws_bytes=4096)])
+def test_gated_prefill_rejects_bad_arguments(lib, kw):
+    assert gated_call(lib, **kw) == binding.Q3A_EINVAL
+
+
+def test_gated_prefill_empty_and_pointer_checks(lib):
+    assert gated_call(lib, B=0) == binding.Q3A_OK
+    assert gated_call(lib, T=0) == binding.Q3A_OK
+    for i in range(6):
+        for bad in (0, FAKE + 2):
+            a = [FAKE] * 6
+            a[i] = bad
+            st = lib.q3a_gated_prefill(*a, 1, 4, 16, 2, 256, 64, 1e7, 1e-6, FAKE, 1 << 40, None)
+            assert st == binding.Q3A_EINVAL
+    # the two halves check the same way
+    assert lib.q3a_gated_prefill_prologue(FAKE, FAKE, FAKE, FAKE, 1, 4, 16, 2, 256, 24, 1e7,
+                                          1e-6, FAKE, 1 << 40, None) == binding.Q3A_EINVAL
+    assert lib.q3a_gated_prefill_attention(FAKE, FAKE, FAKE + 8, 1, 4, 16, 2, 256, FAKE,
+                                           1 << 40, None) == binding.Q3A_EINVAL
+
+
+def test_gated_workspace_size(lib):
+    B, T, Hq, Hkv = 4, 4096, 16, 2
+    ws = binding.gated_prefill_workspace_size(B, T, Hq, Hkv)
+    assert ws >= 256 + B * T * (Hq + Hkv) * 256 * 2
+    assert binding.gated_prefill_workspace_size(B, T, Hq, Hkv, 128) == 0

@@ -1,0 +1,152 @@
+"""Gated global attention of Qwen3-Next / Qwen3.5 (K5 prologue + K6 attention)
+on the GPU against the fp64 oracle, via the C ABI."""
+import pytest
+import torch
+
+import oracle
+from qwen3_qk_norm_gb300 import binding, inputs
+from qwen3_qk_norm_gb300.inputs import WORKLOADS
+from gpu_util import assert_close_attention, assert_within_one_ulp
+
+pytestmark = pytest.mark.gpu
+
+D = 256
+
+
+def run_gated(x, d_r, theta, eps=1e-6, workspace=None):
+    d = {k: t.cuda() for k, t in x.items()}
+    out = binding.gated_prefill(d["qg"], d["k"], d["v"], d["q_w"], d["k_w"], d_r, theta, eps,
+                                workspace=workspace)
+    torch.cuda.synchronize()
+    return out
+
+
+def workspace_views(ws, B, T, Hq, Hkv):
+    """Qhat [B,T,Hq,256] and Khat [B,Hkv,T,256] inside a gated workspace."""
+    q_bytes = B * T * Hq * D * 2
+    k_off = 256 + ((q_bytes + 255) // 256) * 256
+    qhat = ws[256:256 + q_bytes].view(torch.bfloat16).view(B, T, Hq, D)
+    khat = ws[k_off:k_off + B * T * Hkv * D * 2].view(torch.bfloat16).view(B, Hkv, T, D)
+    return qhat, khat
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d_r,theta", [(1, 37, 8, 2, 64, 1e7), (2, 20, 16, 2, 64, 1e7),
+                                                  (1, 9, 4, 4, 256, 1e6), (1, 5, 4, 2, 0, 1e7),
+                                                  (1, 70000, 1, 1, 64, 1e7)])
+def test_gated_prologue_within_one_ulp(cuda_lib, B, T, Hq, Hkv, d_r, theta):
+    """Zero-centred norm + partial RoPE: one rounding of the fp32 result, so at
+    most one bf16 ulp from the exact value (positions up to 70000)."""
+    x = inputs.gated_inputs(B, T, Hq, Hkv, seed=T + Hq)
+    d = {k: t.cuda() for k, t in x.items()}
+    ws = torch.zeros(binding.gated_prefill_workspace_size(B, T, Hq, Hkv), dtype=torch.uint8,
+                     device="cuda")
+    binding.gated_prefill_prologue(d["qg"], d["k"], d["q_w"], d["k_w"], d_r, theta, 1e-6, ws)
+    torch.cuda.synchronize()
+    qhat, khat = workspace_views(ws, B, T, Hq, Hkv)
+    ref_q = oracle.gated_qknorm_rope(x["qg"], x["q_w"], D, d_r, theta, 1e-6)
+    ref_k = oracle.gated_qknorm_rope(x["k"], x["k_w"], D, d_r, theta, 1e-6)
+    assert_within_one_ulp(qhat, ref_q, "qhat")
+    assert_within_one_ulp(khat.permute(0, 2, 1, 3), ref_k, "khat")
+    # the bound the attention kernel's fixed-shift softmax relies on
+    bound = float(ws[8:12].view(torch.float32).item())
+    gq = float((1.0 + x["q_w"].double()).abs().max())
+    gk = float((1.0 + x["k_w"].double()).abs().max())
+    assert bound == pytest.approx(16 * gq * gk * 1.4426950408889634, rel=1e-6)
+
+
+# small shapes: several M tiles and KV tiles, ragged tails, every g
+@pytest.mark.parametrize("B,T,Hq,Hkv,d_r,theta", [
+    (1, 1, 8, 2, 64, 1e7),      # a single token
+    (1, 2, 2, 2, 64, 1e7),      # g = 1
+    (1, 63, 8, 2, 64, 1e7),     # one KV tile minus one
+    (2, 65, 4, 2, 64, 1e7),     # one KV tile plus one, B > 1
+    (1, 200, 16, 1, 64, 1e7),   # g = 16
+    (1, 300, 16, 2, 64, 1e7),   # g = 8, Qwen3-Next heads
+    (2, 150, 8, 8, 64, 1e6),    # g = 1, ragged
+    (1, 129, 8, 4, 256, 1e6),   # full rotary
+    (1, 100, 4, 2, 0, 1e7),     # no rotary
+])
+def test_gated_prefill_small_shapes(cuda_lib, B, T, Hq, Hkv, d_r, theta):
+    x = inputs.gated_inputs(B, T, Hq, Hkv, seed=B * 1000 + T)
+    ref = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], d_r, theta, 1e-6)
+    assert_close_attention(run_gated(x, d_r, theta), ref,
+                           f"gated B{B} T{T} Hq{Hq} Hkv{Hkv} d_r{d_r}")
+
+
+def test_gated_qwen35_08b_t300_full(cuda_lib):
+    w = WORKLOADS["qwen3.5-0.8b-gated-b1-t300"]
+    x = inputs.workload_inputs(w)
+    ref = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], w.d_r, w.theta, w.eps)
+    assert_close_attention(run_gated(x, w.d_r, w.theta), ref, w.name)
+
+
+@pytest.mark.parametrize("wmax", [0.5, 1.2, 2.5])  # bound <= 52, ~112, ~283 (log2 units)
+def test_gated_both_softmax_paths(cuda_lib, wmax):
+    """The norm bounds the logits by 16 max|1 + w_q| max|1 + w_k|; above the
+    kernel's limit the online-max path runs. Both must match the oracle."""
+    x = inputs.gated_inputs(1, 300, 8, 2, seed=int(wmax * 10))
+    g = torch.Generator().manual_seed(78)
+    x["q_w"] = (torch.rand(D, generator=g) * 2 * wmax - wmax).to(torch.bfloat16)
+    x["k_w"] = (torch.rand(D, generator=g) * 2 * wmax - wmax).to(torch.bfloat16)
+    ref = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    assert_close_attention(run_gated(x, 64, 1e7), ref, f"w max {wmax}")
+
+
+def test_gated_closed_and_open_gates(cuda_lib):
+    """Gates at -100 give exact zeros; the output is elementwise in the gate."""
+    x = inputs.gated_inputs(1, 90, 8, 2, seed=9)
+    x["qg"][:, :, 3, D:] = -100.0
+    ref = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    out = run_gated(x, 64, 1e7)
+    assert bool((out[:, :, 3] == 0).all())
+    assert_close_attention(out, ref, "closed gate of head 3")
+
+
+def test_gated_halves_equal_whole_call(cuda_lib):
+    B, T, Hq, Hkv = 2, 150, 16, 2
+    x = inputs.gated_inputs(B, T, Hq, Hkv, seed=10)
+    d = {k: t.cuda() for k, t in x.items()}
+    whole = run_gated(x, 64, 1e7)
+    ws = torch.empty(binding.gated_prefill_workspace_size(B, T, Hq, Hkv), dtype=torch.uint8,
+                     device="cuda")
+    binding.gated_prefill_prologue(d["qg"], d["k"], d["q_w"], d["k_w"], 64, 1e7, 1e-6, ws)
+    out = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device="cuda")
+    binding.gated_prefill_attention(d["qg"], d["v"], out, ws)
+    torch.cuda.synchronize()
+    assert binding.last_device_error(ws) == binding.Q3A_OK
+    assert torch.equal(out, whole)
+
+
+def test_gated_is_deterministic(cuda_lib):
+    x = inputs.gated_inputs(1, 260, 16, 2, seed=11)
+    a = run_gated(x, 64, 1e7)
+    b = run_gated(x, 64, 1e7)
+    assert torch.equal(a, b)
+
+
+def sample_rows(B, T, Hq, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    fixed = [(0, 0, 0), (B - 1, T - 1, Hq - 1), (0, T - 1, 0), (B - 1, 63, 1 % Hq),
+             (0, 64, Hq // 2), (0, min(T - 1, 4095), Hq - 1)]
+    rnd = [(int(torch.randint(0, B, (1,), generator=g)), int(torch.randint(0, T, (1,), generator=g)),
+            int(torch.randint(0, Hq, (1,), generator=g))) for _ in range(n)]
+    return torch.tensor(fixed + rnd, dtype=torch.int32)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["qwen3-next-80b-gated-b4-t4096", "qwen3.5-397b-gated-b1-t8192"])
+def test_gated_full_size_sampled_rows(cuda_lib, name):
+    """Full-size workloads, launched as the benchmark launches them; sampled
+    output rows against the oracle computed one by one."""
+    w = WORKLOADS[name]
+    x = inputs.workload_inputs(w, device="cuda")
+    out = binding.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], w.d_r, w.theta,
+                                w.eps)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    rows = sample_rows(w.B, w.T, w.Hq, 30, seed=w.seed)
+    cpu = {k: t.cpu() for k, t in x.items()}
+    ref = oracle.gated_prefill_rows(cpu["qg"], cpu["k"], cpu["v"], cpu["q_w"], cpu["k_w"], w.d_r,
+                                    w.theta, w.eps, rows)
+    got = torch.stack([out[b, t, h] for b, t, h in rows.tolist()])
+    assert_close_attention(got, ref, name)

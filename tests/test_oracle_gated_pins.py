@@ -305,3 +305,16 @@ def test_qwen3_next_global_kv_bytes_match_the_pages():
         ctx["Qwen3-8B"], abs=0.05)
     assert kv_cache_bytes_per_token(12, 2, 256) * 100000 / 2 ** 30 == pytest.approx(
         ctx["Qwen3-Next-80B-A3B global layers"], abs=0.05)
+
+
+def test_gated_qknorm_rope_rows_are_the_pinned_steps():
+    """The row-array form applies g2 then g3 to the first d elements of each
+    row (the query half of a query/gate block), at position pos0 + t."""
+    x = inputs.gated_inputs(2, 3, 2, 1, d=32, seed=36)
+    got = oracle.gated_qknorm_rope(x["qg"], x["q_w"], 32, 8, 1e7, 1e-6, pos0=4)
+    for b in range(2):
+        for t in range(3):
+            for h in range(2):
+                ref = oracle.partial_rope_row(
+                    oracle.zc_rmsnorm_row(x["qg"][b, t, h, :32], x["q_w"], 1e-6), 8, 4 + t, 1e7)
+                assert torch.equal(got[b, t, h], ref)
