@@ -14,8 +14,10 @@
 // kv*g + r%g) by a 4-D TMA box, so every K/V byte a CTA loads serves 128
 // query rows. With d = 256 a 128-row Q tile is 64 KB of shared memory and its
 // fp32 O tile 256 TMEM columns, so one Q tile per CTA is what fits; KV tiles
-// are 64 keys, in 8 KB blocks (64 rows x 64 dims) through an 18-block ring,
-// so that two KV tiles ahead of the MMAs are in flight.
+// are 64 keys (32 KB: four 64-dim blocks of 8 KB) through a ring of four tile
+// slots. A V tile's four blocks are contiguous, so O += P V is one N = 256
+// MMA per 16 keys (an MMA's cost has a large per-instruction part: N = 64
+// steps run at about half the tensor rate).
 //
 // Roles (640 threads):
 //   WG 0..3  softmax + epilogue. Warp w serves TMEM lanes 32(w%4).. (its rows)
@@ -55,12 +57,13 @@ constexpr int BN = 64;   // keys per KV tile
 constexpr int D = kGatedD;
 constexpr int kSoftmaxWGs = 4;
 constexpr int kThreads = (kSoftmaxWGs + 1) * 128;
-constexpr int kSlots = 18;            // ring blocks
+constexpr int kSlots = 4;             // ring tile slots
 constexpr uint32_t kQBlock = 16384;   // 128 rows x 128 bytes (64 dims of the Q tile)
 constexpr uint32_t kBlock = 8192;     // 64 rows x 128 bytes (64 dims of a K or V tile)
+constexpr uint32_t kTileBytes = 4 * kBlock;
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + 4 * kQBlock;
-constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kBlock;
+constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kTileBytes;
 // tile maxima [2 parities][4 quarters][128] fp32, then partial sums [4][128]
 constexpr uint32_t OFF_XCHG = OFF_BAR + 512;
 constexpr uint32_t kSmemBytes = OFF_XCHG + (2 * 4 * 128 + 4 * 128) * 4 + 1024;
@@ -85,22 +88,21 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
-// Blocks are consumed (and loaded) in the order K_0, K_1, V_0, K_2, V_1, ...;
-// block n of that sequence sits in ring slot n % kSlots.
+// Tiles are consumed (and loaded) in the order K_0, K_1, V_0, K_2, V_1, ...;
+// tile n of that sequence sits in ring slot n % kSlots.
 __device__ __forceinline__ uint32_t slot_of(uint32_t n) { return n % kSlots; }
 __device__ __forceinline__ uint32_t use_of(uint32_t n) { return (n / kSlots) & 1u; }
 
 // S = Q K_j^T: 16 steps of 16 dims. Q block c = dims 64c..64c+63 (16 KB
-// apart); K block c of the tile is ring block first + c.
+// apart); K block c = dims 64c.. of the tile in ring slot `slot` (8 KB apart).
 __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64_t ring_k,
-                                        uint32_t first) {
+                                        uint32_t slot) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk) {
     const int c = kk >> 2;
     const uint64_t a = q_desc + (uint64_t)((c * kQBlock + (kk & 3) * 32) >> 4);
-    const uint64_t b =
-        ring_k + (uint64_t)((slot_of(first + c) * kBlock + (kk & 3) * 32) >> 4);
+    const uint64_t b = ring_k + (uint64_t)((slot * kTileBytes + c * kBlock + (kk & 3) * 32) >> 4);
     if (kk == 0)
       mma_ss<0>(tmem_s, a, b, idesc);
     else
@@ -109,19 +111,17 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64
 }
 
 // O += P_j V_j: 4 steps of 16 keys (P columns 16kk.. of the S buffer, written
-// by key quarter kk); each step is four N = 64 MMAs, one per 64-dim V block
-// (MN-major, 8-key groups 1 KB apart, 16 keys = 2 KB per step).
+// by key quarter kk), each one N = 256 MMA. B = V, MN-major: 64-dim blocks
+// 8 KB apart (the descriptor's leading offset), 8-key groups 1 KB apart, 16
+// keys = 2 KB per step.
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t ring_v,
-                                         uint32_t first, bool accumulate_first) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);
+                                         uint32_t slot, bool accumulate_first) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint64_t b = ring_v + (uint64_t)((slot_of(first + c) * kBlock + kk * 2048) >> 4);
-      mma_bf16_ts(tmem_o + 64 * c, tmem_p + 16 * kk, b, idesc,
-                  (accumulate_first || kk > 0) ? 1u : 0u);
-    }
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint64_t b = ring_v + (uint64_t)((slot * kTileBytes + kk * 2048) >> 4);
+    mma_bf16_ts(tmem_o, tmem_p + 16 * kk, b, idesc, (accumulate_first || kk > 0) ? 1u : 0u);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], kSoftmaxWGs * 128);
+      mbar_init(&bars->p_full[t], kSoftmaxWGs * 4);  // one arrive per softmax warp
     }
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->xmax_full, kSoftmaxWGs * 128);
@@ -178,23 +178,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bars->q_full, 4 * kQBlock);
       for (int c = 0; c < 4; ++c)
         tma_load_4d(smem + OFF_Q + c * kQBlock, &a.tm_q, &bars->q_full, 64 * c, kv * g, t0, b);
-      uint32_t n = 0;  // blocks issued
+      uint32_t n = 0;  // tiles issued
       bool ok = true;
       auto load_tile = [&](bool is_k, int j) {
-        for (int c = 0; c < 4 && ok; ++c) {
-          const uint32_t s = slot_of(n);
-          if (!mbar_wait(&bars->slot_empty[s], use_of(n) ^ 1u, a.err, kDevTimeoutTma, abort)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->slot_full[s], kBlock);
-          uint8_t* dst = smem + OFF_RING + s * kBlock;
-          if (is_k)
-            tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 64 * c, j * BN, b * a.Hkv + kv);
-          else
-            tma_load_4d(dst, &a.tm_v, &bars->slot_full[s], 64 * c, kv, j * BN, b);
-          ++n;
+        if (!ok) return;
+        const uint32_t s = slot_of(n);
+        if (!mbar_wait(&bars->slot_empty[s], use_of(n) ^ 1u, a.err, kDevTimeoutTma, abort)) {
+          ok = false;
+          return;
         }
+        mbar_arrive_expect_tx(&bars->slot_full[s], kTileBytes);
+        uint8_t* dst = smem + OFF_RING + s * kTileBytes;
+        for (int c = 0; c < 4; ++c) {
+          if (is_k)
+            tma_load_3d(dst + c * kBlock, &a.tm_k, &bars->slot_full[s], 64 * c, j * BN,
+                        b * a.Hkv + kv);
+          else
+            tma_load_4d(dst + c * kBlock, &a.tm_v, &bars->slot_full[s], 64 * c, kv, j * BN, b);
+        }
+        ++n;
       };
       load_tile(true, 0);
       if (n_tiles > 1) load_tile(true, 1);
@@ -214,47 +216,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring = smem_u32(smem + OFF_RING);
       const uint64_t q_desc = smem_desc_sw128(q_addr, 16, 1024);
       const uint64_t ring_k = smem_desc_sw128(ring, 16, 1024);     // K-major K blocks
-      const uint64_t ring_v = smem_desc_sw128(ring, kBlock, 1024);  // MN-major V blocks
-      auto wait_tile = [&](uint32_t first) {
-        for (uint32_t c = 0; c < 4; ++c)
-          if (!mbar_poll(&bars->slot_full[slot_of(first + c)], use_of(first + c), a.err,
-                         kDevTimeoutMma, abort))
-            return false;
-        return true;
+      const uint64_t ring_v = smem_desc_sw128(ring, kBlock, 1024);  // MN-major V tiles
+      auto wait_tile = [&](uint32_t t) {
+        return mbar_poll(&bars->slot_full[slot_of(t)], use_of(t), a.err, kDevTimeoutMma, abort);
       };
-      uint32_t n = 0;  // blocks consumed
+      // An mbarrier wait issued after a tcgen05.commit stalls this thread
+      // until the commit resolves, which would let the tensor pipe drain
+      // every tile. So the inputs of the next PV (P_{j+1}, V_{j+1}) are waited
+      // for before the commit that publishes S_{j+2}; that commit only gates
+      // softmax j+2, which cannot start before softmax j+1 has produced
+      // P_{j+1} anyway. (The online-max path commits after each PV, since its
+      // softmax may wait for PV_j before producing P_{j+1}.)
+      auto wait_pv_inputs = [&](int j, uint32_t first) {
+        return mbar_poll(&bars->p_full[j & 1], (j >> 1) & 1, a.err, kDevTimeoutMma, abort) &&
+               wait_tile(first);
+      };
+      uint32_t n = 0;  // tiles consumed
       bool ok = mbar_poll(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) && wait_tile(0);
       if (ok) {
         tc_fence_after();
-        issue_s(tmem, q_desc, ring_k, 0);
-        mma_commit(&bars->s_full[0]);
-        n = 4;
-      }
-      if (ok && n_tiles > 1) {
-        ok = wait_tile(4);
-        if (ok) {
-          tc_fence_after();
-          issue_s(tmem + BN, q_desc, ring_k, 4);
-          mma_commit(&bars->s_full[1]);
-          n = 8;
+        issue_s(tmem, q_desc, ring_k, slot_of(0));
+        n = 1;
+        if (n_tiles > 1) {
+          ok = wait_tile(1);  // K_1
+          mma_commit(&bars->s_full[0]);
+          if (ok) {
+            tc_fence_after();
+            issue_s(tmem + BN, q_desc, ring_k, slot_of(1));
+            n = 2;
+            ok = wait_pv_inputs(0, n);  // P_0, V_0
+            mma_commit(&bars->s_full[1]);
+          }
+        } else {
+          mma_commit(&bars->s_full[0]);
+          ok = wait_pv_inputs(0, n);
         }
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        ok = mbar_poll(&bars->p_full[j & 1], (j >> 1) & 1, a.err, kDevTimeoutMma, abort) &&
-             wait_tile(n);
-        if (!ok) break;
+        // P_j and V_j (tile n) have been waited for
         tc_fence_after();
-        issue_pv(tmem + kTmemO, tmem + (j & 1) * BN, ring_v, n, j > 0);
-        n += 4;
+        issue_pv(tmem + kTmemO, tmem + (j & 1) * BN, ring_v, slot_of(n), j > 0);
+        n += 1;
         if (!fixed_max) mma_commit(&bars->pv_done);
-        if (j + 2 < n_tiles) {
-          ok = wait_tile(n);
+        const bool next_s = j + 2 < n_tiles;
+        if (next_s) {
+          ok = wait_tile(n);  // K_{j+2}
           if (!ok) break;
           tc_fence_after();
-          issue_s(tmem + (j & 1) * BN, q_desc, ring_k, n);
-          n += 4;
-          mma_commit(&bars->s_full[j & 1]);
+          issue_s(tmem + (j & 1) * BN, q_desc, ring_k, slot_of(n));
+          n += 1;
         }
+        if (j + 1 < n_tiles) ok = wait_pv_inputs(j + 1, n);  // P_{j+1}, V_{j+1}
+        if (next_s) mma_commit(&bars->s_full[j & 1]);
       }
       if (ok) mma_commit(&bars->o_final);
       // drain: every MMA issued above has completed once this phase completes
@@ -274,13 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t released = 0;  // ring blocks handed back (thread 0)
     for (int j = 0; j < n_tiles; ++j) {
-      ok = __all_sync(kFull, mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, a.err,
+      ok = __all_sync(kFull, mbar_poll(&bars->s_full[j & 1], (j >> 1) & 1, a.err,
                                        kDevTimeoutSoftmax, abort));
       if (!ok) break;
       // S_j is complete and so is every earlier MMA: K_0..K_j and V_0..V_{j-2}
-      // (blocks 0 .. 8j-1; 0..3 for j = 0) are no longer read
+      // (tiles 0 .. 2j-1 of the load order; tile 0 for j = 0) are no longer read
       if (threadIdx.x == 0) {
-        const uint32_t upto = j == 0 ? 4u : 8u * (uint32_t)j;
+        const uint32_t upto = j == 0 ? 1u : 2u * (uint32_t)j;
         for (; released < upto; ++released) mbar_arrive(&bars->slot_empty[slot_of(released)]);
       }
       tc_fence_after();
@@ -351,8 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float s0, s1;
       f2_unpack(sum2, s0, s1);
       l += s0 + s1;
+      // the warp's tcgen05.st has completed (wait::st above, warp-collective):
+      // one arrive per warp publishes all 32 rows' P
       tc_fence_before();
-      mbar_arrive(&bars->p_full[j & 1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
     }
     // ---- epilogue: the row's four partial sums, then O / l * sigmoid(gate)
     ok = __all_sync(kFull, ok && !*abort);
