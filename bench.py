@@ -38,6 +38,7 @@ METRIC = "causal prefill attention TFLOP/s and decode GB/s at 1 GB300, % of roof
 PREFILL_WORKLOAD = "qwen3-8b-prefill-b4-t4096"
 DECODE_WORKLOAD = "qwen3-8b-decode-b64"
 CHUNK_WORKLOAD = "qwen3-8b-chunk-b4-t1024-at3072"
+GATED_WORKLOAD = "qwen3-next-80b-gated-b4-t4096"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2 ** 20
 
@@ -157,6 +158,9 @@ KERNEL_SOURCES = {  # the kernel's file and every header it includes
     "qknorm_rope_kernel": ["qknorm_rope.cu", "q3a_rope.cuh", "q3a_device.cuh", "q3a_internal.h"],
     "decode_split_kernel": ["decode_attention.cu", "q3a_rope.cuh", "q3a_device.cuh",
                             "q3a_internal.h"],
+    "gated_attention_kernel": ["gated_attention.cu", "q3a_device.cuh", "q3a_internal.h"],
+    "gated_prologue_kernel": ["gated_prologue.cu", "q3a_rope.cuh", "q3a_device.cuh",
+                              "q3a_internal.h"],
 }
 
 
@@ -355,6 +359,45 @@ def bench_chunk(binding, device, steps: int, warmup: int, world: int):
     return w, start, ms
 
 
+def bench_gated(binding, device, steps: int, warmup: int, world: int):
+    """Gated global attention of Qwen3-Next / Qwen3.5: the prologue and the
+    attention kernel timed separately within each step (inputs above L2)."""
+    w = WORKLOADS[GATED_WORKLOAD]
+    x = inputs.workload_inputs(w, device=device)
+    out = torch.empty((w.B, w.T, w.Hq, w.d), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(binding.gated_prefill_workspace_size(w.B, w.T, w.Hq, w.Hkv),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        binding.gated_prefill_prologue(x["qg"], x["k"], x["q_w"], x["k_w"], w.d_r, w.theta, w.eps,
+                                       ws)
+        if ev is not None:
+            ev[1].record(stream)
+        binding.gated_prefill_attention(x["qg"], x["v"], out, ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(world, device)
+    synchronize_all(device)
+    for i in range(steps):
+        step(evs[i])
+    synchronize_all(device)
+    barrier(world, device)
+    status = binding.last_device_error(ws)
+    if status != 0:
+        raise RuntimeError(f"gated device error word: {status}")
+    pro = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    att = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    tot = statistics.mean(e[0].elapsed_time(e[2]) for e in evs)
+    return w, tot, pro, att
+
+
 def cpu_baseline_prefill(w, x_cpu: dict, budget_s: float = 12.0, seed: int = 0) -> dict:
     """The fp64 oracle on a bounded sample of the prefill workload's query rows
     (random (b, t, h)), on all host cores, for about ``budget_s`` seconds."""
@@ -394,6 +437,8 @@ def run_profile_case(which: str) -> None:
             binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], w.theta, w.eps)
     elif which == "chunk":
         bench_chunk(binding, device, 3, 0, 1)
+    elif which == "gated":
+        bench_gated(binding, device, 3, 0, 1)
     else:
         w = WORKLOADS[DECODE_WORKLOAD]
         B = 16  # a quarter of the batch: 2 GiB of cache instead of 8
@@ -430,6 +475,9 @@ def run_ours(args) -> None:
         cw, c_start, ch_ms = (None, None, None)
         if not args.no_chunk:
             cw, c_start, ch_ms = bench_chunk(binding, device, args.steps, args.warmup, world)
+        gw, g_ms, gp_ms, ga_ms = (None, None, None, None)
+        if not args.no_gated:
+            gw, g_ms, gp_ms, ga_ms = bench_gated(binding, device, args.steps, args.warmup, world)
     clocks = clk.summary()
 
     flops = accounting.prefill_flops(w.B, w.T, w.Hq, w.d)
@@ -525,6 +573,31 @@ def run_ours(args) -> None:
                          "peak_source": f"{peak_src} bf16 dense burst", "traffic": None},
             "gpu_launches": 2 * args.steps,
         }
+    if g_ms is not None:
+        gflops = accounting.prefill_flops(gw.B, gw.T, gw.Hq, gw.d)
+        g_max, ga_max, gp_max = (max_over_ranks(v, world, device) for v in (g_ms, ga_ms, gp_ms))
+        att = gflops / (ga_max / 1e3) / 1e12
+        gp_bytes = 2 * gw.B * gw.T * (gw.Hq + gw.Hkv) * gw.d * 2 + 2 * gw.d * 2
+        line["gated"] = {
+            "value": round(whole_job_rate(gflops, world, g_max / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s", "ms_per_step": round(g_max, 4),
+            "config": {"workload": gw.name, "B": gw.B, "T": gw.T, "Hq": gw.Hq, "Hkv": gw.Hkv,
+                       "d": gw.d, "d_rot": gw.d_r, "theta": gw.theta, "flops_per_step": gflops,
+                       "api": "q3a_gated_prefill_prologue + q3a_gated_prefill_attention"},
+            "roofline": {"bound": "tensor", "kernel": "gated_attention_kernel",
+                         "achieved": round(att, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(att / peaks["bf16_tflops"], 4),
+                         "peak_source": f"{peak_src} bf16 dense burst",
+                         "traffic": ncu_traffic("gated_attention_kernel"),
+                         "ms_per_launch": round(ga_max, 4)},
+            "prologue": {"kernel": "gated_prologue_kernel", "ms_per_launch": round(gp_max, 4),
+                         "bytes_per_launch": gp_bytes,
+                         "achieved_gbs": round(gp_bytes / (gp_max / 1e3) / 1e9, 1),
+                         "frac_of_hbm": round(gp_bytes / (gp_max / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                              4),
+                         "traffic": ncu_traffic("gated_prologue_kernel")},
+            "gpu_launches": 2 * args.steps,
+        }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x_cpu = {k: t.cpu() for k, t in x.items()}
         line["cpu_baseline"] = cpu_baseline_prefill(w, x_cpu)
@@ -591,10 +664,11 @@ def main(argv=None) -> None:
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunk", action="store_true")
+    ap.add_argument("--no-gated", action="store_true")
     ap.add_argument("--prefill-workload", default=PREFILL_WORKLOAD,
                     choices=[n for n, w in WORKLOADS.items() if w.kind == "prefill"],
                     help="prefill workload of the step (the default is the headline one)")
-    ap.add_argument("--profile-case", choices=["prefill", "decode", "chunk"],
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "chunk", "gated"],
                     help="run a few launches of one kernel for an ncu capture, print no JSON")
     args = ap.parse_args(argv)
     if args.profile_case:
