@@ -158,7 +158,8 @@ KERNEL_SOURCES = {  # the kernel's file and every header it includes
     "qknorm_rope_kernel": ["qknorm_rope.cu", "q3a_rope.cuh", "q3a_device.cuh", "q3a_internal.h"],
     "decode_split_kernel": ["decode_attention.cu", "q3a_rope.cuh", "q3a_device.cuh",
                             "q3a_internal.h"],
-    "gated_attention_kernel": ["gated_attention.cu", "q3a_device.cuh", "q3a_internal.h"],
+    "gated_attention_pair_kernel": ["gated_attention_pair.cu", "q3a_pair.cuh", "q3a_device.cuh",
+                                    "q3a_internal.h"],
     "gated_prologue_kernel": ["gated_prologue.cu", "q3a_rope.cuh", "q3a_device.cuh",
                               "q3a_internal.h"],
 }
@@ -584,11 +585,11 @@ def run_ours(args) -> None:
             "config": {"workload": gw.name, "B": gw.B, "T": gw.T, "Hq": gw.Hq, "Hkv": gw.Hkv,
                        "d": gw.d, "d_rot": gw.d_r, "theta": gw.theta, "flops_per_step": gflops,
                        "api": "q3a_gated_prefill_prologue + q3a_gated_prefill_attention"},
-            "roofline": {"bound": "tensor", "kernel": "gated_attention_kernel",
+            "roofline": {"bound": "tensor", "kernel": "gated_attention_pair_kernel",
                          "achieved": round(att, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(att / peaks["bf16_tflops"], 4),
                          "peak_source": f"{peak_src} bf16 dense burst",
-                         "traffic": ncu_traffic("gated_attention_kernel"),
+                         "traffic": ncu_traffic("gated_attention_pair_kernel"),
                          "ms_per_launch": round(ga_max, 4)},
             "prologue": {"kernel": "gated_prologue_kernel", "ms_per_launch": round(gp_max, 4),
                          "bytes_per_launch": gp_bytes,

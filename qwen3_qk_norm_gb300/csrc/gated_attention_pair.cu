@@ -1,6 +1,6 @@
-// gated_attention.cu — K6, causal grouped-query attention with the sigmoid
-// output gate of the Qwen3-Next / Qwen3.5 global-attention layer (head_dim
-// 256), on tcgen05.
+// gated_attention_pair.cu — K6, causal grouped-query attention with the
+// sigmoid output gate of the Qwen3-Next / Qwen3.5 global-attention layer
+// (head_dim 256), on pairs of CTAs sharing one tcgen05 MMA stream.
 //
 // For every query row (b, i, h), with the normalised, partially rotated qhat
 // and keys khat_j of group h / g:
@@ -9,61 +9,64 @@
 // elementwise by the sigmoid of the gate half of the query projection before
 // the output projection; "14. The Qwen family", Qwen3-Next section.)
 //
-// Tiling. A CTA owns one M tile of 128 query rows: the g heads of one KV
-// group for 128/g consecutive tokens, packed row r = (token r/g, head
-// kv*g + r%g) by a 4-D TMA box, so every K/V byte a CTA loads serves 128
-// query rows. With d = 256 a 128-row Q tile is 64 KB of shared memory and its
-// fp32 O tile 256 TMEM columns, so one Q tile per CTA is what fits; KV tiles
-// are 64 keys (32 KB: four 64-dim blocks of 8 KB) through a ring of four tile
-// slots. A V tile's four blocks are contiguous, so O += P V is one N = 256
-// MMA per 16 keys (an MMA's cost has a large per-instruction part: N = 64
-// steps run at about half the tensor rate).
+// Why pairs. With d = 256 a 128-row Q tile is 64 KB of shared memory and its
+// fp32 O tile 256 of the 512 TMEM columns, so a CTA holds one Q tile, and a
+// lone CTA's QK^T runs as small-N MMAs whose cost is dominated by the
+// per-instruction operand reads. A cluster of two CTAs issues M = 256 MMAs
+// (tcgen05.mma.cta_group::2): each CTA holds its own 128 query rows (A) and
+// half of every K/V tile (B), so QK^T runs as N = 128 steps and PV as N = 256
+// steps, each CTA loads half the K/V bytes, and a 128-key tile costs each CTA
+// 64 KB of its ring.
 //
-// Roles (640 threads):
-//   WG 0..3  softmax + epilogue. Warp w serves TMEM lanes 32(w%4).. (its rows)
-//            and the key quarter c = w/4 of every S tile (16 keys), and O
-//            columns 64c..64c+63 in the epilogue;
-//   warp 16  TMA producer (Q once, then K_0, K_1, V_0, K_2, V_1, ... in the
-//            order the MMAs consume them);
-//   warp 17  MMA issuer (one thread).
-// TMEM: S0 | S1 (64 fp32 columns each, double-buffered) ... O (256 columns at
-// 256). A softmax thread writes its 16 probabilities as 8 bf16-pair columns
-// over the first half of its own S columns; PV reads them from there
-// (tcgen05.mma with A in tensor memory). MMA stream: S_0, S_1, then per KV tile
-// j: PV_j, S_{j+2} — the tensor core computes the next scores while the
-// softmax works on S_j, and S_{j+2} overwrites S_j/P_j only after PV_j has
-// read it (one thread's tcgen05.mma execute in issue order).
-// The commit that marks S_j complete also covers every earlier MMA (K_j and
-// V_{j-2} are no longer read), so one softmax thread hands those ring blocks
-// back to the producer when it sees S_j.
+// Tiling. The pair owns 256 query rows: two 128-row tiles of the g heads of one
+// KV group for 128/g consecutive tokens each, packed row r = (token r/g, head
+// kv*g + r%g) by a 4-D TMA box; the even CTA holds the first tile. KV tiles are
+// 128 keys. CTA c holds keys 64c..64c+63 of each K tile (four 8 KB blocks of
+// 64 dims) and dims 128c..128c+127 of each V tile (two 16 KB blocks of 64
+// dims), in a ring of four 32 KB slots, loaded in the order the MMAs read them
+// (K_0, K_1, V_0, K_2, V_1, ...).
 //
-// Softmax: the fixed shift of the Qwen3 kernel applies (the zero-centred norm
-// bounds |qhat| by 16 max|1 + w_q| and |khat| by 16 max|1 + w_k|; the
-// prologue writes the bound); above its limit, an online max exchanged
-// between the four key quarters of a row through shared memory, with O
-// rescaled in TMEM after the previous PV has completed.
+// Roles (640 threads per CTA):
+//   WG 0..3  softmax + epilogue of the CTA's own 128 rows. Warp w serves TMEM
+//            lanes 32(w%4).. and the key quarter c = w/4 of every S tile (32
+//            keys), and O columns 64c..64c+63 in the epilogue;
+//   warp 16  TMA producer of the CTA's Q tile and ring;
+//   warp 17  (even CTA) the MMA issuer of the pair;
+//   warp 18  (odd CTA) forwards its ring's "tile landed" events to the even
+//            CTA, whose MMA issuer waits for both halves.
+// TMEM per CTA: S0 | S1 (128 fp32 columns each, double-buffered) | O (256).
+// P goes back as bf16 pairs over the first half of each thread's own S
+// columns and PV reads it from there. MMA stream: S_0, S_1, then per KV tile
+// j: PV_j, S_{j+2}. Commits arrive on the barriers of both CTAs.
 //
-// Every mbarrier wait is bounded; a timeout sets the error word, all roles
-// unwind, in-flight copies and MMAs are drained and TMEM is freed.
-#include "q3a_device.cuh"
+// Softmax: fixed shift from the norm's logit bound (16 max|1 + w_q|
+// max|1 + w_k|, written by the prologue), or above its limit an online max
+// exchanged between the four key quarters of a row, with O rescaled in TMEM
+// after the previous PV has completed.
+//
+// Every mbarrier wait is bounded; a timeout sets the error word and every
+// role unwinds; the MMA issuer drains its MMAs and both CTAs meet at a cluster
+// barrier before freeing tensor memory.
 #include "q3a_internal.h"
+#include "q3a_pair.cuh"
 
 namespace q3a {
 
 namespace {
 
-constexpr int BM = 128;  // query rows per CTA
-constexpr int BN = 64;   // keys per KV tile
+constexpr int BM = 128;  // query rows per CTA (256 per pair)
+constexpr int BN = 128;  // keys per KV tile
 constexpr int D = kGatedD;
 constexpr int kSoftmaxWGs = 4;
 constexpr int kThreads = (kSoftmaxWGs + 1) * 128;
-constexpr int kSlots = 4;             // ring tile slots
-constexpr uint32_t kQBlock = 16384;   // 128 rows x 128 bytes (64 dims of the Q tile)
-constexpr uint32_t kBlock = 8192;     // 64 rows x 128 bytes (64 dims of a K or V tile)
-constexpr uint32_t kTileBytes = 4 * kBlock;
+constexpr int kSlots = 4;
+constexpr uint32_t kQBlock = 16384;  // 128 rows x 128 bytes: 64 dims of the Q tile
+constexpr uint32_t kKBlock = 8192;   // 64 keys x 128 bytes: 64 dims of a K half tile
+constexpr uint32_t kVBlock = 16384;  // 128 keys x 128 bytes: 64 dims of a V half tile
+constexpr uint32_t kSlotBytes = 32768;
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + 4 * kQBlock;
-constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kTileBytes;
+constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kSlotBytes;
 // tile maxima [2 parities][4 quarters][128] fp32, then partial sums [4][128]
 constexpr uint32_t OFF_XCHG = OFF_BAR + 512;
 constexpr uint32_t kSmemBytes = OFF_XCHG + (2 * 4 * 128 + 4 * 128) * 4 + 1024;
@@ -76,11 +79,12 @@ constexpr float kFixedMaxLimit = 60.0f;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct Bars {
-  uint64_t q_full;
-  uint64_t slot_full[kSlots], slot_empty[kSlots];
-  uint64_t s_full[2], p_full[2];
-  uint64_t pv_done;    // fallback path: PV_j complete (one phase per KV tile)
-  uint64_t xmax_full;  // fallback path: all four quarters posted their tile max
+  uint64_t q_full, q_peer;
+  uint64_t slot_full[kSlots], slot_peer[kSlots], slot_empty[kSlots];
+  uint64_t s_full[2];
+  uint64_t p_full[2];  // even CTA: all 32 softmax warps of the pair
+  uint64_t pv_done;    // online-max path: PV_j complete (one phase per KV tile)
+  uint64_t xmax_full;  // online-max path: the CTA's four quarters posted their tile max
   uint64_t o_final;
   uint64_t drain;
   uint32_t tmem_base;
@@ -88,72 +92,79 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
-// Tiles are consumed (and loaded) in the order K_0, K_1, V_0, K_2, V_1, ...;
-// tile n of that sequence sits in ring slot n % kSlots.
 __device__ __forceinline__ uint32_t slot_of(uint32_t n) { return n % kSlots; }
 __device__ __forceinline__ uint32_t use_of(uint32_t n) { return (n / kSlots) & 1u; }
 
-// S = Q K_j^T: 16 steps of 16 dims. Q block c = dims 64c..64c+63 (16 KB
-// apart); K block c = dims 64c.. of the tile in ring slot `slot` (8 KB apart).
+// S = Q K_j^T over the pair: 16 steps of 16 dims, M = 256, N = 128. Q block c
+// holds dims 64c..64c+63 (16 KB apart); the K half tile's block c likewise
+// (8 KB apart) in ring slot `slot`.
 __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64_t ring_k,
                                         uint32_t slot) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
+  constexpr uint32_t idesc = idesc_bf16_f32(256, BN, 0, 0);
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk) {
     const int c = kk >> 2;
     const uint64_t a = q_desc + (uint64_t)((c * kQBlock + (kk & 3) * 32) >> 4);
-    const uint64_t b = ring_k + (uint64_t)((slot * kTileBytes + c * kBlock + (kk & 3) * 32) >> 4);
+    const uint64_t b =
+        ring_k + (uint64_t)((slot * kSlotBytes + c * kKBlock + (kk & 3) * 32) >> 4);
     if (kk == 0)
-      mma_ss<0>(tmem_s, a, b, idesc);
+      mma_pair_ss<0>(tmem_s, a, b, idesc);
     else
-      mma_ss<1>(tmem_s, a, b, idesc);
+      mma_pair_ss<1>(tmem_s, a, b, idesc);
   }
 }
 
-// O += P_j V_j: 4 steps of 16 keys (P columns 16kk.. of the S buffer, written
-// by key quarter kk), each one N = 256 MMA. B = V, MN-major: 64-dim blocks
-// 8 KB apart (the descriptor's leading offset), 8-key groups 1 KB apart, 16
-// keys = 2 KB per step.
+// O += P_j V_j over the pair: 8 steps of 16 keys, M = 256, N = 256. P for
+// keys 32q..32q+31 sits in S columns 32q..32q+15 (bf16 pairs); B = the V half
+// tile, MN-major: its two 64-dim blocks 16 KB apart (the leading offset),
+// 8-key groups 1 KB apart, 16 keys = 2 KB per step.
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t ring_v,
                                          uint32_t slot, bool accumulate_first) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
+  constexpr uint32_t idesc = idesc_bf16_f32(256, 256, 0, 1);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    const uint64_t b = ring_v + (uint64_t)((slot * kTileBytes + kk * 2048) >> 4);
-    mma_bf16_ts(tmem_o, tmem_p + 16 * kk, b, idesc, (accumulate_first || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t b = ring_v + (uint64_t)((slot * kSlotBytes + kk * 2048) >> 4);
+    mma_pair_ts(tmem_o, tmem_p + 32 * (kk >> 1) + 8 * (kk & 1), b, idesc,
+                (accumulate_first || kk > 0) ? 1u : 0u);
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    gated_attention_kernel(const __grid_constant__ GatedAttnArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gated_attention_pair_kernel(const __grid_constant__ GatedAttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
   float* xchg = reinterpret_cast<float*>(smem + OFF_XCHG);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: the even CTA, which issues the MMAs
 
-  // ---- work item: longest CTAs first ---------------------------------------
+  // ---- work item: longest pairs first ---------------------------------------
   const int bk_count = a.B * a.Hkv;
-  const int mt = a.n_mtiles - 1 - (int)(blockIdx.x / bk_count);
-  const int bk = (int)(blockIdx.x % bk_count);
+  const int pair = (int)(blockIdx.x >> 1);
+  const int pm = a.n_mtiles - 1 - pair / bk_count;
+  const int bk = pair % bk_count;
   const int b = bk / a.Hkv, kv = bk % a.Hkv;
   const int g = a.g;
-  const int t0 = mt * (BM / g);
-  const int t_last = min(t0 + BM / g, a.T) - 1;
+  const int tile_tok = BM / g;
+  const int t0_pair = pm * 2 * tile_tok;
+  const int t0 = t0_pair + (int)rank * tile_tok;  // this CTA's first token
+  const int t_last = min(t0_pair + 2 * tile_tok, a.T) - 1;
   const int n_tiles = t_last / BN + 1;
   const float bound = *a.logit_bound;
   const bool fixed_max = bound >= 0.f && bound <= kFixedMaxLimit;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_peer, 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->slot_full[s], 1);
+      mbar_init(&bars->slot_peer[s], 1);
       mbar_init(&bars->slot_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], kSoftmaxWGs * 4);  // one arrive per softmax warp
+      mbar_init(&bars->p_full[t], 2 * kSoftmaxWGs * 4);  // one arrive per softmax warp, both CTAs
     }
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->xmax_full, kSoftmaxWGs * 128);
@@ -162,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc<kTmemCols>(&bars->tmem_base);
+  if (warp == 0) tmem_alloc_pair<kTmemCols>(&bars->tmem_base);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort_flag;
@@ -178,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bars->q_full, 4 * kQBlock);
       for (int c = 0; c < 4; ++c)
         tma_load_4d(smem + OFF_Q + c * kQBlock, &a.tm_q, &bars->q_full, 64 * c, kv * g, t0, b);
-      uint32_t n = 0;  // tiles issued
+      uint32_t n = 0;  // half tiles issued
       bool ok = true;
       auto load_tile = [&](bool is_k, int j) {
         if (!ok) return;
@@ -187,14 +198,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           return;
         }
-        mbar_arrive_expect_tx(&bars->slot_full[s], kTileBytes);
-        uint8_t* dst = smem + OFF_RING + s * kTileBytes;
-        for (int c = 0; c < 4; ++c) {
-          if (is_k)
-            tma_load_3d(dst + c * kBlock, &a.tm_k, &bars->slot_full[s], 64 * c, j * BN,
-                        b * a.Hkv + kv);
-          else
-            tma_load_4d(dst + c * kBlock, &a.tm_v, &bars->slot_full[s], 64 * c, kv, j * BN, b);
+        mbar_arrive_expect_tx(&bars->slot_full[s], kSlotBytes);
+        uint8_t* dst = smem + OFF_RING + s * kSlotBytes;
+        if (is_k) {  // keys 64 rank .. of the tile, all 256 dims
+          for (int c = 0; c < 4; ++c)
+            tma_load_3d(dst + c * kKBlock, &a.tm_k, &bars->slot_full[s], 64 * c,
+                        j * BN + 64 * (int)rank, b * a.Hkv + kv);
+        } else {  // dims 128 rank .. of the tile, all 128 keys
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(dst + c * kVBlock, &a.tm_v, &bars->slot_full[s],
+                        128 * (int)rank + 64 * c, kv, j * BN, b);
         }
         ++n;
       };
@@ -210,15 +223,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t i = n > (uint32_t)kSlots ? n - kSlots : 0u; i < n; ++i)
           mbar_wait(&bars->slot_full[slot_of(i)], use_of(i), nullptr, 0, nullptr);
       }
-    } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == kSoftmaxWGs * 4 + 2 && lane == 0 && rank == 1) {
+      // ----------------------------------------------- forwarder (odd CTA)
+      // the even CTA's MMA issuer reads this CTA's Q and ring too: tell it
+      // when each of them has landed, in load order
+      const uint32_t n_loads = 2u * (uint32_t)n_tiles;
+      if (mbar_wait(&bars->q_full, 0, a.err, kDevTimeoutTma, abort)) {
+        mbar_arrive_cluster(peer_smem_addr(&bars->q_peer, 0));
+        for (uint32_t t = 0; t < n_loads; ++t) {
+          if (!mbar_poll(&bars->slot_full[slot_of(t)], use_of(t), a.err, kDevTimeoutTma, abort))
+            break;
+          mbar_arrive_cluster(peer_smem_addr(&bars->slot_peer[slot_of(t)], 0));
+        }
+      }
+    } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0 && rank == 0) {
+      // ------------------------------------------- MMA issuer (even CTA)
       const uint32_t q_addr = smem_u32(smem + OFF_Q);
       const uint32_t ring = smem_u32(smem + OFF_RING);
       const uint64_t q_desc = smem_desc_sw128(q_addr, 16, 1024);
-      const uint64_t ring_k = smem_desc_sw128(ring, 16, 1024);     // K-major K blocks
-      const uint64_t ring_v = smem_desc_sw128(ring, kBlock, 1024);  // MN-major V tiles
-      auto wait_tile = [&](uint32_t t) {
-        return mbar_poll(&bars->slot_full[slot_of(t)], use_of(t), a.err, kDevTimeoutMma, abort);
+      const uint64_t ring_k = smem_desc_sw128(ring, 16, 1024);        // K-major K halves
+      const uint64_t ring_v = smem_desc_sw128(ring, kVBlock, 1024);   // MN-major V halves
+      auto wait_tile = [&](uint32_t t) {  // both CTAs' halves of load t
+        return mbar_wait_cluster(&bars->slot_full[slot_of(t)], use_of(t), a.err,
+                                 kDevTimeoutMma, abort) &&
+               mbar_wait_cluster(&bars->slot_peer[slot_of(t)], use_of(t), a.err,
+                                 kDevTimeoutMma, abort);
       };
       // An mbarrier wait issued after a tcgen05.commit stalls this thread
       // until the commit resolves, which would let the tensor pipe drain
@@ -227,37 +256,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       // softmax j+2, which cannot start before softmax j+1 has produced
       // P_{j+1} anyway. (The online-max path commits after each PV, since its
       // softmax may wait for PV_j before producing P_{j+1}.)
-      auto wait_pv_inputs = [&](int j, uint32_t first) {
-        return mbar_poll(&bars->p_full[j & 1], (j >> 1) & 1, a.err, kDevTimeoutMma, abort) &&
-               wait_tile(first);
+      auto wait_pv_inputs = [&](int j, uint32_t t) {
+        return mbar_wait_cluster(&bars->p_full[j & 1], (j >> 1) & 1, a.err, kDevTimeoutMma,
+                                 abort) &&
+               wait_tile(t);
       };
-      uint32_t n = 0;  // tiles consumed
-      bool ok = mbar_poll(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) && wait_tile(0);
+      uint32_t n = 0;  // loads consumed
+      bool ok = mbar_wait_cluster(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) &&
+                mbar_wait_cluster(&bars->q_peer, 0, a.err, kDevTimeoutMma, abort) &&
+                wait_tile(0);
       if (ok) {
         tc_fence_after();
         issue_s(tmem, q_desc, ring_k, slot_of(0));
         n = 1;
         if (n_tiles > 1) {
           ok = wait_tile(1);  // K_1
-          mma_commit(&bars->s_full[0]);
+          mma_commit_pair(&bars->s_full[0]);
           if (ok) {
             tc_fence_after();
             issue_s(tmem + BN, q_desc, ring_k, slot_of(1));
             n = 2;
             ok = wait_pv_inputs(0, n);  // P_0, V_0
-            mma_commit(&bars->s_full[1]);
+            mma_commit_pair(&bars->s_full[1]);
           }
         } else {
-          mma_commit(&bars->s_full[0]);
+          mma_commit_pair(&bars->s_full[0]);
           ok = wait_pv_inputs(0, n);
         }
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        // P_j and V_j (tile n) have been waited for
+        // P_j and V_j (load n) have been waited for
         tc_fence_after();
         issue_pv(tmem + kTmemO, tmem + (j & 1) * BN, ring_v, slot_of(n), j > 0);
         n += 1;
-        if (!fixed_max) mma_commit(&bars->pv_done);
+        if (!fixed_max) mma_commit_pair(&bars->pv_done);
         const bool next_s = j + 2 < n_tiles;
         if (next_s) {
           ok = wait_tile(n);  // K_{j+2}
@@ -267,56 +299,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           n += 1;
         }
         if (j + 1 < n_tiles) ok = wait_pv_inputs(j + 1, n);  // P_{j+1}, V_{j+1}
-        if (next_s) mma_commit(&bars->s_full[j & 1]);
+        if (next_s) mma_commit_pair(&bars->s_full[j & 1]);
       }
-      if (ok) mma_commit(&bars->o_final);
+      if (ok) mma_commit_pair(&bars->o_final);
       // drain: every MMA issued above has completed once this phase completes
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, nullptr, 0, nullptr);
+      mma_commit_pair(&bars->drain);
+      mbar_wait_cluster(&bars->drain, 0, nullptr, 0, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax
     const int lq = warp & 3;   // TMEM lane quarter: rows 32 lq ..
-    const int cq = warp >> 2;  // key quarter of each S tile; O columns 64 cq ..
+    const int cq = warp >> 2;  // key quarter of each S tile (32 keys); O columns 64 cq ..
     const int r = lq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(lq * 32) << 16;
     const int tok = t0 + r / g;
     const int h = kv * g + (r % g);
+    const uint32_t p_full_even[2] = {peer_smem_addr(&bars->p_full[0], 0),
+                                     peer_smem_addr(&bars->p_full[1], 0)};
     float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
     float l = 0.f;
     bool ok = true;
-    uint32_t released = 0;  // ring blocks handed back (thread 0)
+    uint32_t released = 0;  // ring loads handed back (thread 0)
     for (int j = 0; j < n_tiles; ++j) {
-      ok = __all_sync(kFull, mbar_poll(&bars->s_full[j & 1], (j >> 1) & 1, a.err,
-                                       kDevTimeoutSoftmax, abort));
+      ok = __all_sync(kFull, mbar_wait_cluster(&bars->s_full[j & 1], (j >> 1) & 1, a.err,
+                                               kDevTimeoutSoftmax, abort));
       if (!ok) break;
       // S_j is complete and so is every earlier MMA: K_0..K_j and V_0..V_{j-2}
-      // (tiles 0 .. 2j-1 of the load order; tile 0 for j = 0) are no longer read
+      // (loads 0 .. 2j-1; load 0 for j = 0) are no longer read
       if (threadIdx.x == 0) {
         const uint32_t upto = j == 0 ? 1u : 2u * (uint32_t)j;
         for (; released < upto; ++released) mbar_arrive(&bars->slot_empty[slot_of(released)]);
       }
       tc_fence_after();
-      const uint32_t tmem_s = tmem + (j & 1) * BN + cq * 16 + lane_off;
-      uint32_t sr[16];
-      tmem_ld16_wait(tmem_s, sr);
-      float s[16];
+      const uint32_t tmem_s = tmem + (j & 1) * BN + cq * 32 + lane_off;
+      uint32_t sr[32];
+      tmem_ld32_wait(tmem_s, sr);
+      float s[32];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) s[e] = __uint_as_float(sr[e]);
-      const int key0 = j * BN + cq * 16;
-      if (key0 + 15 > tok) {
+      for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(sr[e]);
+      const int key0 = j * BN + cq * 32;
+      if (key0 + 31 > tok) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
+        for (int e = 0; e < 32; ++e)
           if (key0 + e > tok) s[e] = -INFINITY;
       }
       bool move = false;
       float alpha = 1.0f;
       if (!fixed_max) {
-        float mx = s[0];
+        float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int e = 1; e < 16; ++e) mx = fmaxf(mx, s[e]);
+        for (int e = 4; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[e]);
         float* xm = xchg + (j & 1) * 4 * 128;  // [quarter][128]
-        xm[cq * 128 + r] = mx;
+        xm[cq * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         mbar_arrive(&bars->xmax_full);
         ok = __all_sync(kFull, mbar_wait(&bars->xmax_full, j & 1, a.err, kDevTimeoutSoftmax,
                                          abort));
@@ -332,23 +366,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // p = 2^(s * scale - m), two at a time on the f32x2 pipes
       const uint64_t scale2 = f2_pack(kScaleLog2, kScaleLog2);
       const uint64_t negm2 = f2_pack(-m, -m);
-      uint64_t sum2 = f2_pack(0.f, 0.f);
-      uint32_t pw[8];
+      uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+      uint32_t pw[16];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
+      for (int e = 0; e < 16; ++e) {
         const uint64_t x = f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
         float x0, x1;
         f2_unpack(x, x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
-        sum2 = f2_add(sum2, f2_pack(p0, p1));
+        sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
         pw[e] = pack_bf16x2(p0, p1);
       }
-      tmem_st8_wait(tmem_s, pw);  // P over the first 8 of this thread's S columns
+      tmem_st16_wait(tmem_s, pw);  // P over the first 16 of this thread's S columns
       if (!fixed_max && j > 0 && __any_sync(kFull, move)) {
         // rescale this thread's O columns once PV_{j-1} has completed, before
         // PV_j adds terms relative to the new max
-        ok = __all_sync(kFull, mbar_wait(&bars->pv_done, (j - 1) & 1, a.err, kDevTimeoutSoftmax,
-                                         abort));
+        ok = __all_sync(kFull, mbar_wait_cluster(&bars->pv_done, (j - 1) & 1, a.err,
+                                                 kDevTimeoutSoftmax, abort));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -361,14 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32_wait(to, o);
         }
       }
-      float s0, s1;
-      f2_unpack(sum2, s0, s1);
-      l += s0 + s1;
+      float a0, a1, b0, b1;
+      f2_unpack(sum2[0], a0, a1);
+      f2_unpack(sum2[1], b0, b1);
+      l += (a0 + a1) + (b0 + b1);
       // the warp's tcgen05.st has completed (wait::st above, warp-collective):
-      // one arrive per warp publishes all 32 rows' P
+      // one arrive per warp, on the even CTA's barrier, publishes its 32 rows
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
+      if (lane == 0) mbar_arrive_cluster(p_full_even[j & 1]);
     }
     // ---- epilogue: the row's four partial sums, then O / l * sigmoid(gate)
     ok = __all_sync(kFull, ok && !*abort);
@@ -378,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_barrier_sync(1, kSoftmaxWGs * 128);
     if (ok) {
       l = (lsum[r] + lsum[128 + r]) + (lsum[256 + r] + lsum[384 + r]);
-      ok = __all_sync(kFull, mbar_wait(&bars->o_final, 0, a.err, kDevTimeoutEpilogue, abort));
+      ok = __all_sync(kFull, mbar_wait_cluster(&bars->o_final, 0, a.err, kDevTimeoutEpilogue,
+                                               abort));
     }
     if (ok) {
       tc_fence_after();
@@ -413,17 +449,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // both CTAs meet here once the pair's MMAs have drained and every TMEM
+  // access of either CTA is done; then each frees its tensor memory
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc<kTmemCols>(tmem);
+    tmem_dealloc_pair<kTmemCols>(tmem);
   }
 }
 
 }  // namespace
 
-int gated_tokens_per_cta(int g) { return BM / g; }
+int gated_tokens_per_cta(int g) { return 2 * (BM / g); }  // per pair of CTAs
 
 cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream) {
   static unsigned long long done_mask = 0;  // per-device dynamic smem opt-in
@@ -431,15 +470,15 @@ cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream) 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(done_mask & (1ull << dev))) {
-    e = cudaFuncSetAttribute(gated_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
+    e = cudaFuncSetAttribute(gated_attention_pair_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) done_mask |= 1ull << dev;
   }
-  const long long grid = (long long)a.n_mtiles * a.B * a.Hkv;
+  const long long grid = 2LL * a.n_mtiles * a.B * a.Hkv;
   if (grid == 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  gated_attention_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(a);
+  if (grid > 0x7ffffffeLL) return cudaErrorInvalidConfiguration;
+  gated_attention_pair_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
 

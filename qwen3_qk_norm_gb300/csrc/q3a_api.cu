@@ -516,7 +516,7 @@ static q3a_status gated_attention_args(GatedAttnArgs& ga, const q3a_bf16* qg, co
   const uint32_t bk[3] = {64, 64, 1};
   const uint64_t dv[4] = {kGatedD, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
   const uint64_t sv[3] = {row, (uint64_t)Hkv * row, (uint64_t)T * Hkv * row};
-  const uint32_t bv[4] = {64, 1, 64, 1};
+  const uint32_t bv[4] = {64, 1, 128, 1};
   if (encode_tensor_map(&ga.tm_q, gated_ws_q(workspace), 4, dq, sq, bq) != CUDA_SUCCESS ||
       encode_tensor_map(&ga.tm_k, gated_ws_k(workspace, B, T, Hq), 3, dk, sk, bk) !=
           CUDA_SUCCESS ||

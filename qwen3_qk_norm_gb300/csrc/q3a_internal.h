@@ -136,20 +136,21 @@ struct GatedPrologueArgs {
 int gated_prologue_max_heads();
 cudaError_t launch_gated_prologue(const GatedPrologueArgs& a, cudaStream_t stream);
 
-// K6: causal GQA attention over Qhat/Khat with the sigmoid output gate.
+// K6: causal GQA attention over Qhat/Khat with the sigmoid output gate, on
+// pairs of CTAs (clusters of two).
 struct GatedAttnArgs {
   CUtensorMap tm_q;  // Qhat [B, T, Hq, 256], box {64, g, 128/g, 1}
-  CUtensorMap tm_k;  // Khat [B*Hkv, T, 256], box {64, 128, 1}
+  CUtensorMap tm_k;  // Khat [B*Hkv, T, 256], box {64, 64, 1}
   CUtensorMap tm_v;  // V [B, T, Hkv, 256], box {64, 1, 128, 1}
   const uint16_t* qg;  // gate = qg[b, t, h, 256 .. 511]
   uint16_t* out;       // [B, T, Hq, 256] bf16
   uint32_t* err;
   const float* logit_bound;
   int B, T, Hq, Hkv, g;
-  int n_mtiles;  // ceil(T / gated_tokens_per_cta(g))
+  int n_mtiles;  // pair tiles: ceil(T / gated_tokens_per_cta(g))
 };
 cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream);
-int gated_tokens_per_cta(int g);
+int gated_tokens_per_cta(int g);  // tokens of one KV group that a pair of CTAs covers
 
 // ----- tensor maps -----------------------------------------------------------
 // cuTensorMapEncodeTiled (bf16, 128-byte swizzle, zero fill out of bounds),
