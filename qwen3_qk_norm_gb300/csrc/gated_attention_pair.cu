@@ -33,7 +33,10 @@
 //   warp 16  TMA producer of the CTA's Q tile and ring;
 //   warp 17  (even CTA) the MMA issuer of the pair;
 //   warp 18  (odd CTA) forwards its ring's "tile landed" events to the even
-//            CTA, whose MMA issuer waits for both halves.
+//            CTA, whose MMA issuer waits for both halves;
+//   warp 19  hands ring slots back to the producer as soon as the MMAs that
+//            read them complete: K_j's when S_j completes, V_j's when PV_j
+//            does (an arrive on "PV done" follows every PV).
 // TMEM per CTA: S0 | S1 (128 fp32 columns each, double-buffered) | O (256).
 // P goes back as bf16 pairs over the first half of each thread's own S
 // columns and PV reads it from there. MMA stream: S_0, S_1, then per KV tile
@@ -83,7 +86,7 @@ struct Bars {
   uint64_t slot_full[kSlots], slot_peer[kSlots], slot_empty[kSlots];
   uint64_t s_full[2];
   uint64_t p_full[2];  // even CTA: all 32 softmax warps of the pair
-  uint64_t pv_done;    // online-max path: PV_j complete (one phase per KV tile)
+  uint64_t pv_done;    // PV_j complete (one phase per KV tile)
   uint64_t xmax_full;  // online-max path: the CTA's four quarters posted their tile max
   uint64_t o_final;
   uint64_t drain;
@@ -236,6 +239,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_cluster(peer_smem_addr(&bars->slot_peer[slot_of(t)], 0));
         }
       }
+    } else if (warp == kSoftmaxWGs * 4 + 3 && lane == 0) {
+      // ------------------------------------------------------------ releaser
+      // Completion order on the tensor pipe: S_0, then per KV tile j:
+      // S_{j+1} (if any), PV_j. Load index of K_j: 0, then 2j - 1; of V_j:
+      // 2j + 2, except the last V at 2n - 1.
+      const int n = n_tiles;
+      if (mbar_wait_cluster(&bars->s_full[0], 0, a.err, kDevTimeoutSoftmax, abort)) {
+        mbar_arrive(&bars->slot_empty[slot_of(0)]);
+        for (int j = 0; j < n; ++j) {
+          if (j + 1 < n) {
+            if (!mbar_wait_cluster(&bars->s_full[(j + 1) & 1], ((j + 1) >> 1) & 1, a.err,
+                                   kDevTimeoutSoftmax, abort))
+              break;
+            mbar_arrive(&bars->slot_empty[slot_of((uint32_t)(2 * j + 1))]);
+          }
+          if (!mbar_wait_cluster(&bars->pv_done, j & 1, a.err, kDevTimeoutSoftmax, abort)) break;
+          mbar_arrive(&bars->slot_empty[slot_of((uint32_t)min(2 * j + 2, 2 * n - 1))]);
+        }
+      }
     } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0 && rank == 0) {
       // ------------------------------------------- MMA issuer (even CTA)
       const uint32_t q_addr = smem_u32(smem + OFF_Q);
@@ -250,17 +272,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                  kDevTimeoutMma, abort);
       };
       // An mbarrier wait issued after a tcgen05.commit stalls this thread
-      // until the commit resolves, which would let the tensor pipe drain
-      // every tile. So the inputs of the next PV (P_{j+1}, V_{j+1}) are waited
-      // for before the commit that publishes S_{j+2}; that commit only gates
-      // softmax j+2, which cannot start before softmax j+1 has produced
-      // P_{j+1} anyway. (The online-max path commits after each PV, since its
-      // softmax may wait for PV_j before producing P_{j+1}.)
+      // until the commit resolves. The waits for a PV's inputs (P, V and the
+      // K tile after next) are therefore placed after the queued MMAs that
+      // keep the tensor pipe busy meanwhile, and before the commit that
+      // publishes S_{j+2}: that commit only gates softmax j+2, which cannot
+      // start before softmax j+1 has produced P_{j+1} anyway.
       auto wait_pv_inputs = [&](int j, uint32_t t) {
         return mbar_wait_cluster(&bars->p_full[j & 1], (j >> 1) & 1, a.err, kDevTimeoutMma,
                                  abort) &&
                wait_tile(t);
       };
+      // load index of K_j: 0, then 2j - 1
+      auto k_load = [](int j) { return j == 0 ? 0u : (uint32_t)(2 * j - 1); };
       uint32_t n = 0;  // loads consumed
       bool ok = mbar_wait_cluster(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) &&
                 mbar_wait_cluster(&bars->q_peer, 0, a.err, kDevTimeoutMma, abort) &&
@@ -276,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_s(tmem + BN, q_desc, ring_k, slot_of(1));
             n = 2;
-            ok = wait_pv_inputs(0, n);  // P_0, V_0
+            ok = wait_pv_inputs(0, n) && (n_tiles <= 2 || wait_tile(k_load(2)));
             mma_commit_pair(&bars->s_full[1]);
           }
         } else {
@@ -285,20 +308,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        // P_j and V_j (load n) have been waited for
+        // P_j, V_j (load n) and K_{j+2} (load n + 1) have been waited for
         tc_fence_after();
         issue_pv(tmem + kTmemO, tmem + (j & 1) * BN, ring_v, slot_of(n), j > 0);
         n += 1;
-        if (!fixed_max) mma_commit_pair(&bars->pv_done);
+        mma_commit_pair(&bars->pv_done);
         const bool next_s = j + 2 < n_tiles;
         if (next_s) {
-          ok = wait_tile(n);  // K_{j+2}
-          if (!ok) break;
-          tc_fence_after();
           issue_s(tmem + (j & 1) * BN, q_desc, ring_k, slot_of(n));
           n += 1;
         }
-        if (j + 1 < n_tiles) ok = wait_pv_inputs(j + 1, n);  // P_{j+1}, V_{j+1}
+        if (j + 1 < n_tiles)  // P_{j+1}, V_{j+1}, K_{j+3}
+          ok = wait_pv_inputs(j + 1, n) && (j + 3 >= n_tiles || wait_tile(k_load(j + 3)));
         if (next_s) mma_commit_pair(&bars->s_full[j & 1]);
       }
       if (ok) mma_commit_pair(&bars->o_final);
@@ -319,17 +340,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
     float l = 0.f;
     bool ok = true;
-    uint32_t released = 0;  // ring loads handed back (thread 0)
     for (int j = 0; j < n_tiles; ++j) {
       ok = __all_sync(kFull, mbar_wait_cluster(&bars->s_full[j & 1], (j >> 1) & 1, a.err,
                                                kDevTimeoutSoftmax, abort));
       if (!ok) break;
-      // S_j is complete and so is every earlier MMA: K_0..K_j and V_0..V_{j-2}
-      // (loads 0 .. 2j-1; load 0 for j = 0) are no longer read
-      if (threadIdx.x == 0) {
-        const uint32_t upto = j == 0 ? 1u : 2u * (uint32_t)j;
-        for (; released < upto; ++released) mbar_arrive(&bars->slot_empty[slot_of(released)]);
-      }
       tc_fence_after();
       const uint32_t tmem_s = tmem + (j & 1) * BN + cq * 32 + lane_off;
       uint32_t sr[32];
