@@ -462,9 +462,11 @@ size_t q3a_gated_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d) {
 static q3a_status gated_check(const void* const* ptrs, int nptrs, int B, int T, int Hq, int Hkv,
                               int d, void* workspace, size_t ws_bytes, bool* empty) {
   *empty = false;
-  if (d != kGatedD || B < 0 || T < 0 || !group_ok(Hq, Hkv)) return Q3A_EINVAL;
+  if (d != kGatedD || B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return Q3A_EINVAL;
   if ((long long)B * T * Hq > 0x7fffffffLL || T > (1 << 30)) return Q3A_EINVAL;
   if (Hq + Hkv > gated_prologue_max_heads()) return Q3A_EINVAL;
+  // a valid grouping that the 128-row GQA packing does not cover (e.g. 24/4)
+  if (!group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;
   if (B == 0 || T == 0) {
     *empty = true;
     return Q3A_OK;

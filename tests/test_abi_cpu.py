@@ -182,8 +182,14 @@ def gated_call(lib, **kw):
                                  a["ws_bytes"], None)
 
 
+def test_gated_unsupported_group_is_notimpl(lib):
+    # Qwen3.5-27B-shaped grouping (24 query heads over 4 KV heads): valid, not implemented
+    assert gated_call(lib, Hq=24, Hkv=4) == binding.Q3A_ENOTIMPL
+    assert gated_call(lib, Hq=64, Hkv=2) == binding.Q3A_ENOTIMPL
+
+
 @pytest.mark.parametrize("kw", [dict(d=128), dict(d_rot=8), dict(d_rot=-16), dict(d_rot=272),
-                                dict(d_rot=65), dict(Hq=12, Hkv=2), dict(Hq=64, Hkv=1),
+                                dict(d_rot=65), dict(Hq=12, Hkv=5), dict(Hq=0, Hkv=1),
                                 dict(Hq=190, Hkv=10), dict(eps=0.0), dict(theta=0.5),
                                 dict(B=-1), dict(ws=FAKE + 16), dict(ws=0),
                                 dict(ws_bytes=4096)])
