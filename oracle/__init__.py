@@ -82,6 +82,9 @@ def _load():
             lib.q3a_oracle_gated_qknorm_rope.argtypes = [_u16p, l, _u16p, i, i, i, i, i, l, d,
                                                          d, _f64p]
             lib.q3a_oracle_gated_qknorm_rope.restype = i
+            lib.q3a_oracle_gated_decode.argtypes = ([_u16p] * 5 + [ctypes.c_void_p] + [_u16p] * 2
+                                                    + [i] * 5 + [l, d, d, _f64p, _f64p])
+            lib.q3a_oracle_gated_decode.restype = i
             _lib = lib
     return _lib
 
@@ -295,3 +298,27 @@ def gated_qknorm_rope(x, w, d: int, d_r: int, theta: float, eps: float,
     if rc:
         raise ValueError(f"oracle gated_qknorm_rope rejected its arguments ({rc})")
     return out
+
+
+def gated_decode(qg, k_new, v_new, k_cache, v_cache, start_pos, q_w, k_w, d_r: int,
+                 theta: float, eps: float):
+    """One gated decode step. qg [B,Hq,2d] (per head: query, then gate), k_new/v_new
+    [B,Hkv,d], caches [B,Hkv,S_max,d]. Returns (out fp64 [B,Hq,d], appended key
+    row fp64 [B,Hkv,d])."""
+    qg, k_new, v_new = _bf16(qg, "qg"), _bf16(k_new, "k_new"), _bf16(v_new, "v_new")
+    k_cache, v_cache = _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    q_w, k_w = _bf16(q_w, "q_w"), _bf16(k_w, "k_w")
+    B, Hq, d2 = qg.shape
+    Hkv, S_max, d = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    if d2 != 2 * d:
+        raise ValueError(f"qg last dim {d2} != 2 * {d}")
+    sp = torch.as_tensor(start_pos, dtype=torch.int32).contiguous()
+    out = torch.zeros((B, Hq, d), dtype=torch.float64)
+    k_row = torch.zeros((B, Hkv, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_gated_decode(_ptr(qg), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                         _ptr(v_cache), _ptr(sp), _ptr(q_w), _ptr(k_w), B, Hq,
+                                         Hkv, d, int(d_r), S_max, float(theta), float(eps),
+                                         _ptr(out), _ptr(k_row))
+    if rc:
+        raise ValueError(f"oracle gated_decode failed ({rc})")
+    return out, k_row

@@ -594,3 +594,68 @@ int q3a_oracle_gated_qknorm_rope(const uint16_t* x, long stride, const uint16_t*
   }
   return 0;
 }
+
+/* Gated decode: one new token per sequence at p = start_pos[b] (g1-g5 with the
+ * KV cache of §20.3): qhat from the query half of qg [B,Hq,2d] at p,
+ * khat_new = g3(g2(k_new)) at p; keys = cache rows 0..p-1 as stored, then
+ * khat_new; values = cache rows 0..p-1, then v_new; z = o * sigmoid(gate).
+ *   caches [B,Hkv,S_max,d]; out fp64 [B,Hq,d]; k_row fp64 [B,Hkv,d]. */
+int q3a_oracle_gated_decode(const uint16_t* qg, const uint16_t* k_new, const uint16_t* v_new,
+                            const uint16_t* k_cache, const uint16_t* v_cache,
+                            const int32_t* start_pos, const uint16_t* q_w, const uint16_t* k_w,
+                            int B, int Hq, int Hkv, int d, int d_r, long S_max, double theta,
+                            double eps, double* out, double* k_row) {
+  if (check_gated(B, 1, Hq, Hkv, d, d_r) || S_max <= 0 || !out || !k_row) return -1;
+  for (int b = 0; b < B; ++b)
+    if (start_pos[b] < 0 || (long)start_pos[b] + 1 > S_max) return -1;
+  int g = Hq / Hkv;
+  long units = (long)B * Hkv;
+  int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(OMP_THREADS)
+#endif
+  for (long u = 0; u < units; ++u) {
+    long b = u / Hkv, kv = u % Hkv;
+    long p = start_pos[b];
+    long nk = p + 1;
+    double* keys = (double*)malloc(sizeof(double) * (size_t)nk * d);
+    double* vals = (double*)malloc(sizeof(double) * (size_t)nk * d);
+    double* scores = (double*)malloc(sizeof(double) * (size_t)nk);
+    double* qhat = (double*)malloc(sizeof(double) * d);
+    if (!keys || !vals || !scores || !qhat) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      failed = 1;
+    } else {
+      const uint16_t* kc = k_cache + (b * Hkv + kv) * S_max * d;
+      const uint16_t* vc = v_cache + (b * Hkv + kv) * S_max * d;
+      for (long j = 0; j < p; ++j)
+        for (int c = 0; c < d; ++c) {
+          keys[j * d + c] = widen_bf16(kc[j * d + c]);
+          vals[j * d + c] = widen_bf16(vc[j * d + c]);
+        }
+      double* kn = keys + p * d;
+      q3a_oracle_zc_rmsnorm_row(k_new + (b * Hkv + kv) * d, k_w, d, eps, kn);
+      q3a_oracle_partial_rope_row(kn, d, d_r, (double)p, theta);
+      for (int c = 0; c < d; ++c) {
+        k_row[(b * Hkv + kv) * d + c] = kn[c];
+        vals[p * d + c] = widen_bf16(v_new[(b * Hkv + kv) * d + c]);
+      }
+      for (long h = kv * g; h < (kv + 1) * g; ++h) {
+        const uint16_t* qrow = qg + (b * Hq + h) * 2L * d; /* g1 */
+        const uint16_t* grow = qrow + d;
+        double* o = out + (b * Hq + h) * d;
+        q3a_oracle_zc_rmsnorm_row(qrow, q_w, d, eps, qhat);
+        q3a_oracle_partial_rope_row(qhat, d, d_r, (double)p, theta);
+        attend_row(qhat, keys, vals, nk, d, scores, o);
+        for (int c = 0; c < d; ++c) o[c] *= sigmoid(widen_bf16(grow[c]));
+      }
+    }
+    free(keys);
+    free(vals);
+    free(scores);
+    free(qhat);
+  }
+  return failed ? -2 : 0;
+}

@@ -24,6 +24,9 @@ Recipe (all draws from a ``torch.Generator`` seeded with the workload's seed):
            V [B,T,Hkv,d] ~ N(0,1) in fp32, in that order; then the zero-centred
            norm weights w_q, w_k ~ U(-0.5, 0.5) [d] (scales 1 + w in [0.5, 1.5],
            the range of the gammas above); rounded to bf16 at the end.
+  gated decode: start_pos as for decode; then cache K, cache V [B,Hkv,S_max,d]
+           ~ N(0,1) (rows start_pos[b].. set to NaN); then QG [B,Hq,2d], k_new,
+           v_new [B,Hkv,d] ~ N(0,1); then w_q, w_k ~ U(-0.5, 0.5).
 
 Large workloads are drawn on the GPU (``device="cuda"``) with torch's CUDA
 generator; small ones on the CPU. Either way the draws are deterministic for a
@@ -39,7 +42,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "prefill", "decode", "chunk" or "gated"
+    kind: str  # "prefill", "decode", "chunk", "gated" or "gated_decode"
     B: int
     Hq: int
     Hkv: int
@@ -86,6 +89,9 @@ WORKLOADS = {
         Workload("qwen3.5-397b-gated-b1-t8192", "gated", B=1, T=8192, Hq=32, Hkv=2, d=256,
                  d_r=64, theta=1e7, seed=8,
                  note="Qwen3.5-397B-A17B-shaped gated global attention prefill (g = 16)"),
+        Workload("qwen3-next-80b-gated-decode-b64", "gated_decode", B=64, Hq=16, Hkv=2, d=256,
+                 S_max=32768, sp_lo=1024, sp_hi=32768, d_r=64, theta=1e7, seed=9,
+                 note="Qwen3-Next-80B-A3B-shaped gated decode, start_pos ~ U[1024, 32768)"),
     ]
 }
 
@@ -161,7 +167,37 @@ def gated_inputs(B: int, T: int, Hq: int, Hkv: int, d: int = 256, seed: int = 0,
     return dict(qg=qg.to(bf), k=k.to(bf), v=v.to(bf), q_w=q_w.to(bf), k_w=k_w.to(bf))
 
 
+def gated_decode_inputs(B: int, Hq: int, Hkv: int, S_max: int, sp_lo: int, sp_hi: int,
+                        d: int = 256, seed: int = 0, device="cpu", start_pos=None) -> dict:
+    """Gated decode-step inputs. ``start_pos`` (host int32 [B]) is drawn unless given."""
+    dev = torch.device(device)
+    if start_pos is None:
+        start_pos = torch.randint(sp_lo, sp_hi, (B,), generator=_gen("cpu", seed),
+                                  dtype=torch.int64).to(torch.int32)
+    else:
+        start_pos = torch.as_tensor(start_pos, dtype=torch.int32).clone()
+    g = _gen(dev, seed + 7919)
+    bf = torch.bfloat16
+    k_cache = torch.randn((B, Hkv, S_max, d), generator=g, device=dev, dtype=bf)
+    v_cache = torch.randn((B, Hkv, S_max, d), generator=g, device=dev, dtype=bf)
+    f32 = torch.float32
+    qg = torch.randn((B, Hq, 2 * d), generator=g, device=dev, dtype=f32)
+    k_new = torch.randn((B, Hkv, d), generator=g, device=dev, dtype=f32)
+    v_new = torch.randn((B, Hkv, d), generator=g, device=dev, dtype=f32)
+    q_w = torch.rand((d,), generator=g, device=dev, dtype=f32) - 0.5
+    k_w = torch.rand((d,), generator=g, device=dev, dtype=f32) - 0.5
+    for b in range(B):
+        p = int(start_pos[b])
+        k_cache[b, :, p:, :] = float("nan")
+        v_cache[b, :, p:, :] = float("nan")
+    return dict(qg=qg.to(bf), k_new=k_new.to(bf), v_new=v_new.to(bf), k_cache=k_cache,
+                v_cache=v_cache, start_pos=start_pos, q_w=q_w.to(bf), k_w=k_w.to(bf))
+
+
 def workload_inputs(w: Workload, device="cpu") -> dict:
+    if w.kind == "gated_decode":
+        return gated_decode_inputs(w.B, w.Hq, w.Hkv, w.S_max, w.sp_lo, w.sp_hi, w.d, w.seed,
+                                   device=device)
     if w.kind == "gated":
         return gated_inputs(w.B, w.T, w.Hq, w.Hkv, w.d, w.seed, device=device)
     if w.kind == "chunk":  # whole prompts; the caller splits them

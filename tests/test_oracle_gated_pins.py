@@ -318,3 +318,103 @@ def test_gated_qknorm_rope_rows_are_the_pinned_steps():
                 ref = oracle.partial_rope_row(
                     oracle.zc_rmsnorm_row(x["qg"][b, t, h, :32], x["q_w"], 1e-6), 8, 4 + t, 1e7)
                 assert torch.equal(got[b, t, h], ref)
+
+
+# ----------------------------------------------------------------------------
+# Gated decode (§20.3's cache protocol on the gated layer)
+# ----------------------------------------------------------------------------
+
+def test_gated_decode_at_position_zero_is_gated_v_new():
+    """One key: the attention output is v_new, so z = v_new * sigmoid(gate)."""
+    B, Hq, Hkv, S, d = 2, 4, 2, 3, 32
+    x = inputs.gated_decode_inputs(B, Hq, Hkv, S, 0, 1, d=d, seed=40, start_pos=[0, 0])
+    out, k_row = oracle.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"],
+                                     x["v_cache"], x["start_pos"], x["q_w"], x["k_w"], 8, 1e7,
+                                     1e-6)
+    for b in range(B):
+        for h in range(Hq):
+            gate = x["qg"][b, h, d:].to(torch.float64)
+            ref = x["v_new"][b, h // 2].to(torch.float64) / (1.0 + torch.exp(-gate))
+            assert torch.allclose(out[b, h], ref, atol=1e-15, rtol=1e-15)
+        for kv in range(Hkv):  # RoPE at position 0 is the identity
+            assert torch.equal(k_row[b, kv], oracle.zc_rmsnorm_row(x["k_new"][b, kv], x["k_w"],
+                                                                   1e-6))
+
+
+def _brute_force_gated_decode(x, d_r, theta, eps):
+    qg = x["qg"].to(torch.float64)
+    B, Hq, d2 = qg.shape
+    d = d2 // 2
+    kn, vn = x["k_new"].to(torch.float64).tolist(), x["v_new"].to(torch.float64).tolist()
+    kc, vc = x["k_cache"].to(torch.float64), x["v_cache"].to(torch.float64)
+    sq = [1.0 + e for e in x["q_w"].to(torch.float64).tolist()]
+    sk = [1.0 + e for e in x["k_w"].to(torch.float64).tolist()]
+    Hkv = len(kn[0])
+    g, half = Hq // Hkv, d_r // 2
+
+    def norm(row, scale):
+        inv = 1.0 / math.sqrt(math.fsum(e * e for e in row) / d + eps)
+        return [row[c] * inv * scale[c] for c in range(d)]
+
+    def rotate(row, p):
+        res = list(row)
+        for i in range(half):
+            ang = p * theta ** (-2.0 * i / d_r)
+            c, s = math.cos(ang), math.sin(ang)
+            res[i] = c * row[i] - s * row[i + half]
+            res[i + half] = s * row[i] + c * row[i + half]
+        return res
+
+    out = torch.zeros((B, Hq, d), dtype=torch.float64)
+    flat = qg.reshape(B, Hq * d2).tolist()
+    for b in range(B):
+        p = int(x["start_pos"][b])
+        for h in range(Hq):
+            kv = h // g
+            keys = [kc[b, kv, j].tolist() for j in range(p)] + [rotate(norm(kn[b][kv], sk), p)]
+            vals = [vc[b, kv, j].tolist() for j in range(p)] + [vn[b][kv]]
+            query = flat[b][h * d2:h * d2 + d]
+            gate = flat[b][h * d2 + d:h * d2 + 2 * d]
+            qh = rotate(norm(query, sq), p)
+            w = [math.exp(math.fsum(qh[c] * kr[c] for c in range(d)) / math.sqrt(d))
+                 for kr in keys]
+            z = math.fsum(w)
+            for c in range(d):
+                o = math.fsum(w[j] * vals[j][c] for j in range(len(keys))) / z
+                out[b, h, c] = o * math.exp(gate[c]) / (1.0 + math.exp(gate[c]))
+    return out
+
+
+def test_gated_decode_matches_brute_force_with_cache_used_as_stored():
+    x = inputs.gated_decode_inputs(2, 4, 2, 12, 3, 11, d=32, seed=41)
+    out, _ = oracle.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                                 x["start_pos"], x["q_w"], x["k_w"], 8, 1e7, 1e-6)
+    ref = _brute_force_gated_decode(x, 8, 1e7, 1e-6)
+    assert (out - ref).abs().max() < 1e-12
+
+
+def test_gated_decode_of_last_token_equals_last_prefill_row():
+    """Prefill -> decode equivalence on the gated layer: the cache holds the
+    rounded normalised+rotated keys, so agreement is to bf16 rounding."""
+    T, Hq, Hkv, d = 20, 4, 2, 256
+    x = inputs.gated_inputs(1, T, Hq, Hkv, d=d, seed=42)
+    full = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    khat = oracle.gated_qknorm_rope(x["k"], x["k_w"], d, 64, 1e7, 1e-6).to(torch.bfloat16)
+    S = T + 3
+    k_cache = torch.zeros((1, Hkv, S, d), dtype=torch.bfloat16)
+    v_cache = torch.zeros((1, Hkv, S, d), dtype=torch.bfloat16)
+    k_cache[0, :, : T - 1] = khat[0, : T - 1].transpose(0, 1)
+    v_cache[0, :, : T - 1] = x["v"][0, : T - 1].transpose(0, 1)
+    out, k_row = oracle.gated_decode(x["qg"][:, T - 1].contiguous(), x["k"][:, T - 1].contiguous(),
+                                     x["v"][:, T - 1].contiguous(), k_cache, v_cache, [T - 1],
+                                     x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    assert (out[0] - full[0, T - 1]).abs().max() < 1e-2
+    ref_k = oracle.gated_qknorm_rope(x["k"], x["k_w"], d, 64, 1e7, 1e-6)[0, T - 1]
+    assert torch.equal(k_row[0], ref_k)
+
+
+def test_gated_decode_rejects_context_overflow():
+    x = inputs.gated_decode_inputs(1, 2, 1, 4, 0, 1, d=16, seed=43, start_pos=[0])
+    with pytest.raises(ValueError):
+        oracle.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], [4],
+                            x["q_w"], x["k_w"], 4, 1e7, 1e-6)
