@@ -319,6 +319,38 @@ q3a_status q3a_gated_prefill_attention(const q3a_bf16* qg, const q3a_bf16* v, q3
                                        void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * q3a_gated_decode — one decode step of the gated global-attention layer of
+ * Qwen3-Next / Qwen3.5 against a KV cache, appending the new token
+ * ("Chapter 20, Qwen3 and Qwen3.5" §20.3 cache protocol, §20.4 layer).
+ *
+ *   qg      [B, Hq, 2d] bf16: per head, the query (first d) and the gate (last d).
+ *   k_new, v_new [B, Hkv, d] bf16: the new token's projected key and value.
+ *   k_cache, v_cache [B, Hkv, S_max, d] bf16, caller-owned: rows
+ *           0..start_pos[b]-1 are read as stored (normalised and rotated by
+ *           earlier calls with the same k_w, d_rot and theta); row start_pos[b]
+ *           receives the new token's normalised, rotated key and its value.
+ *   start_pos [B] int32 on the HOST: position of each sequence's new token.
+ *   q_w, k_w [d] bf16 zero-centred norm weights (scale 1 + w).
+ *   out     [B, Hq, d] bf16: sigmoid(gate) * softmax(q k^T / sqrt(d)) v.
+ *   d = 256; d_rot a multiple of 16 in 0..256; Hq / Hkv in {1, 2, 4, 8, 16}
+ *   (another whole ratio returns Q3A_ENOTIMPL); B <= 2048; S_max <= 2^30.
+ *   workspace: at least q3a_gated_decode_workspace_size() bytes, 256-byte
+ *           aligned, caller-owned, not shared by concurrent calls.
+ *   Every argument is checked before anything is written; a start_pos[b] < 0
+ *   or >= S_max returns Q3A_ERANGE with the caches untouched.
+ * ------------------------------------------------------------------------- */
+size_t q3a_gated_decode_workspace_size(int B, int Hq, int Hkv, int d, int S_max);
+
+q3a_status q3a_gated_decode(const q3a_bf16* qg, const q3a_bf16* k_new, const q3a_bf16* v_new,
+                            q3a_bf16* k_cache, q3a_bf16* v_cache,
+                            const int32_t* start_pos,
+                            const q3a_bf16* q_w, const q3a_bf16* k_w,
+                            q3a_bf16* out,
+                            int B, int Hq, int Hkv, int d, int d_rot, int S_max,
+                            double theta, float eps,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_last_device_error — reads, synchronously on `stream`, the error word
  * that the kernels of the last call which used `workspace` left in its first
  * bytes (prefill and decode workspaces both keep it at offset 0).

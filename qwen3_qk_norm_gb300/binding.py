@@ -23,7 +23,8 @@ EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size"
             "q3a_prefill_chunk", "q3a_decode_workspace_size",
             "q3a_decode", "q3a_decode_device_pos", "q3a_decode_noalloc",
             "q3a_last_device_error", "q3a_gated_prefill_workspace_size", "q3a_gated_prefill",
-            "q3a_gated_prefill_prologue", "q3a_gated_prefill_attention"]
+            "q3a_gated_prefill_prologue", "q3a_gated_prefill_attention",
+            "q3a_gated_decode_workspace_size", "q3a_gated_decode"]
 
 _lock = threading.Lock()
 _lib = None
@@ -88,6 +89,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_gated_prefill_prologue.restype = i
         lib.q3a_gated_prefill_attention.argtypes = [vp] * 3 + [i] * 5 + [vp, sz, vp]
         lib.q3a_gated_prefill_attention.restype = i
+        lib.q3a_gated_decode_workspace_size.argtypes = [i] * 5
+        lib.q3a_gated_decode_workspace_size.restype = sz
+        lib.q3a_gated_decode.argtypes = [vp] * 9 + [i] * 6 + [d, f, vp, sz, vp]
+        lib.q3a_gated_decode.restype = i
         _lib = lib
         return lib
 
@@ -375,4 +380,41 @@ def gated_prefill_attention(qg, v, out, workspace: torch.Tensor) -> torch.Tensor
                                             Hq, Hkv, d, workspace.data_ptr(), workspace.numel(),
                                             _stream(v.device))
     _raise(st, "q3a_gated_prefill_attention")
+    return out
+
+
+def gated_decode_workspace_size(B: int, Hq: int, Hkv: int, S_max: int, d: int = 256) -> int:
+    return int(load().q3a_gated_decode_workspace_size(B, Hq, Hkv, d, S_max))
+
+
+def gated_decode(qg, k_new, v_new, k_cache, v_cache, start_pos, q_w, k_w, d_rot: int,
+                 theta: float, eps: float, out=None,
+                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """One gated decode step: qg [B,Hq,512] (query | gate per head), k_new/v_new
+    [B,Hkv,256], caches [B,Hkv,S_max,256] (row start_pos[b] is appended), start_pos
+    host int32 [B] -> out [B,Hq,256]."""
+    B, Hq, d2 = qg.shape
+    d = d2 // 2
+    Hkv, S_max = k_cache.shape[1], k_cache.shape[2]
+    _check(qg, "qg")
+    _check(k_new, "k_new", (B, Hkv, d))
+    _check(v_new, "v_new", (B, Hkv, d))
+    _check(k_cache, "k_cache", (B, Hkv, S_max, d))
+    _check(v_cache, "v_cache", (B, Hkv, S_max, d))
+    _check(q_w, "q_w", (d,))
+    _check(k_w, "k_w", (d,))
+    sp = _host_positions(start_pos, B)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=qg.device)
+    _check(out, "out", (B, Hq, d))
+    need = gated_decode_workspace_size(B, Hq, Hkv, S_max, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=qg.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_gated_decode(qg.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                 k_cache.data_ptr(), v_cache.data_ptr(), sp.data_ptr(),
+                                 q_w.data_ptr(), k_w.data_ptr(), out.data_ptr(), B, Hq, Hkv, d,
+                                 int(d_rot), S_max, float(theta), float(eps),
+                                 workspace.data_ptr(), workspace.numel(), _stream(qg.device))
+    _raise(st, "q3a_gated_decode")
     return out

@@ -26,6 +26,15 @@
 // K4: grid (head, b), one thread per output column: merges the splits of a
 // head with their log-sum-exp weights and writes bf16.
 //
+// Gated decode (the global layer of Qwen3-Next / Qwen3.5, "Chapter 20, Qwen3
+// and Qwen3.5" §20.4): the same kernels at head_dim 256, with the query taken
+// from the first half of each head's 512-element query/gate block, the
+// zero-centred norm (scale 1 + w), RoPE on the first d_rot coordinates only
+// (frequencies theta^(-2i/d_rot)), and K4 multiplying each output column by
+// sigmoid of the gate half. A warp normalises one row there (lane L holds
+// elements 8L..8L+7; rotated pairs sit in lanes L and L + d_rot/16), and a
+// 64-key stage is 64 KB, so one CTA runs per SM with three stages in flight.
+//
 // The attention arithmetic is HBM-bound (about 4 flops per cache byte), so the
 // design goal is the copy engine never idling: 64 KB+ of loads in flight per
 // SM, no per-key shuffles, and the tensor cores doing the dot products.
@@ -40,22 +49,29 @@ constexpr int kKeysPerTile = 64;
 constexpr int kStages = 3;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr uint32_t kBox = 8192;                 // 64 keys x 64 d x bf16
-constexpr uint32_t kKTile = 2 * kBox;           // 64 keys x 128 d
-constexpr uint32_t kStageBytes = 2 * kKTile;    // K + V
-constexpr uint32_t OFF_STAGES = 0;
-constexpr uint32_t OFF_Q = OFF_STAGES + kStages * kStageBytes;  // bf16 [16][128]
-constexpr uint32_t OFF_KNEW = OFF_Q + 16 * 128 * 2;             // bf16 [128]
-constexpr uint32_t OFF_VNEW = OFF_KNEW + 256;                   // bf16 [128]
-constexpr uint32_t OFF_CS = OFF_VNEW + 256;                     // float2 [64]
-constexpr uint32_t OFF_BAR = OFF_CS + 512;
-constexpr uint32_t kSmemBytes = OFF_BAR + 128 + 1024;  // + alignment slack
-constexpr float kScaleLog2 = 0.12751743074380046f;     // log2(e) / sqrt(128)
+constexpr uint32_t kBox = 8192;  // 64 keys x 64 d x bf16
 constexpr float kRescaleThreshold = 8.0f;
 constexpr unsigned kFull = 0xffffffffu;
-// merge area (reuses the stage ring once every tile has been consumed)
-constexpr uint32_t kMergeAcc = kConsumerWarps * 16 * 128 * 4;
-static_assert(kMergeAcc + kConsumerWarps * 16 * 8 <= kStages * kStageBytes, "merge area");
+
+// Shared-memory layout for head_dim D (128 or 256).
+template <int D>
+struct DecLayout {
+  static constexpr uint32_t kKTile = (D / 64) * kBox;       // 64 keys x D
+  static constexpr uint32_t kStageBytes = 2 * kKTile;       // K + V
+  static constexpr uint32_t OFF_STAGES = 0;
+  static constexpr uint32_t OFF_Q = OFF_STAGES + kStages * kStageBytes;  // bf16 [16][D]
+  static constexpr uint32_t OFF_KNEW = OFF_Q + 16 * D * 2;              // bf16 [D]
+  static constexpr uint32_t OFF_VNEW = OFF_KNEW + D * 2;                // bf16 [D]
+  static constexpr uint32_t OFF_CS = OFF_VNEW + D * 2;                  // float2 [D / 2]
+  static constexpr uint32_t OFF_BAR = OFF_CS + D * 4;
+  static constexpr uint32_t kSmemBytes = OFF_BAR + 128 + 1024;  // + alignment slack
+  // merge area (reuses the stage ring once every tile has been consumed)
+  static constexpr uint32_t kMergeAcc = kConsumerWarps * 16 * D * 4;
+  static_assert(kMergeAcc + kConsumerWarps * 16 * 8 <= kStages * kStageBytes, "merge area");
+  static constexpr int kMinBlocks = D == 128 ? 2 : 1;  // CTAs per SM the registers allow for
+  static constexpr float kScaleLog2 = D == 128 ? 0.12751743074380046f   // log2(e) / sqrt(128)
+                                               : 0.09016844005556021f;  // log2(e) / sqrt(256)
+};
 
 struct DecBars {
   uint64_t full[kStages], empty[kStages];
@@ -85,8 +101,8 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// byte offset of 16-byte chunk gc (0..15 over d) of tile row kt (0..63) in a
-// [64 keys][128 d] tile stored as two 128-byte-swizzled [64][64] boxes
+// byte offset of 16-byte chunk gc (0..D/8-1 over d) of tile row kt (0..63) in a
+// [64 keys][D] tile stored as D/64 128-byte-swizzled [64][64] boxes
 __device__ __forceinline__ uint32_t tile_chunk(int kt, int gc) {
   return (gc >> 3) * kBox + kt * 128 + ((((gc & 7) ^ (kt & 7))) << 4);
 }
@@ -102,9 +118,30 @@ __device__ __forceinline__ int decode_pos(const DecodeArgs& a, int b) {
   return kDevPos ? a.pos_dev[b] : a.start_pos[b];
 }
 
-template <bool kDevPos>
-__global__ void __launch_bounds__(kThreads, 2)
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x);
+  f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y);
+  f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z);
+  f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w);
+  f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+template <int D, bool kGated, bool kDevPos>
+__global__ void __launch_bounds__(kThreads, DecLayout<D>::kMinBlocks)
     decode_split_kernel(const __grid_constant__ DecodeArgs a) {
+  using L_ = DecLayout<D>;
+  constexpr uint32_t kKTile = L_::kKTile, kStageBytes = L_::kStageBytes;
+  constexpr uint32_t OFF_STAGES = L_::OFF_STAGES, OFF_Q = L_::OFF_Q, OFF_KNEW = L_::OFF_KNEW;
+  constexpr uint32_t OFF_VNEW = L_::OFF_VNEW, OFF_CS = L_::OFF_CS, OFF_BAR = L_::OFF_BAR;
+  constexpr float kScaleLog2 = L_::kScaleLog2;
   const int c = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
   if (kDevPos && *a.pos_valid == 0) return;  // some position out of range: write nothing
   const int p = decode_pos<kDevPos>(a, b);
@@ -136,7 +173,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < 64) cs[threadIdx.x] = rope_cos_sin(p, a.turn_freq[threadIdx.x]);
+  if constexpr (kGated) {
+    for (int i = threadIdx.x; i < (a.d_rot >> 1); i += kThreads)
+      cs[i] = rope_cos_sin(p, a.turn_freq[i]);
+  } else if (threadIdx.x < 64) {
+    cs[threadIdx.x] = rope_cos_sin(p, a.turn_freq[threadIdx.x]);
+  }
   __syncthreads();
   volatile int* abort = &bars->abort_flag;
 
@@ -153,10 +195,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int key0 = key_begin + i * kKeysPerTile;
         uint8_t* st = smem + OFF_STAGES + s * kStageBytes;
         mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
-        tma_load_3d(st, &a.tm_kc, &bars->full[s], 0, key0, (int)bkv);
-        tma_load_3d(st + kBox, &a.tm_kc, &bars->full[s], 64, key0, (int)bkv);
-        tma_load_3d(st + kKTile, &a.tm_vc, &bars->full[s], 0, key0, (int)bkv);
-        tma_load_3d(st + kKTile + kBox, &a.tm_vc, &bars->full[s], 64, key0, (int)bkv);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(st + c * kBox, &a.tm_kc, &bars->full[s], 64 * c, key0, (int)bkv);
+          tma_load_3d(st + kKTile + c * kBox, &a.tm_vc, &bars->full[s], 64 * c, key0, (int)bkv);
+        }
         issued = i + 1;
       }
       if (*abort) {
@@ -169,8 +212,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ---------------------------------------------------------------- consumers
   // 1. qhat for the g heads (rows g..15 zero), and khat_new / v_new if this
-  //    split holds position p. Rows are processed two per warp (half-warps).
-  {
+  //    split holds position p.
+  if constexpr (!kGated) {
+    // Qwen3, d = 128: two rows per warp (half-warps), QK-Norm with gamma,
+    // rotate-half RoPE over all 128 coordinates
     const int lane16 = lane & 15;
     float glq[4], ghq[4], glk[4], ghk[4];
     unpack4(reinterpret_cast<const uint2*>(a.q_gamma)[lane16], glq);
@@ -221,23 +266,81 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int idx = threadIdx.x; idx < (16 - g) * 64; idx += 128)
       reinterpret_cast<uint32_t*>(qs + g * 128)[idx] = 0u;
   }
+  if constexpr (kGated) {
+    // gated layer, d = 256: one row per warp, zero-centred norm (scale 1 + w),
+    // RoPE of the first d_rot coordinates; the query is the first half of the
+    // head's 512-element query/gate block
+    float sq[8], sk[8];
+    unpack8(reinterpret_cast<const uint4*>(a.q_gamma)[lane], sq);
+    unpack8(reinterpret_cast<const uint4*>(a.k_gamma)[lane], sk);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sq[e] += 1.0f;
+      sk[e] += 1.0f;
+    }
+    const int hl = a.d_rot >> 4;  // rotated pairs sit in lanes L and L + hl
+    const bool rotated = lane < 2 * hl;
+    const bool lower = lane < hl;
+    const int partner = rotated ? (lower ? lane + hl : lane - hl) : lane;
+    const int ang0 = rotated ? 8 * (lower ? lane : lane - hl) : 0;
+    const int n_rows = g + (holds_new ? 1 : 0);
+    for (int r = warp; r < n_rows; r += kConsumerWarps) {
+      const bool is_k = r == g;
+      const uint16_t* src =
+          is_k ? a.k_new + bkv * D : a.q + ((long long)b * a.Hq + (long long)kv * g + r) * (2 * D);
+      float x[8], y[8], o8[8];
+      unpack8(reinterpret_cast<const uint4*>(src)[lane], x);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(kFull, ss, off);
+      const float inv_rms = rsqrtf(ss * (1.0f / D) + a.eps);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = x[e] * inv_rms * (is_k ? sk[e] : sq[e]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float yp = __shfl_sync(kFull, y[e], partner);
+        if (rotated) {
+          const float2 c_s = cs[ang0 + e];
+          o8[e] = lower ? y[e] * c_s.x - yp * c_s.y : y[e] * c_s.x + yp * c_s.y;
+        } else {
+          o8[e] = y[e];
+        }
+      }
+      const uint4 packed = pack8(o8);
+      if (is_k) {
+        // append: k_cache[b, kv, p] = bf16(khat_new), v_cache[b, kv, p] = v_new
+        const uint4 vn = reinterpret_cast<const uint4*>(a.v_new + bkv * D)[lane];
+        reinterpret_cast<uint4*>(a.k_cache + (bkv * a.S_max + p) * D)[lane] = packed;
+        reinterpret_cast<uint4*>(a.v_cache + (bkv * a.S_max + p) * D)[lane] = vn;
+        reinterpret_cast<uint4*>(knew_s)[lane] = packed;
+        reinterpret_cast<uint4*>(vnew_s)[lane] = vn;
+      } else {
+        reinterpret_cast<uint4*>(qs + r * D)[lane] = packed;
+      }
+    }
+    // zero the padding rows g..15 of qhat
+    for (int idx = threadIdx.x; idx < (16 - g) * (D / 2); idx += 128)
+      reinterpret_cast<uint32_t*>(qs + g * D)[idx] = 0u;
+  }
   consumer_sync();
 
-  // 2. A fragments of qhat (16 x 128): rows lane/4 and lane/4 + 8
+  // 2. A fragments of qhat (16 x D): rows lane/4 and lane/4 + 8
   const int r0 = lane >> 2, cq = lane & 3;
-  uint32_t qa[8][4];
+  uint32_t qa[D / 16][4];
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
+  for (int ks = 0; ks < D / 16; ++ks) {
     const int col = ks * 16 + 2 * cq;
-    qa[ks][0] = *reinterpret_cast<const uint32_t*>(qs + r0 * 128 + col);
-    qa[ks][1] = *reinterpret_cast<const uint32_t*>(qs + (r0 + 8) * 128 + col);
-    qa[ks][2] = *reinterpret_cast<const uint32_t*>(qs + r0 * 128 + col + 8);
-    qa[ks][3] = *reinterpret_cast<const uint32_t*>(qs + (r0 + 8) * 128 + col + 8);
+    qa[ks][0] = *reinterpret_cast<const uint32_t*>(qs + r0 * D + col);
+    qa[ks][1] = *reinterpret_cast<const uint32_t*>(qs + (r0 + 8) * D + col);
+    qa[ks][2] = *reinterpret_cast<const uint32_t*>(qs + r0 * D + col + 8);
+    qa[ks][3] = *reinterpret_cast<const uint32_t*>(qs + (r0 + 8) * D + col + 8);
   }
 
-  float o[16][4];
+  float o[D / 8][4];
 #pragma unroll
-  for (int dn = 0; dn < 16; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+  for (int dn = 0; dn < D / 8; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
   float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
 
   bool ok = true;
@@ -255,16 +358,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int rr = 0; rr < 16; ++rr) {
           const int key = kw0 + rr;
           if (key < L - 1) continue;
-          const int gc = lane & 15;
           const bool is_v = lane >= 16;
-          uint8_t* dst = st + (is_v ? kKTile : 0) + tile_chunk(kt0 + rr, gc);
-          uint4 val = make_uint4(0u, 0u, 0u, 0u);
-          if (key == L - 1) {
-            val = reinterpret_cast<const uint4*>(is_v ? vnew_s : knew_s)[gc];
-          } else if (!is_v) {
-            continue;  // keys past the end are masked; only their values are zeroed
+          // keys past the end are masked; only their values are zeroed
+          if (key != L - 1 && !is_v) continue;
+#pragma unroll
+          for (int gc = lane & 15; gc < D / 8; gc += 16) {
+            uint8_t* dst = st + (is_v ? kKTile : 0) + tile_chunk(kt0 + rr, gc);
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (key == L - 1) val = reinterpret_cast<const uint4*>(is_v ? vnew_s : knew_s)[gc];
+            *reinterpret_cast<uint4*>(dst) = val;
           }
-          *reinterpret_cast<uint4*>(dst) = val;
         }
         __syncwarp();
       }
@@ -277,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
         const int kt = kt0 + nt * 8 + (lane & 7);
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
+        for (int kp = 0; kp < D / 32; ++kp) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kbase + tile_chunk(kt, 4 * kp + (lane >> 3)), b0, b1, b2, b3);
           mma16816(sc[nt], qa[2 * kp], b0, b1);
@@ -308,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         lA *= alA;
         lB *= alB;
 #pragma unroll
-        for (int dn = 0; dn < 16; ++dn) {
+        for (int dn = 0; dn < D / 8; ++dn) {
           o[dn][0] *= alA;
           o[dn][1] *= alA;
           o[dn][2] *= alB;
@@ -327,10 +430,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
                               pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
-      // O += P V over the 16 keys: 16 n8 tiles of d
+      // O += P V over the 16 keys: D/8 n8 tiles of d
       const int vkt = kt0 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
+      for (int dp = 0; dp < D / 16; ++dp) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vbase + tile_chunk(vkt, 2 * dp + (lane >> 4)), b0, b1, b2, b3);
         mma16816(o[2 * dp], pa, b0, b1);
@@ -348,15 +451,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   lB += __shfl_xor_sync(kFull, lB, 2);
   consumer_sync();  // every consumer is past its last tile read
   ok = ok && !*abort;
-  float* acc_s = reinterpret_cast<float*>(smem + OFF_STAGES);  // [4][16][128]
-  float* ml_s = acc_s + kConsumerWarps * 16 * 128;             // [4][16][2]
+  float* acc_s = reinterpret_cast<float*>(smem + OFF_STAGES);  // [4][16][D]
+  float* ml_s = acc_s + kConsumerWarps * 16 * D;               // [4][16][2]
 #pragma unroll
-  for (int dn = 0; dn < 16; ++dn) {
+  for (int dn = 0; dn < D / 8; ++dn) {
     const int col = dn * 8 + 2 * cq;
-    acc_s[(warp * 16 + r0) * 128 + col] = o[dn][0];
-    acc_s[(warp * 16 + r0) * 128 + col + 1] = o[dn][1];
-    acc_s[(warp * 16 + r0 + 8) * 128 + col] = o[dn][2];
-    acc_s[(warp * 16 + r0 + 8) * 128 + col + 1] = o[dn][3];
+    acc_s[(warp * 16 + r0) * D + col] = o[dn][0];
+    acc_s[(warp * 16 + r0) * D + col + 1] = o[dn][1];
+    acc_s[(warp * 16 + r0 + 8) * D + col] = o[dn][2];
+    acc_s[(warp * 16 + r0 + 8) * D + col + 1] = o[dn][3];
   }
   if (cq == 0) {
     ml_s[(warp * 16 + r0) * 2] = mA;
@@ -366,9 +469,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   consumer_sync();
   if (!ok) return;
-  float* part = a.partial + ((bkv * a.split_stride + c) * g) * kDecodePartialFloats;
-  for (int idx = threadIdx.x; idx < g * 128; idx += 128) {
-    const int h = idx >> 7, d = idx & 127;
+  constexpr int kPartial = decode_partial_floats(D);
+  float* part = a.partial + ((bkv * a.split_stride + c) * g) * kPartial;
+  for (int idx = threadIdx.x; idx < g * D; idx += 128) {
+    const int h = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ml_s[(w * 16 + h) * 2]);
@@ -378,9 +482,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float mw = ml_s[(w * 16 + h) * 2];
       const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
       lsum += wt * ml_s[(w * 16 + h) * 2 + 1];
-      acc += wt * acc_s[(w * 16 + h) * 128 + d];
+      acc += wt * acc_s[(w * 16 + h) * D + d];
     }
-    float* ph = part + h * kDecodePartialFloats;
+    float* ph = part + h * kPartial;
     if (d == 0) {
       ph[0] = M;
       ph[1] = lsum;
@@ -389,16 +493,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <bool kDevPos>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
+template <int D, bool kGated, bool kDevPos>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
+  constexpr int kPartial = decode_partial_floats(D);
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
   if (kDevPos && *a.pos_valid == 0) return;
   const int g = a.g, kv = h / g, j = h % g;
   const int L = decode_pos<kDevPos>(a, b) + 1;
   const int n_splits = (L + kDecodeChunk - 1) / kDecodeChunk;
   const float* base =
-      a.partial + ((((long long)b * a.Hkv + kv) * a.split_stride) * g + j) * kDecodePartialFloats;
-  const long long split_step = (long long)g * kDecodePartialFloats;
+      a.partial + ((((long long)b * a.Hkv + kv) * a.split_stride) * g + j) * kPartial;
+  const long long split_step = (long long)g * kPartial;
   float M = -INFINITY;
   for (int c = 0; c < n_splits; ++c) M = fmaxf(M, base[c * split_step]);
   float lsum = 0.f, acc = 0.f;
@@ -408,8 +513,15 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     lsum += wt * pc[1];
     acc += wt * pc[2 + d];
   }
-  const float v = acc / lsum;
-  a.out[((long long)b * a.Hq + h) * 128 + d] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
+  float v = acc / lsum;
+  if constexpr (kGated) {
+    // z = o * sigmoid(gate), the gate being the second half of the head's
+    // query/gate block: sigmoid(x) = 1 / (1 + 2^(-x log2 e))
+    const float gt = __uint_as_float((uint32_t)a.q[((long long)b * a.Hq + h) * (2 * D) + D + d]
+                                     << 16);
+    v *= 1.0f / (1.0f + ex2(-1.4426950408889634f * gt));
+  }
+  a.out[((long long)b * a.Hq + h) * D + d] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
 }
 
 // Device-side validation of positions that live in device memory: every
@@ -431,16 +543,18 @@ __global__ void __launch_bounds__(256) decode_pos_check_kernel(const int32_t* po
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+template <int D, bool kGated>
+static cudaError_t launch(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr uint32_t kSmemBytes = DecLayout<D>::kSmemBytes;
   static unsigned long long attr_done_mask = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(attr_done_mask & (1ull << dev))) {
-    e = cudaFuncSetAttribute(decode_split_kernel<false>,
+    e = cudaFuncSetAttribute(decode_split_kernel<D, kGated, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_split_kernel<true>,
+    e = cudaFuncSetAttribute(decode_split_kernel<D, kGated, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_done_mask |= 1ull << dev;
@@ -454,17 +568,26 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     decode_pos_check_kernel<<<1, 256, 0, stream>>>(a.pos_dev, a.B, a.S_max, a.err, a.pos_valid);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_split_kernel<true><<<grid1, kThreads, kSmemBytes, stream>>>(a);
+    decode_split_kernel<D, kGated, true><<<grid1, kThreads, kSmemBytes, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<true><<<grid2, 128, 0, stream>>>(a);
+    decode_combine_kernel<D, kGated, true><<<grid2, D, 0, stream>>>(a);
     return cudaGetLastError();
   }
-  decode_split_kernel<false><<<grid1, kThreads, kSmemBytes, stream>>>(a);
+  decode_split_kernel<D, kGated, false><<<grid1, kThreads, kSmemBytes, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<false><<<grid2, 128, 0, stream>>>(a);
+  decode_combine_kernel<D, kGated, false><<<grid2, D, 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  return launch<128, false>(a, stream);
+}
+
+cudaError_t launch_gated_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.d_rot < 0 || a.d_rot > 256 || (a.d_rot & 15)) return cudaErrorInvalidValue;
+  return launch<kGatedD, true>(a, stream);
 }
 
 }  // namespace q3a

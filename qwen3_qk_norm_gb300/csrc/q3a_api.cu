@@ -587,6 +587,78 @@ q3a_status q3a_gated_prefill_attention(const q3a_bf16* qg, const q3a_bf16* v, q3
   return from_cuda(launch_gated_attention(aa, static_cast<cudaStream_t>(stream)));
 }
 
+size_t q3a_gated_decode_workspace_size(int B, int Hq, int Hkv, int d, int S_max) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || d != kGatedD || S_max <= 0 || Hq % Hkv) return 0;
+  const size_t parts = (size_t)B * Hkv * decode_split_stride(S_max) * (Hq / Hkv) *
+                       decode_partial_floats(kGatedD) * sizeof(float);
+  return kHeader + align256(parts);
+}
+
+q3a_status q3a_gated_decode(const q3a_bf16* qg, const q3a_bf16* k_new, const q3a_bf16* v_new,
+                            q3a_bf16* k_cache, q3a_bf16* v_cache, const int32_t* start_pos,
+                            const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out, int B,
+                            int Hq, int Hkv, int d, int d_rot, int S_max, double theta, float eps,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  if (d != kGatedD || B < 0 || B > kDecodeMaxB || S_max <= 0 || Hq <= 0 || Hkv <= 0 ||
+      Hq % Hkv)
+    return Q3A_EINVAL;
+  if (S_max > (1 << 30) || !d_rot_ok(d_rot)) return Q3A_EINVAL;
+  if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
+  if (!group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;  // the MMA rows hold at most 16 heads
+  if (B == 0) return Q3A_OK;
+  const void* ptrs[] = {qg, k_new, v_new, k_cache, v_cache, q_w, k_w, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return Q3A_EINVAL;
+  if (!start_pos) return Q3A_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
+  if (ws_bytes < q3a_gated_decode_workspace_size(B, Hq, Hkv, d, S_max)) return Q3A_EINVAL;
+  int max_splits = 0;
+  for (int b = 0; b < B; ++b) {
+    const int32_t p = start_pos[b];
+    if (p < 0 || (long long)p + 1 > S_max) return Q3A_ERANGE;  // nothing written yet
+    const int n = (p + 1 + kDecodeChunk - 1) / kDecodeChunk;
+    if (n > max_splits) max_splits = n;
+  }
+
+  DecodeArgs dargs;  // kernel parameters, staged on the host stack
+  DecodeArgs* da = &dargs;
+  memset(da, 0, sizeof *da);
+  const uint64_t row = kGatedD * 2;
+  const uint64_t dc[3] = {kGatedD, (uint64_t)S_max, (uint64_t)B * Hkv};
+  const uint64_t sc[2] = {row, (uint64_t)S_max * row};
+  const uint32_t bc[3] = {64, 64, 1};
+  if (encode_tensor_map(&da->tm_kc, k_cache, 3, dc, sc, bc) != CUDA_SUCCESS ||
+      encode_tensor_map(&da->tm_vc, v_cache, 3, dc, sc, bc) != CUDA_SUCCESS)
+    return Q3A_ECUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  da->q = qg;
+  da->k_new = k_new;
+  da->v_new = v_new;
+  da->q_gamma = q_w;
+  da->k_gamma = k_w;
+  da->k_cache = k_cache;
+  da->v_cache = v_cache;
+  da->partial = reinterpret_cast<float*>(ws + kHeader);
+  da->out = out;
+  da->err = reinterpret_cast<uint32_t*>(ws);
+  da->B = B;
+  da->Hq = Hq;
+  da->Hkv = Hkv;
+  da->g = Hq / Hkv;
+  da->S_max = S_max;
+  da->split_stride = decode_split_stride(S_max);
+  da->max_splits = max_splits;
+  da->eps = eps;
+  da->d_rot = d_rot;
+  if (d_rot > 0) fill_turn_freq(theta, d_rot, da->turn_freq);
+  for (int b = 0; b < B; ++b) da->start_pos[b] = start_pos[b];
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(da->err, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = launch_gated_decode(*da, st);
+  return from_cuda(e);
+}
+
 q3a_status q3a_last_device_error(const void* workspace, void* stream) {
   if (!workspace) return Q3A_EINVAL;
   uint32_t word = 0;

@@ -79,26 +79,33 @@ cudaError_t launch_prefill_attention(const PrefillChunkArgs& a, cudaStream_t str
 int prefill_tokens_per_cta(int g);
 
 // ----- K3/K4: split-KV decode ------------------------------------------------
+// One kernel pair serves the Qwen3 decode (head_dim 128, QK-Norm with gamma,
+// full rotate-half RoPE) and the gated decode of the Qwen3-Next / Qwen3.5
+// global layer (head_dim 256, zero-centred norm with scale 1 + w, RoPE of the
+// first d_rot coordinates, output multiplied by sigmoid(gate)).
 constexpr int kDecodeMaxB = kMaxBatch;
 constexpr int kDecodeChunk = 1024;  // keys per split
-constexpr int kDecodePartialFloats = 2 + 128;  // m, l, acc[128] per (split, head)
+// m, l, acc[d] per (split, head)
+constexpr int decode_partial_floats(int d) { return 2 + d; }
+constexpr int kDecodePartialFloats = decode_partial_floats(128);
 
 struct DecodeArgs {
-  CUtensorMap tm_kc;  // k_cache [B*Hkv, S_max, 128] bf16, box {64, 64, 1}
+  CUtensorMap tm_kc;  // k_cache [B*Hkv, S_max, d] bf16, box {64, 64, 1}
   CUtensorMap tm_vc;  // v_cache, same
-  const uint16_t* q;      // [B, Hq, 128]
-  const uint16_t* k_new;  // [B, Hkv, 128]
-  const uint16_t* v_new;  // [B, Hkv, 128]
-  const uint16_t* q_gamma;
-  const uint16_t* k_gamma;
+  const uint16_t* q;      // [B, Hq, d]; gated: [B, Hq, 2d], query then gate per head
+  const uint16_t* k_new;  // [B, Hkv, d]
+  const uint16_t* v_new;  // [B, Hkv, d]
+  const uint16_t* q_gamma;  // [d]; gated: the zero-centred weights w_q
+  const uint16_t* k_gamma;  // [d]; gated: w_k
   uint16_t* k_cache;  // for the append
   uint16_t* v_cache;
-  float* partial;     // [B, Hkv, split_stride, g, kDecodePartialFloats] fp32
-  uint16_t* out;      // [B, Hq, 128]
+  float* partial;     // [B, Hkv, split_stride, g, decode_partial_floats(d)] fp32
+  uint16_t* out;      // [B, Hq, d]
   uint32_t* err;
   int B, Hq, Hkv, g, S_max, split_stride, max_splits;
   float eps;
-  unsigned long long turn_freq[64];
+  int d_rot;  // gated: rotated leading coordinates (a multiple of 16)
+  unsigned long long turn_freq[128];  // theta^(-2i/d_rot) / (2 pi); d_rot = 128 for Qwen3
   int start_pos[kDecodeMaxB];  // host positions, copied into the parameters ...
   // ... or, when pos_dev is set, positions read on the device: a one-block
   // check writes *pos_valid (1: every position in range) and the error word
@@ -110,7 +117,8 @@ struct DecodeArgs {
 // error word value of a device-side position check that failed
 constexpr uint32_t kErrWordRange = 0x201;
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);        // d = 128
+cudaError_t launch_gated_decode(const DecodeArgs& a, cudaStream_t stream);  // d = 256
 
 // ----- K5/K6: gated global attention of Qwen3-Next / Qwen3.5 (d = 256) ------
 constexpr int kGatedD = 256;

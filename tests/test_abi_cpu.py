@@ -218,3 +218,28 @@ def test_gated_workspace_size(lib):
     ws = binding.gated_prefill_workspace_size(B, T, Hq, Hkv)
     assert ws >= 256 + B * T * (Hq + Hkv) * 256 * 2
     assert binding.gated_prefill_workspace_size(B, T, Hq, Hkv, 128) == 0
+
+
+def gated_decode_call(lib, start_pos, S_max=64, **kw):
+    B = len(start_pos)
+    sp = (ctypes.c_int32 * max(B, 1))(*start_pos)
+    a = dict(Hq=16, Hkv=2, d=256, d_rot=64, theta=1e7, eps=1e-6, ws=FAKE, ws_bytes=1 << 40)
+    a.update(kw)
+    return lib.q3a_gated_decode(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.addressof(sp), FAKE, FAKE,
+                                FAKE, B, a["Hq"], a["Hkv"], a["d"], a["d_rot"], S_max, a["theta"],
+                                a["eps"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("sp", [[64], [-1], [3, 70]])
+def test_gated_decode_context_overflow_is_erange(lib, sp):
+    assert gated_decode_call(lib, sp) == binding.Q3A_ERANGE
+
+
+def test_gated_decode_rejects_bad_arguments(lib):
+    for kw in (dict(d=128), dict(d_rot=8), dict(d_rot=272), dict(eps=0.0), dict(theta=1.0),
+               dict(ws=FAKE + 8), dict(ws_bytes=1024), dict(Hq=15, Hkv=2)):
+        assert gated_decode_call(lib, [3], **kw) == binding.Q3A_EINVAL, kw
+    assert gated_decode_call(lib, [3], Hq=24, Hkv=4) == binding.Q3A_ENOTIMPL
+    assert gated_decode_call(lib, []) == binding.Q3A_OK
+    ws = binding.gated_decode_workspace_size(64, 16, 2, 32768)
+    assert ws >= 256 + 64 * 2 * 32 * 8 * (2 + 256) * 4

@@ -1,0 +1,86 @@
+"""Gated decode (Qwen3-Next / Qwen3.5 global layer, head_dim 256) on the GPU
+against the fp64 oracle, via the C ABI: outputs, the appended cache rows, and
+a full-size workload on sampled sequences."""
+import pytest
+import torch
+
+import oracle
+from qwen3_qk_norm_gb300 import binding, inputs
+from qwen3_qk_norm_gb300.inputs import WORKLOADS
+from gpu_util import assert_close_attention, assert_within_one_ulp
+
+pytestmark = pytest.mark.gpu
+
+
+def to_dev(x):
+    return {k: (t.cuda() if k != "start_pos" else t) for k, t in x.items()}
+
+
+@pytest.mark.parametrize("Hq,Hkv,d_r,start_pos", [
+    (16, 2, 64, [0, 1, 1023, 1024, 2047]),   # Qwen3-Next heads; split boundaries
+    (8, 2, 64, [5, 700, 1500]),              # Qwen3.5-0.8B heads
+    (32, 2, 64, [2999, 64]),                 # g = 16
+    (4, 4, 256, [300]),                      # g = 1, full rotary
+    (8, 4, 0, [17, 1100]),                   # no rotary
+])
+def test_gated_decode_matches_oracle_and_appends(cuda_lib, Hq, Hkv, d_r, start_pos):
+    B, S = len(start_pos), 3000
+    x = inputs.gated_decode_inputs(B, Hq, Hkv, S, 0, 1, seed=Hq + 5 * Hkv + d_r,
+                                   start_pos=start_pos)
+    d = to_dev(x)
+    out = binding.gated_decode(d["qg"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                               x["start_pos"], d["q_w"], d["k_w"], d_r, 1e7, 1e-6)
+    torch.cuda.synchronize()
+    ref, k_row = oracle.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                                     x["start_pos"], x["q_w"], x["k_w"], d_r, 1e7, 1e-6)
+    assert_close_attention(out, ref, f"gated decode Hq{Hq} Hkv{Hkv} d_r{d_r}")
+    kc, vc = d["k_cache"].cpu(), d["v_cache"].cpu()
+    for b, p in enumerate(start_pos):
+        assert_within_one_ulp(kc[b, :, p], k_row[b], f"appended key b{b}")
+        assert torch.equal(vc[b, :, p].view(torch.int16), x["v_new"][b].view(torch.int16))
+        # rows before p untouched, rows after p still NaN
+        assert torch.equal(kc[b, :, :p].view(torch.int16), x["k_cache"][b, :, :p].view(torch.int16))
+        assert bool(torch.isnan(kc[b, :, p + 1:].float()).all())
+
+
+def test_gated_decode_steps_extend_a_prefill(cuda_lib):
+    """Four decode steps after a 200-token prompt whose keys went into the cache
+    through the oracle: each step's output matches the oracle's prefill row of
+    the grown sequence (to the cache's bf16 rounding)."""
+    T0, steps, Hq, Hkv, D = 200, 4, 16, 2, 256
+    x = inputs.gated_inputs(1, T0 + steps, Hq, Hkv, seed=12)
+    full = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    khat = oracle.gated_qknorm_rope(x["k"], x["k_w"], D, 64, 1e7, 1e-6).to(torch.bfloat16)
+    S = T0 + steps + 8
+    kc = torch.full((1, Hkv, S, D), float("nan"), dtype=torch.bfloat16)
+    vc = torch.full_like(kc, float("nan"))
+    kc[0, :, :T0] = khat[0, :T0].transpose(0, 1)
+    vc[0, :, :T0] = x["v"][0, :T0].transpose(0, 1)
+    kc, vc = kc.cuda(), vc.cuda()
+    qw, kw = x["q_w"].cuda(), x["k_w"].cuda()
+    for s in range(steps):
+        t = T0 + s
+        out = binding.gated_decode(x["qg"][:, t].contiguous().cuda(), x["k"][:, t].contiguous().cuda(),
+                                   x["v"][:, t].contiguous().cuda(), kc, vc, [t], qw, kw, 64, 1e7,
+                                   1e-6)
+        torch.cuda.synchronize()
+        assert_close_attention(out[0], full[0, t], f"step {s}")
+
+
+@pytest.mark.slow
+def test_gated_decode_full_size_sampled_sequences(cuda_lib):
+    """The Qwen3-Next-shaped B64 workload, launched as the benchmark launches it;
+    a few sequences against the oracle."""
+    w = WORKLOADS["qwen3-next-80b-gated-decode-b64"]
+    x = inputs.workload_inputs(w, device="cuda")
+    sel = [0, 17, 40, 63]
+    cpu = {k: (x[k][sel].cpu() if k != "start_pos" else x[k][sel]) for k in x}
+    cpu["q_w"], cpu["k_w"] = x["q_w"].cpu(), x["k_w"].cpu()
+    out = binding.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                               x["start_pos"], x["q_w"], x["k_w"], w.d_r, w.theta, w.eps)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    ref, _ = oracle.gated_decode(cpu["qg"], cpu["k_new"], cpu["v_new"], cpu["k_cache"],
+                                 cpu["v_cache"], cpu["start_pos"], cpu["q_w"], cpu["k_w"], w.d_r,
+                                 w.theta, w.eps)
+    assert_close_attention(out[sel], ref, w.name)
