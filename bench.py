@@ -39,6 +39,7 @@ PREFILL_WORKLOAD = "qwen3-8b-prefill-b4-t4096"
 DECODE_WORKLOAD = "qwen3-8b-decode-b64"
 CHUNK_WORKLOAD = "qwen3-8b-chunk-b4-t1024-at3072"
 GATED_WORKLOAD = "qwen3-next-80b-gated-b4-t4096"
+GATED_DECODE_WORKLOAD = "qwen3-next-80b-gated-decode-b64"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2 ** 20
 
@@ -399,6 +400,38 @@ def bench_gated(binding, device, steps: int, warmup: int, world: int):
     return w, tot, pro, att
 
 
+def bench_gated_decode(binding, device, steps: int, warmup: int, world: int):
+    """One gated decode step (head_dim 256, sigmoid gate) over the Qwen3-Next-shaped
+    B64 caches; every step appends the same rows again."""
+    w = WORKLOADS[GATED_DECODE_WORKLOAD]
+    x = inputs.workload_inputs(w, device=device)
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(binding.gated_decode_workspace_size(w.B, w.Hq, w.Hkv, w.S_max),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        binding.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                             x["start_pos"], x["q_w"], x["k_w"], w.d_r, w.theta, w.eps, out=out,
+                             workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    barrier(world, device)
+    synchronize_all(device)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    synchronize_all(device)
+    barrier(world, device)
+    status = binding.last_device_error(ws)
+    if status != 0:
+        raise RuntimeError(f"gated decode device error word: {status}")
+    return w, x["start_pos"], statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+
+
 def cpu_baseline_prefill(w, x_cpu: dict, budget_s: float = 12.0, seed: int = 0) -> dict:
     """The fp64 oracle on a bounded sample of the prefill workload's query rows
     (random (b, t, h)), on all host cores, for about ``budget_s`` seconds."""
@@ -477,8 +510,11 @@ def run_ours(args) -> None:
         if not args.no_chunk:
             cw, c_start, ch_ms = bench_chunk(binding, device, args.steps, args.warmup, world)
         gw, g_ms, gp_ms, ga_ms = (None, None, None, None)
+        gdw, gd_start, gd_ms = (None, None, None)
         if not args.no_gated:
             gw, g_ms, gp_ms, ga_ms = bench_gated(binding, device, args.steps, args.warmup, world)
+            gdw, gd_start, gd_ms = bench_gated_decode(binding, device, args.steps, args.warmup,
+                                                      world)
     clocks = clk.summary()
 
     flops = accounting.prefill_flops(w.B, w.T, w.Hq, w.d)
@@ -597,6 +633,24 @@ def run_ours(args) -> None:
                          "frac_of_hbm": round(gp_bytes / (gp_max / 1e3) / 1e9 / peaks["hbm_gbs"],
                                               4),
                          "traffic": ncu_traffic("gated_prologue_kernel")},
+            "gpu_launches": 2 * args.steps,
+        }
+    if gd_ms is not None:
+        gbytes = accounting.gated_decode_bytes(gd_start.tolist(), gdw.Hq, gdw.Hkv, gdw.d)
+        gd_max = max_over_ranks(gd_ms, world, device)
+        per_gpu = gbytes / (gd_max / 1e3) / 1e9
+        line["gated_decode"] = {
+            "value": round(whole_job_rate(gbytes, world, gd_max / 1e3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(gd_max, 4),
+            "config": {"workload": gdw.name, "B": gdw.B, "Hq": gdw.Hq, "Hkv": gdw.Hkv, "d": gdw.d,
+                       "d_rot": gdw.d_r, "S_max": gdw.S_max,
+                       "start_pos": f"U[{gdw.sp_lo}, {gdw.sp_hi}) seed {gdw.seed}",
+                       "bytes_per_step": gbytes, "api": "q3a_gated_decode"},
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<256> + "
+                         "decode_combine_kernel<256>",
+                         "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(per_gpu / peaks["hbm_gbs"], 4),
+                         "peak_source": f"{peak_src} copy bandwidth", "traffic": None},
             "gpu_launches": 2 * args.steps,
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

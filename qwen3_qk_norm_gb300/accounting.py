@@ -33,6 +33,18 @@ def decode_bytes(start_pos, Hq: int, Hkv: int, d: int = 128) -> int:
     return cache_read + new_in + writes
 
 
+def gated_decode_bytes(start_pos, Hq: int, Hkv: int, d: int = 256) -> int:
+    """Algorithmic HBM bytes of one gated decode step: as decode_bytes, with
+    the query/gate rows (2d per head) read instead of d-wide queries."""
+    sp = [int(x) for x in start_pos]
+    B = len(sp)
+    row = d * 2
+    cache_read = sum(sp) * Hkv * 2 * row
+    new_in = B * (2 * Hq + 2 * Hkv) * row + 2 * row
+    writes = B * 2 * Hkv * row + B * Hq * row
+    return cache_read + new_in + writes
+
+
 def kv_cache_bytes_per_token(n_layers: int, Hkv: int, d: int = 128, elem_bytes: int = 2) -> int:
     """K and V bytes one token occupies in a cache of ``n_layers`` layers."""
     return n_layers * Hkv * d * 2 * elem_bytes

@@ -25,3 +25,11 @@ def test_decode_bytes_by_hand():
     row = 256
     want = 10 * 2 * row + (2 + 2) * row + 2 * row + 2 * row + 2 * row
     assert accounting.decode_bytes([10], 2, 1) == want
+
+
+def test_gated_decode_bytes_count_query_and_gate_rows():
+    from qwen3_qk_norm_gb300.accounting import gated_decode_bytes
+    # one sequence at p = 10, Hq 2, Hkv 1, d 4 (2-byte elements):
+    # cache 10 rows x (K + V) x 8 B = 160; q|gate 2 x 16 B + k_new, v_new 2 x 8 B + w's 16 B;
+    # writes: appended K, V 16 B + out 2 x 8 B
+    assert gated_decode_bytes([10], 2, 1, 4) == 160 + (32 + 16 + 16) + (16 + 16)
