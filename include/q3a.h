@@ -350,6 +350,24 @@ q3a_status q3a_gated_decode(const q3a_bf16* qg, const q3a_bf16* k_new, const q3a
                             double theta, float eps,
                             void* workspace, size_t ws_bytes, void* stream);
 
+/* q3a_gated_decode_device_pos — q3a_gated_decode with start_pos [B] int32 in
+ * DEVICE memory (4-byte aligned), for steps captured in a CUDA graph: the
+ * positions are checked on the device by a one-block pre-pass; if any
+ * start_pos[b] is < 0 or >= S_max nothing is written and
+ * q3a_last_device_error() returns Q3A_ERANGE. No host read or
+ * synchronisation happens in the call; every split up to S_max is launched
+ * (those past a sequence's length exit at once). Host-checkable argument
+ * errors return as for q3a_gated_decode. */
+q3a_status q3a_gated_decode_device_pos(const q3a_bf16* qg, const q3a_bf16* k_new,
+                                       const q3a_bf16* v_new,
+                                       q3a_bf16* k_cache, q3a_bf16* v_cache,
+                                       const int32_t* start_pos,
+                                       const q3a_bf16* q_w, const q3a_bf16* k_w,
+                                       q3a_bf16* out,
+                                       int B, int Hq, int Hkv, int d, int d_rot, int S_max,
+                                       double theta, float eps,
+                                       void* workspace, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------
  * q3a_last_device_error — reads, synchronously on `stream`, the error word
  * that the kernels of the last call which used `workspace` left in its first

@@ -24,7 +24,8 @@ EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size"
             "q3a_decode", "q3a_decode_device_pos", "q3a_decode_noalloc",
             "q3a_last_device_error", "q3a_gated_prefill_workspace_size", "q3a_gated_prefill",
             "q3a_gated_prefill_prologue", "q3a_gated_prefill_attention",
-            "q3a_gated_decode_workspace_size", "q3a_gated_decode"]
+            "q3a_gated_decode_workspace_size", "q3a_gated_decode",
+            "q3a_gated_decode_device_pos"]
 
 _lock = threading.Lock()
 _lib = None
@@ -93,6 +94,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_gated_decode_workspace_size.restype = sz
         lib.q3a_gated_decode.argtypes = [vp] * 9 + [i] * 6 + [d, f, vp, sz, vp]
         lib.q3a_gated_decode.restype = i
+        lib.q3a_gated_decode_device_pos.argtypes = [vp] * 9 + [i] * 6 + [d, f, vp, sz, vp]
+        lib.q3a_gated_decode_device_pos.restype = i
         _lib = lib
         return lib
 
@@ -417,4 +420,38 @@ def gated_decode(qg, k_new, v_new, k_cache, v_cache, start_pos, q_w, k_w, d_rot:
                                  int(d_rot), S_max, float(theta), float(eps),
                                  workspace.data_ptr(), workspace.numel(), _stream(qg.device))
     _raise(st, "q3a_gated_decode")
+    return out
+
+
+def gated_decode_device_pos(qg, k_new, v_new, k_cache, v_cache, start_pos, q_w, k_w,
+                            d_rot: int, theta: float, eps: float, out=None,
+                            workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """gated_decode with start_pos a CUDA int32 [B] tensor (capturable in a CUDA
+    graph); an out-of-range position writes nothing and is reported by
+    last_device_error(workspace) as Q3A_ERANGE."""
+    B, Hq, d2 = qg.shape
+    d = d2 // 2
+    Hkv, S_max = k_cache.shape[1], k_cache.shape[2]
+    _check(qg, "qg")
+    _check(k_new, "k_new", (B, Hkv, d))
+    _check(v_new, "v_new", (B, Hkv, d))
+    _check(k_cache, "k_cache", (B, Hkv, S_max, d))
+    _check(v_cache, "v_cache", (B, Hkv, S_max, d))
+    _check(q_w, "q_w", (d,))
+    _check(k_w, "k_w", (d,))
+    _check(start_pos, "start_pos", (B,), dtype=torch.int32)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=qg.device)
+    _check(out, "out", (B, Hq, d))
+    need = gated_decode_workspace_size(B, Hq, Hkv, S_max, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=qg.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_gated_decode_device_pos(qg.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                            k_cache.data_ptr(), v_cache.data_ptr(),
+                                            start_pos.data_ptr(), q_w.data_ptr(), k_w.data_ptr(),
+                                            out.data_ptr(), B, Hq, Hkv, d, int(d_rot), S_max,
+                                            float(theta), float(eps), workspace.data_ptr(),
+                                            workspace.numel(), _stream(qg.device))
+    _raise(st, "q3a_gated_decode_device_pos")
     return out

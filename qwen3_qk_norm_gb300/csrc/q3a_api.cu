@@ -594,11 +594,16 @@ size_t q3a_gated_decode_workspace_size(int B, int Hq, int Hkv, int d, int S_max)
   return kHeader + align256(parts);
 }
 
-q3a_status q3a_gated_decode(const q3a_bf16* qg, const q3a_bf16* k_new, const q3a_bf16* v_new,
-                            q3a_bf16* k_cache, q3a_bf16* v_cache, const int32_t* start_pos,
-                            const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out, int B,
-                            int Hq, int Hkv, int d, int d_rot, int S_max, double theta, float eps,
-                            void* workspace, size_t ws_bytes, void* stream) {
+// Shared by q3a_gated_decode (positions on the host) and
+// q3a_gated_decode_device_pos (positions in device memory, checked by a
+// device-side pre-pass; no host read or synchronisation).
+static q3a_status gated_decode_impl(const q3a_bf16* qg, const q3a_bf16* k_new,
+                                    const q3a_bf16* v_new, q3a_bf16* k_cache, q3a_bf16* v_cache,
+                                    const int32_t* start_pos, bool pos_on_device,
+                                    const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out,
+                                    int B, int Hq, int Hkv, int d, int d_rot, int S_max,
+                                    double theta, float eps, void* workspace, size_t ws_bytes,
+                                    void* stream) {
   if (d != kGatedD || B < 0 || B > kDecodeMaxB || S_max <= 0 || Hq <= 0 || Hkv <= 0 ||
       Hq % Hkv)
     return Q3A_EINVAL;
@@ -609,15 +614,18 @@ q3a_status q3a_gated_decode(const q3a_bf16* qg, const q3a_bf16* k_new, const q3a
   const void* ptrs[] = {qg, k_new, v_new, k_cache, v_cache, q_w, k_w, out};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return Q3A_EINVAL;
-  if (!start_pos) return Q3A_EINVAL;
+  if (!start_pos || (reinterpret_cast<uintptr_t>(start_pos) & 3u)) return Q3A_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
   if (ws_bytes < q3a_gated_decode_workspace_size(B, Hq, Hkv, d, S_max)) return Q3A_EINVAL;
-  int max_splits = 0;
-  for (int b = 0; b < B; ++b) {
-    const int32_t p = start_pos[b];
-    if (p < 0 || (long long)p + 1 > S_max) return Q3A_ERANGE;  // nothing written yet
-    const int n = (p + 1 + kDecodeChunk - 1) / kDecodeChunk;
-    if (n > max_splits) max_splits = n;
+  int max_splits = decode_split_stride(S_max);  // device positions: every split may be needed
+  if (!pos_on_device) {
+    max_splits = 0;
+    for (int b = 0; b < B; ++b) {
+      const int32_t p = start_pos[b];
+      if (p < 0 || (long long)p + 1 > S_max) return Q3A_ERANGE;  // nothing written yet
+      const int n = (p + 1 + kDecodeChunk - 1) / kDecodeChunk;
+      if (n > max_splits) max_splits = n;
+    }
   }
 
   DecodeArgs dargs;  // kernel parameters, staged on the host stack
@@ -651,12 +659,36 @@ q3a_status q3a_gated_decode(const q3a_bf16* qg, const q3a_bf16* k_new, const q3a
   da->eps = eps;
   da->d_rot = d_rot;
   if (d_rot > 0) fill_turn_freq(theta, d_rot, da->turn_freq);
-  for (int b = 0; b < B; ++b) da->start_pos[b] = start_pos[b];
-
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pos_on_device) {
+    da->pos_dev = start_pos;
+    da->pos_valid = reinterpret_cast<uint32_t*>(ws + 16);
+    return from_cuda(launch_gated_decode(*da, st));  // the check kernel writes the error word
+  }
+  for (int b = 0; b < B; ++b) da->start_pos[b] = start_pos[b];
   cudaError_t e = cudaMemsetAsync(da->err, 0, sizeof(uint32_t), st);
   if (e == cudaSuccess) e = launch_gated_decode(*da, st);
   return from_cuda(e);
+}
+
+q3a_status q3a_gated_decode(const q3a_bf16* qg, const q3a_bf16* k_new, const q3a_bf16* v_new,
+                            q3a_bf16* k_cache, q3a_bf16* v_cache, const int32_t* start_pos,
+                            const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out, int B,
+                            int Hq, int Hkv, int d, int d_rot, int S_max, double theta, float eps,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  return gated_decode_impl(qg, k_new, v_new, k_cache, v_cache, start_pos, false, q_w, k_w, out,
+                           B, Hq, Hkv, d, d_rot, S_max, theta, eps, workspace, ws_bytes, stream);
+}
+
+q3a_status q3a_gated_decode_device_pos(const q3a_bf16* qg, const q3a_bf16* k_new,
+                                       const q3a_bf16* v_new, q3a_bf16* k_cache,
+                                       q3a_bf16* v_cache, const int32_t* start_pos,
+                                       const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out,
+                                       int B, int Hq, int Hkv, int d, int d_rot, int S_max,
+                                       double theta, float eps, void* workspace,
+                                       size_t ws_bytes, void* stream) {
+  return gated_decode_impl(qg, k_new, v_new, k_cache, v_cache, start_pos, true, q_w, k_w, out,
+                           B, Hq, Hkv, d, d_rot, S_max, theta, eps, workspace, ws_bytes, stream);
 }
 
 q3a_status q3a_last_device_error(const void* workspace, void* stream) {

@@ -84,3 +84,53 @@ def test_gated_decode_full_size_sampled_sequences(cuda_lib):
                                  cpu["v_cache"], cpu["start_pos"], cpu["q_w"], cpu["k_w"], w.d_r,
                                  w.theta, w.eps)
     assert_close_attention(out[sel], ref, w.name)
+
+
+def test_gated_decode_device_positions_and_graph_replay(cuda_lib):
+    """Device-resident positions give the bits of host positions; a captured
+    graph of the step plus the position increment, replayed, equals eager
+    steps; an out-of-range position writes nothing and reports ERANGE."""
+    B, Hq, Hkv, S, steps = 2, 16, 2, 2048, 4
+    start = [10, 1500]
+    x = inputs.gated_decode_inputs(B, Hq, Hkv, S, 0, 1, seed=13, start_pos=start)
+    g = torch.Generator().manual_seed(14)
+    new = [{k: torch.randn(x[k].shape, generator=g).to(torch.bfloat16).cuda()
+            for k in ("qg", "k_new", "v_new")} for _ in range(steps)]
+    qw, kw = x["q_w"].cuda(), x["k_w"].cuda()
+    kc_e, vc_e = x["k_cache"].cuda(), x["v_cache"].cuda()
+    eager = [binding.gated_decode(new[s]["qg"], new[s]["k_new"], new[s]["v_new"], kc_e, vc_e,
+                                  [p + s for p in start], qw, kw, 64, 1e7, 1e-6).clone()
+             for s in range(steps)]
+    kc_g, vc_g = x["k_cache"].cuda(), x["v_cache"].cuda()
+    bufs = {k: torch.empty_like(new[0][k]) for k in ("qg", "k_new", "v_new")}
+    out = torch.empty((B, Hq, 256), dtype=torch.bfloat16, device="cuda")
+    pos = torch.tensor(start, dtype=torch.int32, device="cuda")
+    ws = torch.empty(binding.gated_decode_workspace_size(B, Hq, Hkv, S), dtype=torch.uint8,
+                     device="cuda")
+    for k in bufs:
+        bufs[k].copy_(new[0][k])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        binding.gated_decode_device_pos(bufs["qg"], bufs["k_new"], bufs["v_new"], kc_g, vc_g,
+                                        pos, qw, kw, 64, 1e7, 1e-6, out=out, workspace=ws)
+        pos.add_(1)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        for k in bufs:
+            bufs[k].copy_(new[s][k])
+        graph.replay()
+        torch.cuda.synchronize()
+        assert binding.last_device_error(ws) == binding.Q3A_OK
+        assert torch.equal(out, eager[s]), f"step {s}"
+    assert torch.equal(kc_g.view(torch.int16), kc_e.view(torch.int16))
+    assert torch.equal(vc_g.view(torch.int16), vc_e.view(torch.int16))
+    # out of range: nothing written
+    k0 = kc_g.clone()
+    out.fill_(3.0)
+    bad = torch.tensor([5, S], dtype=torch.int32, device="cuda")
+    binding.gated_decode_device_pos(bufs["qg"], bufs["k_new"], bufs["v_new"], kc_g, vc_g, bad,
+                                    qw, kw, 64, 1e7, 1e-6, out=out, workspace=ws)
+    assert binding.last_device_error(ws) == binding.Q3A_ERANGE
+    assert torch.equal(kc_g.view(torch.int16), k0.view(torch.int16))
+    assert bool((out == 3.0).all())
