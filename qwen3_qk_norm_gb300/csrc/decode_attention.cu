@@ -118,22 +118,6 @@ __device__ __forceinline__ int decode_pos(const DecodeArgs& a, int b) {
   return kDevPos ? a.pos_dev[b] : a.start_pos[b];
 }
 
-__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
-  f[0] = bf16_lo(v.x);
-  f[1] = bf16_hi(v.x);
-  f[2] = bf16_lo(v.y);
-  f[3] = bf16_hi(v.y);
-  f[4] = bf16_lo(v.z);
-  f[5] = bf16_hi(v.z);
-  f[6] = bf16_lo(v.w);
-  f[7] = bf16_hi(v.w);
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                    pack_bf16x2(f[6], f[7]));
-}
-
 template <int D, bool kGated, bool kDevPos>
 __global__ void __launch_bounds__(kThreads, DecLayout<D>::kMinBlocks)
     decode_split_kernel(const __grid_constant__ DecodeArgs a) {

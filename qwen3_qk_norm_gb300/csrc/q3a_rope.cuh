@@ -1,5 +1,5 @@
 // q3a_rope.cuh — device pieces of QK-Norm + rotate-half RoPE shared by the
-// prologue kernel (K1) and the decode kernel (K3).
+// prologue kernels (K1, K5) and the decode kernel (K3).
 //
 //   y = x * rsqrt(mean(x^2) + eps) * gamma                       (fp32)
 //   y'_i = y_i cos a_i - y_{i+64} sin a_i ; y'_{i+64} = y_{i+64} cos a_i + y_i sin a_i
@@ -59,6 +59,22 @@ __device__ __forceinline__ void unpack4(uint2 v, float (&f)[4]) {
 
 __device__ __forceinline__ uint2 pack4(const float (&f)[4]) {
   return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+}
+
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x);
+  f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y);
+  f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z);
+  f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w);
+  f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
 }
 
 }  // namespace q3a
