@@ -80,12 +80,16 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0) *a.logit_bound = 16.0f * gq * gk * 1.4426950408889634f;
     }
   }
+  // (b, t) of the CTA's first token; the others by counting
+  const long long b_first = tok0 / a.T;
+  const int t_first = (int)(tok0 - b_first * a.T);
   // rotation table of this CTA's tokens while the rows are in flight
   const int n_ang = a.d_r >> 1;
   for (int e = tid; e < tok_here * n_ang; e += kThreads) {
     const int tt = e / n_ang, i = e - tt * n_ang;
-    const long long tok = tok0 + tt;
-    const long long t = tok - (tok / a.T) * a.T;
+    long long b;
+    int t;
+    token_bt(b_first, t_first, tt, a.T, b, t);
     const float2 c_s = rope_cos_sin(t, a.turn_freq[i]);
     cos_s[tt][i] = c_s.x;
     sin_s[tt][i] = c_s.y;
@@ -127,13 +131,11 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = 0; e < 8; ++e) y[e] = x[e] * inv_rms * (is_q ? sq[e] : sk[e]);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
+      // rotated lanes: y c -+ y_partner s; the others keep y (c = 1, s = 0)
       const float yp = __shfl_sync(0xffffffffu, y[e], partner);
-      if (rotated) {
-        const float c = cos_s[tt][ang0 + e], s = sin_s[tt][ang0 + e];
-        o[e] = lower ? y[e] * c - yp * s : y[e] * c + yp * s;
-      } else {
-        o[e] = y[e];
-      }
+      const float c = rotated ? cos_s[tt][ang0 + e] : 1.0f;
+      const float sn = rotated ? (lower ? -sin_s[tt][ang0 + e] : sin_s[tt][ang0 + e]) : 0.0f;
+      o[e] = fmaf(yp, sn, y[e] * c);
     }
     reinterpret_cast<uint4*>(row)[lane] = pack8(o);
   }
@@ -147,8 +149,9 @@ __global__ void __launch_bounds__(kThreads)
   }
   for (int rr = tid; rr < tok_here * Hkv; rr += kThreads) {
     const int tt = rr / Hkv, kv = rr - tt * Hkv;
-    const long long tok = tok0 + tt;
-    const long long b = tok / a.T, t = tok - b * a.T;
+    long long b;
+    int t;
+    token_bt(b_first, t_first, tt, a.T, b, t);
     bulk_store(a.khat + ((b * Hkv + kv) * a.T + t) * kGatedD, rows_k + (size_t)rr * kGatedD,
                kRowBytes);
     issued = true;

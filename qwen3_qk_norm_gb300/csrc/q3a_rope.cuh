@@ -50,6 +50,19 @@ __device__ __forceinline__ void qknorm_rope_halfwarp(const float (&xl)[4], const
   }
 }
 
+// Sequence b and in-sequence index t of token first + tt of a [B, T] token
+// range, given those of `first` (computed once per CTA): a CTA owns a few
+// consecutive tokens, so counting forward replaces a 64-bit division per use.
+__device__ __forceinline__ void token_bt(long long b_first, int t_first, int tt, int T,
+                                         long long& b, int& t) {
+  b = b_first;
+  t = t_first + tt;
+  while (t >= T) {
+    t -= T;
+    ++b;
+  }
+}
+
 __device__ __forceinline__ void unpack4(uint2 v, float (&f)[4]) {
   f[0] = bf16_lo(v.x);
   f[1] = bf16_hi(v.x);

@@ -81,11 +81,15 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
       if (l == 0) *a.logit_bound = 11.313708498984761f * gq * gk * 1.4426950408889634f;
     }
   }
+  // (b, t) of the CTA's first token; the others by counting
+  const long long b_first = tok0 / a.T;
+  const int t_first = (int)(tok0 - b_first * a.T);
   // rotation table of this CTA's tokens while the rows are in flight
   for (int e = tid; e < tok_here * 64; e += kThreads) {
     const int tt = e >> 6, i = e & 63;
-    const long long tok = tok0 + tt;
-    const long long b = tok / a.T, t = tok - b * a.T;
+    long long b;
+    int t;
+    token_bt(b_first, t_first, tt, a.T, b, t);
     const long long pos = (a.per_b_pos ? (long long)a.pos_b[b] : a.pos0) + t;
     const float2 c_s = rope_cos_sin(pos, a.turn_freq[i]);
     cos_s[tt][i] = c_s.x;
@@ -163,9 +167,10 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
     } else {
       for (int rr = tid; rr < tok_here * H; rr += kThreads) {
         const int tt = rr / H, h = rr - tt * H;
-        const long long tok = tok0 + tt;
-        const long long b = tok / a.T;
-        const long long t = tok - b * a.T + (at_pos ? (long long)a.pos_b[b] : 0);
+        long long b;
+        int t_in;
+        token_bt(b_first, t_first, tt, a.T, b, t_in);
+        const long long t = t_in + (at_pos ? (long long)a.pos_b[b] : 0);
         bulk_store(y + (b * ysb + t * yst + (long long)h * ysh) * 128, src + (size_t)rr * 128, 256);
         issued = true;
       }
