@@ -319,6 +319,26 @@ q3a_status q3a_gated_prefill_attention(const q3a_bf16* qg, const q3a_bf16* v, q3
                                        void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * q3a_gated_prefill_fill — q3a_gated_prefill of a prompt (positions 0..T-1)
+ * that also fills the KV caches a later q3a_gated_decode continues from
+ * ("Chapter 20" §20.3: the prompt is prefilled, then only new tokens pass):
+ * rows 0..T-1 of k_cache [B, Hkv, S_max, 256] receive the normalised, rotated
+ * keys (bf16, the same values the attention reads) and rows 0..T-1 of v_cache
+ * the values. `out` equals q3a_gated_prefill's bit for bit. T <= S_max (else
+ * Q3A_ERANGE, nothing written); Hq + 2*Hkv <= 192; other rules as
+ * q3a_gated_prefill. The workspace holds only the normalised queries and the
+ * error word: q3a_gated_prefill_fill_workspace_size() bytes.
+ * ------------------------------------------------------------------------- */
+size_t q3a_gated_prefill_fill_workspace_size(int B, int T, int Hq, int Hkv, int d);
+
+q3a_status q3a_gated_prefill_fill(const q3a_bf16* qg, const q3a_bf16* k, const q3a_bf16* v,
+                                  q3a_bf16* k_cache, q3a_bf16* v_cache,
+                                  const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out,
+                                  int B, int T, int Hq, int Hkv, int d, int d_rot, int S_max,
+                                  double theta, float eps,
+                                  void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_gated_decode — one decode step of the gated global-attention layer of
  * Qwen3-Next / Qwen3.5 against a KV cache, appending the new token
  * ("Chapter 20, Qwen3 and Qwen3.5" §20.3 cache protocol, §20.4 layer).

@@ -25,7 +25,8 @@ EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size"
             "q3a_last_device_error", "q3a_gated_prefill_workspace_size", "q3a_gated_prefill",
             "q3a_gated_prefill_prologue", "q3a_gated_prefill_attention",
             "q3a_gated_decode_workspace_size", "q3a_gated_decode",
-            "q3a_gated_decode_device_pos"]
+            "q3a_gated_decode_device_pos", "q3a_gated_prefill_fill_workspace_size",
+            "q3a_gated_prefill_fill"]
 
 _lock = threading.Lock()
 _lib = None
@@ -96,6 +97,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_gated_decode.restype = i
         lib.q3a_gated_decode_device_pos.argtypes = [vp] * 9 + [i] * 6 + [d, f, vp, sz, vp]
         lib.q3a_gated_decode_device_pos.restype = i
+        lib.q3a_gated_prefill_fill_workspace_size.argtypes = [i] * 5
+        lib.q3a_gated_prefill_fill_workspace_size.restype = sz
+        lib.q3a_gated_prefill_fill.argtypes = [vp] * 8 + [i] * 7 + [d, f, vp, sz, vp]
+        lib.q3a_gated_prefill_fill.restype = i
         _lib = lib
         return lib
 
@@ -454,4 +459,35 @@ def gated_decode_device_pos(qg, k_new, v_new, k_cache, v_cache, start_pos, q_w, 
                                             float(theta), float(eps), workspace.data_ptr(),
                                             workspace.numel(), _stream(qg.device))
     _raise(st, "q3a_gated_decode_device_pos")
+    return out
+
+
+def gated_prefill_fill(qg, k, v, k_cache, v_cache, q_w, k_w, d_rot: int, theta: float,
+                       eps: float, out=None, workspace: torch.Tensor | None = None
+                       ) -> torch.Tensor:
+    """gated_prefill of a prompt that also writes the normalised, rotated keys and
+    the values into rows 0..T-1 of the caches [B,Hkv,S_max,256]."""
+    B, T, Hq, Hkv, d = _gated_shapes(qg, k)
+    S_max = k_cache.shape[2]
+    _check(qg, "qg")
+    _check(k, "k", (B, T, Hkv, d))
+    _check(v, "v", (B, T, Hkv, d))
+    _check(k_cache, "k_cache", (B, Hkv, S_max, d))
+    _check(v_cache, "v_cache", (B, Hkv, S_max, d))
+    _check(q_w, "q_w", (d,))
+    _check(k_w, "k_w", (d,))
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=torch.bfloat16, device=qg.device)
+    _check(out, "out", (B, T, Hq, d))
+    need = int(load().q3a_gated_prefill_fill_workspace_size(B, T, Hq, Hkv, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=qg.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_gated_prefill_fill(qg.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                       k_cache.data_ptr(), v_cache.data_ptr(), q_w.data_ptr(),
+                                       k_w.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, d,
+                                       int(d_rot), S_max, float(theta), float(eps),
+                                       workspace.data_ptr(), workspace.numel(),
+                                       _stream(qg.device))
+    _raise(st, "q3a_gated_prefill_fill")
     return out

@@ -208,9 +208,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_3d(dst + c * kKBlock, &a.tm_k, &bars->slot_full[s], 64 * c,
                         j * BN + 64 * (int)rank, b * a.Hkv + kv);
         } else {  // dims 128 rank .. of the tile, all 128 keys
-          for (int c = 0; c < 2; ++c)
-            tma_load_4d(dst + c * kVBlock, &a.tm_v, &bars->slot_full[s],
-                        128 * (int)rank + 64 * c, kv, j * BN, b);
+          for (int c = 0; c < 2; ++c) {
+            if (a.v_head_major)  // a V cache [B*Hkv, rows, 256]
+              tma_load_3d(dst + c * kVBlock, &a.tm_v, &bars->slot_full[s],
+                          128 * (int)rank + 64 * c, j * BN, b * a.Hkv + kv);
+            else  // the projection's V [B, T, Hkv, 256]
+              tma_load_4d(dst + c * kVBlock, &a.tm_v, &bars->slot_full[s],
+                          128 * (int)rank + 64 * c, kv, j * BN, b);
+          }
         }
         ++n;
       };

@@ -49,15 +49,18 @@ __global__ void __launch_bounds__(kThreads)
   const int tok_here = (int)min((long long)a.tok_per_cta, n_tok - tok0);
   uint16_t* rows_q = reinterpret_cast<uint16_t*>(smem);  // [tok][Hq][256]
   uint16_t* rows_k = rows_q + (size_t)a.tok_per_cta * Hq * kGatedD;  // [tok][Hkv][256]
+  uint16_t* rows_v = rows_k + (size_t)a.tok_per_cta * Hkv * kGatedD;  // [tok][Hkv][256]
   const uint32_t q_bytes = (uint32_t)tok_here * Hq * kRowBytes;
   const uint32_t k_bytes = (uint32_t)tok_here * Hkv * kRowBytes;
+  const uint32_t v_bytes = a.v ? k_bytes : 0u;
 
   if (warp == 0) {
     if (lane == 0) {
       mbar_init(&bar, 1);
       fence_mbar_init();
-      mbar_arrive_expect_tx(&bar, q_bytes + k_bytes);
+      mbar_arrive_expect_tx(&bar, q_bytes + k_bytes + v_bytes);
       bulk_load(rows_k, a.k + tok0 * Hkv * kGatedD, k_bytes, &bar);
+      if (v_bytes) bulk_load(rows_v, a.v + tok0 * Hkv * kGatedD, v_bytes, &bar);
     }
     __syncwarp();
     for (int r = lane; r < tok_here * Hq; r += 32)  // query halves of the q|gate blocks
@@ -152,8 +155,9 @@ __global__ void __launch_bounds__(kThreads)
     long long b;
     int t;
     token_bt(b_first, t_first, tt, a.T, b, t);
-    bulk_store(a.khat + ((b * Hkv + kv) * a.T + t) * kGatedD, rows_k + (size_t)rr * kGatedD,
-               kRowBytes);
+    const long long dst_row = (b * Hkv + kv) * a.khat_rows + t;
+    bulk_store(a.khat + dst_row * kGatedD, rows_k + (size_t)rr * kGatedD, kRowBytes);
+    if (v_bytes) bulk_store(a.v_cache + dst_row * kGatedD, rows_v + (size_t)rr * kGatedD, kRowBytes);
     issued = true;
   }
   if (issued) bulk_commit_and_wait_read();  // shared memory stays valid until read
@@ -167,7 +171,7 @@ cudaError_t launch_gated_prologue(const GatedPrologueArgs& a_in, cudaStream_t st
   const long long n_tok = (long long)a_in.B * a_in.T;
   if (n_tok == 0) return cudaSuccess;
   GatedPrologueArgs a = a_in;
-  const int rows_per_tok = a.Hq + a.Hkv;
+  const int rows_per_tok = a.Hq + (a.v ? 2 : 1) * a.Hkv;  // staged rows per token
   if (a.Hq <= 0 || a.Hkv <= 0 || rows_per_tok > kMaxRows) return cudaErrorInvalidValue;
   if (a.d_r < 0 || a.d_r > kGatedD || (a.d_r & 15)) return cudaErrorInvalidValue;
   int tok = (40 * 1024) / (rows_per_tok * kRowBytes);

@@ -493,6 +493,7 @@ static void gated_prologue_args(GatedPrologueArgs& ga, const q3a_bf16* qg, const
   ga.k_w = k_w;
   ga.qhat = gated_ws_q(workspace);
   ga.khat = gated_ws_k(workspace, B, T, Hq);
+  ga.khat_rows = T;
   ga.err_clear = reinterpret_cast<uint32_t*>(workspace);
   ga.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
   ga.B = B;
@@ -535,6 +536,42 @@ static q3a_status gated_attention_args(GatedAttnArgs& ga, const q3a_bf16* qg, co
   ga.g = g;
   const int tok = gated_tokens_per_cta(g);
   ga.n_mtiles = (T + tok - 1) / tok;
+  return Q3A_OK;
+}
+
+// K6 reading K and V from head-major caches [B, Hkv, S_max, 256] (rows
+// 0..T-1 written by the prologue): the maps stop at row T, so the tensor-memory
+// unit returns zeros past the prompt whatever the cache holds there.
+static q3a_status gated_attention_cache_args(GatedAttnArgs& ga, const q3a_bf16* qg,
+                                             const q3a_bf16* k_cache, const q3a_bf16* v_cache,
+                                             q3a_bf16* out, int B, int T, int Hq, int Hkv,
+                                             int S_max, void* workspace) {
+  memset(&ga, 0, sizeof ga);
+  const int g = Hq / Hkv;
+  const uint64_t row = kGatedD * 2;
+  const uint64_t dq[4] = {kGatedD, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
+  const uint64_t sq[3] = {row, (uint64_t)Hq * row, (uint64_t)T * Hq * row};
+  const uint32_t bq[4] = {64, (uint32_t)g, (uint32_t)(128 / g), 1};
+  const uint64_t dc[3] = {kGatedD, (uint64_t)T, (uint64_t)B * Hkv};
+  const uint64_t sc[2] = {row, (uint64_t)S_max * row};
+  const uint32_t bk[3] = {64, 64, 1};
+  const uint32_t bv[3] = {64, 128, 1};
+  if (encode_tensor_map(&ga.tm_q, gated_ws_q(workspace), 4, dq, sq, bq) != CUDA_SUCCESS ||
+      encode_tensor_map(&ga.tm_k, k_cache, 3, dc, sc, bk) != CUDA_SUCCESS ||
+      encode_tensor_map(&ga.tm_v, v_cache, 3, dc, sc, bv) != CUDA_SUCCESS)
+    return Q3A_ECUDA;
+  ga.qg = qg;
+  ga.out = out;
+  ga.err = reinterpret_cast<uint32_t*>(workspace);
+  ga.logit_bound = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + 8);
+  ga.B = B;
+  ga.T = T;
+  ga.Hq = Hq;
+  ga.Hkv = Hkv;
+  ga.g = g;
+  const int tok = gated_tokens_per_cta(g);
+  ga.n_mtiles = (T + tok - 1) / tok;
+  ga.v_head_major = 1;
   return Q3A_OK;
 }
 
@@ -592,6 +629,45 @@ size_t q3a_gated_decode_workspace_size(int B, int Hq, int Hkv, int d, int S_max)
   const size_t parts = (size_t)B * Hkv * decode_split_stride(S_max) * (Hq / Hkv) *
                        decode_partial_floats(kGatedD) * sizeof(float);
   return kHeader + align256(parts);
+}
+
+size_t q3a_gated_prefill_fill_workspace_size(int B, int T, int Hq, int Hkv, int d) {
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || d != kGatedD) return 0;
+  return kHeader + align256(gated_q_bytes(B, T, Hq));
+}
+
+q3a_status q3a_gated_prefill_fill(const q3a_bf16* qg, const q3a_bf16* k, const q3a_bf16* v,
+                                  q3a_bf16* k_cache, q3a_bf16* v_cache, const q3a_bf16* q_w,
+                                  const q3a_bf16* k_w, q3a_bf16* out, int B, int T, int Hq,
+                                  int Hkv, int d, int d_rot, int S_max, double theta, float eps,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+  if (!scalars_ok(theta, eps) || !d_rot_ok(d_rot)) return Q3A_EINVAL;
+  if (d != kGatedD || B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return Q3A_EINVAL;
+  if (S_max <= 0 || S_max > (1 << 30)) return Q3A_EINVAL;
+  if ((long long)B * T * Hq > 0x7fffffffLL) return Q3A_EINVAL;
+  if (Hq + 2 * Hkv > gated_prologue_max_heads()) return Q3A_EINVAL;
+  if (!group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;
+  if (T > S_max) return Q3A_ERANGE;  // the prompt does not fit the caches; nothing written
+  if (B == 0 || T == 0) return Q3A_OK;
+  const void* ptrs[] = {qg, k, v, k_cache, v_cache, q_w, k_w, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return Q3A_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
+  if (ws_bytes < q3a_gated_prefill_fill_workspace_size(B, T, Hq, Hkv, d)) return Q3A_EINVAL;
+  GatedAttnArgs aa;  // tensor maps first: a failure there launches nothing
+  q3a_status s = gated_attention_cache_args(aa, qg, k_cache, v_cache, out, B, T, Hq, Hkv, S_max,
+                                            workspace);
+  if (s != Q3A_OK) return s;
+  GatedPrologueArgs pa;
+  gated_prologue_args(pa, qg, k, q_w, k_w, B, T, Hq, Hkv, d_rot, theta, eps, workspace);
+  pa.khat = k_cache;  // normalised, rotated keys straight into cache rows 0..T-1
+  pa.khat_rows = S_max;
+  pa.v = v;
+  pa.v_cache = v_cache;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_gated_prologue(pa, st);
+  if (e == cudaSuccess) e = launch_gated_attention(aa, st);
+  return from_cuda(e);
 }
 
 // Shared by q3a_gated_decode (positions on the host) and

@@ -131,7 +131,12 @@ struct GatedPrologueArgs {
   const uint16_t* q_w;  // [256] zero-centred weights: the scale is 1 + w
   const uint16_t* k_w;
   uint16_t* qhat;       // [B, T, Hq, 256]
-  uint16_t* khat;       // [B, Hkv, T, 256] (head-major)
+  uint16_t* khat;       // head-major: row (b, kv, t) at ((b * Hkv + kv) * khat_rows + t) * 256
+  long long khat_rows;  // T for the workspace, S_max for a K cache
+  // if non-null: v [B, T, Hkv, 256] is copied unchanged into v_cache rows
+  // (same head-major addressing as khat)
+  const uint16_t* v;
+  uint16_t* v_cache;
   uint32_t* err_clear;  // block 0 zeroes this error word
   // block 0 writes here sqrt(256) * max|1 + w_q| * max|1 + w_k| * log2(e), the
   // bound on |qhat . khat| / sqrt(256) * log2(e) that the norm guarantees
@@ -149,13 +154,15 @@ cudaError_t launch_gated_prologue(const GatedPrologueArgs& a, cudaStream_t strea
 struct GatedAttnArgs {
   CUtensorMap tm_q;  // Qhat [B, T, Hq, 256], box {64, g, 128/g, 1}
   CUtensorMap tm_k;  // Khat [B*Hkv, T, 256], box {64, 64, 1}
-  CUtensorMap tm_v;  // V [B, T, Hkv, 256], box {64, 1, 128, 1}
+  CUtensorMap tm_v;  // V [B, T, Hkv, 256], box {64, 1, 128, 1}; or, when v_head_major,
+                     // a V cache [B*Hkv, T rows, 256] (row stride S_max), box {64, 128, 1}
   const uint16_t* qg;  // gate = qg[b, t, h, 256 .. 511]
   uint16_t* out;       // [B, T, Hq, 256] bf16
   uint32_t* err;
   const float* logit_bound;
   int B, T, Hq, Hkv, g;
   int n_mtiles;  // pair tiles: ceil(T / gated_tokens_per_cta(g))
+  int v_head_major;
 };
 cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream);
 int gated_tokens_per_cta(int g);  // tokens of one KV group that a pair of CTAs covers

@@ -243,3 +243,16 @@ def test_gated_decode_rejects_bad_arguments(lib):
     assert gated_decode_call(lib, []) == binding.Q3A_OK
     ws = binding.gated_decode_workspace_size(64, 16, 2, 32768)
     assert ws >= 256 + 64 * 2 * 32 * 8 * (2 + 256) * 4
+
+
+def test_gated_prefill_fill_host_checks(lib):
+    def call(B=1, T=4, Hq=16, Hkv=2, d=256, d_rot=64, S_max=8, ws_bytes=1 << 40):
+        return lib.q3a_gated_prefill_fill(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, T, Hq,
+                                          Hkv, d, d_rot, S_max, 1e7, 1e-6, FAKE, ws_bytes, None)
+    assert call(T=9, S_max=8) == binding.Q3A_ERANGE
+    assert call(Hq=24, Hkv=4) == binding.Q3A_ENOTIMPL
+    assert call(d=128) == binding.Q3A_EINVAL
+    assert call(ws_bytes=1024) == binding.Q3A_EINVAL
+    assert call(Hq=160, Hkv=20) == binding.Q3A_EINVAL  # 160 + 2*20 staged rows per token > 192
+    assert call(T=0) == binding.Q3A_OK
+    assert lib.q3a_gated_prefill_fill_workspace_size(2, 100, 16, 2, 256) >= 256 + 2 * 100 * 16 * 512

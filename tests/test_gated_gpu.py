@@ -150,3 +150,47 @@ def test_gated_full_size_sampled_rows(cuda_lib, name):
                                     w.theta, w.eps, rows)
     got = torch.stack([out[b, t, h] for b, t, h in rows.tolist()])
     assert_close_attention(got, ref, name)
+
+
+def test_gated_prefill_fill_writes_caches_and_matches_prefill(cuda_lib):
+    """The cache-filling prefill gives the plain gated prefill's output bits and
+    leaves the normalised, rotated keys and the values in cache rows 0..T-1."""
+    B, T, Hq, Hkv, S = 2, 170, 16, 2, 300
+    x = inputs.gated_inputs(B, T, Hq, Hkv, seed=15)
+    d = {k: t.cuda() for k, t in x.items()}
+    plain = binding.gated_prefill(d["qg"], d["k"], d["v"], d["q_w"], d["k_w"], 64, 1e7, 1e-6)
+    kc = torch.full((B, Hkv, S, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    out = binding.gated_prefill_fill(d["qg"], d["k"], d["v"], kc, vc, d["q_w"], d["k_w"], 64,
+                                     1e7, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain)
+    ref_k = oracle.gated_qknorm_rope(x["k"], x["k_w"], D, 64, 1e7, 1e-6)
+    assert_within_one_ulp(kc[:, :, :T].permute(0, 2, 1, 3), ref_k, "cached keys")
+    assert torch.equal(vc[:, :, :T].cpu(), x["v"].transpose(1, 2))
+    assert bool(torch.isnan(kc[:, :, T:].float()).all()) and bool(torch.isnan(vc[:, :, T:].float()).all())
+
+
+def test_gated_prefill_fill_then_decode_continues_the_sequence(cuda_lib):
+    """Prompt through q3a_gated_prefill_fill, then three q3a_gated_decode steps
+    on the caches it filled: each step's output is the oracle's prefill row of
+    the grown sequence (to the bf16 rounding of the cached keys)."""
+    T0, steps, Hq, Hkv = 257, 3, 8, 2
+    x = inputs.gated_inputs(1, T0 + steps, Hq, Hkv, seed=16)
+    full = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    d = {k: t.cuda() for k, t in x.items()}
+    S = 512
+    kc = torch.full((1, Hkv, S, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    out = binding.gated_prefill_fill(d["qg"][:, :T0].contiguous(), d["k"][:, :T0].contiguous(),
+                                     d["v"][:, :T0].contiguous(), kc, vc, d["q_w"], d["k_w"], 64,
+                                     1e7, 1e-6)
+    torch.cuda.synchronize()
+    assert_close_attention(out, full[:, :T0], "prompt")
+    for s in range(steps):
+        t = T0 + s
+        o = binding.gated_decode(d["qg"][:, t].contiguous(), d["k"][:, t].contiguous(),
+                                 d["v"][:, t].contiguous(), kc, vc, [t], d["q_w"], d["k_w"], 64,
+                                 1e7, 1e-6)
+        torch.cuda.synchronize()
+        assert_close_attention(o[0], full[0, t], f"decode step {s}")
