@@ -163,6 +163,8 @@ KERNEL_SOURCES = {  # the kernel's file and every header it includes
                                     "q3a_internal.h"],
     "gated_prologue_kernel": ["gated_prologue.cu", "q3a_rope.cuh", "q3a_device.cuh",
                               "q3a_internal.h"],
+    "decode_split_kernel<256>": ["decode_attention.cu", "q3a_rope.cuh", "q3a_device.cuh",
+                                 "q3a_internal.h"],
 }
 
 
@@ -497,6 +499,16 @@ def run_profile_case(which: str) -> None:
         bench_chunk(binding, device, 3, 0, 1)
     elif which == "gated":
         bench_gated(binding, device, 3, 0, 1)
+    elif which == "gated_decode":
+        w = WORKLOADS[GATED_DECODE_WORKLOAD]
+        B = 16  # a quarter of the batch: about 1 GB of cache
+        x = inputs.gated_decode_inputs(B, w.Hq, w.Hkv, w.S_max, w.sp_lo, w.sp_hi, w.d, w.seed,
+                                       device=device)
+        for _ in range(3):
+            binding.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                                 x["start_pos"], x["q_w"], x["k_w"], w.d_r, w.theta, w.eps)
+        print(json.dumps({"gated_decode_bytes_per_step": accounting.gated_decode_bytes(
+            x["start_pos"].tolist(), w.Hq, w.Hkv, w.d), "B": B}))
     else:
         w = WORKLOADS[DECODE_WORKLOAD]
         B = 16  # a quarter of the batch: 2 GiB of cache instead of 8
@@ -675,7 +687,8 @@ def run_ours(args) -> None:
                          "decode_combine_kernel<256>",
                          "achieved": round(per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(per_gpu / peaks["hbm_gbs"], 4),
-                         "peak_source": f"{peak_src} copy bandwidth", "traffic": None},
+                         "peak_source": f"{peak_src} copy bandwidth",
+                         "traffic": ncu_traffic("decode_split_kernel<256>")},
             "gpu_launches": 2 * args.steps,
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -748,7 +761,8 @@ def main(argv=None) -> None:
     ap.add_argument("--prefill-workload", default=PREFILL_WORKLOAD,
                     choices=[n for n, w in WORKLOADS.items() if w.kind == "prefill"],
                     help="prefill workload of the step (the default is the headline one)")
-    ap.add_argument("--profile-case", choices=["prefill", "decode", "chunk", "gated"],
+    ap.add_argument("--profile-case",
+                    choices=["prefill", "decode", "chunk", "gated", "gated_decode"],
                     help="run a few launches of one kernel for an ncu capture, print no JSON")
     args = ap.parse_args(argv)
     if args.profile_case:
