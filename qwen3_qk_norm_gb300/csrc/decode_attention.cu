@@ -130,10 +130,11 @@ __global__ void __launch_bounds__(kThreads, DecLayout<D>::kMinBlocks)
   if (kDevPos && *a.pos_valid == 0) return;  // some position out of range: write nothing
   const int p = decode_pos<kDevPos>(a, b);
   const int L = p + 1;  // keys of this sequence, the new one included
-  const int n_splits = (L + kDecodeChunk - 1) / kDecodeChunk;
+  constexpr int kChunk = decode_chunk_keys(D);
+  const int n_splits = (L + kChunk - 1) / kChunk;
   if (c >= n_splits) return;
-  const int key_begin = c * kDecodeChunk;
-  const int key_end = min(key_begin + kDecodeChunk, L);
+  const int key_begin = c * kChunk;
+  const int key_end = min(key_begin + kChunk, L);
   const int n_tiles = (key_end - key_begin + kKeysPerTile - 1) / kKeysPerTile;
   const bool holds_new = (c == n_splits - 1);
   const int g = a.g;
@@ -484,7 +485,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const __grid_constant
   if (kDevPos && *a.pos_valid == 0) return;
   const int g = a.g, kv = h / g, j = h % g;
   const int L = decode_pos<kDevPos>(a, b) + 1;
-  const int n_splits = (L + kDecodeChunk - 1) / kDecodeChunk;
+  const int n_splits = (L + decode_chunk_keys(D) - 1) / decode_chunk_keys(D);
   const float* base =
       a.partial + ((((long long)b * a.Hkv + kv) * a.split_stride) * g + j) * kPartial;
   const long long split_step = (long long)g * kPartial;

@@ -53,7 +53,9 @@ q3a_status from_cuda(cudaError_t e) { return e == cudaSuccess ? Q3A_OK : Q3A_ECU
 size_t prefill_q_bytes(int B, int T, int Hq) { return (size_t)B * T * Hq * 128 * 2; }
 size_t prefill_k_bytes(int B, int T, int Hkv) { return (size_t)B * T * Hkv * 128 * 2; }
 
-int decode_split_stride(int S_max) { return (S_max + kDecodeChunk - 1) / kDecodeChunk; }
+int decode_split_stride(int S_max, int d = 128) {
+  return (S_max + decode_chunk_keys(d) - 1) / decode_chunk_keys(d);
+}
 
 }  // namespace
 
@@ -626,7 +628,7 @@ q3a_status q3a_gated_prefill_attention(const q3a_bf16* qg, const q3a_bf16* v, q3
 
 size_t q3a_gated_decode_workspace_size(int B, int Hq, int Hkv, int d, int S_max) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || d != kGatedD || S_max <= 0 || Hq % Hkv) return 0;
-  const size_t parts = (size_t)B * Hkv * decode_split_stride(S_max) * (Hq / Hkv) *
+  const size_t parts = (size_t)B * Hkv * decode_split_stride(S_max, kGatedD) * (Hq / Hkv) *
                        decode_partial_floats(kGatedD) * sizeof(float);
   return kHeader + align256(parts);
 }
@@ -693,13 +695,14 @@ static q3a_status gated_decode_impl(const q3a_bf16* qg, const q3a_bf16* k_new,
   if (!start_pos || (reinterpret_cast<uintptr_t>(start_pos) & 3u)) return Q3A_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
   if (ws_bytes < q3a_gated_decode_workspace_size(B, Hq, Hkv, d, S_max)) return Q3A_EINVAL;
-  int max_splits = decode_split_stride(S_max);  // device positions: every split may be needed
+  // device positions: every split may be needed
+  int max_splits = decode_split_stride(S_max, kGatedD);
   if (!pos_on_device) {
     max_splits = 0;
     for (int b = 0; b < B; ++b) {
       const int32_t p = start_pos[b];
       if (p < 0 || (long long)p + 1 > S_max) return Q3A_ERANGE;  // nothing written yet
-      const int n = (p + 1 + kDecodeChunk - 1) / kDecodeChunk;
+      const int n = (p + decode_chunk_keys(kGatedD)) / decode_chunk_keys(kGatedD);
       if (n > max_splits) max_splits = n;
     }
   }
@@ -730,7 +733,7 @@ static q3a_status gated_decode_impl(const q3a_bf16* qg, const q3a_bf16* k_new,
   da->Hkv = Hkv;
   da->g = Hq / Hkv;
   da->S_max = S_max;
-  da->split_stride = decode_split_stride(S_max);
+  da->split_stride = decode_split_stride(S_max, kGatedD);
   da->max_splits = max_splits;
   da->eps = eps;
   da->d_rot = d_rot;

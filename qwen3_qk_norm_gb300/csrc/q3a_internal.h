@@ -84,7 +84,10 @@ int prefill_tokens_per_cta(int g);
 // global layer (head_dim 256, zero-centred norm with scale 1 + w, RoPE of the
 // first d_rot coordinates, output multiplied by sigmoid(gate)).
 constexpr int kDecodeMaxB = kMaxBatch;
-constexpr int kDecodeChunk = 1024;  // keys per split
+constexpr int kDecodeChunk = 1024;  // keys per split at head_dim 128
+// keys per split: at head_dim 256 one CTA runs per SM, so longer splits
+// amortise each split's fixed start and merge over more streamed keys
+constexpr int decode_chunk_keys(int d) { return d == 128 ? kDecodeChunk : 2 * kDecodeChunk; }
 // m, l, acc[d] per (split, head)
 constexpr int decode_partial_floats(int d) { return 2 + d; }
 constexpr int kDecodePartialFloats = decode_partial_floats(128);

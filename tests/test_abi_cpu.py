@@ -242,7 +242,7 @@ def test_gated_decode_rejects_bad_arguments(lib):
     assert gated_decode_call(lib, [3], Hq=24, Hkv=4) == binding.Q3A_ENOTIMPL
     assert gated_decode_call(lib, []) == binding.Q3A_OK
     ws = binding.gated_decode_workspace_size(64, 16, 2, 32768)
-    assert ws >= 256 + 64 * 2 * 32 * 8 * (2 + 256) * 4
+    assert ws >= 256 + 64 * 2 * 16 * 8 * (2 + 256) * 4  # 2048-key splits at d = 256
 
 
 def test_gated_prefill_fill_host_checks(lib):
