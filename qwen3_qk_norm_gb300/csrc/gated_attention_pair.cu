@@ -19,8 +19,10 @@
 // 64 KB of its ring.
 //
 // Tiling. The pair owns 256 query rows: two 128-row tiles of the g heads of one
-// KV group for 128/g consecutive tokens each, packed row r = (token r/g, head
-// kv*g + r%g) by a 4-D TMA box; the even CTA holds the first tile. KV tiles are
+// KV group for floor(128/g) consecutive tokens each, packed row r = (token r/g,
+// head kv*g + r%g) by a 4-D TMA box; the even CTA holds the first tile. When g
+// does not divide 128 (g = 6, 12) the last 128 - g*floor(128/g) rows of a
+// tile are padding: computed on stale shared memory, never stored. KV tiles are
 // 128 keys. CTA c holds keys 64c..64c+63 of each K tile (four 8 KB blocks of
 // 64 dims) and dims 128c..128c+127 of each V tile (two 16 KB blocks of 64
 // dims), in a ring of four 32 KB slots, loaded in the order the MMAs read them
@@ -189,7 +191,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, 4 * kQBlock);
+      // g * floor(128/g) rows of 128 bytes per 64-dim block (126 or 120 when g
+      // does not divide 128)
+      mbar_arrive_expect_tx(&bars->q_full, 4u * (uint32_t)(g * tile_tok) * 128u);
       for (int c = 0; c < 4; ++c)
         tma_load_4d(smem + OFF_Q + c * kQBlock, &a.tm_q, &bars->q_full, 64 * c, kv * g, t0, b);
       uint32_t n = 0;  // half tiles issued
@@ -438,7 +442,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const bool store = tok < a.T;  // rows past the sequence are padding
+      // rows past the sequence, and the 128 - g * (128 / g) rows after the last
+      // whole token when g does not divide 128, are padding
+      const bool store = tok < a.T && r < g * tile_tok;
       const long long row = ((long long)b * a.T + tok) * a.Hq + h;
       const uint16_t* grow = a.qg + row * (2 * D) + D + cq * 64;
       uint16_t* orow = a.out + row * D + cq * 64;

@@ -19,6 +19,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Gated layer: any whole ratio up to 16 (the decode kernel's MMA rows hold 16
+// heads; the attention tile holds g heads for floor(128/g) tokens)
+bool gated_group_ok(int Hq, int Hkv) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return false;
+  return Hq / Hkv <= 16;
+}
+
 bool group_ok(int Hq, int Hkv) {
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return false;
   const int g = Hq / Hkv;
@@ -468,7 +475,7 @@ static q3a_status gated_check(const void* const* ptrs, int nptrs, int B, int T, 
   if ((long long)B * T * Hq > 0x7fffffffLL || T > (1 << 30)) return Q3A_EINVAL;
   if (Hq + Hkv > gated_prologue_max_heads()) return Q3A_EINVAL;
   // a valid grouping that the 128-row GQA packing does not cover (e.g. 24/4)
-  if (!group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;
+  if (!gated_group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;
   if (B == 0 || T == 0) {
     *empty = true;
     return Q3A_OK;
@@ -648,7 +655,7 @@ q3a_status q3a_gated_prefill_fill(const q3a_bf16* qg, const q3a_bf16* k, const q
   if (S_max <= 0 || S_max > (1 << 30)) return Q3A_EINVAL;
   if ((long long)B * T * Hq > 0x7fffffffLL) return Q3A_EINVAL;
   if (Hq + 2 * Hkv > gated_prologue_max_heads()) return Q3A_EINVAL;
-  if (!group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;
+  if (!gated_group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;
   if (T > S_max) return Q3A_ERANGE;  // the prompt does not fit the caches; nothing written
   if (B == 0 || T == 0) return Q3A_OK;
   const void* ptrs[] = {qg, k, v, k_cache, v_cache, q_w, k_w, out};
@@ -687,7 +694,7 @@ static q3a_status gated_decode_impl(const q3a_bf16* qg, const q3a_bf16* k_new,
     return Q3A_EINVAL;
   if (S_max > (1 << 30) || !d_rot_ok(d_rot)) return Q3A_EINVAL;
   if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
-  if (!group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;  // the MMA rows hold at most 16 heads
+  if (!gated_group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;  // the MMA rows hold at most 16 heads
   if (B == 0) return Q3A_OK;
   const void* ptrs[] = {qg, k_new, v_new, k_cache, v_cache, q_w, k_w, out};
   for (const void* p : ptrs)

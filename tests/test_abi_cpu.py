@@ -183,9 +183,9 @@ def gated_call(lib, **kw):
 
 
 def test_gated_unsupported_group_is_notimpl(lib):
-    # Qwen3.5-27B-shaped grouping (24 query heads over 4 KV heads): valid, not implemented
-    assert gated_call(lib, Hq=24, Hkv=4) == binding.Q3A_ENOTIMPL
+    # more than 16 query heads per KV head: a whole ratio, not implemented
     assert gated_call(lib, Hq=64, Hkv=2) == binding.Q3A_ENOTIMPL
+    assert gated_call(lib, Hq=68, Hkv=2) == binding.Q3A_ENOTIMPL
 
 
 @pytest.mark.parametrize("kw", [dict(d=128), dict(d_rot=8), dict(d_rot=-16), dict(d_rot=272),
@@ -239,7 +239,7 @@ def test_gated_decode_rejects_bad_arguments(lib):
     for kw in (dict(d=128), dict(d_rot=8), dict(d_rot=272), dict(eps=0.0), dict(theta=1.0),
                dict(ws=FAKE + 8), dict(ws_bytes=1024), dict(Hq=15, Hkv=2)):
         assert gated_decode_call(lib, [3], **kw) == binding.Q3A_EINVAL, kw
-    assert gated_decode_call(lib, [3], Hq=24, Hkv=4) == binding.Q3A_ENOTIMPL
+    assert gated_decode_call(lib, [3], Hq=34, Hkv=2) == binding.Q3A_ENOTIMPL
     assert gated_decode_call(lib, []) == binding.Q3A_OK
     ws = binding.gated_decode_workspace_size(64, 16, 2, 32768)
     assert ws >= 256 + 64 * 2 * 16 * 8 * (2 + 256) * 4  # 2048-key splits at d = 256
@@ -250,7 +250,7 @@ def test_gated_prefill_fill_host_checks(lib):
         return lib.q3a_gated_prefill_fill(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, T, Hq,
                                           Hkv, d, d_rot, S_max, 1e7, 1e-6, FAKE, ws_bytes, None)
     assert call(T=9, S_max=8) == binding.Q3A_ERANGE
-    assert call(Hq=24, Hkv=4) == binding.Q3A_ENOTIMPL
+    assert call(Hq=36, Hkv=2) == binding.Q3A_ENOTIMPL
     assert call(d=128) == binding.Q3A_EINVAL
     assert call(ws_bytes=1024) == binding.Q3A_EINVAL
     assert call(Hq=160, Hkv=20) == binding.Q3A_EINVAL  # 160 + 2*20 staged rows per token > 192

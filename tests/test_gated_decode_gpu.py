@@ -22,6 +22,8 @@ def to_dev(x):
     (32, 2, 64, [2999, 64]),                 # g = 16
     (4, 4, 256, [300]),                      # g = 1, full rotary
     (8, 4, 0, [17, 1100]),                   # no rotary
+    (24, 4, 64, [900, 2500]),                # g = 6 (Qwen3.5-27B heads)
+    (24, 2, 64, [3, 2100]),                  # g = 12
 ])
 def test_gated_decode_matches_oracle_and_appends(cuda_lib, Hq, Hkv, d_r, start_pos):
     B, S = len(start_pos), 3000

@@ -65,6 +65,8 @@ def test_gated_prologue_within_one_ulp(cuda_lib, B, T, Hq, Hkv, d_r, theta):
     (2, 150, 8, 8, 64, 1e6),    # g = 1, ragged
     (1, 129, 8, 4, 256, 1e6),   # full rotary
     (1, 100, 4, 2, 0, 1e7),     # no rotary
+    (1, 180, 24, 4, 64, 1e7),   # g = 6 (Qwen3.5-27B heads): 126-row tiles, 2 padding rows
+    (2, 90, 24, 2, 64, 1e7),    # g = 12 (Qwen3.8-Flash-Next heads): 120-row tiles
 ])
 def test_gated_prefill_small_shapes(cuda_lib, B, T, Hq, Hkv, d_r, theta):
     x = inputs.gated_inputs(B, T, Hq, Hkv, seed=B * 1000 + T)
