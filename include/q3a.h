@@ -288,8 +288,8 @@ q3a_status q3a_decode_noalloc(const q3a_bf16* q, const q3a_bf16* k_new, const q3
  *   first d_rot coordinates are rotated (rotate-half pairs (i, i + d_rot/2),
  *   frequencies theta^(-2i/d_rot), positions 0..T-1); the others pass through.
  *   d must be 256; d_rot a multiple of 16 in 0..256 (Qwen3-Next / Qwen3.5: 64).
- *   Hq / Hkv in {1, 2, 4, 8, 16} (another whole ratio, e.g. 24/4, returns
- *   Q3A_ENOTIMPL); Hq + Hkv <= 192; B*T*Hq <= 2^31 - 1.
+ *   Hq / Hkv any whole ratio up to 16 (e.g. 16/2, 24/4, 32/2; above 16
+ *   returns Q3A_ENOTIMPL); Hq + Hkv <= 192; B*T*Hq <= 2^31 - 1.
  *   workspace: device scratch of at least q3a_gated_prefill_workspace_size()
  *           bytes, 256-byte aligned, caller-owned, not shared by concurrent
  *           calls; it holds the normalised+rotated Q and K and the error word.
@@ -352,8 +352,8 @@ q3a_status q3a_gated_prefill_fill(const q3a_bf16* qg, const q3a_bf16* k, const q
  *   start_pos [B] int32 on the HOST: position of each sequence's new token.
  *   q_w, k_w [d] bf16 zero-centred norm weights (scale 1 + w).
  *   out     [B, Hq, d] bf16: sigmoid(gate) * softmax(q k^T / sqrt(d)) v.
- *   d = 256; d_rot a multiple of 16 in 0..256; Hq / Hkv in {1, 2, 4, 8, 16}
- *   (another whole ratio returns Q3A_ENOTIMPL); B <= 2048; S_max <= 2^30.
+ *   d = 256; d_rot a multiple of 16 in 0..256; Hq / Hkv any whole ratio up
+ *   to 16 (above 16 returns Q3A_ENOTIMPL); B <= 2048; S_max <= 2^30.
  *   workspace: at least q3a_gated_decode_workspace_size() bytes, 256-byte
  *           aligned, caller-owned, not shared by concurrent calls.
  *   Every argument is checked before anything is written; a start_pos[b] < 0
