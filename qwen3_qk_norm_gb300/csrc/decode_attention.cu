@@ -9,14 +9,14 @@
 // ("Chapter 20, Qwen3 and Qwen3.5", book.ozine.me, §20.3: the new K is
 // rotated at start_pos and concatenated; old K already carries its position).
 //
-// K3: grid (split, kv, b). A split is 1024 consecutive keys of one (b, kv).
-// Warp 4 streams the split's K and V in 64-key tiles with TMA (128-byte
-// swizzle, 3-stage ring, 32 KB per stage). Warps 0-3 each take 16 keys of a
+// K3: grid (split, kv, b). A split is 1024 consecutive keys of one (b, kv)
+// (2048 at head_dim 256). Warp 4 streams the split's K and V in 64-key tiles
+// with TMA (128-byte swizzle, 3-stage ring, 32 KB per stage at d = 128). Warps 0-3 each take 16 keys of a
 // tile: S = Qhat K^T and O += P V run on the tensor cores as m16n8k16 bf16
 // MMAs with the g query heads of the group as the M rows (padded to 16), so
 // one pass over the keys serves all g heads. Each warp keeps its own online
 // softmax (exp2 domain, lazy rescale); the four warps are merged at the end
-// and the split writes (m, l, acc[128]) per head to the workspace.
+// and the split writes (m, l, acc[d]) per head to the workspace.
 // The split that holds position p also normalises and rotates k_new, appends
 // it and v_new to the caches, and patches them into its shared-memory tile in
 // place of the cache row it read (which the caller may not have written yet).
@@ -33,7 +33,8 @@
 // (frequencies theta^(-2i/d_rot)), and K4 multiplying each output column by
 // sigmoid of the gate half. A warp normalises one row there (lane L holds
 // elements 8L..8L+7; rotated pairs sit in lanes L and L + d_rot/16), and a
-// 64-key stage is 64 KB, so one CTA runs per SM with three stages in flight.
+// 64-key stage is 64 KB, so one CTA runs per SM with three stages in flight
+// and splits are twice as long, to spread each split's fixed start and merge.
 //
 // The attention arithmetic is HBM-bound (about 4 flops per cache byte), so the
 // design goal is the copy engine never idling: 64 KB+ of loads in flight per
