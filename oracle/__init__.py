@@ -85,6 +85,10 @@ def _load():
             lib.q3a_oracle_gated_decode.argtypes = ([_u16p] * 5 + [ctypes.c_void_p] + [_u16p] * 2
                                                     + [i] * 5 + [l, d, d, _f64p, _f64p])
             lib.q3a_oracle_gated_decode.restype = i
+            lib.q3a_oracle_gated_prefill_chunk.argtypes = ([_u16p] * 5 + [ctypes.c_void_p]
+                                                           + [_u16p] * 2 + [i] * 6
+                                                           + [l, d, d, _f64p, _f64p])
+            lib.q3a_oracle_gated_prefill_chunk.restype = i
             _lib = lib
     return _lib
 
@@ -322,3 +326,28 @@ def gated_decode(qg, k_new, v_new, k_cache, v_cache, start_pos, q_w, k_w, d_r: i
     if rc:
         raise ValueError(f"oracle gated_decode failed ({rc})")
     return out, k_row
+
+
+def gated_prefill_chunk(qg, k, v, k_cache, v_cache, start_pos, q_w, k_w, d_r: int,
+                        theta: float, eps: float):
+    """Gated chunk of Tq tokens per sequence against the caches. qg [B,Tq,Hq,2d],
+    k/v [B,Tq,Hkv,d], caches [B,Hkv,S_max,d]. Returns (out fp64 [B,Tq,Hq,d],
+    the chunk's keys fp64 [B,Tq,Hkv,d])."""
+    qg, k, v = _bf16(qg, "qg"), _bf16(k, "k"), _bf16(v, "v")
+    k_cache, v_cache = _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    q_w, k_w = _bf16(q_w, "q_w"), _bf16(k_w, "k_w")
+    B, Tq, Hq, d2 = qg.shape
+    Hkv, S_max, d = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    if d2 != 2 * d:
+        raise ValueError(f"qg last dim {d2} != 2 * {d}")
+    sp = torch.as_tensor(start_pos, dtype=torch.int32).contiguous()
+    out = torch.zeros((B, Tq, Hq, d), dtype=torch.float64)
+    k_rows = torch.zeros((B, Tq, Hkv, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_gated_prefill_chunk(_ptr(qg), _ptr(k), _ptr(v), _ptr(k_cache),
+                                                _ptr(v_cache), _ptr(sp), _ptr(q_w), _ptr(k_w),
+                                                B, Tq, Hq, Hkv, d, int(d_r), S_max,
+                                                float(theta), float(eps), _ptr(out),
+                                                _ptr(k_rows))
+    if rc:
+        raise ValueError(f"oracle gated_prefill_chunk failed ({rc})")
+    return out, k_rows

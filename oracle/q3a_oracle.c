@@ -659,3 +659,75 @@ int q3a_oracle_gated_decode(const uint16_t* qg, const uint16_t* k_new, const uin
   }
   return failed ? -2 : 0;
 }
+
+/* Gated chunked prefill against a KV cache (§20.3 protocol on the gated
+ * layer): Tq new tokens of sequence b at positions start_pos[b] + t; keys =
+ * cache rows 0..start_pos[b]-1 as stored, then the chunk's own keys (g2-g3 at
+ * their positions); the causal mask starts at start_pos[b]; z = o * sigmoid(gate).
+ *   qg [B,Tq,Hq,2d], k/v [B,Tq,Hkv,d]; caches [B,Hkv,S_max,d];
+ *   out fp64 [B,Tq,Hq,d]; k_rows fp64 [B,Tq,Hkv,d] = the chunk's keys. */
+int q3a_oracle_gated_prefill_chunk(const uint16_t* qg, const uint16_t* k, const uint16_t* v,
+                                   const uint16_t* k_cache, const uint16_t* v_cache,
+                                   const int32_t* start_pos, const uint16_t* q_w,
+                                   const uint16_t* k_w, int B, int Tq, int Hq, int Hkv, int d,
+                                   int d_r, long S_max, double theta, double eps, double* out,
+                                   double* k_rows) {
+  if (check_gated(B, Tq, Hq, Hkv, d, d_r) || S_max <= 0 || !out || !k_rows) return -1;
+  for (int b = 0; b < B; ++b)
+    if (start_pos[b] < 0 || (long)start_pos[b] + Tq > S_max) return -1;
+  int g = Hq / Hkv;
+  long units = (long)B * Hkv;
+  int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(OMP_THREADS)
+#endif
+  for (long u = 0; u < units; ++u) {
+    long b = u / Hkv, kv = u % Hkv;
+    long p0 = start_pos[b];
+    long n_all = p0 + Tq;
+    double* keys = (double*)malloc(sizeof(double) * (size_t)(n_all > 0 ? n_all : 1) * d);
+    double* vals = (double*)malloc(sizeof(double) * (size_t)(n_all > 0 ? n_all : 1) * d);
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(n_all > 0 ? n_all : 1));
+    double* qhat = (double*)malloc(sizeof(double) * d);
+    if (!keys || !vals || !scores || !qhat) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      failed = 1;
+    } else {
+      const uint16_t* kc = k_cache + (b * Hkv + kv) * S_max * d;
+      const uint16_t* vc = v_cache + (b * Hkv + kv) * S_max * d;
+      for (long j = 0; j < p0; ++j)
+        for (int c = 0; c < d; ++c) {
+          keys[j * d + c] = widen_bf16(kc[j * d + c]);
+          vals[j * d + c] = widen_bf16(vc[j * d + c]);
+        }
+      for (long t = 0; t < Tq; ++t) {
+        long r = ((b * Tq + t) * Hkv + kv) * d;
+        double* kn = keys + (p0 + t) * d;
+        q3a_oracle_zc_rmsnorm_row(k + r, k_w, d, eps, kn);
+        q3a_oracle_partial_rope_row(kn, d, d_r, (double)(p0 + t), theta);
+        for (int c = 0; c < d; ++c) {
+          k_rows[r + c] = kn[c];
+          vals[(p0 + t) * d + c] = widen_bf16(v[r + c]);
+        }
+      }
+      for (long t = 0; t < Tq; ++t)
+        for (long h = kv * g; h < (kv + 1) * g; ++h) {
+          long rq = (b * Tq + t) * Hq + h;
+          const uint16_t* qrow = qg + rq * 2L * d; /* g1 */
+          const uint16_t* grow = qrow + d;
+          double* o = out + rq * d;
+          q3a_oracle_zc_rmsnorm_row(qrow, q_w, d, eps, qhat);
+          q3a_oracle_partial_rope_row(qhat, d, d_r, (double)(p0 + t), theta);
+          attend_row(qhat, keys, vals, p0 + t + 1, d, scores, o);
+          for (int c = 0; c < d; ++c) o[c] *= sigmoid(widen_bf16(grow[c]));
+        }
+    }
+    free(keys);
+    free(vals);
+    free(scores);
+    free(qhat);
+  }
+  return failed ? -2 : 0;
+}

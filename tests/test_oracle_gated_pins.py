@@ -418,3 +418,56 @@ def test_gated_decode_rejects_context_overflow():
     with pytest.raises(ValueError):
         oracle.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], [4],
                             x["q_w"], x["k_w"], 4, 1e7, 1e-6)
+
+
+# ----------------------------------------------------------------------------
+# Gated chunk against a cache (§20.3: rectangular causal mask from pos_start)
+# ----------------------------------------------------------------------------
+
+def test_gated_chunk_at_position_zero_is_gated_prefill():
+    x = inputs.gated_inputs(2, 9, 4, 2, d=32, seed=50)
+    kc = torch.zeros((2, 2, 12, 32), dtype=torch.bfloat16)
+    out, k_rows = oracle.gated_prefill_chunk(x["qg"], x["k"], x["v"], kc, kc.clone(), [0, 0],
+                                             x["q_w"], x["k_w"], 8, 1e7, 1e-6)
+    ref = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 8, 1e7, 1e-6)
+    assert torch.equal(out, ref)
+    assert torch.equal(k_rows, oracle.gated_qknorm_rope(x["k"], x["k_w"], 32, 8, 1e7, 1e-6))
+
+
+def test_gated_chunk_of_one_token_is_gated_decode():
+    x = inputs.gated_decode_inputs(2, 4, 2, 16, 3, 12, d=32, seed=51)
+    out, _ = oracle.gated_prefill_chunk(x["qg"][:, None], x["k_new"][:, None],
+                                        x["v_new"][:, None], x["k_cache"], x["v_cache"],
+                                        x["start_pos"], x["q_w"], x["k_w"], 8, 1e7, 1e-6)
+    ref, _ = oracle.gated_decode(x["qg"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                                 x["start_pos"], x["q_w"], x["k_w"], 8, 1e7, 1e-6)
+    assert torch.equal(out[:, 0], ref)
+
+
+def test_gated_chunks_in_sequence_equal_one_prefill():
+    """Chunks [0:2], [2:5], [5:6] of a prompt through a bf16 cache give the
+    full prefill's rows (the first chunk exactly, the later ones to the
+    rounding of the cached keys)."""
+    T, Hq, Hkv, d = 6, 4, 2, 32
+    x = inputs.gated_inputs(1, T, Hq, Hkv, d=d, seed=52)
+    full = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 8, 1e7, 1e-6)
+    kc = torch.zeros((1, Hkv, 8, d), dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    for i, (a, b) in enumerate([(0, 2), (2, 5), (5, 6)]):
+        part, k_rows = oracle.gated_prefill_chunk(
+            x["qg"][:, a:b].contiguous(), x["k"][:, a:b].contiguous(), x["v"][:, a:b].contiguous(),
+            kc, vc, [a], x["q_w"], x["k_w"], 8, 1e7, 1e-6)
+        if i == 0:
+            assert torch.equal(part, full[:, a:b])
+        else:
+            assert (part - full[:, a:b]).abs().max() < 1e-2
+        kc[0, :, a:b] = k_rows[0].transpose(0, 1).to(torch.bfloat16)
+        vc[0, :, a:b] = x["v"][0, a:b].transpose(0, 1)
+
+
+def test_gated_chunk_rejects_overflow():
+    x = inputs.gated_inputs(1, 3, 2, 1, d=16, seed=53)
+    kc = torch.zeros((1, 1, 4, 16), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        oracle.gated_prefill_chunk(x["qg"], x["k"], x["v"], kc, kc, [2], x["q_w"], x["k_w"], 4,
+                                   1e7, 1e-6)
