@@ -40,6 +40,7 @@ DECODE_WORKLOAD = "qwen3-8b-decode-b64"
 CHUNK_WORKLOAD = "qwen3-8b-chunk-b4-t1024-at3072"
 GATED_WORKLOAD = "qwen3-next-80b-gated-b4-t4096"
 GATED_DECODE_WORKLOAD = "qwen3-next-80b-gated-decode-b64"
+GATED_CHUNK_WORKLOAD = "qwen3-next-80b-gated-chunk-b4-t1024-at3072"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2 ** 20
 
@@ -387,6 +388,48 @@ def bench_chunk(binding, device, steps: int, warmup: int, world: int):
     return w, start, ms
 
 
+def bench_gated_chunk(binding, device, steps: int, warmup: int, world: int):
+    """Gated chunked prefill: as bench_chunk, on the Qwen3-Next-shaped gated
+    layer (the caches hold each prompt's first sp_lo tokens; the timed step is
+    the last T tokens as one chunk)."""
+    w = WORKLOADS[GATED_CHUNK_WORKLOAD]
+    x = inputs.workload_inputs(w, device=device)
+    p0 = w.sp_lo
+    kc = torch.full((w.B, w.Hkv, w.S_max, w.d), float("nan"), dtype=torch.bfloat16, device=device)
+    vc = torch.full_like(kc, float("nan"))
+    head = {k: x[k][:, :p0].contiguous() for k in ("qg", "k", "v")}
+    tail = {k: x[k][:, p0:].contiguous() for k in ("qg", "k", "v")}
+    binding.gated_prefill_chunk(head["qg"], head["k"], head["v"], kc, vc, [0] * w.B, x["q_w"],
+                                x["k_w"], w.d_r, w.theta, w.eps)
+    del head
+    out = torch.empty((w.B, w.T, w.Hq, w.d), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(binding.gated_prefill_chunk_workspace_size(w.B, w.T, w.Hq, w.Hkv),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    start = [p0] * w.B
+
+    def step():
+        binding.gated_prefill_chunk(tail["qg"], tail["k"], tail["v"], kc, vc, start, x["q_w"],
+                                    x["k_w"], w.d_r, w.theta, w.eps, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    barrier(world, device)
+    synchronize_all(device)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    synchronize_all(device)
+    barrier(world, device)
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    status = binding.last_device_error(ws)
+    if status != 0:
+        raise RuntimeError(f"gated chunk device error word: {status}")
+    return w, start, ms
+
+
 def bench_gated(binding, device, steps: int, warmup: int, world: int):
     """Gated global attention of Qwen3-Next / Qwen3.5: the prologue and the
     attention kernel timed separately within each step (inputs above L2)."""
@@ -499,6 +542,8 @@ def run_profile_case(which: str) -> None:
         bench_chunk(binding, device, 3, 0, 1)
     elif which == "gated":
         bench_gated(binding, device, 3, 0, 1)
+    elif which == "gated_chunk":
+        bench_gated_chunk(binding, device, 3, 0, 1)
     elif which == "gated_decode":
         w = WORKLOADS[GATED_DECODE_WORKLOAD]
         B = 16  # a quarter of the batch: about 1 GB of cache
@@ -547,10 +592,14 @@ def run_ours(args) -> None:
             cw, c_start, ch_ms = bench_chunk(binding, device, args.steps, args.warmup, world)
         gw, g_ms, gp_ms, ga_ms = (None, None, None, None)
         gdw, gd_start, gd_ms = (None, None, None)
+        gcw, gc_start, gc_ms = (None, None, None)
         if not args.no_gated:
             gw, g_ms, gp_ms, ga_ms = bench_gated(binding, device, args.steps, args.warmup, world)
             gdw, gd_start, gd_ms = bench_gated_decode(binding, device, args.steps, args.warmup,
                                                       world)
+            if not args.no_chunk:
+                gcw, gc_start, gc_ms = bench_gated_chunk(binding, device, args.steps, args.warmup,
+                                                         world)
     clocks = clk.summary()
 
     flops = accounting.prefill_flops(w.B, w.T, w.Hq, w.d)
@@ -691,6 +740,25 @@ def run_ours(args) -> None:
                          "traffic": ncu_traffic("decode_split_kernel<256>")},
             "gpu_launches": 2 * args.steps,
         }
+    if gc_ms is not None:
+        cflops = accounting.chunk_flops(gc_start, gcw.T, gcw.Hq, gcw.d)
+        gc_max = max_over_ranks(gc_ms, world, device)
+        per_gpu = cflops / (gc_max / 1e3) / 1e12
+        line["gated_chunk"] = {
+            "value": round(whole_job_rate(cflops, world, gc_max / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s", "ms_per_step": round(gc_max, 4),
+            "config": {"workload": gcw.name, "B": gcw.B, "Tq": gcw.T, "start_pos": gcw.sp_lo,
+                       "Hq": gcw.Hq, "Hkv": gcw.Hkv, "d": gcw.d, "d_rot": gcw.d_r,
+                       "S_max": gcw.S_max, "flops_per_step": cflops,
+                       "api": "q3a_gated_prefill_chunk (prologue writes the chunk into the "
+                              "caches, attention reads them)"},
+            "roofline": {"bound": "tensor", "kernel": "gated_prologue_kernel<chunk> + "
+                         "gated_attention_pair_kernel<GatedAttnChunkArgs>",
+                         "achieved": round(per_gpu, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(per_gpu / peaks["bf16_tflops"], 4),
+                         "peak_source": f"{peak_src} bf16 dense burst", "traffic": None},
+            "gpu_launches": 2 * args.steps,
+        }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x_cpu = {k: t.cpu() for k, t in x.items()}
         line["cpu_baseline"] = cpu_baseline_prefill(w, x_cpu)
@@ -762,7 +830,8 @@ def main(argv=None) -> None:
                     choices=[n for n, w in WORKLOADS.items() if w.kind == "prefill"],
                     help="prefill workload of the step (the default is the headline one)")
     ap.add_argument("--profile-case",
-                    choices=["prefill", "decode", "chunk", "gated", "gated_decode"],
+                    choices=["prefill", "decode", "chunk", "gated", "gated_decode",
+                             "gated_chunk"],
                     help="run a few launches of one kernel for an ncu capture, print no JSON")
     args = ap.parse_args(argv)
     if args.profile_case:

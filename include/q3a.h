@@ -339,6 +339,47 @@ q3a_status q3a_gated_prefill_fill(const q3a_bf16* qg, const q3a_bf16* k, const q
                                   void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * q3a_gated_prefill_chunk — a chunk of Tq new tokens per sequence of the
+ * gated global-attention layer against its KV caches, appending the chunk.
+ *
+ *   qg      [B, Tq, Hq, 2d] bf16: per head, the query (first d) and the gate.
+ *   k, v    [B, Tq, Hkv, d] bf16 projected keys / values of the chunk.
+ *   k_cache, v_cache [B, Hkv, S_max, d] bf16: rows 0..start_pos[b]-1 hold the
+ *           sequence's earlier keys (zero-centred-normalised with the same
+ *           k_w and partially rotated, as this library writes them) and values.
+ *   start_pos HOST int32 [B]: token t of sequence b sits at start_pos[b] + t.
+ *   out     [B, Tq, Hq, d] bf16: token t attends to cache rows
+ *           0..start_pos[b]-1 and the chunk's keys 0..t, and the result is
+ *           multiplied by sigmoid(gate).
+ *   Side effect: k_cache[b, :, start_pos[b] + t] = the chunk's normalised,
+ *   rotated keys and v_cache[b, :, start_pos[b] + t] = v, for t < Tq; other
+ *   rows are neither written nor, past start_pos[b] + Tq, used (the kernel
+ *   reads them but gives them zero weight and zeroes their values on chip, so
+ *   a NaN there does not reach the output).
+ *   With every start_pos[b] = 0 this is q3a_gated_prefill_fill; with Tq = 1
+ *   it computes what q3a_gated_decode computes.
+ *   Requires 0 <= start_pos[b] and start_pos[b] + Tq <= S_max for every b,
+ *   else Q3A_ERANGE with the caches untouched. B <= 2048, S_max <= 2^30,
+ *   Hq + 2 Hkv <= 192, d = 256, d_rot a multiple of 16 up to 256; groupings
+ *   as q3a_gated_prefill.
+ *   workspace: at least q3a_gated_prefill_chunk_workspace_size() bytes,
+ *   256-byte aligned, owned by the caller (normalised queries, error word).
+ *   B == 0 or Tq == 0: returns Q3A_OK and launches nothing.
+ * Source: "Chapter 20, Qwen3 and Qwen3.5" §20.3 (position counter, cached
+ * keys then new ones, rectangular causal mask starting at pos_start; chunks
+ * [0:2], [2:5], [5:6] against one forward) applied to the §20.4 gated layer.
+ * ------------------------------------------------------------------------- */
+size_t q3a_gated_prefill_chunk_workspace_size(int B, int Tq, int Hq, int Hkv, int d);
+
+q3a_status q3a_gated_prefill_chunk(const q3a_bf16* qg, const q3a_bf16* k, const q3a_bf16* v,
+                                   q3a_bf16* k_cache, q3a_bf16* v_cache,
+                                   const int32_t* start_pos,
+                                   const q3a_bf16* q_w, const q3a_bf16* k_w, q3a_bf16* out,
+                                   int B, int Tq, int Hq, int Hkv, int d, int d_rot, int S_max,
+                                   double theta, float eps,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_gated_decode — one decode step of the gated global-attention layer of
  * Qwen3-Next / Qwen3.5 against a KV cache, appending the new token
  * ("Chapter 20, Qwen3 and Qwen3.5" §20.3 cache protocol, §20.4 layer).

@@ -26,7 +26,8 @@ EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size"
             "q3a_gated_prefill_prologue", "q3a_gated_prefill_attention",
             "q3a_gated_decode_workspace_size", "q3a_gated_decode",
             "q3a_gated_decode_device_pos", "q3a_gated_prefill_fill_workspace_size",
-            "q3a_gated_prefill_fill"]
+            "q3a_gated_prefill_fill", "q3a_gated_prefill_chunk_workspace_size",
+            "q3a_gated_prefill_chunk"]
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +102,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_gated_prefill_fill_workspace_size.restype = sz
         lib.q3a_gated_prefill_fill.argtypes = [vp] * 8 + [i] * 7 + [d, f, vp, sz, vp]
         lib.q3a_gated_prefill_fill.restype = i
+        lib.q3a_gated_prefill_chunk_workspace_size.argtypes = [i] * 5
+        lib.q3a_gated_prefill_chunk_workspace_size.restype = sz
+        lib.q3a_gated_prefill_chunk.argtypes = [vp] * 9 + [i] * 7 + [d, f, vp, sz, vp]
+        lib.q3a_gated_prefill_chunk.restype = i
         _lib = lib
         return lib
 
@@ -490,4 +495,44 @@ def gated_prefill_fill(qg, k, v, k_cache, v_cache, q_w, k_w, d_rot: int, theta: 
                                        workspace.data_ptr(), workspace.numel(),
                                        _stream(qg.device))
     _raise(st, "q3a_gated_prefill_fill")
+    return out
+
+
+def gated_prefill_chunk_workspace_size(B: int, Tq: int, Hq: int, Hkv: int, d: int = 256) -> int:
+    return int(load().q3a_gated_prefill_chunk_workspace_size(B, Tq, Hq, Hkv, d))
+
+
+def gated_prefill_chunk(qg, k, v, k_cache, v_cache, start_pos, q_w, k_w, d_rot: int,
+                        theta: float, eps: float, out=None,
+                        workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """A chunk of Tq tokens per sequence of the gated layer against its caches,
+    which it extends by the chunk's normalised, rotated keys and its values.
+
+    qg [B,Tq,Hq,512], k/v [B,Tq,Hkv,256] bf16; caches [B,Hkv,S_max,256] bf16;
+    start_pos: host int32 [B], position of each sequence's first chunk token.
+    """
+    B, Tq, Hq, Hkv, d = _gated_shapes(qg, k)
+    S_max = k_cache.shape[2]
+    _check(qg, "qg")
+    _check(k, "k", (B, Tq, Hkv, d))
+    _check(v, "v", (B, Tq, Hkv, d))
+    _check(k_cache, "k_cache", (B, Hkv, S_max, d))
+    _check(v_cache, "v_cache", (B, Hkv, S_max, d))
+    _check(q_w, "q_w", (d,))
+    _check(k_w, "k_w", (d,))
+    sp = _host_positions(start_pos, B)
+    if out is None:
+        out = torch.empty((B, Tq, Hq, d), dtype=torch.bfloat16, device=qg.device)
+    _check(out, "out", (B, Tq, Hq, d))
+    need = gated_prefill_chunk_workspace_size(B, Tq, Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=qg.device)
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_gated_prefill_chunk(qg.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                        k_cache.data_ptr(), v_cache.data_ptr(), sp.data_ptr(),
+                                        q_w.data_ptr(), k_w.data_ptr(), out.data_ptr(), B, Tq, Hq,
+                                        Hkv, d, int(d_rot), S_max, float(theta), float(eps),
+                                        workspace.data_ptr(), workspace.numel(),
+                                        _stream(qg.device))
+    _raise(st, "q3a_gated_prefill_chunk")
     return out

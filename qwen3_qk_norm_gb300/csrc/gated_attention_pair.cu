@@ -49,6 +49,16 @@
 // exchanged between the four key quarters of a row, with O rescaled in TMEM
 // after the previous PV has completed.
 //
+// A chunk against the caches ("Chapter 20, Qwen3 and Qwen3.5" §20.3: cached
+// keys followed by the chunk's own, a causal mask that starts at the chunk's
+// first position) is the same kernel with K and V read from the head-major
+// caches and a per-sequence start position p0: token t sees keys 0..p0 + t.
+// Rows of the last V tile past p0 + T hold whatever the cache holds there (a
+// NaN there would turn a zero weight into a NaN in PV), so each CTA's producer
+// warp clears them in its own V half once that tile has landed; the odd CTA
+// then forwards "tail cleared" instead of "tile landed" for that load, and the
+// MMA issuer waits for the even CTA's own "tail cleared".
+//
 // Every mbarrier wait is bounded; a timeout sets the error word and every
 // role unwinds; the MMA issuer drains its MMAs and both CTAs meet at a cluster
 // barrier before freeing tensor memory.
@@ -92,6 +102,7 @@ struct Bars {
   uint64_t xmax_full;  // online-max path: the CTA's four quarters posted their tile max
   uint64_t o_final;
   uint64_t drain;
+  uint64_t vtail;      // chunk: the last V half tile's rows past the valid keys cleared
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -134,8 +145,28 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
   }
 }
 
+// The plain prefill and the chunk against the caches are two instantiations,
+// so the plain one carries none of the chunk's bookkeeping.
+__host__ __device__ __forceinline__ const GatedAttnArgs& base_args(const GatedAttnArgs& a) {
+  return a;
+}
+__host__ __device__ __forceinline__ const GatedAttnArgs& base_args(const GatedAttnChunkArgs& a) {
+  return a.base;
+}
+__device__ __forceinline__ int chunk_start(const GatedAttnArgs&, int) { return 0; }
+__device__ __forceinline__ int chunk_start(const GatedAttnChunkArgs& a, int b) {
+  return a.pos_b[b];
+}
+__device__ __forceinline__ bool fixed_shift_allowed(const GatedAttnArgs&) { return true; }
+__device__ __forceinline__ bool fixed_shift_allowed(const GatedAttnChunkArgs& a) {
+  return a.fixed_shift_ok != 0;
+}
+
+template <class Args>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gated_attention_pair_kernel(const __grid_constant__ GatedAttnArgs a) {
+    gated_attention_pair_kernel(const __grid_constant__ Args args) {
+  constexpr bool kChunk = sizeof(Args) != sizeof(GatedAttnArgs);
+  const GatedAttnArgs& a = base_args(args);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -155,9 +186,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int t0_pair = pm * 2 * tile_tok;
   const int t0 = t0_pair + (int)rank * tile_tok;  // this CTA's first token
   const int t_last = min(t0_pair + 2 * tile_tok, a.T) - 1;
-  const int n_tiles = t_last / BN + 1;
+  // token t of this sequence sits at position p0 + t (p0 = 0 for a plain
+  // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
+  const int p0 = chunk_start(args, b);
+  const int n_tiles = (p0 + t_last) / BN + 1;
+  const int n_keys = p0 + a.T;
   const float bound = *a.logit_bound;
-  const bool fixed_max = bound >= 0.f && bound <= kFixedMaxLimit;
+  const bool fixed_max = fixed_shift_allowed(args) && bound >= 0.f && bound <= kFixedMaxLimit;
+  // chunk: load index of the last V half tile, and whether it holds rows past
+  // the valid keys
+  const uint32_t last_load = 2u * (uint32_t)n_tiles - 1u;
+  const bool v_tail = kChunk && n_tiles * BN > n_keys;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -175,6 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars->xmax_full, kSoftmaxWGs * 128);
     mbar_init(&bars->o_final, 1);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->vtail, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -186,7 +226,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort = &bars->abort_flag;
 
   if (warp >= kSoftmaxWGs * 4) {
-    if (warp == kSoftmaxWGs * 4 && lane == 0) {
+    if (warp == kSoftmaxWGs * 4) {
+     if (lane == 0) {
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_k);
@@ -235,6 +276,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (uint32_t i = n > (uint32_t)kSlots ? n - kSlots : 0u; i < n; ++i)
           mbar_wait(&bars->slot_full[slot_of(i)], use_of(i), nullptr, 0, nullptr);
       }
+     }
+      if (v_tail) {
+        // every load has been issued (lane 0 is past its loop), so the slot's
+        // barrier is in the phase of the last load: wait for it, clear this
+        // CTA's rows past the valid keys in both 64-dim blocks (a cleared row
+        // is 128 bytes whatever the swizzle), and publish that
+        __syncwarp();
+        const bool landed = __all_sync(
+            kFull, mbar_wait(&bars->slot_full[slot_of(last_load)], use_of(last_load), a.err,
+                             kDevTimeoutTma, abort));
+        if (landed) {
+          uint8_t* vt = smem + OFF_RING + slot_of(last_load) * kSlotBytes;
+          const int first = n_keys - (n_tiles - 1) * BN;  // first key row to clear
+          const int chunks = (BN - first) * 16;           // 16-byte chunks, both blocks
+          for (int c = lane; c < chunks; c += 32) {
+            const int row = first + (c >> 4), blk = (c >> 3) & 1, q16 = c & 7;
+            *reinterpret_cast<uint4*>(vt + blk * kVBlock + row * 128 + q16 * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();  // the tensor pipe reads these rows next
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->vtail);
+        }
+      }
     } else if (warp == kSoftmaxWGs * 4 + 2 && lane == 0 && rank == 1) {
       // ----------------------------------------------- forwarder (odd CTA)
       // the even CTA's MMA issuer reads this CTA's Q and ring too: tell it
@@ -243,7 +308,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (mbar_wait(&bars->q_full, 0, a.err, kDevTimeoutTma, abort)) {
         mbar_arrive_cluster(peer_smem_addr(&bars->q_peer, 0));
         for (uint32_t t = 0; t < n_loads; ++t) {
-          if (!mbar_poll(&bars->slot_full[slot_of(t)], use_of(t), a.err, kDevTimeoutTma, abort))
+          const bool tail = v_tail && t == last_load;
+          if (!mbar_poll(tail ? &bars->vtail : &bars->slot_full[slot_of(t)],
+                         tail ? 0u : use_of(t), a.err, kDevTimeoutTma, abort))
             break;
           mbar_arrive_cluster(peer_smem_addr(&bars->slot_peer[slot_of(t)], 0));
         }
@@ -275,8 +342,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t ring_k = smem_desc_sw128(ring, 16, 1024);        // K-major K halves
       const uint64_t ring_v = smem_desc_sw128(ring, kVBlock, 1024);   // MN-major V halves
       auto wait_tile = [&](uint32_t t) {  // both CTAs' halves of load t
-        return mbar_wait_cluster(&bars->slot_full[slot_of(t)], use_of(t), a.err,
-                                 kDevTimeoutMma, abort) &&
+        const bool tail = v_tail && t == last_load;
+        return mbar_wait_cluster(tail ? &bars->vtail : &bars->slot_full[slot_of(t)],
+                                 tail ? 0u : use_of(t), a.err, kDevTimeoutMma, abort) &&
                mbar_wait_cluster(&bars->slot_peer[slot_of(t)], use_of(t), a.err,
                                  kDevTimeoutMma, abort);
       };
@@ -344,6 +412,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(lq * 32) << 16;
     const int tok = t0 + r / g;
     const int h = kv * g + (r % g);
+    // last key this row sees: padding rows of a chunk stop at the last valid
+    // key, so they never read rows past the valid keys either
+    const int key_last = kChunk ? p0 + min(tok, a.T - 1) : tok;
     const uint32_t p_full_even[2] = {peer_smem_addr(&bars->p_full[0], 0),
                                      peer_smem_addr(&bars->p_full[1], 0)};
     float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
@@ -361,10 +432,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(sr[e]);
       const int key0 = j * BN + cq * 32;
-      if (key0 + 31 > tok) {
+      if (key0 + 31 > key_last) {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (key0 + e > tok) s[e] = -INFINITY;
+          if (key0 + e > key_last) s[e] = -INFINITY;
       }
       bool move = false;
       float alpha = 1.0f;
@@ -485,17 +556,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-int gated_tokens_per_cta(int g) { return 2 * (BM / g); }  // per pair of CTAs
-
-cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream) {
-  static unsigned long long done_mask = 0;  // per-device dynamic smem opt-in
+template <class Args>
+cudaError_t launch(const Args& args, cudaStream_t stream) {
+  const GatedAttnArgs& a = base_args(args);
+  static unsigned long long done_mask = 0;  // per-device dynamic smem opt-in, per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(done_mask & (1ull << dev))) {
-    e = cudaFuncSetAttribute(gated_attention_pair_kernel,
+    e = cudaFuncSetAttribute(gated_attention_pair_kernel<Args>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) done_mask |= 1ull << dev;
@@ -503,8 +572,21 @@ cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream) 
   const long long grid = 2LL * a.n_mtiles * a.B * a.Hkv;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7ffffffeLL) return cudaErrorInvalidConfiguration;
-  gated_attention_pair_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(a);
+  gated_attention_pair_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int gated_tokens_per_cta(int g) { return 2 * (BM / g); }  // per pair of CTAs
+
+cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream) {
+  return launch(a, stream);
+}
+
+cudaError_t launch_gated_attention(const GatedAttnChunkArgs& a, cudaStream_t stream) {
+  if (a.base.B > kMaxBatch || !a.base.v_head_major) return cudaErrorInvalidValue;
+  return launch(a, stream);
 }
 
 }  // namespace q3a

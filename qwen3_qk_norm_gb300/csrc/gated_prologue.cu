@@ -23,6 +23,11 @@
 // so one shuffle per element brings the partner. Q rows go back out as one
 // block per CTA ([B, T, Hq, 256] keeps the token order), K rows one 512-byte
 // store each into the head-major [B, Hkv, T, 256] layout.
+//
+// A chunk against the caches ("Chapter 20, Qwen3 and Qwen3.5" §20.3: the
+// position counter starts at the number of cached tokens) is the same kernel
+// with a per-sequence start position: token t of sequence b is rotated at
+// pos_b[b] + t and its key and value land in cache row pos_b[b] + t.
 #include "q3a_internal.h"
 #include "q3a_rope.cuh"
 
@@ -36,8 +41,24 @@ constexpr int kMaxTok = 8;
 constexpr int kRowBytes = kGatedD * 2;
 constexpr int kMaxRows = 192;  // (Hq + Hkv) rows of one token must fit the staging buffer
 
+__host__ __device__ __forceinline__ const GatedPrologueArgs& base_args(const GatedPrologueArgs& a) {
+  return a;
+}
+__host__ __device__ __forceinline__ const GatedPrologueArgs& base_args(
+    const GatedPrologueChunkArgs& a) {
+  return a.base;
+}
+GatedPrologueArgs& base_args(GatedPrologueArgs& a) { return a; }
+GatedPrologueArgs& base_args(GatedPrologueChunkArgs& a) { return a.base; }
+__device__ __forceinline__ int chunk_start(const GatedPrologueArgs&, long long) { return 0; }
+__device__ __forceinline__ int chunk_start(const GatedPrologueChunkArgs& a, long long b) {
+  return a.pos_b[b];
+}
+
+template <class Args>
 __global__ void __launch_bounds__(kThreads)
-    gated_prologue_kernel(const __grid_constant__ GatedPrologueArgs a) {
+    gated_prologue_kernel(const __grid_constant__ Args args) {
+  const GatedPrologueArgs& a = base_args(args);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) float cos_s[kMaxTok][128];
   __shared__ __align__(16) float sin_s[kMaxTok][128];
@@ -93,7 +114,7 @@ __global__ void __launch_bounds__(kThreads)
     long long b;
     int t;
     token_bt(b_first, t_first, tt, a.T, b, t);
-    const float2 c_s = rope_cos_sin(t, a.turn_freq[i]);
+    const float2 c_s = rope_cos_sin((long long)chunk_start(args, b) + t, a.turn_freq[i]);
     cos_s[tt][i] = c_s.x;
     sin_s[tt][i] = c_s.y;
   }
@@ -155,7 +176,7 @@ __global__ void __launch_bounds__(kThreads)
     long long b;
     int t;
     token_bt(b_first, t_first, tt, a.T, b, t);
-    const long long dst_row = (b * Hkv + kv) * a.khat_rows + t;
+    const long long dst_row = (b * Hkv + kv) * a.khat_rows + chunk_start(args, b) + t;
     bulk_store(a.khat + dst_row * kGatedD, rows_k + (size_t)rr * kGatedD, kRowBytes);
     if (v_bytes) bulk_store(a.v_cache + dst_row * kGatedD, rows_v + (size_t)rr * kGatedD, kRowBytes);
     issued = true;
@@ -163,14 +184,12 @@ __global__ void __launch_bounds__(kThreads)
   if (issued) bulk_commit_and_wait_read();  // shared memory stays valid until read
 }
 
-}  // namespace
-
-int gated_prologue_max_heads() { return kMaxRows; }
-
-cudaError_t launch_gated_prologue(const GatedPrologueArgs& a_in, cudaStream_t stream) {
-  const long long n_tok = (long long)a_in.B * a_in.T;
+template <class Args>
+cudaError_t launch(const Args& args_in, cudaStream_t stream) {
+  Args args = args_in;
+  GatedPrologueArgs& a = base_args(args);
+  const long long n_tok = (long long)a.B * a.T;
   if (n_tok == 0) return cudaSuccess;
-  GatedPrologueArgs a = a_in;
   const int rows_per_tok = a.Hq + (a.v ? 2 : 1) * a.Hkv;  // staged rows per token
   if (a.Hq <= 0 || a.Hkv <= 0 || rows_per_tok > kMaxRows) return cudaErrorInvalidValue;
   if (a.d_r < 0 || a.d_r > kGatedD || (a.d_r & 15)) return cudaErrorInvalidValue;
@@ -178,20 +197,33 @@ cudaError_t launch_gated_prologue(const GatedPrologueArgs& a_in, cudaStream_t st
   tok = tok < 1 ? 1 : (tok > kMaxTok ? kMaxTok : tok);
   a.tok_per_cta = tok;
   const size_t smem = (size_t)tok * rows_per_tok * kRowBytes;
-  static unsigned long long attr_mask = 0;  // per-device dynamic smem opt-in
+  static unsigned long long attr_mask = 0;  // per-device dynamic smem opt-in, per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(attr_mask & (1ull << dev))) {
-    e = cudaFuncSetAttribute(gated_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gated_prologue_kernel<Args>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kMaxRows * kRowBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_mask |= 1ull << dev;
   }
   const long long grid = (n_tok + tok - 1) / tok;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  gated_prologue_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(a);
+  gated_prologue_kernel<Args><<<(unsigned)grid, kThreads, smem, stream>>>(args);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int gated_prologue_max_heads() { return kMaxRows; }
+
+cudaError_t launch_gated_prologue(const GatedPrologueArgs& a, cudaStream_t stream) {
+  return launch(a, stream);
+}
+
+cudaError_t launch_gated_prologue(const GatedPrologueChunkArgs& a, cudaStream_t stream) {
+  if (a.base.B > kMaxBatch) return cudaErrorInvalidValue;
+  return launch(a, stream);
 }
 
 }  // namespace q3a

@@ -679,6 +679,93 @@ q3a_status q3a_gated_prefill_fill(const q3a_bf16* qg, const q3a_bf16* k, const q
   return from_cuda(e);
 }
 
+size_t q3a_gated_prefill_chunk_workspace_size(int B, int Tq, int Hq, int Hkv, int d) {
+  return q3a_gated_prefill_fill_workspace_size(B, Tq, Hq, Hkv, d);
+}
+
+q3a_status q3a_gated_prefill_chunk(const q3a_bf16* qg, const q3a_bf16* k, const q3a_bf16* v,
+                                   q3a_bf16* k_cache, q3a_bf16* v_cache,
+                                   const int32_t* start_pos, const q3a_bf16* q_w,
+                                   const q3a_bf16* k_w, q3a_bf16* out, int B, int Tq, int Hq,
+                                   int Hkv, int d, int d_rot, int S_max, double theta, float eps,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+  if (!scalars_ok(theta, eps) || !d_rot_ok(d_rot)) return Q3A_EINVAL;
+  if (d != kGatedD || B < 0 || Tq < 0 || B > kMaxBatch || Hq <= 0 || Hkv <= 0 || Hq % Hkv)
+    return Q3A_EINVAL;
+  if (S_max <= 0 || S_max > (1 << 30)) return Q3A_EINVAL;
+  if ((long long)B * Tq * Hq > 0x7fffffffLL) return Q3A_EINVAL;
+  if (Hq + 2 * Hkv > gated_prologue_max_heads()) return Q3A_EINVAL;
+  if (!gated_group_ok(Hq, Hkv)) return Q3A_ENOTIMPL;
+  if (B == 0 || Tq == 0) return Q3A_OK;
+  const void* ptrs[] = {qg, k, v, k_cache, v_cache, q_w, k_w, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return Q3A_EINVAL;
+  if (!start_pos) return Q3A_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
+  if (ws_bytes < q3a_gated_prefill_chunk_workspace_size(B, Tq, Hq, Hkv, d)) return Q3A_EINVAL;
+  bool all_at_zero = true;
+  for (int b = 0; b < B; ++b) {
+    const int32_t p = start_pos[b];
+    if (p < 0 || (long long)p + Tq > S_max) return Q3A_ERANGE;  // nothing written yet
+    all_at_zero = all_at_zero && p == 0;
+  }
+  const int g = Hq / Hkv;
+  uint16_t* qhat = gated_ws_q(workspace);
+
+  // tensor maps first: a failure there launches nothing. K and V maps cover
+  // all S_max rows of each (b, kv): the valid rows differ per sequence, so the
+  // attention kernel masks the keys and clears the V rows past them itself
+  GatedAttnChunkArgs ca;
+  memset(&ca, 0, sizeof ca);
+  GatedAttnArgs& aa = ca.base;
+  {
+    const uint64_t row = kGatedD * 2;
+    const uint64_t dq[4] = {kGatedD, (uint64_t)Hq, (uint64_t)Tq, (uint64_t)B};
+    const uint64_t sq[3] = {row, (uint64_t)Hq * row, (uint64_t)Tq * Hq * row};
+    const uint32_t bq[4] = {64, (uint32_t)g, (uint32_t)(128 / g), 1};
+    const uint64_t dc[3] = {kGatedD, (uint64_t)S_max, (uint64_t)B * Hkv};
+    const uint64_t sc[2] = {row, (uint64_t)S_max * row};
+    const uint32_t bk[3] = {64, 64, 1};
+    const uint32_t bv[3] = {64, 128, 1};
+    if (encode_tensor_map(&aa.tm_q, qhat, 4, dq, sq, bq) != CUDA_SUCCESS ||
+        encode_tensor_map(&aa.tm_k, k_cache, 3, dc, sc, bk) != CUDA_SUCCESS ||
+        encode_tensor_map(&aa.tm_v, v_cache, 3, dc, sc, bv) != CUDA_SUCCESS)
+      return Q3A_ECUDA;
+  }
+  aa.qg = qg;
+  aa.out = out;
+  aa.err = reinterpret_cast<uint32_t*>(workspace);
+  aa.logit_bound = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + 8);
+  aa.B = B;
+  aa.T = Tq;
+  aa.Hq = Hq;
+  aa.Hkv = Hkv;
+  aa.g = g;
+  const int tok = gated_tokens_per_cta(g);
+  aa.n_mtiles = (Tq + tok - 1) / tok;
+  aa.v_head_major = 1;
+  // cached keys come from earlier calls: only a chunk with no cached keys
+  // may use the logit bound of this call's weights
+  ca.fixed_shift_ok = all_at_zero ? 1 : 0;
+  for (int b = 0; b < B; ++b) ca.pos_b[b] = start_pos[b];
+
+  // Q -> Qhat [B, Tq, Hq]; K -> k_cache rows start_pos[b] + t (normalised,
+  // rotated at their positions); V -> v_cache rows start_pos[b] + t (copied)
+  GatedPrologueChunkArgs pc;
+  memset(&pc, 0, sizeof pc);
+  gated_prologue_args(pc.base, qg, k, q_w, k_w, B, Tq, Hq, Hkv, d_rot, theta, eps, workspace);
+  pc.base.khat = k_cache;
+  pc.base.khat_rows = S_max;
+  pc.base.v = v;
+  pc.base.v_cache = v_cache;
+  for (int b = 0; b < B; ++b) pc.pos_b[b] = start_pos[b];
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_gated_prologue(pc, st);
+  if (e == cudaSuccess) e = launch_gated_attention(ca, st);
+  return from_cuda(e);
+}
+
 // Shared by q3a_gated_decode (positions on the host) and
 // q3a_gated_decode_device_pos (positions in device memory, checked by a
 // device-side pre-pass; no host read or synchronisation).

@@ -149,8 +149,16 @@ struct GatedPrologueArgs {
   int tok_per_cta;  // set by launch_gated_prologue
   unsigned long long turn_freq[128];  // theta^(-2i/d_r) / (2 pi), i < d_r/2
 };
+// A chunk against the caches: token t of sequence b is rotated at position
+// pos_b[b] + t and its key and value go to cache row pos_b[b] + t
+// (khat = k_cache, khat_rows = S_max, v and v_cache set).
+struct GatedPrologueChunkArgs {
+  GatedPrologueArgs base;
+  int pos_b[kMaxBatch];
+};
 int gated_prologue_max_heads();
 cudaError_t launch_gated_prologue(const GatedPrologueArgs& a, cudaStream_t stream);
+cudaError_t launch_gated_prologue(const GatedPrologueChunkArgs& a, cudaStream_t stream);
 
 // K6: causal GQA attention over Qhat/Khat with the sigmoid output gate, on
 // pairs of CTAs (clusters of two).
@@ -167,7 +175,16 @@ struct GatedAttnArgs {
   int n_mtiles;  // pair tiles: ceil(T / gated_tokens_per_cta(g))
   int v_head_major;
 };
+// A chunk against the caches: K and V come from the head-major caches (maps
+// over all S_max rows, v_head_major set) and token t of sequence b sits at
+// position pos_b[b] + t, seeing keys 0..pos_b[b] + t.
+struct GatedAttnChunkArgs {
+  GatedAttnArgs base;
+  int fixed_shift_ok;  // 0: cached keys present, always use the online max
+  int pos_b[kMaxBatch];
+};
 cudaError_t launch_gated_attention(const GatedAttnArgs& a, cudaStream_t stream);
+cudaError_t launch_gated_attention(const GatedAttnChunkArgs& a, cudaStream_t stream);
 int gated_tokens_per_cta(int g);  // tokens of one KV group that a pair of CTAs covers
 
 // ----- tensor maps -----------------------------------------------------------

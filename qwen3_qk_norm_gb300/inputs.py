@@ -27,6 +27,9 @@ Recipe (all draws from a ``torch.Generator`` seeded with the workload's seed):
   gated decode: start_pos as for decode; then cache K, cache V [B,Hkv,S_max,d]
            ~ N(0,1) (rows start_pos[b].. set to NaN); then QG [B,Hq,2d], k_new,
            v_new [B,Hkv,d] ~ N(0,1); then w_q, w_k ~ U(-0.5, 0.5).
+  gated chunk: whole prompts of sp_lo + T tokens drawn as for gated; the first
+           sp_lo go into the caches through an earlier chunk, the last T are
+           the timed chunk. Caches start as NaN.
 
 Large workloads are drawn on the GPU (``device="cuda"``) with torch's CUDA
 generator; small ones on the CPU. Either way the draws are deterministic for a
@@ -42,7 +45,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "prefill", "decode", "chunk", "gated" or "gated_decode"
+    kind: str  # "prefill", "decode", "chunk", "gated", "gated_decode" or "gated_chunk"
     B: int
     Hq: int
     Hkv: int
@@ -92,6 +95,11 @@ WORKLOADS = {
         Workload("qwen3-next-80b-gated-decode-b64", "gated_decode", B=64, Hq=16, Hkv=2, d=256,
                  S_max=32768, sp_lo=1024, sp_hi=32768, d_r=64, theta=1e7, seed=9,
                  note="Qwen3-Next-80B-A3B-shaped gated decode, start_pos ~ U[1024, 32768)"),
+        Workload("qwen3-next-80b-gated-chunk-b4-t1024-at3072", "gated_chunk", B=4, T=1024,
+                 Hq=16, Hkv=2, d=256, S_max=4096, sp_lo=3072, sp_hi=3073, d_r=64, theta=1e7,
+                 seed=10,
+                 note="Qwen3-Next-80B-A3B-shaped gated chunked prefill: the last 1024 tokens "
+                      "of 4096-token prompts whose first 3072 tokens are already cached"),
     ]
 }
 
@@ -200,6 +208,8 @@ def workload_inputs(w: Workload, device="cpu") -> dict:
                                    device=device)
     if w.kind == "gated":
         return gated_inputs(w.B, w.T, w.Hq, w.Hkv, w.d, w.seed, device=device)
+    if w.kind == "gated_chunk":  # whole prompts; the caller splits them
+        return gated_inputs(w.B, w.sp_lo + w.T, w.Hq, w.Hkv, w.d, w.seed, device=device)
     if w.kind == "chunk":  # whole prompts; the caller splits them
         return prefill_inputs(w.B, w.sp_lo + w.T, w.Hq, w.Hkv, w.d, w.seed, device=device)
     if w.kind == "prefill":

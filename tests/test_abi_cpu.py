@@ -256,3 +256,24 @@ def test_gated_prefill_fill_host_checks(lib):
     assert call(Hq=160, Hkv=20) == binding.Q3A_EINVAL  # 160 + 2*20 staged rows per token > 192
     assert call(T=0) == binding.Q3A_OK
     assert lib.q3a_gated_prefill_fill_workspace_size(2, 100, 16, 2, 256) >= 256 + 2 * 100 * 16 * 512
+
+
+def test_gated_prefill_chunk_host_checks(lib):
+    def call(sp=(3,), Tq=4, Hq=16, Hkv=2, d=256, d_rot=64, S_max=8, ws_bytes=1 << 40):
+        B = len(sp)
+        arr = (ctypes.c_int32 * max(B, 1))(*sp)
+        return lib.q3a_gated_prefill_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.addressof(arr),
+                                           FAKE, FAKE, FAKE, B, Tq, Hq, Hkv, d, d_rot, S_max,
+                                           1e7, 1e-6, FAKE, ws_bytes, None)
+    assert call(sp=(5,)) == binding.Q3A_ERANGE      # 5 + 4 > 8
+    assert call(sp=(0, -1)) == binding.Q3A_ERANGE
+    assert call(sp=(0, 5)) == binding.Q3A_ERANGE      # any sequence out of range
+    assert call(Hq=36, Hkv=2) == binding.Q3A_ENOTIMPL
+    for kw in (dict(d=128), dict(d_rot=8), dict(ws_bytes=1024), dict(Hq=15, Hkv=2),
+               dict(Hq=160, Hkv=20), dict(S_max=0)):
+        assert call(**kw) == binding.Q3A_EINVAL, kw
+    assert call(sp=tuple([0] * 2049)) == binding.Q3A_EINVAL  # more sequences than one call takes
+    assert call(Tq=0) == binding.Q3A_OK
+    assert call(sp=()) == binding.Q3A_OK
+    assert (lib.q3a_gated_prefill_chunk_workspace_size(2, 100, 16, 2, 256)
+            == lib.q3a_gated_prefill_fill_workspace_size(2, 100, 16, 2, 256))

@@ -196,3 +196,134 @@ def test_gated_prefill_fill_then_decode_continues_the_sequence(cuda_lib):
                                  1e7, 1e-6)
         torch.cuda.synchronize()
         assert_close_attention(o[0], full[0, t], f"decode step {s}")
+
+
+# ----------------------------------------------------------------------------
+# Gated chunk against the caches (q3a_gated_prefill_chunk)
+# ----------------------------------------------------------------------------
+
+def gated_chunk_case(B, Tq, Hq, Hkv, S, start_pos, seed):
+    """Chunk inputs plus caches whose rows 0..start_pos[b]-1 hold random keys
+    and values and whose later rows are NaN."""
+    x = inputs.gated_inputs(B, Tq, Hq, Hkv, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    kc = torch.randn((B, Hkv, S, D), generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, Hkv, S, D), generator=g).to(torch.bfloat16)
+    for b, p in enumerate(start_pos):
+        kc[b, :, p:] = float("nan")
+        vc[b, :, p:] = float("nan")
+    return x, kc, vc
+
+
+@pytest.mark.parametrize("Tq,Hq,Hkv,d_r,start_pos", [
+    (37, 16, 2, 64, [0, 1, 127, 128, 1000]),   # Qwen3-Next heads; tile boundaries
+    (300, 8, 2, 64, [5, 700]),                 # several pair tiles, ragged tail
+    (1, 16, 2, 64, [0, 300, 2047]),            # one token per sequence
+    (130, 32, 2, 64, [64, 200]),               # g = 16
+    (50, 4, 4, 256, [90]),                     # g = 1, full rotary
+    (70, 24, 4, 64, [33, 513]),                # g = 6
+    (40, 24, 2, 0, [129, 7]),                  # g = 12, no rotary
+])
+def test_gated_chunk_matches_oracle_and_appends(cuda_lib, Tq, Hq, Hkv, d_r, start_pos):
+    B, S = len(start_pos), 2400
+    x, kc, vc = gated_chunk_case(B, Tq, Hq, Hkv, S, start_pos, seed=Tq + Hq + d_r)
+    d = {k: t.cuda() for k, t in x.items()}
+    kc_d, vc_d = kc.cuda(), vc.cuda()
+    out = binding.gated_prefill_chunk(d["qg"], d["k"], d["v"], kc_d, vc_d, start_pos, d["q_w"],
+                                      d["k_w"], d_r, 1e7, 1e-6)
+    torch.cuda.synchronize()
+    ref, k_rows = oracle.gated_prefill_chunk(x["qg"], x["k"], x["v"], kc, vc, start_pos,
+                                             x["q_w"], x["k_w"], d_r, 1e7, 1e-6)
+    assert bool(torch.isfinite(out).all())
+    assert_close_attention(out, ref, f"gated chunk Tq{Tq} Hq{Hq} Hkv{Hkv}")
+    kc_o, vc_o = kc_d.cpu(), vc_d.cpu()
+    for b, p in enumerate(start_pos):
+        assert_within_one_ulp(kc_o[b, :, p:p + Tq].transpose(0, 1), k_rows[b], f"keys b{b}")
+        assert torch.equal(vc_o[b, :, p:p + Tq].view(torch.int16),
+                           x["v"][b].transpose(0, 1).view(torch.int16))
+        assert torch.equal(kc_o[b, :, :p].view(torch.int16), kc[b, :, :p].view(torch.int16))
+        assert bool(torch.isnan(kc_o[b, :, p + Tq:].float()).all())
+        assert bool(torch.isnan(vc_o[b, :, p + Tq:].float()).all())
+
+
+def test_gated_chunk_at_zero_is_the_filling_prefill(cuda_lib):
+    """Every start position 0: the chunk gives q3a_gated_prefill_fill's output
+    and caches bit for bit (the same logit-bound path, the same tiles)."""
+    B, T, Hq, Hkv, S = 2, 170, 16, 2, 300
+    x = inputs.gated_inputs(B, T, Hq, Hkv, seed=21)
+    d = {k: t.cuda() for k, t in x.items()}
+    kc1 = torch.full((B, Hkv, S, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc1, kc2, vc2 = kc1.clone(), kc1.clone(), kc1.clone()
+    fill = binding.gated_prefill_fill(d["qg"], d["k"], d["v"], kc1, vc1, d["q_w"], d["k_w"], 64,
+                                      1e7, 1e-6)
+    chunk = binding.gated_prefill_chunk(d["qg"], d["k"], d["v"], kc2, vc2, [0, 0], d["q_w"],
+                                        d["k_w"], 64, 1e7, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(chunk, fill)
+    assert torch.equal(kc1.view(torch.int16), kc2.view(torch.int16))
+    assert torch.equal(vc1.view(torch.int16), vc2.view(torch.int16))
+
+
+def test_gated_chunks_in_sequence_equal_one_prefill(cuda_lib):
+    """A 600-token prompt as chunks [0:130], [130:300], [300:301], [301:600]
+    through the caches: every chunk's rows match the oracle's one-shot gated
+    prefill of the whole prompt (to the cache's bf16 rounding of the keys)."""
+    T, Hq, Hkv = 600, 16, 2
+    x = inputs.gated_inputs(1, T, Hq, Hkv, seed=22)
+    full = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    d = {k: t.cuda() for k, t in x.items()}
+    kc = torch.full((1, Hkv, 1024, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    for a, e in [(0, 130), (130, 300), (300, 301), (301, 600)]:
+        out = binding.gated_prefill_chunk(d["qg"][:, a:e].contiguous(), d["k"][:, a:e].contiguous(),
+                                          d["v"][:, a:e].contiguous(), kc, vc, [a], d["q_w"],
+                                          d["k_w"], 64, 1e7, 1e-6)
+        torch.cuda.synchronize()
+        assert_close_attention(out, full[:, a:e], f"chunk [{a}:{e}]")
+
+
+def test_gated_chunk_erange_writes_nothing(cuda_lib):
+    x, kc, vc = gated_chunk_case(2, 10, 16, 2, 64, [3, 60], seed=23)
+    d = {k: t.cuda() for k, t in x.items()}
+    kc_d, vc_d = kc.cuda(), vc.cuda()
+    out = torch.full((2, 10, 16, D), 3.0, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.Q3AError) as err:
+        binding.gated_prefill_chunk(d["qg"], d["k"], d["v"], kc_d, vc_d, [3, 60], d["q_w"],
+                                    d["k_w"], 64, 1e7, 1e-6, out=out)
+    assert err.value.status == binding.Q3A_ERANGE
+    torch.cuda.synchronize()
+    assert torch.equal(kc_d.cpu().view(torch.int16), kc.view(torch.int16))
+    assert bool((out == 3.0).all())
+
+
+@pytest.mark.slow
+def test_gated_chunk_workload_sampled_rows(cuda_lib):
+    """The gated chunk workload as the benchmark launches it (each prompt's
+    first 3072 tokens written by a chunk from position 0, then the last 1024
+    as one chunk); sampled rows against the oracle's gated prefill rows of the
+    whole prompt, computed one by one."""
+    w = WORKLOADS["qwen3-next-80b-gated-chunk-b4-t1024-at3072"]
+    x = inputs.workload_inputs(w, device="cuda")
+    p0 = w.sp_lo
+    kc = torch.full((w.B, w.Hkv, w.S_max, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    sl = lambda t, a, b: t[:, a:b].contiguous()  # noqa: E731
+    binding.gated_prefill_chunk(sl(x["qg"], 0, p0), sl(x["k"], 0, p0), sl(x["v"], 0, p0), kc, vc,
+                                [0] * w.B, x["q_w"], x["k_w"], w.d_r, w.theta, w.eps)
+    out = binding.gated_prefill_chunk(sl(x["qg"], p0, None), sl(x["k"], p0, None),
+                                      sl(x["v"], p0, None), kc, vc, [p0] * w.B, x["q_w"],
+                                      x["k_w"], w.d_r, w.theta, w.eps)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    g = torch.Generator().manual_seed(w.seed)
+    rows = [(0, 0, 0), (w.B - 1, w.T - 1, w.Hq - 1)]
+    rows += [(int(torch.randint(0, w.B, (1,), generator=g)),
+              int(torch.randint(0, w.T, (1,), generator=g)),
+              int(torch.randint(0, w.Hq, (1,), generator=g))) for _ in range(24)]
+    cpu = {k: t.cpu() for k, t in x.items()}
+    ref = oracle.gated_prefill_rows(cpu["qg"], cpu["k"], cpu["v"], cpu["q_w"], cpu["k_w"], w.d_r,
+                                    w.theta, w.eps,
+                                    torch.tensor([(b, p0 + t, h) for b, t, h in rows],
+                                                 dtype=torch.int32))
+    got = torch.stack([out[b, t, h] for b, t, h in rows])
+    assert_close_attention(got, ref, w.name)
