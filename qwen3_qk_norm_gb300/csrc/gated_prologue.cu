@@ -18,9 +18,12 @@
 // Layout of the work (HBM-bound stream, as in the Qwen3 prologue): a CTA owns
 // a few consecutive tokens. Their key rows are contiguous and come in with one
 // bulk copy; each query row is a 512-byte bulk copy out of the interleaved
-// query/gate projection. A warp owns a row, lane L holding elements
-// 8L..8L+7; the rotated pairs (i, i + d_r/2) sit in lanes L and L + d_r/16,
-// so one shuffle per element brings the partner. Q rows go back out as one
+// query/gate projection. A warp owns a row. Lanes L < d_r/8 hold rotated
+// pairs: elements 4L..4L+3 and their partners d_r/2 + 4L..d_r/2 + 4L+3, so
+// each pair (i, i + d_r/2) sits in one lane and the rotation needs no
+// exchange; the other lanes hold eight consecutive pass-through elements from
+// d_r on, and rotate by the angle 0 (cos 1, sin 0) with the same
+// instructions, so no lane branches. Q rows go back out as one
 // block per CTA ([B, T, Hq, 256] keeps the token order), K rows one 512-byte
 // store each into the head-major [B, Hkv, T, 256] layout.
 //
@@ -60,8 +63,10 @@ __global__ void __launch_bounds__(kThreads)
     gated_prologue_kernel(const __grid_constant__ Args args) {
   const GatedPrologueArgs& a = base_args(args);
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(16) float cos_s[kMaxTok][128];
-  __shared__ __align__(16) float sin_s[kMaxTok][128];
+  // per (token, lane): the cos / sin of the lane's four pair angles
+  // (1 and 0 for lanes without rotated pairs)
+  __shared__ __align__(16) float4 cos_s[kMaxTok][32];
+  __shared__ __align__(16) float4 sin_s[kMaxTok][32];
   __shared__ uint64_t bar;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = a.Hq, Hkv = a.Hkv;
@@ -107,61 +112,77 @@ __global__ void __launch_bounds__(kThreads)
   // (b, t) of the CTA's first token; the others by counting
   const long long b_first = tok0 / a.T;
   const int t_first = (int)(tok0 - b_first * a.T);
+  // lane layout (see the top of the file)
+  const int nrot = a.d_r >> 3;  // lanes holding rotated pairs
+  const bool rotated = lane < nrot;
+  const int off_a = rotated ? 4 * lane : a.d_r + 8 * (lane - nrot);
+  const int off_b = rotated ? (a.d_r >> 1) + 4 * lane : off_a + 4;
   // rotation table of this CTA's tokens while the rows are in flight
-  const int n_ang = a.d_r >> 1;
-  for (int e = tid; e < tok_here * n_ang; e += kThreads) {
-    const int tt = e / n_ang, i = e - tt * n_ang;
-    long long b;
-    int t;
-    token_bt(b_first, t_first, tt, a.T, b, t);
-    const float2 c_s = rope_cos_sin((long long)chunk_start(args, b) + t, a.turn_freq[i]);
-    cos_s[tt][i] = c_s.x;
-    sin_s[tt][i] = c_s.y;
+  float* cos_f = reinterpret_cast<float*>(cos_s);
+  float* sin_f = reinterpret_cast<float*>(sin_s);
+  for (int e = tid; e < tok_here * 128; e += kThreads) {
+    const int tt = e >> 7, i = e & 127;  // i = 4 * lane + j
+    float c = 1.0f, sn = 0.0f;
+    if (i < (a.d_r >> 1)) {
+      long long b;
+      int t;
+      token_bt(b_first, t_first, tt, a.T, b, t);
+      const float2 c_s = rope_cos_sin((long long)chunk_start(args, b) + t, a.turn_freq[i]);
+      c = c_s.x;
+      sn = c_s.y;
+    }
+    cos_f[e] = c;
+    sin_f[e] = sn;
   }
-  // this lane's scales 1 + w for elements 8L .. 8L+7
-  float sq[8], sk[8];
-  unpack8(reinterpret_cast<const uint4*>(a.q_w)[lane], sq);
-  unpack8(reinterpret_cast<const uint4*>(a.k_w)[lane], sk);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    sq[e] += 1.0f;
-    sk[e] += 1.0f;
-  }
-  // rotated lanes: L < d_r/8; partner lane L +- d_r/16
-  const int hl = a.d_r >> 4;
-  const bool rotated = lane < 2 * hl;
-  const bool lower = lane < hl;
-  const int partner = rotated ? (lower ? lane + hl : lane - hl) : lane;
-  const int ang0 = rotated ? 8 * (lower ? lane : lane - hl) : 0;
   __syncthreads();  // barrier initialised, table written
   mbar_wait(&bar, 0, nullptr, 0, nullptr);
 
   const int RQ = tok_here * Hq;
   const int rows = RQ + tok_here * Hkv;
+  // token of a row: (rr + 0.5) / H is below kMaxTok and at least 0.5 / H >=
+  // 2^-9 away from an integer, far more than its fp32 error, so truncation
+  // gives rr / H exactly
+  const float inv_hq = 1.0f / (float)Hq, inv_hkv = 1.0f / (float)Hkv;
+  // scales 1 + w of the lane's elements for the current tensor (a warp's rows
+  // run through Q first, then K: one reload at the switch)
+  float sa[4], sb[4];
+  int scale_of = -1;
   for (int q = warp; q < rows; q += kWarps) {
-    const bool is_q = q < RQ;
+    const int is_q = q < RQ ? 1 : 0;
+    if (is_q != scale_of) {
+      const uint16_t* w = is_q ? a.q_w : a.k_w;
+      unpack4(*reinterpret_cast<const uint2*>(w + off_a), sa);
+      unpack4(*reinterpret_cast<const uint2*>(w + off_b), sb);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        sa[j] += 1.0f;
+        sb[j] += 1.0f;
+      }
+      scale_of = is_q;
+    }
     const int rr = is_q ? q : q - RQ;
-    const int tt = is_q ? rr / Hq : rr / Hkv;
+    const int tt = (int)(((float)rr + 0.5f) * (is_q ? inv_hq : inv_hkv));
     uint16_t* row = (is_q ? rows_q : rows_k) + (size_t)rr * kGatedD;
-    float x[8], y[8], o[8];
-    unpack8(reinterpret_cast<const uint4*>(row)[lane], x);
+    float xa[4], xb[4], oa[4], ob[4];
+    unpack4(*reinterpret_cast<const uint2*>(row + off_a), xa);
+    unpack4(*reinterpret_cast<const uint2*>(row + off_b), xb);
     float ss = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+    for (int j = 0; j < 4; ++j) ss = fmaf(xa[j], xa[j], fmaf(xb[j], xb[j], ss));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float inv_rms = rsqrtf(ss * (1.0f / kGatedD) + a.eps);
+    const float4 c4 = cos_s[tt][lane], s4 = sin_s[tt][lane];
+    const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = x[e] * inv_rms * (is_q ? sq[e] : sk[e]);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      // rotated lanes: y c -+ y_partner s; the others keep y (c = 1, s = 0)
-      const float yp = __shfl_sync(0xffffffffu, y[e], partner);
-      const float c = rotated ? cos_s[tt][ang0 + e] : 1.0f;
-      const float sn = rotated ? (lower ? -sin_s[tt][ang0 + e] : sin_s[tt][ang0 + e]) : 0.0f;
-      o[e] = fmaf(yp, sn, y[e] * c);
+    for (int j = 0; j < 4; ++j) {
+      const float ya = xa[j] * inv_rms * sa[j];
+      const float yb = xb[j] * inv_rms * sb[j];
+      oa[j] = fmaf(yb, -sn[j], ya * c[j]);  // y_i c - y_{i+d_r/2} s
+      ob[j] = fmaf(ya, sn[j], yb * c[j]);   // y_{i+d_r/2} c + y_i s
     }
-    reinterpret_cast<uint4*>(row)[lane] = pack8(o);
+    *reinterpret_cast<uint2*>(row + off_a) = pack4(oa);
+    *reinterpret_cast<uint2*>(row + off_b) = pack4(ob);
   }
   fence_proxy_async_smem();  // the bulk stores below read what was just written
   __syncthreads();
