@@ -50,32 +50,6 @@ __device__ __forceinline__ void qknorm_rope_halfwarp(const float (&xl)[4], const
   }
 }
 
-// One head row held by a quarter-warp: lane L (0..7 of its quarter) holds
-// x[8L..8L+7] in xl and their rotate-half partners x[64+8L..64+8L+7] in xh,
-// with the matching gamma slices and the cos / sin of angles 8L..8L+7. The
-// reduction shuffles stay inside the quarter (`mask` = its eight lanes), so
-// the quarters of a warp may work on different rows or branches.
-__device__ __forceinline__ void qknorm_rope_quarterwarp(const float (&xl)[8], const float (&xh)[8],
-                                                        const float (&gl)[8], const float (&gh)[8],
-                                                        const float (&c)[8], const float (&sn)[8],
-                                                        float eps, unsigned mask, float (&ol)[8],
-                                                        float (&oh)[8]) {
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) ss = fmaf(xl[j], xl[j], fmaf(xh[j], xh[j], ss));
-  ss += __shfl_xor_sync(mask, ss, 4);
-  ss += __shfl_xor_sync(mask, ss, 2);
-  ss += __shfl_xor_sync(mask, ss, 1);
-  const float inv_rms = rsqrtf(ss * (1.0f / 128.0f) + eps);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float yl = xl[j] * inv_rms * gl[j];
-    const float yh = xh[j] * inv_rms * gh[j];
-    ol[j] = yl * c[j] - yh * sn[j];
-    oh[j] = yh * c[j] + yl * sn[j];
-  }
-}
-
 // Sequence b and in-sequence index t of token first + tt of a [B, T] token
 // range, given those of `first` (computed once per CTA): a CTA owns a few
 // consecutive tokens, so counting forward replaces a 64-bit division per use.
