@@ -166,6 +166,8 @@ KERNEL_SOURCES = {  # the kernel's file and every header it includes
                               "q3a_internal.h"],
     "decode_split_kernel<256>": ["decode_attention.cu", "q3a_rope.cuh", "q3a_device.cuh",
                                  "q3a_internal.h"],
+    "gated_attention_pair_kernel<chunk>": ["gated_attention_pair.cu", "q3a_pair.cuh",
+                                           "q3a_device.cuh", "q3a_internal.h"],
 }
 
 
@@ -756,7 +758,8 @@ def run_ours(args) -> None:
                          "gated_attention_pair_kernel<GatedAttnChunkArgs>",
                          "achieved": round(per_gpu, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(per_gpu / peaks["bf16_tflops"], 4),
-                         "peak_source": f"{peak_src} bf16 dense burst", "traffic": None},
+                         "peak_source": f"{peak_src} bf16 dense burst",
+                         "traffic": ncu_traffic("gated_attention_pair_kernel<chunk>")},
             "gpu_launches": 2 * args.steps,
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
