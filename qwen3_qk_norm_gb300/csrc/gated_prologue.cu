@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kThreads)
   // (1 and 0 for lanes without rotated pairs)
   __shared__ __align__(16) float4 cos_s[kMaxTok][32];
   __shared__ __align__(16) float4 sin_s[kMaxTok][32];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar[2];  // one per half of the CTA's tokens
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = a.Hq, Hkv = a.Hkv;
   const long long n_tok = (long long)a.B * a.T;
@@ -76,22 +76,33 @@ __global__ void __launch_bounds__(kThreads)
   uint16_t* rows_q = reinterpret_cast<uint16_t*>(smem);  // [tok][Hq][256]
   uint16_t* rows_k = rows_q + (size_t)a.tok_per_cta * Hq * kGatedD;  // [tok][Hkv][256]
   uint16_t* rows_v = rows_k + (size_t)a.tok_per_cta * Hkv * kGatedD;  // [tok][Hkv][256]
-  const uint32_t q_bytes = (uint32_t)tok_here * Hq * kRowBytes;
-  const uint32_t k_bytes = (uint32_t)tok_here * Hkv * kRowBytes;
-  const uint32_t v_bytes = a.v ? k_bytes : 0u;
+  // The tokens are taken in two halves, each with its own barrier: the first
+  // half is normalised and its stores are issued while the second is still
+  // arriving. Half h covers tokens [h ? tok_a : 0, h ? tok_here : tok_a).
+  const int tok_a = (tok_here + 1) >> 1;
+  const int vrows = a.v ? Hkv : 0;
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_init(&bar, 1);
+      mbar_init(&bar[0], 1);
+      mbar_init(&bar[1], 1);
       fence_mbar_init();
-      mbar_arrive_expect_tx(&bar, q_bytes + k_bytes + v_bytes);
-      bulk_load(rows_k, a.k + tok0 * Hkv * kGatedD, k_bytes, &bar);
-      if (v_bytes) bulk_load(rows_v, a.v + tok0 * Hkv * kGatedD, v_bytes, &bar);
+      for (int h = 0; h < 2; ++h) {
+        const int t_lo = h ? tok_a : 0, n = (h ? tok_here : tok_a) - t_lo;
+        if (n == 0) continue;
+        const uint32_t kv_bytes = (uint32_t)n * Hkv * kRowBytes;
+        mbar_arrive_expect_tx(&bar[h], (uint32_t)n * (Hq + Hkv + vrows) * kRowBytes);
+        bulk_load(rows_k + (size_t)t_lo * Hkv * kGatedD, a.k + (tok0 + t_lo) * Hkv * kGatedD,
+                  kv_bytes, &bar[h]);
+        if (vrows)
+          bulk_load(rows_v + (size_t)t_lo * Hkv * kGatedD, a.v + (tok0 + t_lo) * Hkv * kGatedD,
+                    kv_bytes, &bar[h]);
+      }
     }
     __syncwarp();
     for (int r = lane; r < tok_here * Hq; r += 32)  // query halves of the q|gate blocks
       bulk_load(rows_q + (size_t)r * kGatedD, a.qg + (tok0 * Hq + r) * (2 * kGatedD), kRowBytes,
-                &bar);
+                &bar[r >= tok_a * Hq ? 1 : 0]);
   }
   if (blockIdx.x == 0 && warp == 1) {
     if (a.err_clear && lane == 0) *a.err_clear = 0u;
@@ -134,73 +145,79 @@ __global__ void __launch_bounds__(kThreads)
     cos_f[e] = c;
     sin_f[e] = sn;
   }
-  __syncthreads();  // barrier initialised, table written
-  mbar_wait(&bar, 0, nullptr, 0, nullptr);
+  __syncthreads();  // barriers initialised, table written
 
-  const int RQ = tok_here * Hq;
-  const int rows = RQ + tok_here * Hkv;
   // token of a row: (rr + 0.5) / H is below kMaxTok and at least 0.5 / H >=
   // 2^-9 away from an integer, far more than its fp32 error, so truncation
   // gives rr / H exactly
   const float inv_hq = 1.0f / (float)Hq, inv_hkv = 1.0f / (float)Hkv;
-  // scales 1 + w of the lane's elements for the current tensor (a warp's rows
-  // run through Q first, then K: one reload at the switch)
-  float sa[4], sb[4];
-  int scale_of = -1;
-  for (int q = warp; q < rows; q += kWarps) {
-    const int is_q = q < RQ ? 1 : 0;
-    if (is_q != scale_of) {
-      const uint16_t* w = is_q ? a.q_w : a.k_w;
-      unpack4(*reinterpret_cast<const uint2*>(w + off_a), sa);
-      unpack4(*reinterpret_cast<const uint2*>(w + off_b), sb);
+  bool issued = false;
+  for (int h = 0; h < 2; ++h) {
+    const int t_lo = h ? tok_a : 0, t_hi = h ? tok_here : tok_a;
+    if (t_hi == t_lo) break;  // one token: no second half (uniform over the CTA)
+    mbar_wait(&bar[h], 0, nullptr, 0, nullptr);
+    const int nq = (t_hi - t_lo) * Hq;
+    const int rows = nq + (t_hi - t_lo) * Hkv;
+    // scales 1 + w of the lane's elements for the current tensor (a warp's
+    // rows run through Q first, then K: one reload at the switch)
+    float sa[4], sb[4];
+    int scale_of = -1;
+    for (int q = warp; q < rows; q += kWarps) {
+      const int is_q = q < nq ? 1 : 0;
+      if (is_q != scale_of) {
+        const uint16_t* w = is_q ? a.q_w : a.k_w;
+        unpack4(*reinterpret_cast<const uint2*>(w + off_a), sa);
+        unpack4(*reinterpret_cast<const uint2*>(w + off_b), sb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          sa[j] += 1.0f;
+          sb[j] += 1.0f;
+        }
+        scale_of = is_q;
+      }
+      const int rr = is_q ? t_lo * Hq + q : t_lo * Hkv + (q - nq);  // row within the CTA
+      const int tt = (int)(((float)rr + 0.5f) * (is_q ? inv_hq : inv_hkv));
+      uint16_t* row = (is_q ? rows_q : rows_k) + (size_t)rr * kGatedD;
+      float xa[4], xb[4], oa[4], ob[4];
+      unpack4(*reinterpret_cast<const uint2*>(row + off_a), xa);
+      unpack4(*reinterpret_cast<const uint2*>(row + off_b), xb);
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ss = fmaf(xa[j], xa[j], fmaf(xb[j], xb[j], ss));
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float inv_rms = rsqrtf(ss * (1.0f / kGatedD) + a.eps);
+      const float4 c4 = cos_s[tt][lane], s4 = sin_s[tt][lane];
+      const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        sa[j] += 1.0f;
-        sb[j] += 1.0f;
+        const float ya = xa[j] * inv_rms * sa[j];
+        const float yb = xb[j] * inv_rms * sb[j];
+        oa[j] = fmaf(yb, -sn[j], ya * c[j]);  // y_i c - y_{i+d_r/2} s
+        ob[j] = fmaf(ya, sn[j], yb * c[j]);   // y_{i+d_r/2} c + y_i s
       }
-      scale_of = is_q;
+      *reinterpret_cast<uint2*>(row + off_a) = pack4(oa);
+      *reinterpret_cast<uint2*>(row + off_b) = pack4(ob);
     }
-    const int rr = is_q ? q : q - RQ;
-    const int tt = (int)(((float)rr + 0.5f) * (is_q ? inv_hq : inv_hkv));
-    uint16_t* row = (is_q ? rows_q : rows_k) + (size_t)rr * kGatedD;
-    float xa[4], xb[4], oa[4], ob[4];
-    unpack4(*reinterpret_cast<const uint2*>(row + off_a), xa);
-    unpack4(*reinterpret_cast<const uint2*>(row + off_b), xb);
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ss = fmaf(xa[j], xa[j], fmaf(xb[j], xb[j], ss));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float inv_rms = rsqrtf(ss * (1.0f / kGatedD) + a.eps);
-    const float4 c4 = cos_s[tt][lane], s4 = sin_s[tt][lane];
-    const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float ya = xa[j] * inv_rms * sa[j];
-      const float yb = xb[j] * inv_rms * sb[j];
-      oa[j] = fmaf(yb, -sn[j], ya * c[j]);  // y_i c - y_{i+d_r/2} s
-      ob[j] = fmaf(ya, sn[j], yb * c[j]);   // y_{i+d_r/2} c + y_i s
-    }
-    *reinterpret_cast<uint2*>(row + off_a) = pack4(oa);
-    *reinterpret_cast<uint2*>(row + off_b) = pack4(ob);
-  }
-  fence_proxy_async_smem();  // the bulk stores below read what was just written
-  __syncthreads();
+    fence_proxy_async_smem();  // the bulk stores below read what was just written
+    __syncthreads();
 
-  bool issued = false;
-  if (tid == 0) {
-    bulk_store(a.qhat + tok0 * Hq * kGatedD, rows_q, q_bytes);
-    issued = true;
-  }
-  for (int rr = tid; rr < tok_here * Hkv; rr += kThreads) {
-    const int tt = rr / Hkv, kv = rr - tt * Hkv;
-    long long b;
-    int t;
-    token_bt(b_first, t_first, tt, a.T, b, t);
-    const long long dst_row = (b * Hkv + kv) * a.khat_rows + chunk_start(args, b) + t;
-    bulk_store(a.khat + dst_row * kGatedD, rows_k + (size_t)rr * kGatedD, kRowBytes);
-    if (v_bytes) bulk_store(a.v_cache + dst_row * kGatedD, rows_v + (size_t)rr * kGatedD, kRowBytes);
-    issued = true;
+    if (tid == 0) {
+      bulk_store(a.qhat + (tok0 + t_lo) * Hq * kGatedD, rows_q + (size_t)t_lo * Hq * kGatedD,
+                 (uint32_t)nq * kRowBytes);
+      issued = true;
+    }
+    for (int rr = t_lo * Hkv + tid; rr < t_hi * Hkv; rr += kThreads) {
+      const int tt = rr / Hkv, kv = rr - tt * Hkv;
+      long long b;
+      int t;
+      token_bt(b_first, t_first, tt, a.T, b, t);
+      const long long dst_row = (b * Hkv + kv) * a.khat_rows + chunk_start(args, b) + t;
+      bulk_store(a.khat + dst_row * kGatedD, rows_k + (size_t)rr * kGatedD, kRowBytes);
+      if (vrows)
+        bulk_store(a.v_cache + dst_row * kGatedD, rows_v + (size_t)rr * kGatedD, kRowBytes);
+      issued = true;
+    }
   }
   if (issued) bulk_commit_and_wait_read();  // shared memory stays valid until read
 }
