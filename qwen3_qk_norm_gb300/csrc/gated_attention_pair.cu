@@ -40,6 +40,9 @@
 //            read them complete: K_j's when S_j completes, V_j's when PV_j
 //            does (an arrive on "PV done" follows every PV).
 // TMEM per CTA: S0 | S1 (128 fp32 columns each, double-buffered) | O (256).
+// "P ready" is the even CTA's barrier: its own softmax warps arrive with CTA
+// scope, the odd CTA's with cluster scope (the wider release costs each of
+// those warps a memory barrier, so the even CTA's do not pay it).
 // P goes back as bf16 pairs over the first half of each thread's own S
 // columns and PV reads it from there. MMA stream: S_0, S_1, then per KV tile
 // j: PV_j, S_{j+2}. Commits arrive on the barriers of both CTAs.
@@ -497,7 +500,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // one arrive per warp, on the even CTA's barrier, publishes its 32 rows
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(p_full_even[j & 1]);
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&bars->p_full[j & 1]);  // the issuer's own CTA: CTA scope suffices
+        else
+          mbar_arrive_cluster(p_full_even[j & 1]);
+      }
     }
     // ---- epilogue: the row's four partial sums, then O / l * sigmoid(gate)
     ok = __all_sync(kFull, ok && !*abort);
