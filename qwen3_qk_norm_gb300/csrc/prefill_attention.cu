@@ -14,12 +14,22 @@
 // so each K/V byte is read once per 256/g tokens. KV tiles above the causal
 // diagonal are never loaded; diagonal tiles are masked per element.
 //
-// Roles (640 threads, five warpgroups):
+// Work items and persistence. An item is one pair of Q tiles of one KV group
+// (longest items first). The plain prefill runs one CTA per SM, each walking
+// its items in rounds of gridDim.x in snake order (forward in even rounds,
+// backward in odd ones, so long and short items pair up across CTAs); the
+// tensor pipe does not drain between items: the next item's Q pair is loaded
+// as soon as the current item's last QK^T has completed ("Q free"), the K/V
+// ring and every barrier phase run on across items, and the next item's
+// first PV of a tile waits only for that tile's epilogue to have read O
+// ("O free"). A chunk against the caches runs one CTA per item.
+//
+// Roles (576 threads):
 //   WG 0..3   softmax + epilogue. WG w serves Q tile t = w/2 and the column
 //             half c = w%2 of its rows: thread r of the warpgroup owns TMEM
 //             lane r (row r) and columns 64c..64c+63 of S_t and O_t;
-//   WG 4      warp 16: TMA producer (Q0, Q1 once, then K_j, V_j through a
-//             ring of four 32 KB slots); warp 17: MMA issuer (one thread).
+//   warp 16   TMA producer (per item: Q0, Q1, then K_j, V_j through a ring
+//             of four 32 KB slots); warp 17: MMA issuer (one thread).
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each. A softmax
 // thread writes its 64 probabilities as bf16 pairs (32 columns) over the first
 // half of its own S columns, and O_t += P_t V_j reads them from there
@@ -74,16 +84,19 @@ constexpr int BN = 128;  // keys per KV tile
 constexpr int kQTiles = 2;
 constexpr int kSoftmaxWGs = 4;  // two column halves per Q tile
 constexpr int kSlots = 4;       // K/V ring slots
-constexpr int kThreads = (kSoftmaxWGs + 1) * 128;
+// four softmax warpgroups, then the producer warp and the MMA warp (576
+// threads: the register file then allows 112 registers per thread)
+constexpr int kThreads = kSoftmaxWGs * 128 + 64;
 constexpr uint32_t kHalf = 16384;      // 128 rows x 128 bytes
 constexpr uint32_t kTile = 2 * kHalf;  // 128 rows x 128 bf16
 constexpr uint32_t OFF_Q = 0;          // two Q tiles
 constexpr uint32_t OFF_RING = OFF_Q + kQTiles * kTile;
 constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kTile;
 // row-half exchange: tile maxima [2 tiles][2 halves][2 parities][128] fp32,
-// then partial sums [2 tiles][2 halves][128] fp32
+// then partial sums [2 item parities][2 tiles][2 halves][128] fp32
 constexpr uint32_t OFF_XCHG = OFF_BAR + 256;
-constexpr uint32_t kSmemBytes = OFF_XCHG + (kQTiles * 2 * 2 * 128 + kQTiles * 2 * 128) * 4 + 1024;
+constexpr uint32_t kSmemBytes =
+    OFF_XCHG + (kQTiles * 2 * 2 * 128 + 2 * kQTiles * 2 * 128) * 4 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kScaleLog2 = 0.12751743074380046f;  // log2(e) / sqrt(128)
 constexpr float kRescaleThreshold = 8.0f;
@@ -93,9 +106,10 @@ constexpr float kFixedMaxLimit = 60.0f;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;  // Q pair landed / free again (the item's last QK^T completed)
   uint64_t slot_full[kSlots], slot_empty[kSlots];
   uint64_t s_full[kQTiles], p_full[kQTiles], o_final[kQTiles];
+  uint64_t o_free[kQTiles];  // the item's epilogue has read O_t
   uint64_t xmax_full[kQTiles];  // fallback path: both row halves posted their tile max
   uint64_t vtail;               // cache V: rows past the valid keys cleared in the last tile
   uint64_t drain;
@@ -155,23 +169,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xchg = reinterpret_cast<float*>(smem + OFF_XCHG);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: longest CTAs first ---------------------------------------
+  // ---- work items ------------------------------------------------------------
+  // Item i (longest first): Q tile pair mt = n_mtiles - 1 - i / (B * Hkv) of
+  // group (b, kv) = i % (B * Hkv). A CTA takes items in rounds of gridDim.x,
+  // in snake order (forward in even rounds, backward in odd ones), so the
+  // long and short items of consecutive rounds pair up across CTAs.
   const int bk_count = a.B * a.Hkv;
-  const int mt = a.n_mtiles - 1 - (int)(blockIdx.x / bk_count);
-  const int bk = (int)(blockIdx.x % bk_count);
-  const int b = bk / a.Hkv, kv = bk % a.Hkv;
+  const int n_items = a.n_mtiles * bk_count;
   const int g = a.g;
   const int tile_tok = BM / g;  // tokens per Q tile
-  const int t0 = mt * kQTiles * tile_tok;
-  const int t_last = min(t0 + kQTiles * tile_tok, a.T) - 1;
-  // token t of this sequence sits at position p0 + t (p0 = 0 for a plain
-  // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
-  const int p0 = chunk_start(args, b);
-  const int n_tiles = (p0 + t_last) / BN + 1;
-  const int n_keys = p0 + a.T;
+  const int G = (int)gridDim.x, c = (int)blockIdx.x;
+  auto item_of_round = [&](int r) { return r * G + ((r & 1) ? G - 1 - c : c); };
+  struct Item {
+    int b, kv, t0, p0, n_tiles, n_keys;
+  };
+  auto item_at = [&](int i) {
+    Item it;
+    const int mt = a.n_mtiles - 1 - i / bk_count;
+    const int bk = i % bk_count;
+    it.b = bk / a.Hkv;
+    it.kv = bk % a.Hkv;
+    it.t0 = mt * kQTiles * tile_tok;
+    const int t_last = min(it.t0 + kQTiles * tile_tok, a.T) - 1;
+    // token t of the sequence sits at position p0 + t (p0 = 0 for a plain
+    // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
+    it.p0 = chunk_start(args, it.b);
+    it.n_tiles = (it.p0 + t_last) / BN + 1;
+    it.n_keys = it.p0 + a.T;
+    return it;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->slot_full[s], 1);
       mbar_init(&bars->slot_empty[s], kQTiles);  // one arrive per Q tile's softmax
@@ -180,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 256);
       mbar_init(&bars->o_final[t], 1);
+      mbar_init(&bars->o_free[t], 256);
       mbar_init(&bars->xmax_full[t], 256);
     }
     mbar_init(&bars->drain, 1);
@@ -194,64 +225,89 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort_flag;
 
-  // Cache V (chunked prefill): the last V tile holds rows past the valid keys
-  // (whatever the cache holds there). Their weights are 0, but 0 x NaN is NaN
-  // in the PV product, so the producer warp clears them before PV reads them.
-  const bool v_tail = kChunk && n_tiles * BN > n_keys;
   if (warp >= kSoftmaxWGs * 4) {
     if (warp == kSoftmaxWGs * 4) {
+      // Cache V (chunked prefill, one item per CTA): the last V tile holds
+      // rows past the valid keys (whatever the cache holds there). Their
+      // weights are 0, but 0 x NaN is NaN in the PV product, so the producer
+      // warp clears them before PV reads them.
+      bool v_tail = false;
+      int tail_first = 0;
+      uint32_t tail_load = 0;
      if (lane == 0) {
       // ---------------------------------------------------------- producer
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, kQTiles * kTile);
-      for (int t = 0; t < kQTiles; ++t) {
-        uint8_t* qd = smem + OFF_Q + t * kTile;
-        const int tq = t0 + t * tile_tok;
-        tma_load_4d(qd, &a.tm_q, &bars->q_full, 0, kv * g, tq, b);
-        tma_load_4d(qd + kHalf, &a.tm_q, &bars->q_full, 64, kv * g, tq, b);
-      }
-      const int n_loads = 2 * n_tiles;  // K_0, V_0, K_1, V_1, ...
-      int issued = 0;
-      for (int i = 0; i < n_loads; ++i) {
-        const int s = i % kSlots;
-        if (!mbar_wait(&bars->slot_empty[s], ((i / kSlots) & 1) ^ 1, a.err, kDevTimeoutTma, abort))
+      uint32_t L = 0;       // first load index of the current item
+      uint32_t issued = 0;  // loads issued
+      uint32_t n_q = 0;     // Q pairs issued
+      bool ok = true;
+      for (int r = 0; ok && item_of_round(r) < n_items; ++r) {
+        const Item it = item_at(item_of_round(r));
+        // the Q tiles are free once the previous item's last QK^T completed
+        if (n_q > 0 && !mbar_wait(&bars->q_empty, (n_q - 1) & 1, a.err, kDevTimeoutTma, abort)) {
+          ok = false;
           break;
-        mbar_arrive_expect_tx(&bars->slot_full[s], kTile);
-        uint8_t* dst = smem + OFF_RING + s * kTile;
-        const int j = i >> 1;
-        if ((i & 1) == 0) {
-          tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 0, j * BN, b * a.Hkv + kv);
-          tma_load_3d(dst + kHalf, &a.tm_k, &bars->slot_full[s], 64, j * BN, b * a.Hkv + kv);
-        } else if (kChunk) {
-          tma_load_3d(dst, &a.tm_v, &bars->slot_full[s], 0, j * BN, b * a.Hkv + kv);
-          tma_load_3d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, j * BN, b * a.Hkv + kv);
-        } else {
-          tma_load_4d(dst, &a.tm_v, &bars->slot_full[s], 0, kv, j * BN, b);
-          tma_load_4d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, kv, j * BN, b);
         }
-        issued = i + 1;
+        mbar_arrive_expect_tx(&bars->q_full, kQTiles * kTile);
+        for (int t = 0; t < kQTiles; ++t) {
+          uint8_t* qd = smem + OFF_Q + t * kTile;
+          const int tq = it.t0 + t * tile_tok;
+          tma_load_4d(qd, &a.tm_q, &bars->q_full, 0, it.kv * g, tq, it.b);
+          tma_load_4d(qd + kHalf, &a.tm_q, &bars->q_full, 64, it.kv * g, tq, it.b);
+        }
+        ++n_q;
+        const int row3 = it.b * a.Hkv + it.kv;
+        for (int i = 0; i < 2 * it.n_tiles; ++i) {  // K_0, V_0, K_1, V_1, ...
+          const uint32_t li = L + (uint32_t)i;
+          const int s = (int)(li % kSlots);
+          if (!mbar_wait(&bars->slot_empty[s], ((li / kSlots) & 1) ^ 1, a.err, kDevTimeoutTma,
+                         abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->slot_full[s], kTile);
+          uint8_t* dst = smem + OFF_RING + s * kTile;
+          const int j = i >> 1;
+          if ((i & 1) == 0) {
+            tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 0, j * BN, row3);
+            tma_load_3d(dst + kHalf, &a.tm_k, &bars->slot_full[s], 64, j * BN, row3);
+          } else if (kChunk) {
+            tma_load_3d(dst, &a.tm_v, &bars->slot_full[s], 0, j * BN, row3);
+            tma_load_3d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, j * BN, row3);
+          } else {
+            tma_load_4d(dst, &a.tm_v, &bars->slot_full[s], 0, it.kv, j * BN, it.b);
+            tma_load_4d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, it.kv, j * BN, it.b);
+          }
+          issued = li + 1;
+          if (i + 1 == 2 * it.n_tiles && kChunk && it.n_tiles * BN > it.n_keys) {
+            v_tail = true;
+            tail_first = it.n_keys - (it.n_tiles - 1) * BN;
+            tail_load = li;
+          }
+        }
+        if (ok) L += 2u * (uint32_t)it.n_tiles;
       }
       if (*abort) {
         // let every copy that was issued land before the CTA goes away
-        mbar_wait(&bars->q_full, 0, nullptr, 0, nullptr);
-        for (int i = max(0, issued - kSlots); i < issued; ++i)
+        if (n_q > 0) mbar_wait(&bars->q_full, (n_q - 1) & 1, nullptr, 0, nullptr);
+        for (uint32_t i = issued > (uint32_t)kSlots ? issued - kSlots : 0u; i < issued; ++i)
           mbar_wait(&bars->slot_full[i % kSlots], (i / kSlots) & 1, nullptr, 0, nullptr);
       }
      }
-      if (v_tail) {
-        __syncwarp();
-        const int iv = 2 * n_tiles - 1;  // load index of the last V tile
-        const bool ok = __all_sync(kFull, mbar_wait(&bars->slot_full[iv % kSlots],
-                                                    (iv / kSlots) & 1, a.err, kDevTimeoutTma,
-                                                    abort));
+      v_tail = __shfl_sync(kFull, v_tail, 0);
+      if (kChunk && v_tail) {
+        tail_first = __shfl_sync(kFull, tail_first, 0);
+        tail_load = __shfl_sync(kFull, tail_load, 0);
+        const bool ok = __all_sync(kFull, mbar_wait(&bars->slot_full[tail_load % kSlots],
+                                                    (tail_load / kSlots) & 1, a.err,
+                                                    kDevTimeoutTma, abort));
         if (ok) {
-          uint8_t* vt = smem + OFF_RING + (iv % kSlots) * kTile;
-          const int first = n_keys - (n_tiles - 1) * BN;  // first row to clear
-          const int chunks = (BN - first) * 16;           // 16-byte chunks, both halves
-          for (int c = lane; c < chunks; c += 32) {
-            const int row = first + (c >> 4), half = (c >> 3) & 1, q16 = c & 7;
+          uint8_t* vt = smem + OFF_RING + (tail_load % kSlots) * kTile;
+          const int chunks = (BN - tail_first) * 16;  // 16-byte chunks, both halves
+          for (int ch = lane; ch < chunks; ch += 32) {
+            const int row = tail_first + (ch >> 4), half = (ch >> 3) & 1, q16 = ch & 7;
             *reinterpret_cast<uint4*>(vt + half * kHalf + row * 128 + q16 * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
           }
@@ -271,53 +327,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t slot_k0 = smem_desc_sw128(ring, 16, 1024);
       const uint64_t slot_v0 = smem_desc_sw128(ring, kHalf, 1024);
       constexpr uint64_t kSlotStep = kTile >> 4;  // descriptor units per slot
-      // An mbarrier wait issued by this thread after a tcgen05.commit stalls
-      // until that commit resolves, i.e. until every earlier MMA has finished.
-      // So each commit below is followed by a full MMA group before the next
-      // wait, by which time it has resolved: the waits for a group's inputs
-      // are placed before the commit of the previous group.
-      auto wait_inputs = [&](int j) {  // V_j, K_{j+1} (or the cleared V tail) and P0_j
-        const int iv = 2 * j + 1, ik = 2 * j + 2;
-        const bool last = j + 1 == n_tiles;
-        uint64_t* second = last ? (v_tail ? &bars->vtail : &bars->slot_full[iv % kSlots])
-                                : &bars->slot_full[ik % kSlots];
-        const uint32_t second_par = last ? (v_tail ? 0u : (uint32_t)((iv / kSlots) & 1))
-                                         : (uint32_t)((ik / kSlots) & 1);
-        return mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, second, second_par,
-                          &bars->p_full[0], j & 1, a.err, kDevTimeoutMma, abort);
-      };
-      bool ok = mbar_wait(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) &&
-                mbar_wait(&bars->slot_full[0], 0, a.err, kDevTimeoutMma, abort);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(tmem, q_desc0, slot_k0);
-        mma_commit(&bars->s_full[0]);
-        issue_qk(tmem + 128, q_desc1, slot_k0);
-        ok = wait_inputs(0);
-        mma_commit(&bars->s_full[1]);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int iv = 2 * j + 1, ik = 2 * j + 2;  // loads holding V_j and K_{j+1}
-        const bool more = j + 1 < n_tiles;
-        const uint64_t v_desc = slot_v0 + (uint64_t)(iv % kSlots) * kSlotStep;
-        const uint64_t k_desc = slot_k0 + (uint64_t)(ik % kSlots) * kSlotStep;
-        // tile 0: PV0_j, S0_{j+1} (inputs waited for above)
-        tc_fence_after();
-        issue_pv(tmem + 256, tmem, v_desc, j > 0 ? 1u : 0u);
-        if (more) issue_qk(tmem, q_desc0, k_desc);
-        ok = mbar_poll(&bars->p_full[1], j & 1, a.err, kDevTimeoutMma, abort);
-        mma_commit(more ? &bars->s_full[0] : &bars->o_final[0]);
+      uint32_t L = 0;  // loads consumed before the current item
+      uint32_t S = 0;  // S steps (per Q tile) before the current item
+      int k = 0;       // items done
+      bool ok = true;
+      for (int r = 0; ok && item_of_round(r) < n_items; ++r, ++k) {
+        const Item it = item_at(item_of_round(r));
+        const int n_tiles = it.n_tiles;
+        const bool v_tail = kChunk && n_tiles * BN > it.n_keys;
+        // An mbarrier wait issued by this thread after a tcgen05.commit stalls
+        // until that commit resolves, i.e. until every earlier MMA has
+        // finished. So each commit below is followed by a full MMA group
+        // before the next wait, by which time it has resolved: the waits for
+        // a group's inputs are placed before the commit of the previous group.
+        auto wait_inputs = [&](int j) {  // V_j, K_{j+1} (or the cleared V tail) and P0_j
+          const uint32_t iv = L + 2u * j + 1u, ik = L + 2u * j + 2u;
+          const bool last = j + 1 == n_tiles;
+          uint64_t* second = last ? (v_tail ? &bars->vtail : &bars->slot_full[iv % kSlots])
+                                  : &bars->slot_full[ik % kSlots];
+          const uint32_t second_par = last ? (v_tail ? 0u : (iv / kSlots) & 1)
+                                           : (ik / kSlots) & 1;
+          return mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, second, second_par,
+                            &bars->p_full[0], (S + j) & 1, a.err, kDevTimeoutMma, abort);
+        };
+        ok = mbar_wait(&bars->q_full, k & 1, a.err, kDevTimeoutMma, abort) &&
+             mbar_wait(&bars->slot_full[L % kSlots], (L / kSlots) & 1, a.err, kDevTimeoutMma,
+                       abort);
         if (!ok) break;
-        // tile 1: PV1_j, S1_{j+1}
+        const uint64_t k_desc0 = slot_k0 + (uint64_t)(L % kSlots) * kSlotStep;
         tc_fence_after();
-        issue_pv(tmem + 256 + 128, tmem + 128, v_desc, j > 0 ? 1u : 0u);
-        if (more) {
-          issue_qk(tmem + 128, q_desc1, k_desc);
-          ok = wait_inputs(j + 1);
-          mma_commit(&bars->s_full[1]);
-        } else {
-          mma_commit(&bars->o_final[1]);
+        issue_qk(tmem, q_desc0, k_desc0);
+        mma_commit(&bars->s_full[0]);
+        issue_qk(tmem + 128, q_desc1, k_desc0);
+        // PV0_0 overwrites O0: the previous item's tile-0 epilogue must have
+        // read it
+        ok = wait_inputs(0) &&
+             (k == 0 || mbar_poll(&bars->o_free[0], (k - 1) & 1, a.err, kDevTimeoutMma, abort));
+        mma_commit(&bars->s_full[1]);
+        if (n_tiles == 1) mma_commit(&bars->q_empty);  // the item's last QK^T is issued
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const uint32_t iv = L + 2u * j + 1u, ik = L + 2u * j + 2u;  // V_j and K_{j+1}
+          const bool more = j + 1 < n_tiles;
+          const uint64_t v_desc = slot_v0 + (uint64_t)(iv % kSlots) * kSlotStep;
+          const uint64_t k_desc = slot_k0 + (uint64_t)(ik % kSlots) * kSlotStep;
+          // tile 0: PV0_j, S0_{j+1} (inputs waited for above)
+          tc_fence_after();
+          issue_pv(tmem + 256, tmem, v_desc, j > 0 ? 1u : 0u);
+          if (more) issue_qk(tmem, q_desc0, k_desc);
+          ok = mbar_poll(&bars->p_full[1], (S + j) & 1, a.err, kDevTimeoutMma, abort) &&
+               (j > 0 || k == 0 ||
+                mbar_poll(&bars->o_free[1], (k - 1) & 1, a.err, kDevTimeoutMma, abort));
+          mma_commit(more ? &bars->s_full[0] : &bars->o_final[0]);
+          if (!ok) break;
+          // tile 1: PV1_j, S1_{j+1}
+          tc_fence_after();
+          issue_pv(tmem + 256 + 128, tmem + 128, v_desc, j > 0 ? 1u : 0u);
+          if (more) {
+            issue_qk(tmem + 128, q_desc1, k_desc);
+            ok = wait_inputs(j + 1);
+            mma_commit(&bars->s_full[1]);
+            if (j + 2 == n_tiles) mma_commit(&bars->q_empty);  // the item's last QK^T
+          } else {
+            mma_commit(&bars->o_final[1]);
+          }
         }
+        L += 2u * (uint32_t)n_tiles;
+        S += (uint32_t)n_tiles;
       }
       // drain: every MMA issued above has completed once this phase completes
       mma_commit(&bars->drain);
@@ -334,138 +409,163 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_o = tmem + 256 + t * 128 + hc * 64 + lane_off;
     const uint32_t bar_id = 1 + t;      // named barrier of the two halves of tile t (epilogue)
     float* xmax = xchg + (t * 2) * 2 * 128;  // [half][parity][128]
-    const int tok = t0 + t * tile_tok + r / g;
-    const int tok_pos = p0 + tok;  // position of this row's token
     const float bound = *a.logit_bound;
     const bool fixed_max = fixed_shift_allowed(args) && bound >= 0.f && bound <= kFixedMaxLimit;
-    float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
-    float l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      ok = __all_sync(kFull,
-                      mbar_wait(&bars->s_full[t], j & 1, a.err, kDevTimeoutSoftmax, abort));
-      if (!ok) break;
-      // S_t,j is complete, and so is every earlier MMA of the issuing thread:
-      // K_j is no longer read by tile t, nor V_{j-1} (read by PV_t,j-1)
-      if (hc == 0 && r == 0) {
-        mbar_arrive(&bars->slot_empty[(2 * j) % kSlots]);
-        if (j > 0) mbar_arrive(&bars->slot_empty[(2 * j - 1) % kSlots]);
+    uint32_t L = 0;  // loads of the CTA's earlier items
+    uint32_t S = 0;  // S steps of the CTA's earlier items
+    // Every thread runs every item of the CTA (even after an abort, when each
+    // wait returns at once), so the named barrier of the epilogue is reached
+    // the same number of times by both halves of a tile.
+    for (int rr = 0, k = 0; item_of_round(rr) < n_items; ++rr, ++k) {
+      const int item = item_of_round(rr);
+      int n_tiles, tok_pos;  // only these live through the loop
+      {
+        const Item it = item_at(item);
+        n_tiles = it.n_tiles;
+        tok_pos = it.p0 + it.t0 + t * tile_tok + r / g;  // position of this row's token
       }
-      tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld64_wait(tmem_s, sr);
-
-      float s[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c * 32 + e]);
-      const int key0 = j * BN + hc * 64;
-      if (key0 + 63 > tok_pos) {
-#pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (key0 + e > tok_pos) s[e] = -INFINITY;
-      }
-      bool move = false;
-      float alpha = 1.0f;
-      if (!fixed_max) {
-        float mx[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = s[e];
-#pragma unroll
-        for (int e = 8; e < 64; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-        // the other half of the row: exchange tile maxima (two parity slots)
-        xmax[(hc * 2 + (j & 1)) * 128 + r] = mx[0];
-        mbar_arrive(&bars->xmax_full[t]);
-        ok = __all_sync(kFull, mbar_wait(&bars->xmax_full[t], j & 1, a.err, kDevTimeoutSoftmax,
-                                         abort));
+      float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
+      float l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n_tiles; ++j) {
+        const uint32_t step = S + (uint32_t)j;
+        ok = __all_sync(kFull,
+                        mbar_wait(&bars->s_full[t], step & 1, a.err, kDevTimeoutSoftmax, abort));
         if (!ok) break;
-        const float mrow = fmaxf(mx[0], xmax[((hc ^ 1) * 2 + (j & 1)) * 128 + r]);
-        const float m_tile = mrow * kScaleLog2;
-        move = m_tile > m + kRescaleThreshold;
-        const float m_new = move ? m_tile : m;
-        alpha = move ? ex2(m - m_new) : 1.0f;
-        m = m_new;
-        l *= alpha;
-      }
-
-      // p = 2^(s * scale - m), two at a time on the f32x2 pipes
-      const uint64_t scale2 = f2_pack(kScaleLog2, kScaleLog2);
-      const uint64_t negm2 = f2_pack(-m, -m);
-      uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-      uint32_t pw[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const uint64_t x = f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
-        float x0, x1;
-        f2_unpack(x, x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
-        pw[e] = pack_bf16x2(p0, p1);
-      }
-      tmem_st32_wait(tmem_s, pw);  // P over the first 32 of this thread's S columns
-      // O_t holds every PV up to j-1 here (the S_t,j commit covers them);
-      // rescale this thread's O columns before PV_t,j adds terms relative to
-      // the new max
-      if (!fixed_max && j > 0 && __any_sync(kFull, move)) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o[32];
-          tmem_ld32_wait(tmem_o + c * 32, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32_wait(tmem_o + c * 32, o);
+        // S_t,j is complete, and so is every earlier MMA of the issuing
+        // thread: K_j is no longer read by tile t, nor the V before it (read
+        // by the previous PV_t, possibly of the previous item)
+        if (hc == 0 && r == 0) {
+          const uint32_t lk = L + 2u * (uint32_t)j;
+          mbar_arrive(&bars->slot_empty[lk % kSlots]);
+          if (lk > 0) mbar_arrive(&bars->slot_empty[(lk - 1) % kSlots]);
         }
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld64_wait(tmem_s, sr);
+
+        float s[64];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(sr[cc * 32 + e]);
+        const int key0 = j * BN + hc * 64;
+        if (key0 + 63 > tok_pos) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (key0 + e > tok_pos) s[e] = -INFINITY;
+        }
+        bool move = false;
+        float alpha = 1.0f;
+        if (!fixed_max) {
+          float mx[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = s[e];
+#pragma unroll
+          for (int e = 8; e < 64; ++e) mx[e & 7] = fmaxf(mx[e & 7], s[e]);
+#pragma unroll
+          for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+          // the other half of the row: exchange tile maxima (two parity slots)
+          xmax[(hc * 2 + (step & 1)) * 128 + r] = mx[0];
+          mbar_arrive(&bars->xmax_full[t]);
+          ok = __all_sync(kFull, mbar_wait(&bars->xmax_full[t], step & 1, a.err,
+                                           kDevTimeoutSoftmax, abort));
+          if (!ok) break;
+          const float mrow = fmaxf(mx[0], xmax[((hc ^ 1) * 2 + (step & 1)) * 128 + r]);
+          const float m_tile = mrow * kScaleLog2;
+          move = m_tile > m + kRescaleThreshold;
+          const float m_new = move ? m_tile : m;
+          alpha = move ? ex2(m - m_new) : 1.0f;
+          m = m_new;
+          l *= alpha;
+        }
+
+        // p = 2^(s * scale - m), two at a time on the f32x2 pipes
+        const uint64_t scale2 = f2_pack(kScaleLog2, kScaleLog2);
+        const uint64_t negm2 = f2_pack(-m, -m);
+        uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        uint32_t pw[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const uint64_t x = f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
+          pw[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32_wait(tmem_s, pw);  // P over the first 32 of this thread's S columns
+        // O_t holds every PV of this item up to j-1 here (the S_t,j commit
+        // covers them); rescale this thread's O columns before PV_t,j adds
+        // terms relative to the new max
+        if (!fixed_max && j > 0 && __any_sync(kFull, move)) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t o[32];
+            tmem_ld32_wait(tmem_o + cc * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32_wait(tmem_o + cc * 32, o);
+          }
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(sum2[0], a0, a1);
+        f2_unpack(sum2[1], b0, b1);
+        l += (a0 + a1) + (b0 + b1);
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
       }
-      float a0, a1, b0, b1;
-      f2_unpack(sum2[0], a0, a1);
-      f2_unpack(sum2[1], b0, b1);
-      l += (a0 + a1) + (b0 + b1);
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
-    }
-    // ---- epilogue: the row's two partial sums, then O / l -> bf16 -> out
-    ok = __all_sync(kFull, ok && !*abort);
-    // the partial sums go to a slot the loop never uses; every thread of both
-    // halves reaches this barrier exactly once (aborted or not)
-    float* lsum = xchg + kQTiles * 2 * 2 * 128 + t * 2 * 128;  // [tile][half][128]
-    lsum[hc * 128 + r] = l;
-    named_barrier_sync(bar_id, 256);
-    if (ok) {
-      l += lsum[(hc ^ 1) * 128 + r];
-      ok = __all_sync(kFull, mbar_wait(&bars->o_final[t], 0, a.err, kDevTimeoutEpilogue, abort));
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l;
-      const bool store = tok < a.T;  // rows of tokens past the chunk are padding
-      uint16_t* orow = a.out +
-                       (((long long)b * a.T + tok) * a.Hq + (long long)kv * g + (r % g)) * 128 +
-                       hc * 64;
+      // ---- epilogue: the row's two partial sums, then O / l -> bf16 -> out
+      ok = __all_sync(kFull, ok && !*abort);
+      // the partial sums go to a slot the loop never uses, double-buffered by
+      // item; every thread of both halves reaches this barrier once per item
+      float* lsum = xchg + kQTiles * 2 * 2 * 128 + ((k & 1) * kQTiles + t) * 2 * 128;
+      lsum[hc * 128 + r] = l;
+      named_barrier_sync(bar_id, 256);
+      if (ok) {
+        l += lsum[(hc ^ 1) * 128 + r];
+        ok = __all_sync(kFull, mbar_wait(&bars->o_final[t], k & 1, a.err, kDevTimeoutEpilogue,
+                                         abort));
+      }
+      if (ok) {
+        tc_fence_after();
+        const Item it = item_at(item);
+        const int tok = it.t0 + t * tile_tok + r / g;
+        const float inv_l = 1.0f / l;
+        const bool store = tok < a.T;  // rows of tokens past the chunk are padding
+        uint16_t* orow = a.out +
+                         (((long long)it.b * a.T + tok) * a.Hq + (long long)it.kv * g + (r % g)) *
+                             128 +
+                         hc * 64;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        tmem_ld32_wait(tmem_o + c * 32, o);
-        if (store) {
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t o[32];
+          tmem_ld32_wait(tmem_o + cc * 32, o);
+          if (store) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
-                              __uint_as_float(o[q4 * 8 + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
-                              __uint_as_float(o[q4 * 8 + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
-                              __uint_as_float(o[q4 * 8 + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
-                              __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-            reinterpret_cast<uint4*>(orow + c * 32)[q4] = w;
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
+                                __uint_as_float(o[q4 * 8 + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
+                                __uint_as_float(o[q4 * 8 + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
+                                __uint_as_float(o[q4 * 8 + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
+                                __uint_as_float(o[q4 * 8 + 7]) * inv_l);
+              reinterpret_cast<uint4*>(orow + cc * 32)[q4] = w;
+            }
           }
         }
       }
+      // O_t has been read: the next item's first PV of this tile may
+      // overwrite it
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
+      L += 2u * (uint32_t)n_tiles;
+      S += (uint32_t)n_tiles;
     }
   }
 
@@ -499,9 +599,20 @@ static cudaError_t launch(const Args& args, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 64) done_mask |= 1ull << dev;
   }
-  const long long grid = (long long)a.n_mtiles * a.B * a.Hkv;
-  if (grid == 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // the plain prefill runs one persistent CTA per SM over all items; a chunk
+  // runs one CTA per item
+  constexpr bool kChunk = sizeof(Args) != sizeof(PrefillArgs);
+  const long long items = (long long)a.n_mtiles * a.B * a.Hkv;
+  if (items == 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  static int sm_count[64];
+  int n_sm = dev < 64 ? sm_count[dev] : 0;
+  if (n_sm == 0) {
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) sm_count[dev] = n_sm;
+  }
+  const long long grid = kChunk ? items : (items < n_sm ? items : (long long)n_sm);
   prefill_attention_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();
 }
