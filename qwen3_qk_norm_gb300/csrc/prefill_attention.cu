@@ -539,24 +539,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                          (((long long)it.b * a.T + tok) * a.Hq + (long long)it.kv * g + (r % g)) *
                              128 +
                          hc * 64;
+        uint32_t o[64];
+        tmem_ld64_wait(tmem_o, o);  // all 64 columns, one wait
+        if (store) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t o[32];
-          tmem_ld32_wait(tmem_o + cc * 32, o);
-          if (store) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
-                                __uint_as_float(o[q4 * 8 + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
-                                __uint_as_float(o[q4 * 8 + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
-                                __uint_as_float(o[q4 * 8 + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
-                                __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-              reinterpret_cast<uint4*>(orow + cc * 32)[q4] = w;
-            }
+          for (int q8 = 0; q8 < 8; ++q8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[q8 * 8 + 0]) * inv_l,
+                              __uint_as_float(o[q8 * 8 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[q8 * 8 + 2]) * inv_l,
+                              __uint_as_float(o[q8 * 8 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[q8 * 8 + 4]) * inv_l,
+                              __uint_as_float(o[q8 * 8 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[q8 * 8 + 6]) * inv_l,
+                              __uint_as_float(o[q8 * 8 + 7]) * inv_l);
+            reinterpret_cast<uint4*>(orow)[q8] = w;
           }
         }
       }
