@@ -168,6 +168,8 @@ KERNEL_SOURCES = {  # the kernel's file and every header it includes
                                  "q3a_internal.h"],
     "gated_attention_pair_kernel<chunk>": ["gated_attention_pair.cu", "q3a_pair.cuh",
                                            "q3a_device.cuh", "q3a_internal.h"],
+    "prefill_attention_kernel<chunk>": ["prefill_attention.cu", "q3a_device.cuh",
+                                        "q3a_internal.h"],
 }
 
 
@@ -695,7 +697,8 @@ def run_ours(args) -> None:
                          "prefill_attention_kernel<PrefillChunkArgs>",
                          "achieved": round(per_gpu, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(per_gpu / peaks["bf16_tflops"], 4),
-                         "peak_source": f"{peak_src} bf16 dense burst", "traffic": None},
+                         "peak_source": f"{peak_src} bf16 dense burst",
+                         "traffic": ncu_traffic("prefill_attention_kernel<chunk>")},
             "gpu_launches": 2 * args.steps,
         }
     if g_ms is not None:
