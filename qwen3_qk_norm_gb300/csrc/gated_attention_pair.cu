@@ -28,6 +28,15 @@
 // dims), in a ring of four 32 KB slots, loaded in the order the MMAs read them
 // (K_0, K_1, V_0, K_2, V_1, ...).
 //
+// Persistence. The plain prefill runs one pair per two SMs, each walking its
+// work items (a 256-row pair tile of one KV group, longest first) in rounds
+// of the number of pairs, in snake order. The MMA stream runs on across
+// items: the next item's Q tiles load once the item's last QK^T has completed
+// ("Q free", committed to both CTAs), the ring, the S buffers and every
+// barrier phase continue, and the next item's first PV waits only for every
+// softmax warp of the pair to have read O ("O free"). A chunk against the
+// caches runs one pair per item.
+//
 // Roles (640 threads per CTA):
 //   WG 0..3  softmax + epilogue of the CTA's own 128 rows. Warp w serves TMEM
 //            lanes 32(w%4).. and the key quarter c = w/4 of every S tile (32
@@ -85,9 +94,10 @@ constexpr uint32_t kSlotBytes = 32768;
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + 4 * kQBlock;
 constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kSlotBytes;
-// tile maxima [2 parities][4 quarters][128] fp32, then partial sums [4][128]
+// tile maxima [2 parities][4 quarters][128] fp32, then partial sums
+// [2 item parities][4 quarters][128]
 constexpr uint32_t OFF_XCHG = OFF_BAR + 512;
-constexpr uint32_t kSmemBytes = OFF_XCHG + (2 * 4 * 128 + 4 * 128) * 4 + 1024;
+constexpr uint32_t kSmemBytes = OFF_XCHG + (2 * 4 * 128 + 2 * 4 * 128) * 4 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;
@@ -98,12 +108,14 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct Bars {
   uint64_t q_full, q_peer;
+  uint64_t q_empty;  // the Q tile is free again: the item's last QK^T completed
   uint64_t slot_full[kSlots], slot_peer[kSlots], slot_empty[kSlots];
   uint64_t s_full[2];
   uint64_t p_full[2];  // even CTA: all 32 softmax warps of the pair
   uint64_t pv_done;    // PV_j complete (one phase per KV tile)
   uint64_t xmax_full;  // online-max path: the CTA's four quarters posted their tile max
   uint64_t o_final;
+  uint64_t o_free;   // even CTA: every softmax warp of the pair has read O
   uint64_t drain;
   uint64_t vtail;      // chunk: the last V half tile's rows past the valid keys cleared
   uint32_t tmem_base;
@@ -178,32 +190,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: the even CTA, which issues the MMAs
 
-  // ---- work item: longest pairs first ---------------------------------------
+  // ---- work items ------------------------------------------------------------
+  // Item i (longest first): pair tile pm = n_mtiles - 1 - i / (B * Hkv) of
+  // group (b, kv) = i % (B * Hkv). A pair takes items in rounds of the number
+  // of pairs, in snake order (forward in even rounds, backward in odd ones).
   const int bk_count = a.B * a.Hkv;
-  const int pair = (int)(blockIdx.x >> 1);
-  const int pm = a.n_mtiles - 1 - pair / bk_count;
-  const int bk = pair % bk_count;
-  const int b = bk / a.Hkv, kv = bk % a.Hkv;
+  const int n_items = a.n_mtiles * bk_count;
   const int g = a.g;
   const int tile_tok = BM / g;
-  const int t0_pair = pm * 2 * tile_tok;
-  const int t0 = t0_pair + (int)rank * tile_tok;  // this CTA's first token
-  const int t_last = min(t0_pair + 2 * tile_tok, a.T) - 1;
-  // token t of this sequence sits at position p0 + t (p0 = 0 for a plain
-  // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
-  const int p0 = chunk_start(args, b);
-  const int n_tiles = (p0 + t_last) / BN + 1;
-  const int n_keys = p0 + a.T;
+  const int G = (int)(gridDim.x >> 1), c = (int)(blockIdx.x >> 1);
+  auto item_of_round = [&](int r) { return r * G + ((r & 1) ? G - 1 - c : c); };
+  struct Item {
+    int b, kv, t0_pair, p0, n_tiles, n_keys;
+  };
+  auto item_at = [&](int i) {
+    Item it;
+    const int pm = a.n_mtiles - 1 - i / bk_count;
+    const int bk = i % bk_count;
+    it.b = bk / a.Hkv;
+    it.kv = bk % a.Hkv;
+    it.t0_pair = pm * 2 * tile_tok;
+    const int t_last = min(it.t0_pair + 2 * tile_tok, a.T) - 1;
+    // token t of the sequence sits at position p0 + t (p0 = 0 for a plain
+    // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
+    it.p0 = chunk_start(args, it.b);
+    it.n_tiles = (it.p0 + t_last) / BN + 1;
+    it.n_keys = it.p0 + a.T;
+    return it;
+  };
   const float bound = *a.logit_bound;
   const bool fixed_max = fixed_shift_allowed(args) && bound >= 0.f && bound <= kFixedMaxLimit;
-  // chunk: load index of the last V half tile, and whether it holds rows past
-  // the valid keys
-  const uint32_t last_load = 2u * (uint32_t)n_tiles - 1u;
-  const bool v_tail = kChunk && n_tiles * BN > n_keys;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_peer, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->slot_full[s], 1);
       mbar_init(&bars->slot_peer[s], 1);
@@ -216,6 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->xmax_full, kSoftmaxWGs * 128);
     mbar_init(&bars->o_final, 1);
+    mbar_init(&bars->o_free, 2 * kSoftmaxWGs * 4);  // one arrive per softmax warp, both CTAs
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->vtail, 1);
     bars->abort_flag = 0;
@@ -228,73 +250,100 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort_flag;
 
+  // Per item the loads are K_0, K_1, then per KV tile j: V_j, K_{j+2}: load
+  // index of K_j is 0, then 2j - 1; of V_j 2j + 2, except the last V at
+  // 2n - 1. Indices below are global over the pair's items (item base L).
   if (warp >= kSoftmaxWGs * 4) {
     if (warp == kSoftmaxWGs * 4) {
+      // chunk (one item per pair): the last V half tile's rows past the valid
+      // keys are cleared by this warp once the tile has landed
+      bool v_tail = false;
+      int tail_first = 0;
+      uint32_t tail_load = 0;
      if (lane == 0) {
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
-      // g * floor(128/g) rows of 128 bytes per 64-dim block (126 or 120 when g
-      // does not divide 128)
-      mbar_arrive_expect_tx(&bars->q_full, 4u * (uint32_t)(g * tile_tok) * 128u);
-      for (int c = 0; c < 4; ++c)
-        tma_load_4d(smem + OFF_Q + c * kQBlock, &a.tm_q, &bars->q_full, 64 * c, kv * g, t0, b);
-      uint32_t n = 0;  // half tiles issued
+      uint32_t n = 0;    // half tiles issued (global)
+      uint32_t n_q = 0;  // Q tiles issued
       bool ok = true;
-      auto load_tile = [&](bool is_k, int j) {
-        if (!ok) return;
-        const uint32_t s = slot_of(n);
-        if (!mbar_wait(&bars->slot_empty[s], use_of(n) ^ 1u, a.err, kDevTimeoutTma, abort)) {
+      for (int r = 0; ok && item_of_round(r) < n_items; ++r) {
+        const Item it = item_at(item_of_round(r));
+        const int row3 = it.b * a.Hkv + it.kv;
+        // this CTA's Q tile, once the previous item's last QK^T has completed
+        if (n_q > 0 && !mbar_wait(&bars->q_empty, (n_q - 1) & 1, a.err, kDevTimeoutTma, abort)) {
           ok = false;
-          return;
+          break;
         }
-        mbar_arrive_expect_tx(&bars->slot_full[s], kSlotBytes);
-        uint8_t* dst = smem + OFF_RING + s * kSlotBytes;
-        if (is_k) {  // keys 64 rank .. of the tile, all 256 dims
-          for (int c = 0; c < 4; ++c)
-            tma_load_3d(dst + c * kKBlock, &a.tm_k, &bars->slot_full[s], 64 * c,
-                        j * BN + 64 * (int)rank, b * a.Hkv + kv);
-        } else {  // dims 128 rank .. of the tile, all 128 keys
-          for (int c = 0; c < 2; ++c) {
-            if (a.v_head_major)  // a V cache [B*Hkv, rows, 256]
-              tma_load_3d(dst + c * kVBlock, &a.tm_v, &bars->slot_full[s],
-                          128 * (int)rank + 64 * c, j * BN, b * a.Hkv + kv);
-            else  // the projection's V [B, T, Hkv, 256]
-              tma_load_4d(dst + c * kVBlock, &a.tm_v, &bars->slot_full[s],
-                          128 * (int)rank + 64 * c, kv, j * BN, b);
+        // g * floor(128/g) rows of 128 bytes per 64-dim block (126 or 120 when
+        // g does not divide 128)
+        mbar_arrive_expect_tx(&bars->q_full, 4u * (uint32_t)(g * tile_tok) * 128u);
+        const int t0 = it.t0_pair + (int)rank * tile_tok;
+        for (int cc = 0; cc < 4; ++cc)
+          tma_load_4d(smem + OFF_Q + cc * kQBlock, &a.tm_q, &bars->q_full, 64 * cc, it.kv * g, t0,
+                      it.b);
+        ++n_q;
+        auto load_tile = [&](bool is_k, int j) {
+          if (!ok) return;
+          const uint32_t s = slot_of(n);
+          if (!mbar_wait(&bars->slot_empty[s], use_of(n) ^ 1u, a.err, kDevTimeoutTma, abort)) {
+            ok = false;
+            return;
           }
+          mbar_arrive_expect_tx(&bars->slot_full[s], kSlotBytes);
+          uint8_t* dst = smem + OFF_RING + s * kSlotBytes;
+          if (is_k) {  // keys 64 rank .. of the tile, all 256 dims
+            for (int cc = 0; cc < 4; ++cc)
+              tma_load_3d(dst + cc * kKBlock, &a.tm_k, &bars->slot_full[s], 64 * cc,
+                          j * BN + 64 * (int)rank, row3);
+          } else {  // dims 128 rank .. of the tile, all 128 keys
+            for (int cc = 0; cc < 2; ++cc) {
+              if (a.v_head_major)  // a V cache [B*Hkv, rows, 256]
+                tma_load_3d(dst + cc * kVBlock, &a.tm_v, &bars->slot_full[s],
+                            128 * (int)rank + 64 * cc, j * BN, row3);
+              else  // the projection's V [B, T, Hkv, 256]
+                tma_load_4d(dst + cc * kVBlock, &a.tm_v, &bars->slot_full[s],
+                            128 * (int)rank + 64 * cc, it.kv, j * BN, it.b);
+            }
+          }
+          ++n;
+        };
+        load_tile(true, 0);
+        if (it.n_tiles > 1) load_tile(true, 1);
+        for (int j = 0; ok && j < it.n_tiles; ++j) {
+          load_tile(false, j);
+          if (j + 2 < it.n_tiles) load_tile(true, j + 2);
         }
-        ++n;
-      };
-      load_tile(true, 0);
-      if (n_tiles > 1) load_tile(true, 1);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        load_tile(false, j);
-        if (j + 2 < n_tiles) load_tile(true, j + 2);
+        if (kChunk && ok && it.n_tiles * BN > it.n_keys) {
+          v_tail = true;
+          tail_first = it.n_keys - (it.n_tiles - 1) * BN;
+          tail_load = n - 1;
+        }
       }
       if (*abort) {
         // let every copy that was issued land before the CTA goes away
-        mbar_wait(&bars->q_full, 0, nullptr, 0, nullptr);
+        if (n_q > 0) mbar_wait(&bars->q_full, (n_q - 1) & 1, nullptr, 0, nullptr);
         for (uint32_t i = n > (uint32_t)kSlots ? n - kSlots : 0u; i < n; ++i)
           mbar_wait(&bars->slot_full[slot_of(i)], use_of(i), nullptr, 0, nullptr);
       }
      }
-      if (v_tail) {
+      v_tail = __shfl_sync(kFull, v_tail, 0);
+      if (kChunk && v_tail) {
         // every load has been issued (lane 0 is past its loop), so the slot's
         // barrier is in the phase of the last load: wait for it, clear this
         // CTA's rows past the valid keys in both 64-dim blocks (a cleared row
         // is 128 bytes whatever the swizzle), and publish that
-        __syncwarp();
+        tail_first = __shfl_sync(kFull, tail_first, 0);
+        tail_load = __shfl_sync(kFull, tail_load, 0);
         const bool landed = __all_sync(
-            kFull, mbar_wait(&bars->slot_full[slot_of(last_load)], use_of(last_load), a.err,
+            kFull, mbar_wait(&bars->slot_full[slot_of(tail_load)], use_of(tail_load), a.err,
                              kDevTimeoutTma, abort));
         if (landed) {
-          uint8_t* vt = smem + OFF_RING + slot_of(last_load) * kSlotBytes;
-          const int first = n_keys - (n_tiles - 1) * BN;  // first key row to clear
-          const int chunks = (BN - first) * 16;           // 16-byte chunks, both blocks
-          for (int c = lane; c < chunks; c += 32) {
-            const int row = first + (c >> 4), blk = (c >> 3) & 1, q16 = c & 7;
+          uint8_t* vt = smem + OFF_RING + slot_of(tail_load) * kSlotBytes;
+          const int chunks = (BN - tail_first) * 16;  // 16-byte chunks, both blocks
+          for (int ch = lane; ch < chunks; ch += 32) {
+            const int row = tail_first + (ch >> 4), blk = (ch >> 3) & 1, q16 = ch & 7;
             *reinterpret_cast<uint4*>(vt + blk * kVBlock + row * 128 + q16 * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
           }
@@ -307,35 +356,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ----------------------------------------------- forwarder (odd CTA)
       // the even CTA's MMA issuer reads this CTA's Q and ring too: tell it
       // when each of them has landed, in load order
-      const uint32_t n_loads = 2u * (uint32_t)n_tiles;
-      if (mbar_wait(&bars->q_full, 0, a.err, kDevTimeoutTma, abort)) {
+      uint32_t L = 0;
+      bool ok = true;
+      for (int r = 0, k = 0; ok && item_of_round(r) < n_items; ++r, ++k) {
+        const Item it = item_at(item_of_round(r));
+        const bool v_tail = kChunk && it.n_tiles * BN > it.n_keys;
+        const uint32_t n_loads = 2u * (uint32_t)it.n_tiles;
+        if (!mbar_wait(&bars->q_full, k & 1, a.err, kDevTimeoutTma, abort)) break;
         mbar_arrive_cluster(peer_smem_addr(&bars->q_peer, 0));
         for (uint32_t t = 0; t < n_loads; ++t) {
-          const bool tail = v_tail && t == last_load;
-          if (!mbar_poll(tail ? &bars->vtail : &bars->slot_full[slot_of(t)],
-                         tail ? 0u : use_of(t), a.err, kDevTimeoutTma, abort))
+          const uint32_t gt = L + t;
+          const bool tail = v_tail && t + 1 == n_loads;
+          if (!mbar_poll(tail ? &bars->vtail : &bars->slot_full[slot_of(gt)],
+                         tail ? 0u : use_of(gt), a.err, kDevTimeoutTma, abort)) {
+            ok = false;
             break;
-          mbar_arrive_cluster(peer_smem_addr(&bars->slot_peer[slot_of(t)], 0));
+          }
+          mbar_arrive_cluster(peer_smem_addr(&bars->slot_peer[slot_of(gt)], 0));
         }
+        L += n_loads;
       }
     } else if (warp == kSoftmaxWGs * 4 + 3 && lane == 0) {
       // ------------------------------------------------------------ releaser
-      // Completion order on the tensor pipe: S_0, then per KV tile j:
-      // S_{j+1} (if any), PV_j. Load index of K_j: 0, then 2j - 1; of V_j:
-      // 2j + 2, except the last V at 2n - 1.
-      const int n = n_tiles;
-      if (mbar_wait_cluster(&bars->s_full[0], 0, a.err, kDevTimeoutSoftmax, abort)) {
-        mbar_arrive(&bars->slot_empty[slot_of(0)]);
+      // Completion order on the tensor pipe: per item S_0, then per KV tile j:
+      // S_{j+1} (if any), PV_j.
+      uint32_t L = 0, S = 0;  // loads and steps of the pair's earlier items
+      bool ok = true;
+      for (int r = 0; ok && item_of_round(r) < n_items; ++r) {
+        const int n = item_at(item_of_round(r)).n_tiles;
+        if (!mbar_wait_cluster(&bars->s_full[S & 1], (S >> 1) & 1, a.err, kDevTimeoutSoftmax,
+                               abort))
+          break;
+        mbar_arrive(&bars->slot_empty[slot_of(L)]);
         for (int j = 0; j < n; ++j) {
+          const uint32_t s = S + (uint32_t)j;
           if (j + 1 < n) {
-            if (!mbar_wait_cluster(&bars->s_full[(j + 1) & 1], ((j + 1) >> 1) & 1, a.err,
-                                   kDevTimeoutSoftmax, abort))
+            if (!mbar_wait_cluster(&bars->s_full[(s + 1) & 1], ((s + 1) >> 1) & 1, a.err,
+                                   kDevTimeoutSoftmax, abort)) {
+              ok = false;
               break;
-            mbar_arrive(&bars->slot_empty[slot_of((uint32_t)(2 * j + 1))]);
+            }
+            mbar_arrive(&bars->slot_empty[slot_of(L + (uint32_t)(2 * j + 1))]);
           }
-          if (!mbar_wait_cluster(&bars->pv_done, j & 1, a.err, kDevTimeoutSoftmax, abort)) break;
-          mbar_arrive(&bars->slot_empty[slot_of((uint32_t)min(2 * j + 2, 2 * n - 1))]);
+          if (!mbar_wait_cluster(&bars->pv_done, s & 1, a.err, kDevTimeoutSoftmax, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive(&bars->slot_empty[slot_of(L + (uint32_t)min(2 * j + 2, 2 * n - 1))]);
         }
+        L += 2u * (uint32_t)n;
+        S += (uint32_t)n;
       }
     } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0 && rank == 0) {
       // ------------------------------------------- MMA issuer (even CTA)
@@ -344,65 +414,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t q_desc = smem_desc_sw128(q_addr, 16, 1024);
       const uint64_t ring_k = smem_desc_sw128(ring, 16, 1024);        // K-major K halves
       const uint64_t ring_v = smem_desc_sw128(ring, kVBlock, 1024);   // MN-major V halves
-      auto wait_tile = [&](uint32_t t) {  // both CTAs' halves of load t
-        const bool tail = v_tail && t == last_load;
-        return mbar_wait_cluster(tail ? &bars->vtail : &bars->slot_full[slot_of(t)],
-                                 tail ? 0u : use_of(t), a.err, kDevTimeoutMma, abort) &&
-               mbar_wait_cluster(&bars->slot_peer[slot_of(t)], use_of(t), a.err,
-                                 kDevTimeoutMma, abort);
-      };
-      // An mbarrier wait issued after a tcgen05.commit stalls this thread
-      // until the commit resolves. The waits for a PV's inputs (P, V and the
-      // K tile after next) are therefore placed after the queued MMAs that
-      // keep the tensor pipe busy meanwhile, and before the commit that
-      // publishes S_{j+2}: that commit only gates softmax j+2, which cannot
-      // start before softmax j+1 has produced P_{j+1} anyway.
-      auto wait_pv_inputs = [&](int j, uint32_t t) {
-        return mbar_wait_cluster(&bars->p_full[j & 1], (j >> 1) & 1, a.err, kDevTimeoutMma,
-                                 abort) &&
-               wait_tile(t);
-      };
-      // load index of K_j: 0, then 2j - 1
-      auto k_load = [](int j) { return j == 0 ? 0u : (uint32_t)(2 * j - 1); };
-      uint32_t n = 0;  // loads consumed
-      bool ok = mbar_wait_cluster(&bars->q_full, 0, a.err, kDevTimeoutMma, abort) &&
-                mbar_wait_cluster(&bars->q_peer, 0, a.err, kDevTimeoutMma, abort) &&
-                wait_tile(0);
-      if (ok) {
+      uint32_t L = 0, S = 0;  // loads and steps of the pair's earlier items
+      bool ok = true;
+      for (int r = 0, k = 0; ok && item_of_round(r) < n_items; ++r, ++k) {
+        const Item it = item_at(item_of_round(r));
+        const int n_tiles = it.n_tiles;
+        const bool v_tail = kChunk && n_tiles * BN > it.n_keys;
+        const uint32_t last_load = L + 2u * (uint32_t)n_tiles - 1u;
+        auto wait_tile = [&](uint32_t t) {  // both CTAs' halves of (global) load t
+          const bool tail = v_tail && t == last_load;
+          return mbar_wait_cluster(tail ? &bars->vtail : &bars->slot_full[slot_of(t)],
+                                   tail ? 0u : use_of(t), a.err, kDevTimeoutMma, abort) &&
+                 mbar_wait_cluster(&bars->slot_peer[slot_of(t)], use_of(t), a.err,
+                                   kDevTimeoutMma, abort);
+        };
+        // An mbarrier wait issued after a tcgen05.commit stalls this thread
+        // until the commit resolves. The waits for a PV's inputs (P, V and the
+        // K tile after next) are therefore placed after the queued MMAs that
+        // keep the tensor pipe busy meanwhile, and before the commit that
+        // publishes S_{j+2}: that commit only gates softmax j+2, which cannot
+        // start before softmax j+1 has produced P_{j+1} anyway. Before the
+        // item's first PV, O must have been read by the previous epilogue.
+        auto wait_pv_inputs = [&](int j, uint32_t t) {
+          const uint32_t s = S + (uint32_t)j;
+          return mbar_wait_cluster(&bars->p_full[s & 1], (s >> 1) & 1, a.err, kDevTimeoutMma,
+                                   abort) &&
+                 wait_tile(t) &&
+                 (j > 0 || k == 0 ||
+                  mbar_wait_cluster(&bars->o_free, (k - 1) & 1, a.err, kDevTimeoutMma, abort));
+        };
+        // load index of K_j: 0, then 2j - 1
+        auto k_load = [&](int j) { return L + (j == 0 ? 0u : (uint32_t)(2 * j - 1)); };
+        auto s_col = [&](int j) { return tmem + ((S + (uint32_t)j) & 1u) * BN; };
+        uint32_t n = L;  // loads consumed
+        ok = mbar_wait_cluster(&bars->q_full, k & 1, a.err, kDevTimeoutMma, abort) &&
+             mbar_wait_cluster(&bars->q_peer, k & 1, a.err, kDevTimeoutMma, abort) &&
+             wait_tile(n);
+        if (!ok) break;
         tc_fence_after();
-        issue_s(tmem, q_desc, ring_k, slot_of(0));
-        n = 1;
+        issue_s(s_col(0), q_desc, ring_k, slot_of(n));
+        n += 1;
         if (n_tiles > 1) {
-          ok = wait_tile(1);  // K_1
-          mma_commit_pair(&bars->s_full[0]);
-          if (ok) {
-            tc_fence_after();
-            issue_s(tmem + BN, q_desc, ring_k, slot_of(1));
-            n = 2;
-            ok = wait_pv_inputs(0, n) && (n_tiles <= 2 || wait_tile(k_load(2)));
-            mma_commit_pair(&bars->s_full[1]);
-          }
+          ok = wait_tile(n);  // K_1
+          mma_commit_pair(&bars->s_full[S & 1]);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(s_col(1), q_desc, ring_k, slot_of(n));
+          n += 1;
+          ok = wait_pv_inputs(0, n) && (n_tiles <= 2 || wait_tile(k_load(2)));
+          mma_commit_pair(&bars->s_full[(S + 1) & 1]);
+          if (n_tiles == 2) mma_commit_pair(&bars->q_empty);  // the item's last QK^T
         } else {
-          mma_commit_pair(&bars->s_full[0]);
+          mma_commit_pair(&bars->s_full[S & 1]);
+          mma_commit_pair(&bars->q_empty);  // the item's last QK^T
           ok = wait_pv_inputs(0, n);
         }
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        // P_j, V_j (load n) and K_{j+2} (load n + 1) have been waited for
-        tc_fence_after();
-        issue_pv(tmem + kTmemO, tmem + (j & 1) * BN, ring_v, slot_of(n), j > 0);
-        n += 1;
-        mma_commit_pair(&bars->pv_done);
-        const bool next_s = j + 2 < n_tiles;
-        if (next_s) {
-          issue_s(tmem + (j & 1) * BN, q_desc, ring_k, slot_of(n));
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          // P_j, V_j (load n) and K_{j+2} (load n + 1) have been waited for
+          tc_fence_after();
+          issue_pv(tmem + kTmemO, s_col(j), ring_v, slot_of(n), j > 0);
           n += 1;
+          mma_commit_pair(&bars->pv_done);
+          const bool next_s = j + 2 < n_tiles;
+          if (next_s) {
+            issue_s(s_col(j), q_desc, ring_k, slot_of(n));
+            n += 1;
+          }
+          if (j + 1 < n_tiles)  // P_{j+1}, V_{j+1}, K_{j+3}
+            ok = wait_pv_inputs(j + 1, n) && (j + 3 >= n_tiles || wait_tile(k_load(j + 3)));
+          if (next_s) {
+            mma_commit_pair(&bars->s_full[(S + (uint32_t)j) & 1]);
+            if (j + 3 == n_tiles) mma_commit_pair(&bars->q_empty);  // the item's last QK^T
+          }
         }
-        if (j + 1 < n_tiles)  // P_{j+1}, V_{j+1}, K_{j+3}
-          ok = wait_pv_inputs(j + 1, n) && (j + 3 >= n_tiles || wait_tile(k_load(j + 3)));
-        if (next_s) mma_commit_pair(&bars->s_full[j & 1]);
+        if (ok) mma_commit_pair(&bars->o_final);
+        L += 2u * (uint32_t)n_tiles;
+        S += (uint32_t)n_tiles;
       }
-      if (ok) mma_commit_pair(&bars->o_final);
       // drain: every MMA issued above has completed once this phase completes
       mma_commit_pair(&bars->drain);
       mbar_wait_cluster(&bars->drain, 0, nullptr, 0, nullptr);
@@ -413,143 +501,170 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int cq = warp >> 2;  // key quarter of each S tile (32 keys); O columns 64 cq ..
     const int r = lq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(lq * 32) << 16;
-    const int tok = t0 + r / g;
-    const int h = kv * g + (r % g);
-    // last key this row sees: padding rows of a chunk stop at the last valid
-    // key, so they never read rows past the valid keys either
-    const int key_last = kChunk ? p0 + min(tok, a.T - 1) : tok;
     const uint32_t p_full_even[2] = {peer_smem_addr(&bars->p_full[0], 0),
                                      peer_smem_addr(&bars->p_full[1], 0)};
-    float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
-    float l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      ok = __all_sync(kFull, mbar_wait_cluster(&bars->s_full[j & 1], (j >> 1) & 1, a.err,
-                                               kDevTimeoutSoftmax, abort));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tmem_s = tmem + (j & 1) * BN + cq * 32 + lane_off;
-      uint32_t sr[32];
-      tmem_ld32_wait(tmem_s, sr);
-      float s[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(sr[e]);
-      const int key0 = j * BN + cq * 32;
-      if (key0 + 31 > key_last) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (key0 + e > key_last) s[e] = -INFINITY;
+    const uint32_t o_free_even = peer_smem_addr(&bars->o_free, 0);
+    uint32_t S = 0;  // steps of the pair's earlier items
+    // Every thread runs every item of the pair (even after an abort, when each
+    // wait returns at once), so the named barrier of the epilogue is reached
+    // the same number of times by all softmax threads of the CTA.
+    for (int rr = 0, k = 0; item_of_round(rr) < n_items; ++rr, ++k) {
+      const int item = item_of_round(rr);
+      int n_tiles, tok, key_last;  // what lives through the loop
+      {
+        const Item it = item_at(item);
+        n_tiles = it.n_tiles;
+        tok = it.t0_pair + (int)rank * tile_tok + r / g;
+        // last key this row sees: padding rows of a chunk stop at the last
+        // valid key, so they never read rows past the valid keys either
+        key_last = kChunk ? it.p0 + min(tok, a.T - 1) : tok;
       }
-      bool move = false;
-      float alpha = 1.0f;
-      if (!fixed_max) {
-        float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-        for (int e = 4; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[e]);
-        float* xm = xchg + (j & 1) * 4 * 128;  // [quarter][128]
-        xm[cq * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        mbar_arrive(&bars->xmax_full);
-        ok = __all_sync(kFull, mbar_wait(&bars->xmax_full, j & 1, a.err, kDevTimeoutSoftmax,
-                                         abort));
-        if (!ok) break;
-        const float mrow = fmaxf(fmaxf(xm[r], xm[128 + r]), fmaxf(xm[256 + r], xm[384 + r]));
-        const float m_tile = mrow * kScaleLog2;
-        move = m_tile > m + kRescaleThreshold;
-        const float m_new = move ? m_tile : m;
-        alpha = move ? ex2(m - m_new) : 1.0f;
-        m = m_new;
-        l *= alpha;
-      }
-      // p = 2^(s * scale - m), two at a time on the f32x2 pipes
-      const uint64_t scale2 = f2_pack(kScaleLog2, kScaleLog2);
-      const uint64_t negm2 = f2_pack(-m, -m);
-      uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-      uint32_t pw[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const uint64_t x = f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
-        float x0, x1;
-        f2_unpack(x, x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
-        pw[e] = pack_bf16x2(p0, p1);
-      }
-      tmem_st16_wait(tmem_s, pw);  // P over the first 16 of this thread's S columns
-      if (!fixed_max && j > 0 && __any_sync(kFull, move)) {
-        // rescale this thread's O columns once PV_{j-1} has completed, before
-        // PV_j adds terms relative to the new max
-        ok = __all_sync(kFull, mbar_wait_cluster(&bars->pv_done, (j - 1) & 1, a.err,
+      float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
+      float l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n_tiles; ++j) {
+        const uint32_t s = S + (uint32_t)j;
+        ok = __all_sync(kFull, mbar_wait_cluster(&bars->s_full[s & 1], (s >> 1) & 1, a.err,
                                                  kDevTimeoutSoftmax, abort));
         if (!ok) break;
         tc_fence_after();
+        const uint32_t tmem_s = tmem + (s & 1) * BN + cq * 32 + lane_off;
+        uint32_t sr[32];
+        tmem_ld32_wait(tmem_s, sr);
+        float sv[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o[32];
-          const uint32_t to = tmem + kTmemO + cq * 64 + c * 32 + lane_off;
-          tmem_ld32_wait(to, o);
+        for (int e = 0; e < 32; ++e) sv[e] = __uint_as_float(sr[e]);
+        const int key0 = j * BN + cq * 32;
+        if (key0 + 31 > key_last) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32_wait(to, o);
+          for (int e = 0; e < 32; ++e)
+            if (key0 + e > key_last) sv[e] = -INFINITY;
+        }
+        bool move = false;
+        float alpha = 1.0f;
+        if (!fixed_max) {
+          float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+          for (int e = 4; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], sv[e]);
+          float* xm = xchg + (s & 1) * 4 * 128;  // [quarter][128]
+          xm[cq * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          mbar_arrive(&bars->xmax_full);
+          ok = __all_sync(kFull, mbar_wait(&bars->xmax_full, s & 1, a.err, kDevTimeoutSoftmax,
+                                           abort));
+          if (!ok) break;
+          const float mrow = fmaxf(fmaxf(xm[r], xm[128 + r]), fmaxf(xm[256 + r], xm[384 + r]));
+          const float m_tile = mrow * kScaleLog2;
+          move = m_tile > m + kRescaleThreshold;
+          const float m_new = move ? m_tile : m;
+          alpha = move ? ex2(m - m_new) : 1.0f;
+          m = m_new;
+          l *= alpha;
+        }
+        // p = 2^(s * scale - m), two at a time on the f32x2 pipes
+        const uint64_t scale2 = f2_pack(kScaleLog2, kScaleLog2);
+        const uint64_t negm2 = f2_pack(-m, -m);
+        uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        uint32_t pw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint64_t x = f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), scale2, negm2);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
+          pw[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16_wait(tmem_s, pw);  // P over the first 16 of this thread's S columns
+        if (!fixed_max && j > 0 && __any_sync(kFull, move)) {
+          // rescale this thread's O columns once PV_{j-1} has completed,
+          // before PV_j adds terms relative to the new max
+          ok = __all_sync(kFull, mbar_wait_cluster(&bars->pv_done, (s - 1) & 1, a.err,
+                                                   kDevTimeoutSoftmax, abort));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t o[32];
+            const uint32_t to = tmem + kTmemO + cq * 64 + cc * 32 + lane_off;
+            tmem_ld32_wait(to, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32_wait(to, o);
+          }
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(sum2[0], a0, a1);
+        f2_unpack(sum2[1], b0, b1);
+        l += (a0 + a1) + (b0 + b1);
+        // the warp's tcgen05.st has completed (wait::st above, warp-collective):
+        // one arrive per warp, on the even CTA's barrier, publishes its 32 rows
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(&bars->p_full[s & 1]);  // the issuer's own CTA: CTA scope suffices
+          else
+            mbar_arrive_cluster(p_full_even[s & 1]);
         }
       }
-      float a0, a1, b0, b1;
-      f2_unpack(sum2[0], a0, a1);
-      f2_unpack(sum2[1], b0, b1);
-      l += (a0 + a1) + (b0 + b1);
-      // the warp's tcgen05.st has completed (wait::st above, warp-collective):
-      // one arrive per warp, on the even CTA's barrier, publishes its 32 rows
+      // ---- epilogue: the row's four partial sums, then O / l * sigmoid(gate)
+      ok = __all_sync(kFull, ok && !*abort);
+      const Item it = item_at(item);
+      // rows past the sequence, and the 128 - g * (128 / g) rows after the last
+      // whole token when g does not divide 128, are padding
+      const bool store = ok && tok < a.T && r < g * tile_tok;
+      const long long row = ((long long)it.b * a.T + tok) * a.Hq + (it.kv * g + (r % g));
+      // the partial sums go to a slot double-buffered by item; every thread of
+      // the four warpgroups reaches this barrier once per item
+      float* lsum = xchg + 2 * 4 * 128 + (k & 1) * 4 * 128;  // [quarter][128]
+      lsum[cq * 128 + r] = l;
+      named_barrier_sync(1, kSoftmaxWGs * 128);
+      if (ok) {
+        l = (lsum[r] + lsum[128 + r]) + (lsum[256 + r] + lsum[384 + r]);
+        ok = __all_sync(kFull, mbar_wait_cluster(&bars->o_final, k & 1, a.err,
+                                                 kDevTimeoutEpilogue, abort));
+      }
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+        uint16_t* orow = a.out + row * D + cq * 64;
+        const uint4* grow = reinterpret_cast<const uint4*>(a.qg + row * (2 * D) + D + cq * 64);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t o[32];
+          tmem_ld32_wait(tmem + kTmemO + cq * 64 + cc * 32 + lane_off, o);
+          if (store) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint4 g4 = grow[cc * 4 + q4];
+              const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+              uint32_t zw[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // sigmoid(x) = 1 / (1 + 2^(-x log2 e))
+                const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
+                const float sg0 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g0));
+                const float sg1 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g1));
+                zw[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l * sg0,
+                                    __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l * sg1);
+              }
+              reinterpret_cast<uint4*>(orow + cc * 32)[q4] =
+                  make_uint4(zw[0], zw[1], zw[2], zw[3]);
+            }
+          }
+        }
+      }
+      // O has been read: the next item's first PV may overwrite it (one
+      // arrive per warp of both CTAs, on the even CTA's barrier)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if (rank == 0)
-          mbar_arrive(&bars->p_full[j & 1]);  // the issuer's own CTA: CTA scope suffices
+          mbar_arrive(&bars->o_free);
         else
-          mbar_arrive_cluster(p_full_even[j & 1]);
+          mbar_arrive_cluster(o_free_even);
       }
-    }
-    // ---- epilogue: the row's four partial sums, then O / l * sigmoid(gate)
-    ok = __all_sync(kFull, ok && !*abort);
-    // every thread of the four warpgroups reaches this barrier exactly once
-    float* lsum = xchg + 2 * 4 * 128;  // [quarter][128]
-    lsum[cq * 128 + r] = l;
-    named_barrier_sync(1, kSoftmaxWGs * 128);
-    if (ok) {
-      l = (lsum[r] + lsum[128 + r]) + (lsum[256 + r] + lsum[384 + r]);
-      ok = __all_sync(kFull, mbar_wait_cluster(&bars->o_final, 0, a.err, kDevTimeoutEpilogue,
-                                               abort));
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l;
-      // rows past the sequence, and the 128 - g * (128 / g) rows after the last
-      // whole token when g does not divide 128, are padding
-      const bool store = tok < a.T && r < g * tile_tok;
-      const long long row = ((long long)b * a.T + tok) * a.Hq + h;
-      const uint16_t* grow = a.qg + row * (2 * D) + D + cq * 64;
-      uint16_t* orow = a.out + row * D + cq * 64;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        tmem_ld32_wait(tmem + kTmemO + cq * 64 + c * 32 + lane_off, o);
-        if (store) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint4 gv = reinterpret_cast<const uint4*>(grow + c * 32)[q4];
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-            uint32_t zw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              // sigmoid(x) = 1 / (1 + 2^(-x log2 e))
-              const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
-              const float sg0 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g0));
-              const float sg1 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g1));
-              zw[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l * sg0,
-                                  __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l * sg1);
-            }
-            reinterpret_cast<uint4*>(orow + c * 32)[q4] = make_uint4(zw[0], zw[1], zw[2], zw[3]);
-          }
-        }
-      }
+      S += (uint32_t)n_tiles;
     }
   }
 
@@ -577,9 +692,21 @@ cudaError_t launch(const Args& args, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 64) done_mask |= 1ull << dev;
   }
-  const long long grid = 2LL * a.n_mtiles * a.B * a.Hkv;
-  if (grid == 0) return cudaSuccess;
-  if (grid > 0x7ffffffeLL) return cudaErrorInvalidConfiguration;
+  // the plain prefill runs one persistent pair per two SMs over all items; a
+  // chunk runs one pair per item
+  constexpr bool kChunk = sizeof(Args) != sizeof(GatedAttnArgs);
+  const long long items = (long long)a.n_mtiles * a.B * a.Hkv;
+  if (items == 0) return cudaSuccess;
+  if (items > 0x3fffffffLL) return cudaErrorInvalidConfiguration;
+  static int sm_count[64];
+  int n_sm = dev < 64 ? sm_count[dev] : 0;
+  if (n_sm == 0) {
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) sm_count[dev] = n_sm;
+  }
+  const long long pairs = kChunk ? items : (items < n_sm / 2 ? items : (long long)(n_sm / 2));
+  const long long grid = 2 * pairs;
   gated_attention_pair_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();
 }
