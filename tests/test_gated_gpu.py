@@ -327,3 +327,12 @@ def test_gated_chunk_workload_sampled_rows(cuda_lib):
                                                  dtype=torch.int32))
     got = torch.stack([out[b, t, h] for b, t, h in rows])
     assert_close_attention(got, ref, w.name)
+
+
+def test_gated_more_items_than_pairs_full_parity(cuda_lib):
+    """80 pair items (32-token pair tiles of 4 KV groups) on a GPU with fewer
+    than 80 pairs of SMs: some persistent pairs take a second item. Every
+    output row against the oracle."""
+    x = inputs.gated_inputs(2, 640, 16, 2, seed=32)
+    ref = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    assert_close_attention(run_gated(x, 64, 1e7), ref, "80 pair items")

@@ -135,3 +135,13 @@ def test_prefill_full_size_sampled_rows(cuda_lib, name):
                               w.theta, w.eps, rows)
     got = torch.stack([out[b, t, h] for b, t, h in rows.tolist()])
     assert_close_attention(got, ref, name)
+
+
+def test_prefill_more_items_than_ctas_full_parity(cuda_lib):
+    """160 work items (pairs of 32-token Q tiles of 8 KV groups) on a GPU with
+    fewer SMs than that: some persistent CTAs take a second item in the snake
+    order's partial last round. Every output row against the oracle."""
+    B, T, Hq, Hkv = 2, 1280, 32, 4
+    x = inputs.prefill_inputs(B, T, Hq, Hkv, seed=31)
+    ref = oracle.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    assert_close_attention(run_prefill(x, 1e6), ref, "160 items")
