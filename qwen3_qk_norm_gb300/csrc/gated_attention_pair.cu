@@ -35,7 +35,7 @@
 // ("Q free", committed to both CTAs), the ring, the S buffers and every
 // barrier phase continue, and the next item's first PV waits only for every
 // softmax warp of the pair to have read O ("O free"). A chunk against the
-// caches runs one pair per item.
+// caches runs the same way.
 //
 // Roles (640 threads per CTA):
 //   WG 0..3  softmax + epilogue of the CTA's own 128 rows. Warp w serves TMEM
@@ -255,39 +255,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // 2n - 1. Indices below are global over the pair's items (item base L).
   if (warp >= kSoftmaxWGs * 4) {
     if (warp == kSoftmaxWGs * 4) {
-      // chunk (one item per pair): the last V half tile's rows past the valid
-      // keys are cleared by this warp once the tile has landed
-      bool v_tail = false;
-      int tail_first = 0;
-      uint32_t tail_load = 0;
-     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      tma_prefetch_desc(&a.tm_q);
-      tma_prefetch_desc(&a.tm_k);
-      tma_prefetch_desc(&a.tm_v);
-      uint32_t n = 0;    // half tiles issued (global)
-      uint32_t n_q = 0;  // Q tiles issued
-      bool ok = true;
+      // Lane 0 issues the loads. Chunk: an item's last V half tile may hold
+      // rows past the valid keys; the whole warp clears them in this CTA's
+      // half once that tile has landed and publishes it on "V tail" (one phase
+      // per item that has such a tail).
+      if (lane == 0) {
+        tma_prefetch_desc(&a.tm_q);
+        tma_prefetch_desc(&a.tm_k);
+        tma_prefetch_desc(&a.tm_v);
+      }
+      uint32_t n = 0;    // half tiles issued (global; every lane keeps the count)
+      uint32_t n_q = 0;  // Q tiles issued (lane 0)
+      bool ok = kChunk || lane == 0;  // the plain prefill's loop runs on lane 0 only
       for (int r = 0; ok && item_of_round(r) < n_items; ++r) {
         const Item it = item_at(item_of_round(r));
         const int row3 = it.b * a.Hkv + it.kv;
-        // this CTA's Q tile, once the previous item's last QK^T has completed
-        if (n_q > 0 && !mbar_wait(&bars->q_empty, (n_q - 1) & 1, a.err, kDevTimeoutTma, abort)) {
-          ok = false;
-          break;
+        if (lane == 0) {
+          // this CTA's Q tile, once the previous item's last QK^T has completed
+          ok = n_q == 0 || mbar_wait(&bars->q_empty, (n_q - 1) & 1, a.err, kDevTimeoutTma, abort);
+          if (ok) {
+            // g * floor(128/g) rows of 128 bytes per 64-dim block (126 or 120
+            // when g does not divide 128)
+            mbar_arrive_expect_tx(&bars->q_full, 4u * (uint32_t)(g * tile_tok) * 128u);
+            const int t0 = it.t0_pair + (int)rank * tile_tok;
+            for (int cc = 0; cc < 4; ++cc)
+              tma_load_4d(smem + OFF_Q + cc * kQBlock, &a.tm_q, &bars->q_full, 64 * cc, it.kv * g,
+                          t0, it.b);
+            ++n_q;  // lane 0's count
+          }
         }
-        // g * floor(128/g) rows of 128 bytes per 64-dim block (126 or 120 when
-        // g does not divide 128)
-        mbar_arrive_expect_tx(&bars->q_full, 4u * (uint32_t)(g * tile_tok) * 128u);
-        const int t0 = it.t0_pair + (int)rank * tile_tok;
-        for (int cc = 0; cc < 4; ++cc)
-          tma_load_4d(smem + OFF_Q + cc * kQBlock, &a.tm_q, &bars->q_full, 64 * cc, it.kv * g, t0,
-                      it.b);
-        ++n_q;
+        uint32_t n0 = n;  // lane 0 counts its loads from here
         auto load_tile = [&](bool is_k, int j) {
           if (!ok) return;
-          const uint32_t s = slot_of(n);
-          if (!mbar_wait(&bars->slot_empty[s], use_of(n) ^ 1u, a.err, kDevTimeoutTma, abort)) {
+          const uint32_t s = slot_of(n0);
+          if (!mbar_wait(&bars->slot_empty[s], use_of(n0) ^ 1u, a.err, kDevTimeoutTma, abort)) {
             ok = false;
             return;
           }
@@ -307,39 +309,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             128 * (int)rank + 64 * cc, it.kv, j * BN, it.b);
             }
           }
-          ++n;
+          ++n0;
         };
-        load_tile(true, 0);
-        if (it.n_tiles > 1) load_tile(true, 1);
-        for (int j = 0; ok && j < it.n_tiles; ++j) {
-          load_tile(false, j);
-          if (j + 2 < it.n_tiles) load_tile(true, j + 2);
+        if (lane == 0) {
+          load_tile(true, 0);
+          if (it.n_tiles > 1) load_tile(true, 1);
+          for (int j = 0; ok && j < it.n_tiles; ++j) {
+            load_tile(false, j);
+            if (j + 2 < it.n_tiles) load_tile(true, j + 2);
+          }
         }
-        if (kChunk && ok && it.n_tiles * BN > it.n_keys) {
-          v_tail = true;
-          tail_first = it.n_keys - (it.n_tiles - 1) * BN;
-          tail_load = n - 1;
+        if (kChunk) {  // the whole warp runs the loop (it clears V tails)
+          ok = __shfl_sync(kFull, ok, 0);
+          n0 = __shfl_sync(kFull, n0, 0);
         }
-      }
-      if (*abort) {
-        // let every copy that was issued land before the CTA goes away
-        if (n_q > 0) mbar_wait(&bars->q_full, (n_q - 1) & 1, nullptr, 0, nullptr);
-        for (uint32_t i = n > (uint32_t)kSlots ? n - kSlots : 0u; i < n; ++i)
-          mbar_wait(&bars->slot_full[slot_of(i)], use_of(i), nullptr, 0, nullptr);
-      }
-     }
-      v_tail = __shfl_sync(kFull, v_tail, 0);
-      if (kChunk && v_tail) {
-        // every load has been issued (lane 0 is past its loop), so the slot's
-        // barrier is in the phase of the last load: wait for it, clear this
-        // CTA's rows past the valid keys in both 64-dim blocks (a cleared row
-        // is 128 bytes whatever the swizzle), and publish that
-        tail_first = __shfl_sync(kFull, tail_first, 0);
-        tail_load = __shfl_sync(kFull, tail_load, 0);
-        const bool landed = __all_sync(
-            kFull, mbar_wait(&bars->slot_full[slot_of(tail_load)], use_of(tail_load), a.err,
-                             kDevTimeoutTma, abort));
-        if (landed) {
+        if (!ok) {
+          n = n0;
+          break;
+        }
+        n = n0;
+        if (kChunk && it.n_tiles * BN > it.n_keys) {
+          // every load of the item has been issued and none after it, so the
+          // slot's barrier is in the phase of the item's last load: wait for
+          // it, clear this CTA's rows past the valid keys in both 64-dim
+          // blocks (a cleared row is 128 bytes whatever the swizzle), and
+          // publish that
+          const uint32_t tail_load = n - 1;
+          const int tail_first = it.n_keys - (it.n_tiles - 1) * BN;
+          ok = __all_sync(kFull, mbar_wait(&bars->slot_full[slot_of(tail_load)],
+                                           use_of(tail_load), a.err, kDevTimeoutTma, abort));
+          if (!ok) break;
           uint8_t* vt = smem + OFF_RING + slot_of(tail_load) * kSlotBytes;
           const int chunks = (BN - tail_first) * 16;  // 16-byte chunks, both blocks
           for (int ch = lane; ch < chunks; ch += 32) {
@@ -352,11 +351,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&bars->vtail);
         }
       }
+      if (lane == 0 && *abort) {
+        // let every copy that was issued land before the CTA goes away
+        if (n_q > 0) mbar_wait(&bars->q_full, (n_q - 1) & 1, nullptr, 0, nullptr);
+        for (uint32_t i = n > (uint32_t)kSlots ? n - kSlots : 0u; i < n; ++i)
+          mbar_wait(&bars->slot_full[slot_of(i)], use_of(i), nullptr, 0, nullptr);
+      }
     } else if (warp == kSoftmaxWGs * 4 + 2 && lane == 0 && rank == 1) {
       // ----------------------------------------------- forwarder (odd CTA)
       // the even CTA's MMA issuer reads this CTA's Q and ring too: tell it
       // when each of them has landed, in load order
       uint32_t L = 0;
+      uint32_t n_tail = 0;  // earlier items with a cleared V tail
       bool ok = true;
       for (int r = 0, k = 0; ok && item_of_round(r) < n_items; ++r, ++k) {
         const Item it = item_at(item_of_round(r));
@@ -368,13 +374,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t gt = L + t;
           const bool tail = v_tail && t + 1 == n_loads;
           if (!mbar_poll(tail ? &bars->vtail : &bars->slot_full[slot_of(gt)],
-                         tail ? 0u : use_of(gt), a.err, kDevTimeoutTma, abort)) {
+                         tail ? (n_tail & 1) : use_of(gt), a.err, kDevTimeoutTma, abort)) {
             ok = false;
             break;
           }
           mbar_arrive_cluster(peer_smem_addr(&bars->slot_peer[slot_of(gt)], 0));
         }
         L += n_loads;
+        if (v_tail) ++n_tail;
       }
     } else if (warp == kSoftmaxWGs * 4 + 3 && lane == 0) {
       // ------------------------------------------------------------ releaser
@@ -415,6 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t ring_k = smem_desc_sw128(ring, 16, 1024);        // K-major K halves
       const uint64_t ring_v = smem_desc_sw128(ring, kVBlock, 1024);   // MN-major V halves
       uint32_t L = 0, S = 0;  // loads and steps of the pair's earlier items
+      uint32_t n_tail = 0;    // earlier items with a cleared V tail
       bool ok = true;
       for (int r = 0, k = 0; ok && item_of_round(r) < n_items; ++r, ++k) {
         const Item it = item_at(item_of_round(r));
@@ -424,7 +432,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto wait_tile = [&](uint32_t t) {  // both CTAs' halves of (global) load t
           const bool tail = v_tail && t == last_load;
           return mbar_wait_cluster(tail ? &bars->vtail : &bars->slot_full[slot_of(t)],
-                                   tail ? 0u : use_of(t), a.err, kDevTimeoutMma, abort) &&
+                                   tail ? (n_tail & 1) : use_of(t), a.err, kDevTimeoutMma,
+                                   abort) &&
                  mbar_wait_cluster(&bars->slot_peer[slot_of(t)], use_of(t), a.err,
                                    kDevTimeoutMma, abort);
         };
@@ -490,6 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (ok) mma_commit_pair(&bars->o_final);
         L += 2u * (uint32_t)n_tiles;
         S += (uint32_t)n_tiles;
+        if (v_tail) ++n_tail;
       }
       // drain: every MMA issued above has completed once this phase completes
       mma_commit_pair(&bars->drain);
@@ -692,9 +702,7 @@ cudaError_t launch(const Args& args, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 64) done_mask |= 1ull << dev;
   }
-  // the plain prefill runs one persistent pair per two SMs over all items; a
-  // chunk runs one pair per item
-  constexpr bool kChunk = sizeof(Args) != sizeof(GatedAttnArgs);
+  // one persistent pair per two SMs over all items
   const long long items = (long long)a.n_mtiles * a.B * a.Hkv;
   if (items == 0) return cudaSuccess;
   if (items > 0x3fffffffLL) return cudaErrorInvalidConfiguration;
@@ -705,7 +713,7 @@ cudaError_t launch(const Args& args, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 64) sm_count[dev] = n_sm;
   }
-  const long long pairs = kChunk ? items : (items < n_sm / 2 ? items : (long long)(n_sm / 2));
+  const long long pairs = items < n_sm / 2 ? items : (long long)(n_sm / 2);
   const long long grid = 2 * pairs;
   gated_attention_pair_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();

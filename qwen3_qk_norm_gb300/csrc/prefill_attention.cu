@@ -22,7 +22,7 @@
 // as soon as the current item's last QK^T has completed ("Q free"), the K/V
 // ring and every barrier phase run on across items, and the next item's
 // first PV of a tile waits only for that tile's epilogue to have read O
-// ("O free"). A chunk against the caches runs one CTA per item.
+// ("O free"). The chunk against the caches runs the same way.
 //
 // Roles (576 threads):
 //   WG 0..3   softmax + epilogue. WG w serves Q tile t = w/2 and the column
@@ -227,83 +227,72 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kSoftmaxWGs * 4) {
     if (warp == kSoftmaxWGs * 4) {
-      // Cache V (chunked prefill, one item per CTA): the last V tile holds
-      // rows past the valid keys (whatever the cache holds there). Their
-      // weights are 0, but 0 x NaN is NaN in the PV product, so the producer
-      // warp clears them before PV reads them.
-      bool v_tail = false;
-      int tail_first = 0;
-      uint32_t tail_load = 0;
-     if (lane == 0) {
       // ---------------------------------------------------------- producer
-      tma_prefetch_desc(&a.tm_q);
-      tma_prefetch_desc(&a.tm_k);
-      tma_prefetch_desc(&a.tm_v);
+      // Lane 0 issues the loads. Cache V (chunked prefill): an item's last V
+      // tile may hold rows past the valid keys (whatever the cache holds
+      // there). Their weights are 0, but 0 x NaN is NaN in the PV product, so
+      // the whole warp clears them once that tile has landed and publishes it
+      // on "V tail" (one phase per item that has such a tail).
+      if (lane == 0) {
+        tma_prefetch_desc(&a.tm_q);
+        tma_prefetch_desc(&a.tm_k);
+        tma_prefetch_desc(&a.tm_v);
+      }
       uint32_t L = 0;       // first load index of the current item
-      uint32_t issued = 0;  // loads issued
-      uint32_t n_q = 0;     // Q pairs issued
-      bool ok = true;
+      uint32_t issued = 0;  // loads issued (lane 0)
+      uint32_t n_q = 0;     // Q pairs issued (lane 0)
+      bool ok = kChunk || lane == 0;  // the plain prefill's loop runs on lane 0 only
       for (int r = 0; ok && item_of_round(r) < n_items; ++r) {
         const Item it = item_at(item_of_round(r));
-        // the Q tiles are free once the previous item's last QK^T completed
-        if (n_q > 0 && !mbar_wait(&bars->q_empty, (n_q - 1) & 1, a.err, kDevTimeoutTma, abort)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&bars->q_full, kQTiles * kTile);
-        for (int t = 0; t < kQTiles; ++t) {
-          uint8_t* qd = smem + OFF_Q + t * kTile;
-          const int tq = it.t0 + t * tile_tok;
-          tma_load_4d(qd, &a.tm_q, &bars->q_full, 0, it.kv * g, tq, it.b);
-          tma_load_4d(qd + kHalf, &a.tm_q, &bars->q_full, 64, it.kv * g, tq, it.b);
-        }
-        ++n_q;
-        const int row3 = it.b * a.Hkv + it.kv;
-        for (int i = 0; i < 2 * it.n_tiles; ++i) {  // K_0, V_0, K_1, V_1, ...
-          const uint32_t li = L + (uint32_t)i;
-          const int s = (int)(li % kSlots);
-          if (!mbar_wait(&bars->slot_empty[s], ((li / kSlots) & 1) ^ 1, a.err, kDevTimeoutTma,
-                         abort)) {
-            ok = false;
-            break;
+        if (lane == 0) {
+          // the Q tiles are free once the previous item's last QK^T completed
+          ok = n_q == 0 || mbar_wait(&bars->q_empty, (n_q - 1) & 1, a.err, kDevTimeoutTma, abort);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars->q_full, kQTiles * kTile);
+            for (int t = 0; t < kQTiles; ++t) {
+              uint8_t* qd = smem + OFF_Q + t * kTile;
+              const int tq = it.t0 + t * tile_tok;
+              tma_load_4d(qd, &a.tm_q, &bars->q_full, 0, it.kv * g, tq, it.b);
+              tma_load_4d(qd + kHalf, &a.tm_q, &bars->q_full, 64, it.kv * g, tq, it.b);
+            }
+            ++n_q;
           }
-          mbar_arrive_expect_tx(&bars->slot_full[s], kTile);
-          uint8_t* dst = smem + OFF_RING + s * kTile;
-          const int j = i >> 1;
-          if ((i & 1) == 0) {
-            tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 0, j * BN, row3);
-            tma_load_3d(dst + kHalf, &a.tm_k, &bars->slot_full[s], 64, j * BN, row3);
-          } else if (kChunk) {
-            tma_load_3d(dst, &a.tm_v, &bars->slot_full[s], 0, j * BN, row3);
-            tma_load_3d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, j * BN, row3);
-          } else {
-            tma_load_4d(dst, &a.tm_v, &bars->slot_full[s], 0, it.kv, j * BN, it.b);
-            tma_load_4d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, it.kv, j * BN, it.b);
-          }
-          issued = li + 1;
-          if (i + 1 == 2 * it.n_tiles && kChunk && it.n_tiles * BN > it.n_keys) {
-            v_tail = true;
-            tail_first = it.n_keys - (it.n_tiles - 1) * BN;
-            tail_load = li;
+          const int row3 = it.b * a.Hkv + it.kv;
+          for (int i = 0; ok && i < 2 * it.n_tiles; ++i) {  // K_0, V_0, K_1, V_1, ...
+            const uint32_t li = L + (uint32_t)i;
+            const int s = (int)(li % kSlots);
+            if (!mbar_wait(&bars->slot_empty[s], ((li / kSlots) & 1) ^ 1, a.err, kDevTimeoutTma,
+                           abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->slot_full[s], kTile);
+            uint8_t* dst = smem + OFF_RING + s * kTile;
+            const int j = i >> 1;
+            if ((i & 1) == 0) {
+              tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 0, j * BN, row3);
+              tma_load_3d(dst + kHalf, &a.tm_k, &bars->slot_full[s], 64, j * BN, row3);
+            } else if (kChunk) {
+              tma_load_3d(dst, &a.tm_v, &bars->slot_full[s], 0, j * BN, row3);
+              tma_load_3d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, j * BN, row3);
+            } else {
+              tma_load_4d(dst, &a.tm_v, &bars->slot_full[s], 0, it.kv, j * BN, it.b);
+              tma_load_4d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, it.kv, j * BN, it.b);
+            }
+            issued = li + 1;
           }
         }
-        if (ok) L += 2u * (uint32_t)it.n_tiles;
-      }
-      if (*abort) {
-        // let every copy that was issued land before the CTA goes away
-        if (n_q > 0) mbar_wait(&bars->q_full, (n_q - 1) & 1, nullptr, 0, nullptr);
-        for (uint32_t i = issued > (uint32_t)kSlots ? issued - kSlots : 0u; i < issued; ++i)
-          mbar_wait(&bars->slot_full[i % kSlots], (i / kSlots) & 1, nullptr, 0, nullptr);
-      }
-     }
-      v_tail = __shfl_sync(kFull, v_tail, 0);
-      if (kChunk && v_tail) {
-        tail_first = __shfl_sync(kFull, tail_first, 0);
-        tail_load = __shfl_sync(kFull, tail_load, 0);
-        const bool ok = __all_sync(kFull, mbar_wait(&bars->slot_full[tail_load % kSlots],
-                                                    (tail_load / kSlots) & 1, a.err,
-                                                    kDevTimeoutTma, abort));
-        if (ok) {
+        if (kChunk) ok = __shfl_sync(kFull, ok, 0);  // the whole warp runs the loop
+        if (!ok) break;
+        if (kChunk && it.n_tiles * BN > it.n_keys) {
+          // every load of the item has been issued and none after it, so the
+          // slot's barrier is in the phase of the item's last load
+          const uint32_t tail_load = L + 2u * (uint32_t)it.n_tiles - 1u;
+          const int tail_first = it.n_keys - (it.n_tiles - 1) * BN;  // first row to clear
+          ok = __all_sync(kFull, mbar_wait(&bars->slot_full[tail_load % kSlots],
+                                           (tail_load / kSlots) & 1, a.err, kDevTimeoutTma,
+                                           abort));
+          if (!ok) break;
           uint8_t* vt = smem + OFF_RING + (tail_load % kSlots) * kTile;
           const int chunks = (BN - tail_first) * 16;  // 16-byte chunks, both halves
           for (int ch = lane; ch < chunks; ch += 32) {
@@ -315,6 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->vtail);
         }
+        L += 2u * (uint32_t)it.n_tiles;
+      }
+      if (lane == 0 && *abort) {
+        // let every copy that was issued land before the CTA goes away
+        if (n_q > 0) mbar_wait(&bars->q_full, (n_q - 1) & 1, nullptr, 0, nullptr);
+        for (uint32_t i = issued > (uint32_t)kSlots ? issued - kSlots : 0u; i < issued; ++i)
+          mbar_wait(&bars->slot_full[i % kSlots], (i / kSlots) & 1, nullptr, 0, nullptr);
       }
     } else if (warp == kSoftmaxWGs * 4 + 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -327,9 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t slot_k0 = smem_desc_sw128(ring, 16, 1024);
       const uint64_t slot_v0 = smem_desc_sw128(ring, kHalf, 1024);
       constexpr uint64_t kSlotStep = kTile >> 4;  // descriptor units per slot
-      uint32_t L = 0;  // loads consumed before the current item
-      uint32_t S = 0;  // S steps (per Q tile) before the current item
-      int k = 0;       // items done
+      uint32_t L = 0;       // loads consumed before the current item
+      uint32_t S = 0;       // S steps (per Q tile) before the current item
+      uint32_t n_tail = 0;  // earlier items whose last V tile had a cleared tail
+      int k = 0;            // items done
       bool ok = true;
       for (int r = 0; ok && item_of_round(r) < n_items; ++r, ++k) {
         const Item it = item_at(item_of_round(r));
@@ -345,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool last = j + 1 == n_tiles;
           uint64_t* second = last ? (v_tail ? &bars->vtail : &bars->slot_full[iv % kSlots])
                                   : &bars->slot_full[ik % kSlots];
-          const uint32_t second_par = last ? (v_tail ? 0u : (iv / kSlots) & 1)
+          const uint32_t second_par = last ? (v_tail ? n_tail & 1 : (iv / kSlots) & 1)
                                            : (ik / kSlots) & 1;
           return mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, second, second_par,
                             &bars->p_full[0], (S + j) & 1, a.err, kDevTimeoutMma, abort);
@@ -393,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         L += 2u * (uint32_t)n_tiles;
         S += (uint32_t)n_tiles;
+        if (v_tail) ++n_tail;
       }
       // drain: every MMA issued above has completed once this phase completes
       mma_commit(&bars->drain);
@@ -596,9 +594,7 @@ static cudaError_t launch(const Args& args, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 64) done_mask |= 1ull << dev;
   }
-  // the plain prefill runs one persistent CTA per SM over all items; a chunk
-  // runs one CTA per item
-  constexpr bool kChunk = sizeof(Args) != sizeof(PrefillArgs);
+  // one persistent CTA per SM over all items
   const long long items = (long long)a.n_mtiles * a.B * a.Hkv;
   if (items == 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -609,7 +605,7 @@ static cudaError_t launch(const Args& args, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 64) sm_count[dev] = n_sm;
   }
-  const long long grid = kChunk ? items : (items < n_sm ? items : (long long)n_sm);
+  const long long grid = items < n_sm ? items : (long long)n_sm;
   prefill_attention_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();
 }

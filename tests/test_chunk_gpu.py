@@ -224,3 +224,18 @@ def test_chunk_workload_sampled_rows(cuda_lib):
                               torch.tensor([(b, p0 + t, h) for b, t, h in rows], dtype=torch.int32))
     got = torch.stack([out[b, t, h] for b, t, h in rows])
     assert_close_attention(got, ref, w.name)
+
+
+def test_chunk_more_items_than_ctas_with_tails(cuda_lib):
+    """160 work items (five pairs of 32-token Q tiles for each of 32 (b, kv)
+    groups) on persistent CTAs, so several CTAs take more than one item, and
+    every sequence's valid keys end inside a 128-key tile (a NaN-poisoned V
+    tail to clear per item). Every output row against the oracle."""
+    B, Tq, Hq, Hkv, S = 4, 300, 32, 8, 2400
+    x = chunk_inputs(B, Tq, Hq, Hkv, S, [100, 1000, 1501, 1999], seed=33)
+    out, d = run_chunk(x)
+    ref, k_rows = oracle.prefill_chunk(x["q"], x["k"], x["v"], x["k_cache"], x["v_cache"],
+                                       x["start_pos"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    assert bool(torch.isfinite(out).all())
+    assert_close_attention(out, ref, "160 chunk items with tails")
+    check_caches(x, d, k_rows, Tq)

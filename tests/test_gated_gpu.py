@@ -336,3 +336,25 @@ def test_gated_more_items_than_pairs_full_parity(cuda_lib):
     x = inputs.gated_inputs(2, 640, 16, 2, seed=32)
     ref = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
     assert_close_attention(run_gated(x, 64, 1e7), ref, "80 pair items")
+
+
+def test_gated_chunk_more_items_than_pairs_with_tails(cuda_lib):
+    """100 pair items (ten 32-token pair tiles for each of 10 (b, kv) groups)
+    on persistent pairs, so several pairs take more than one item, each
+    sequence's valid keys ending inside a 128-key tile of NaN-poisoned cache
+    rows. Every output row and appended row against the oracle."""
+    B, Tq, Hq, Hkv, S = 5, 320, 16, 2, 2000
+    start_pos = [33, 400, 777, 1200, 1500]
+    x, kc, vc = gated_chunk_case(B, Tq, Hq, Hkv, S, start_pos, seed=34)
+    d = {k: t.cuda() for k, t in x.items()}
+    kc_d, vc_d = kc.cuda(), vc.cuda()
+    out = binding.gated_prefill_chunk(d["qg"], d["k"], d["v"], kc_d, vc_d, start_pos, d["q_w"],
+                                      d["k_w"], 64, 1e7, 1e-6)
+    torch.cuda.synchronize()
+    ref, k_rows = oracle.gated_prefill_chunk(x["qg"], x["k"], x["v"], kc, vc, start_pos,
+                                             x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    assert bool(torch.isfinite(out).all())
+    assert_close_attention(out, ref, "100 gated chunk items with tails")
+    kc_o = kc_d.cpu()
+    for b, p in enumerate(start_pos):
+        assert_within_one_ulp(kc_o[b, :, p:p + Tq].transpose(0, 1), k_rows[b], f"keys b{b}")
