@@ -146,6 +146,10 @@ q3a_status q3a_prefill_attention(const q3a_bf16* v, q3a_bf16* out,
  *   Side effect: k_cache[b, :, start_pos[b] + t] = bf16(RoPE(RMSNorm(k)))
  *   and v_cache[b, :, start_pos[b] + t] = v for t < Tq; other rows are
  *   neither read nor written.
+ *   The softmax relies on the cached keys obeying the norm bound that keys
+ *   normalised with this k_gamma obey (the precondition above); a cache that
+ *   breaks it so far that a softmax sum overflows leaves those output rows
+ *   undefined and q3a_last_device_error() returns Q3A_EINVAL.
  *   With start_pos[b] = 0 for all b this is q3a_prefill that also fills the
  *   cache; with Tq = 1 it computes what q3a_decode computes.
  *   Requires 0 <= start_pos[b] and start_pos[b] + Tq <= S_max for every b,
@@ -356,6 +360,10 @@ q3a_status q3a_gated_prefill_fill(const q3a_bf16* qg, const q3a_bf16* k, const q
  *   rows are neither written nor, past start_pos[b] + Tq, used (the kernel
  *   reads them but gives them zero weight and zeroes their values on chip, so
  *   a NaN there does not reach the output).
+ *   The softmax relies on the cached keys obeying the norm bound of keys
+ *   normalised with this k_w; a cache that breaks it so far that a softmax
+ *   sum overflows leaves those rows undefined and q3a_last_device_error()
+ *   returns Q3A_EINVAL.
  *   With every start_pos[b] = 0 this is q3a_gated_prefill_fill; with Tq = 1
  *   it computes what q3a_gated_decode computes.
  *   Requires 0 <= start_pos[b] and start_pos[b] + Tq <= S_max for every b,
@@ -435,8 +443,10 @@ q3a_status q3a_gated_decode_device_pos(const q3a_bf16* qg, const q3a_bf16* k_new
  * bytes (prefill and decode workspaces both keep it at offset 0).
  * Returns Q3A_OK when the word is zero, Q3A_ERANGE when the device-side
  * position check of q3a_decode_device_pos failed, Q3A_ETIMEOUT when a bounded
- * device wait gave up, Q3A_EINVAL for a NULL workspace, Q3A_ECUDA if the read
- * failed.
+ * device wait gave up, Q3A_EINVAL for a NULL workspace or when a chunk's
+ * cached keys broke their norm precondition so far that a softmax sum
+ * overflowed, Q3A_ECUDA if the read failed. The prologue of each prefill or
+ * chunk call clears the word.
  * ------------------------------------------------------------------------- */
 q3a_status q3a_last_device_error(const void* workspace, void* stream);
 

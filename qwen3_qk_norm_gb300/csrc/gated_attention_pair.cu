@@ -631,6 +631,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       named_barrier_sync(1, kSoftmaxWGs * 128);
       if (ok) {
         l = (lsum[r] + lsum[128 + r]) + (lsum[256 + r] + lsum[384 + r]);
+        // with the fixed shift only a key far outside the norm bound (a cache
+        // breaking its precondition) can overflow the sum: report it
+        if (store && fixed_max && !(l <= 3.0e38f)) record_error(a.err, kErrWordBound);
         ok = __all_sync(kFull, mbar_wait_cluster(&bars->o_final, k & 1, a.err,
                                                  kDevTimeoutEpilogue, abort));
       }

@@ -420,7 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const Item it = item_at(item);
         n_tiles = it.n_tiles;
-        tok_pos = it.p0 + it.t0 + t * tile_tok + r / g;  // position of this row's token
+        // position of this row's token; padding rows of a chunk (tokens past
+        // its end) stop at the last valid key, so they never read cache rows
+        // past the valid keys
+        const int tok = it.t0 + t * tile_tok + r / g;
+        tok_pos = it.p0 + (kChunk ? min(tok, a.T - 1) : tok);
       }
       float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
       float l = 0.f;
@@ -533,6 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok = it.t0 + t * tile_tok + r / g;
         const float inv_l = 1.0f / l;
         const bool store = tok < a.T;  // rows of tokens past the chunk are padding
+        // with the fixed shift only a key far outside the norm bound (a cache
+        // breaking its precondition) can overflow the sum: report it
+        if (fixed_max && store && !(l <= 3.0e38f)) record_error(a.err, kErrWordBound);
         uint16_t* orow = a.out +
                          (((long long)it.b * a.T + tok) * a.Hq + (long long)it.kv * g + (r % g)) *
                              128 +

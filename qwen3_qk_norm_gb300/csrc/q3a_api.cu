@@ -268,11 +268,9 @@ q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf1
   if (!start_pos) return Q3A_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
   if (ws_bytes < q3a_prefill_chunk_workspace_size(B, Tq, Hq, Hkv, d)) return Q3A_EINVAL;
-  bool all_at_zero = true;
   for (int b = 0; b < B; ++b) {
     const int32_t p = start_pos[b];
     if (p < 0 || (long long)p + Tq > S_max) return Q3A_ERANGE;  // nothing written yet
-    all_at_zero = all_at_zero && p == 0;
   }
   const int g = Hq / Hkv;
   uint16_t* qhat = ws_qhat(workspace);
@@ -303,9 +301,11 @@ q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf1
   pa.g = g;
   const int rows_tok = prefill_tokens_per_cta(g);
   pa.n_mtiles = (Tq + rows_tok - 1) / rows_tok;
-  // cached keys come from earlier calls: only a chunk with no cached keys
-  // may use the logit bound of this call's gammas
-  ca.fixed_shift_ok = all_at_zero ? 1 : 0;
+  // cached keys were normalised with the same k_gamma by earlier calls (the
+  // documented precondition), so the logit bound holds for them too; a cache
+  // that breaks it badly enough to overflow a softmax sum is reported
+  // (kErrWordBound)
+  ca.fixed_shift_ok = 1;
   for (int b = 0; b < B; ++b) ca.pos_b[b] = start_pos[b];
 
   RopeArgs ra;
@@ -703,11 +703,9 @@ q3a_status q3a_gated_prefill_chunk(const q3a_bf16* qg, const q3a_bf16* k, const 
   if (!start_pos) return Q3A_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return Q3A_EINVAL;
   if (ws_bytes < q3a_gated_prefill_chunk_workspace_size(B, Tq, Hq, Hkv, d)) return Q3A_EINVAL;
-  bool all_at_zero = true;
   for (int b = 0; b < B; ++b) {
     const int32_t p = start_pos[b];
     if (p < 0 || (long long)p + Tq > S_max) return Q3A_ERANGE;  // nothing written yet
-    all_at_zero = all_at_zero && p == 0;
   }
   const int g = Hq / Hkv;
   uint16_t* qhat = gated_ws_q(workspace);
@@ -744,9 +742,11 @@ q3a_status q3a_gated_prefill_chunk(const q3a_bf16* qg, const q3a_bf16* k, const 
   const int tok = gated_tokens_per_cta(g);
   aa.n_mtiles = (Tq + tok - 1) / tok;
   aa.v_head_major = 1;
-  // cached keys come from earlier calls: only a chunk with no cached keys
-  // may use the logit bound of this call's weights
-  ca.fixed_shift_ok = all_at_zero ? 1 : 0;
+  // cached keys were normalised with the same k_w by earlier calls (the
+  // documented precondition), so the logit bound holds for them too; a cache
+  // that breaks it badly enough to overflow a softmax sum is reported
+  // (kErrWordBound)
+  ca.fixed_shift_ok = 1;
   for (int b = 0; b < B; ++b) ca.pos_b[b] = start_pos[b];
 
   // Q -> Qhat [B, Tq, Hq]; K -> k_cache rows start_pos[b] + t (normalised,
@@ -872,7 +872,9 @@ q3a_status q3a_last_device_error(const void* workspace, void* stream) {
     return Q3A_ECUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return Q3A_ECUDA;
   if (word == 0) return Q3A_OK;
-  return word == kErrWordRange ? Q3A_ERANGE : Q3A_ETIMEOUT;
+  if (word == kErrWordRange) return Q3A_ERANGE;
+  if (word == kErrWordBound) return Q3A_EINVAL;
+  return Q3A_ETIMEOUT;
 }
 
 }  // extern "C"

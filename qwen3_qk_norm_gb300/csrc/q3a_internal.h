@@ -119,6 +119,9 @@ struct DecodeArgs {
 
 // error word value of a device-side position check that failed
 constexpr uint32_t kErrWordRange = 0x201;
+// error word value when a chunk's softmax sum overflowed: its cached keys
+// exceed the norm bound that this library's keys obey by far
+constexpr uint32_t kErrWordBound = 0x301;
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);        // d = 128
 cudaError_t launch_gated_decode(const DecodeArgs& a, cudaStream_t stream);  // d = 256

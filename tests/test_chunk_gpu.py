@@ -239,3 +239,31 @@ def test_chunk_more_items_than_ctas_with_tails(cuda_lib):
     assert bool(torch.isfinite(out).all())
     assert_close_attention(out, ref, "160 chunk items with tails")
     check_caches(x, d, k_rows, Tq)
+
+
+@pytest.mark.parametrize("scale,expect_error", [(1.5, False), (1.0e4, True)])
+def test_chunk_cache_above_the_bound(cuda_lib, scale, expect_error):
+    """The chunk's softmax shift comes from the norm bound of keys written by
+    this library. Cached keys 1.5 times too long break the bound, but the shift
+    cancels: the output still matches the oracle. Keys 10^4 times too long
+    overflow the softmax sum: the call reports Q3A_EINVAL through the error
+    word instead of returning silent NaN."""
+    B, Tq, Hq, Hkv, S = 2, 40, 16, 4, 600
+    x = chunk_inputs(B, Tq, Hq, Hkv, S, [300, 450], seed=35)
+    for b, p in enumerate([300, 450]):
+        x["k_cache"][b, :, :p] = (x["k_cache"][b, :, :p].float() * scale).to(torch.bfloat16)
+    d = {k: (t.cuda() if k != "start_pos" else t) for k, t in x.items()}
+    ws = torch.empty(binding.prefill_chunk_workspace_size(B, Tq, Hq, Hkv), dtype=torch.uint8,
+                     device="cuda")
+    out = binding.prefill_chunk(d["q"], d["k"], d["v"], d["k_cache"], d["v_cache"],
+                                d["start_pos"], d["q_gamma"], d["k_gamma"], 1e6, 1e-6,
+                                workspace=ws)
+    torch.cuda.synchronize()
+    status = binding.last_device_error(ws)
+    if expect_error:
+        assert status == binding.Q3A_EINVAL
+    else:
+        assert status == binding.Q3A_OK
+        ref, _ = oracle.prefill_chunk(x["q"], x["k"], x["v"], x["k_cache"], x["v_cache"],
+                                      x["start_pos"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+        assert_close_attention(out, ref, "cache keys x1.5")

@@ -358,3 +358,30 @@ def test_gated_chunk_more_items_than_pairs_with_tails(cuda_lib):
     kc_o = kc_d.cpu()
     for b, p in enumerate(start_pos):
         assert_within_one_ulp(kc_o[b, :, p:p + Tq].transpose(0, 1), k_rows[b], f"keys b{b}")
+
+
+@pytest.mark.parametrize("scale,expect_error", [(1.5, False), (1.0e4, True)])
+def test_gated_chunk_cache_above_the_bound(cuda_lib, scale, expect_error):
+    """As for the Qwen3 chunk: cached keys 1.5 times longer than this library
+    writes them still give the oracle's output (the shift cancels); keys 10^4
+    times too long overflow the softmax sum and the call reports Q3A_EINVAL."""
+    B, Tq, Hq, Hkv, S = 2, 40, 16, 2, 600
+    start_pos = [300, 450]
+    x, kc, vc = gated_chunk_case(B, Tq, Hq, Hkv, S, start_pos, seed=36)
+    for b, p in enumerate(start_pos):
+        kc[b, :, :p] = (kc[b, :, :p].float() * scale).to(torch.bfloat16)
+    d = {k: t.cuda() for k, t in x.items()}
+    kc_d, vc_d = kc.cuda(), vc.cuda()
+    ws = torch.empty(binding.gated_prefill_chunk_workspace_size(B, Tq, Hq, Hkv),
+                     dtype=torch.uint8, device="cuda")
+    out = binding.gated_prefill_chunk(d["qg"], d["k"], d["v"], kc_d, vc_d, start_pos, d["q_w"],
+                                      d["k_w"], 64, 1e7, 1e-6, workspace=ws)
+    torch.cuda.synchronize()
+    status = binding.last_device_error(ws)
+    if expect_error:
+        assert status == binding.Q3A_EINVAL
+    else:
+        assert status == binding.Q3A_OK
+        ref, _ = oracle.gated_prefill_chunk(x["qg"], x["k"], x["v"], kc, vc, start_pos,
+                                            x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+        assert_close_attention(out, ref, "gated cache keys x1.5")
