@@ -66,8 +66,10 @@
 // last V tile past the valid keys hold whatever the cache holds there (a
 // probability of 0 times a NaN is NaN), so the producer warp clears them in
 // shared memory before the MMA issuer is allowed to read that tile. Cached
-// keys were normalised by earlier calls, so the fixed shift (which relies on
-// this call's gammas) is used only when no sequence has cached keys.
+// keys were normalised by earlier calls with the same gamma (the cache's
+// precondition), so the fixed shift holds for them too; the shift cancels in
+// the normalisation, and only a cache breaking the bound so far that a row
+// sum overflows changes the result, which the epilogue reports.
 //
 // Every mbarrier wait is bounded (q3a_device.cuh); a timeout sets the error
 // word, all roles unwind, in-flight copies and MMAs are drained and TMEM is
