@@ -33,3 +33,14 @@ def test_gated_decode_bytes_count_query_and_gate_rows():
     # cache 10 rows x (K + V) x 8 B = 160; q|gate 2 x 16 B + k_new, v_new 2 x 8 B + w's 16 B;
     # writes: appended K, V 16 B + out 2 x 8 B
     assert gated_decode_bytes([10], 2, 1, 4) == 160 + (32 + 16 + 16) + (16 + 16)
+
+
+def test_chunk_flops_at_head_dim_256():
+    """The gated chunk's work at d = 256: a chunk at position 0 is the gated
+    prefill's work, and the bench's Qwen3-Next chunk (4 x 1024 tokens after
+    3072 cached, 16 heads) is 4 * 256 * 16 * sum_b sum_t (3072 + t + 1)."""
+    assert (accounting.chunk_flops([0, 0, 0], 50, 16, 256)
+            == accounting.prefill_flops(3, 50, 16, 256))
+    per_seq = sum(3072 + t + 1 for t in range(1024))
+    assert accounting.chunk_flops([3072] * 4, 1024, 16, 256) == 4 * 256 * 16 * 4 * per_seq
+    assert accounting.chunk_flops([3072] * 4, 1024, 16, 256) == 240551723008  # 4·256·16·4·(1024·3072 + 1024·1025/2)
