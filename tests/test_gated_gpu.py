@@ -385,3 +385,35 @@ def test_gated_chunk_cache_above_the_bound(cuda_lib, scale, expect_error):
         ref, _ = oracle.gated_prefill_chunk(x["qg"], x["k"], x["v"], kc, vc, start_pos,
                                             x["q_w"], x["k_w"], 64, 1e7, 1e-6)
         assert_close_attention(out, ref, "gated cache keys x1.5")
+
+
+@pytest.mark.parametrize("d_r", [16, 48, 128, 240])
+def test_gated_rotary_widths(cuda_lib, d_r):
+    """Every rotary width the entry points accept is a multiple of 16: the
+    prologue's lane layout (d_r / 8 lanes holding rotated pairs) and the decode
+    kernel's rotation take other shapes than at 64 and 256. Prologue rows to
+    one bf16 ulp, prefill and decode outputs against the oracle."""
+    B, T, Hq, Hkv = 2, 45, 8, 2
+    x = inputs.gated_inputs(B, T, Hq, Hkv, seed=40 + d_r)
+    d = {k: t.cuda() for k, t in x.items()}
+    ws = torch.zeros(binding.gated_prefill_workspace_size(B, T, Hq, Hkv), dtype=torch.uint8,
+                     device="cuda")
+    binding.gated_prefill_prologue(d["qg"], d["k"], d["q_w"], d["k_w"], d_r, 1e7, 1e-6, ws)
+    torch.cuda.synchronize()
+    qhat, khat = workspace_views(ws, B, T, Hq, Hkv)
+    assert_within_one_ulp(qhat, oracle.gated_qknorm_rope(x["qg"], x["q_w"], D, d_r, 1e7, 1e-6),
+                          f"qhat d_r {d_r}")
+    assert_within_one_ulp(khat.permute(0, 2, 1, 3),
+                          oracle.gated_qknorm_rope(x["k"], x["k_w"], D, d_r, 1e7, 1e-6),
+                          f"khat d_r {d_r}")
+    out = run_gated(x, d_r, 1e7)
+    ref = oracle.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], d_r, 1e7, 1e-6)
+    assert_close_attention(out, ref, f"gated prefill d_r {d_r}")
+    y = inputs.gated_decode_inputs(3, Hq, Hkv, 600, 0, 1, seed=41 + d_r, start_pos=[0, 129, 599])
+    dy = {k: (t.cuda() if k != "start_pos" else t) for k, t in y.items()}
+    o2 = binding.gated_decode(dy["qg"], dy["k_new"], dy["v_new"], dy["k_cache"], dy["v_cache"],
+                              y["start_pos"], dy["q_w"], dy["k_w"], d_r, 1e7, 1e-6)
+    torch.cuda.synchronize()
+    r2, _ = oracle.gated_decode(y["qg"], y["k_new"], y["v_new"], y["k_cache"], y["v_cache"],
+                                y["start_pos"], y["q_w"], y["k_w"], d_r, 1e7, 1e-6)
+    assert_close_attention(o2, r2, f"gated decode d_r {d_r}")
