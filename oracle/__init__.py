@@ -61,6 +61,9 @@ def _load():
             lib.q3a_oracle_qknorm_rope.restype = i
             lib.q3a_oracle_prefill.argtypes = [_u16p] * 5 + [i] * 5 + [d, d, _f64p]
             lib.q3a_oracle_prefill.restype = i
+            lib.q3a_oracle_prefill_rounded.argtypes = [_u16p] * 5 + [i] * 5 + [d, d, i, _f64p]
+            lib.q3a_oracle_prefill_rounded.restype = i
+            lib.q3a_oracle_round_bf16.argtypes = [_f64p, l, _f64p]
             lib.q3a_oracle_prefill_rows.argtypes = ([_u16p] * 5 + [i] * 5 + [d, d, l]
                                                     + [ctypes.c_void_p] * 3 + [_f64p])
             lib.q3a_oracle_prefill_rows.restype = i
@@ -154,6 +157,34 @@ def prefill(q, k, v, q_gamma, k_gamma, theta: float, eps: float) -> torch.Tensor
     if rc:
         raise ValueError(f"oracle prefill failed ({rc})")
     return out
+
+
+def prefill_rounded(q, k, v, q_gamma, k_gamma, theta: float, eps: float,
+                    roundings: int = 1) -> torch.Tensor:
+    """The full causal prefill with qhat and khat rounded to bf16 (nearest,
+    ties to even): after RoPE only (``roundings=1``, the bf16 operands of the
+    attention products), or after the norm and again after RoPE
+    (``roundings=2``, the casts of §7.2.1's RMSNorm and apply_rope). Every other
+    step in fp64. -> fp64 [B,T,Hq,d]."""
+    q, k, v = _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v")
+    q_gamma, k_gamma = _bf16(q_gamma, "q_gamma"), _bf16(k_gamma, "k_gamma")
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    out = torch.empty((B, T, Hq, d), dtype=torch.float64)
+    rc = _load().q3a_oracle_prefill_rounded(_ptr(q), _ptr(k), _ptr(v), _ptr(q_gamma),
+                                            _ptr(k_gamma), B, T, Hq, Hkv, d, float(theta),
+                                            float(eps), int(roundings), _ptr(out))
+    if rc:
+        raise ValueError(f"oracle prefill_rounded failed ({rc})")
+    return out
+
+
+def round_bf16(x: torch.Tensor) -> torch.Tensor:
+    """fp64 values rounded to the nearest bf16 value (ties to even), as fp64."""
+    x = x.to(torch.float64).contiguous()
+    y = torch.empty_like(x)
+    _load().q3a_oracle_round_bf16(_ptr(x), x.numel(), _ptr(y))
+    return y
 
 
 def prefill_rows(q, k, v, q_gamma, k_gamma, theta: float, eps: float,

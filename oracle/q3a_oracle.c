@@ -42,11 +42,21 @@
  *           §20.3: the new K is rotated at start_pos and concatenated; old K
  *           already carries its position.
  *
+ *   rounded  the same prefill with qhat and khat rounded to bf16 (nearest,
+ *           ties to even) where a bf16 model rounds them: after step 2 only
+ *           (roundings = 1: the tensors a bf16 attention multiplies), or after
+ *           step 1 and again after step 2 (roundings = 2: §7.2.1's RMSNorm
+ *           returns .to(input_dtype) and apply_rope returns .to(x.dtype)).
+ *           Everything else stays fp64. With large gammas the logits are large
+ *           and these roundings alone move the output by more than the bf16
+ *           output tolerance; this variant is the reference for that regime.
+ *
  * Readings where the pages are silent or disagree (kept in the design notes):
  *   - norm BEFORE RoPE (four pages and the quoted transformers code; the
  *     Qwen1->3 blog page says the opposite);
- *   - no rounding of the normalised or rotated values (the pages' code rounds
- *     to the model dtype after each step; the tolerance of the tests covers it);
+ *   - no rounding of the normalised or rotated values in the plain functions
+ *     (the pages' code rounds to the model dtype after each step; the
+ *     tolerance of the tests covers it at the workloads' gammas);
  *   - prefill positions start at 0.
  *
  * All entry points return 0 on success and a negative value on a bad argument.
@@ -65,6 +75,27 @@ static double widen_bf16(uint16_t bits) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/* fp64 -> nearest bf16 value (8 significant bits, ties to even; subnormal
+ * spacing 2^-133; beyond the largest finite bf16 -> infinity), as fp64. */
+static double round_bf16(double x) {
+  if (!isfinite(x) || x == 0.0) return x;
+  int e;
+  (void)frexp(x, &e); /* |x| = m 2^e, 0.5 <= m < 1 */
+  int q = e - 8;      /* spacing of bf16 values at |x| */
+  if (q < -133) q = -133;
+  double y = ldexp(nearbyint(ldexp(x, -q)), q); /* default mode: ties to even */
+  if (fabs(y) > 3.3895313892515355e38) return copysign(INFINITY, x);
+  return y;
+}
+
+void q3a_oracle_round_bf16(const double* x, long n, double* y) {
+  for (long i = 0; i < n; ++i) y[i] = round_bf16(x[i]);
+}
+
+static void round_row(double* y, int d) {
+  for (int c = 0; c < d; ++c) y[c] = round_bf16(y[c]);
 }
 
 static int g_threads = 0; /* 0: OpenMP default */
@@ -157,10 +188,39 @@ static int check_shape(int B, int T, int Hq, int Hkv, int d) {
   return 0;
 }
 
+/* steps 1-2 on one row, with the bf16 roundings of the "rounded" variant */
+static void norm_rope_rounded(const uint16_t* x, const uint16_t* gamma, int d, double eps,
+                              double pos, double theta, int roundings, double* y) {
+  q3a_oracle_rmsnorm_row(x, gamma, d, eps, y);
+  if (roundings >= 2) round_row(y, d);
+  q3a_oracle_rope_row(y, d, pos, theta);
+  if (roundings >= 1) round_row(y, d);
+}
+
+static int prefill_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const uint16_t* q_gamma, const uint16_t* k_gamma, int B, int T, int Hq,
+                        int Hkv, int d, double theta, double eps, int roundings, double* out);
+
 /* Full causal prefill. q [B,T,Hq,d], k/v [B,T,Hkv,d] bf16; out fp64 [B,T,Hq,d]. */
 int q3a_oracle_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                        const uint16_t* q_gamma, const uint16_t* k_gamma, int B, int T, int Hq,
                        int Hkv, int d, double theta, double eps, double* out) {
+  return prefill_impl(q, k, v, q_gamma, k_gamma, B, T, Hq, Hkv, d, theta, eps, 0, out);
+}
+
+/* The prefill with qhat and khat rounded to bf16: roundings = 1 after step 2,
+ * roundings = 2 after step 1 and after step 2 (see the header). */
+int q3a_oracle_prefill_rounded(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const uint16_t* q_gamma, const uint16_t* k_gamma, int B, int T,
+                               int Hq, int Hkv, int d, double theta, double eps, int roundings,
+                               double* out) {
+  if (roundings < 0 || roundings > 2) return -1;
+  return prefill_impl(q, k, v, q_gamma, k_gamma, B, T, Hq, Hkv, d, theta, eps, roundings, out);
+}
+
+static int prefill_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const uint16_t* q_gamma, const uint16_t* k_gamma, int B, int T, int Hq,
+                        int Hkv, int d, double theta, double eps, int roundings, double* out) {
   if (check_shape(B, T, Hq, Hkv, d) || !q || !k || !v || !q_gamma || !k_gamma || !out) return -1;
   int g = Hq / Hkv;
   long krows = (long)B * T * Hkv;
@@ -179,8 +239,7 @@ int q3a_oracle_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     long b = r / ((long)T * Hkv), t = (r / Hkv) % T, kv = r % Hkv;
     double* kd = khat + (((b * Hkv + kv) * T) + t) * d;
     double* vd = vals + (((b * Hkv + kv) * T) + t) * d;
-    q3a_oracle_rmsnorm_row(k + r * d, k_gamma, d, eps, kd);
-    q3a_oracle_rope_row(kd, d, (double)t, theta);
+    norm_rope_rounded(k + r * d, k_gamma, d, eps, (double)t, theta, roundings, kd);
     for (int c = 0; c < d; ++c) vd[c] = widen_bf16(v[r * d + c]);
   }
   long qrows = (long)B * T * Hq;
@@ -203,8 +262,7 @@ int q3a_oracle_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
       for (long r = 0; r < qrows; ++r) {
         long b = r / ((long)T * Hq), i = (r / Hq) % T, h = r % Hq;
         long kv = h / g;
-        q3a_oracle_rmsnorm_row(q + r * d, q_gamma, d, eps, qhat);
-        q3a_oracle_rope_row(qhat, d, (double)i, theta);
+        norm_rope_rounded(q + r * d, q_gamma, d, eps, (double)i, theta, roundings, qhat);
         const double* kb = khat + (b * Hkv + kv) * (long)T * d;
         const double* vb = vals + (b * Hkv + kv) * (long)T * d;
         attend_row(qhat, kb, vb, i + 1, d, scores, out + r * d);
