@@ -126,34 +126,6 @@ def test_gated_is_deterministic(cuda_lib):
     assert torch.equal(a, b)
 
 
-def sample_rows(B, T, Hq, n, seed):
-    g = torch.Generator().manual_seed(seed)
-    fixed = [(0, 0, 0), (B - 1, T - 1, Hq - 1), (0, T - 1, 0), (B - 1, 63, 1 % Hq),
-             (0, 64, Hq // 2), (0, min(T - 1, 4095), Hq - 1)]
-    rnd = [(int(torch.randint(0, B, (1,), generator=g)), int(torch.randint(0, T, (1,), generator=g)),
-            int(torch.randint(0, Hq, (1,), generator=g))) for _ in range(n)]
-    return torch.tensor(fixed + rnd, dtype=torch.int32)
-
-
-@pytest.mark.slow
-@pytest.mark.parametrize("name", ["qwen3-next-80b-gated-b4-t4096", "qwen3.5-397b-gated-b1-t8192"])
-def test_gated_full_size_sampled_rows(cuda_lib, name):
-    """Full-size workloads, launched as the benchmark launches them; sampled
-    output rows against the oracle computed one by one."""
-    w = WORKLOADS[name]
-    x = inputs.workload_inputs(w, device="cuda")
-    out = binding.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], w.d_r, w.theta,
-                                w.eps)
-    torch.cuda.synchronize()
-    assert bool(torch.isfinite(out).all())
-    rows = sample_rows(w.B, w.T, w.Hq, 30, seed=w.seed)
-    cpu = {k: t.cpu() for k, t in x.items()}
-    ref = oracle.gated_prefill_rows(cpu["qg"], cpu["k"], cpu["v"], cpu["q_w"], cpu["k_w"], w.d_r,
-                                    w.theta, w.eps, rows)
-    got = torch.stack([out[b, t, h] for b, t, h in rows.tolist()])
-    assert_close_attention(got, ref, name)
-
-
 def test_gated_prefill_fill_writes_caches_and_matches_prefill(cuda_lib):
     """The cache-filling prefill gives the plain gated prefill's output bits and
     leaves the normalised, rotated keys and the values in cache rows 0..T-1."""
@@ -294,39 +266,6 @@ def test_gated_chunk_erange_writes_nothing(cuda_lib):
     torch.cuda.synchronize()
     assert torch.equal(kc_d.cpu().view(torch.int16), kc.view(torch.int16))
     assert bool((out == 3.0).all())
-
-
-@pytest.mark.slow
-def test_gated_chunk_workload_sampled_rows(cuda_lib):
-    """The gated chunk workload as the benchmark launches it (each prompt's
-    first 3072 tokens written by a chunk from position 0, then the last 1024
-    as one chunk); sampled rows against the oracle's gated prefill rows of the
-    whole prompt, computed one by one."""
-    w = WORKLOADS["qwen3-next-80b-gated-chunk-b4-t1024-at3072"]
-    x = inputs.workload_inputs(w, device="cuda")
-    p0 = w.sp_lo
-    kc = torch.full((w.B, w.Hkv, w.S_max, D), float("nan"), dtype=torch.bfloat16, device="cuda")
-    vc = torch.full_like(kc, float("nan"))
-    sl = lambda t, a, b: t[:, a:b].contiguous()  # noqa: E731
-    binding.gated_prefill_chunk(sl(x["qg"], 0, p0), sl(x["k"], 0, p0), sl(x["v"], 0, p0), kc, vc,
-                                [0] * w.B, x["q_w"], x["k_w"], w.d_r, w.theta, w.eps)
-    out = binding.gated_prefill_chunk(sl(x["qg"], p0, None), sl(x["k"], p0, None),
-                                      sl(x["v"], p0, None), kc, vc, [p0] * w.B, x["q_w"],
-                                      x["k_w"], w.d_r, w.theta, w.eps)
-    torch.cuda.synchronize()
-    assert bool(torch.isfinite(out).all())
-    g = torch.Generator().manual_seed(w.seed)
-    rows = [(0, 0, 0), (w.B - 1, w.T - 1, w.Hq - 1)]
-    rows += [(int(torch.randint(0, w.B, (1,), generator=g)),
-              int(torch.randint(0, w.T, (1,), generator=g)),
-              int(torch.randint(0, w.Hq, (1,), generator=g))) for _ in range(24)]
-    cpu = {k: t.cpu() for k, t in x.items()}
-    ref = oracle.gated_prefill_rows(cpu["qg"], cpu["k"], cpu["v"], cpu["q_w"], cpu["k_w"], w.d_r,
-                                    w.theta, w.eps,
-                                    torch.tensor([(b, p0 + t, h) for b, t, h in rows],
-                                                 dtype=torch.int32))
-    got = torch.stack([out[b, t, h] for b, t, h in rows])
-    assert_close_attention(got, ref, w.name)
 
 
 def test_gated_more_items_than_pairs_full_parity(cuda_lib):
