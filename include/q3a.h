@@ -256,10 +256,18 @@ q3a_status q3a_decode_device_pos(const q3a_bf16* q, const q3a_bf16* k_new,
  *   S = max over b of ceil((start_pos[b] + 1) / 1024) and g = Hq / Hkv; a
  *   call that needs more than Q3A_DECODE_NOALLOC_SCRATCH_BYTES returns
  *   Q3A_EINVAL before anything is launched or written.
+ *   Device-side errors: its kernels keep their error word at the start of the
+ *   array; q3a_last_device_error(NULL, stream) reads it for the current
+ *   device (Q3A_ETIMEOUT if a bounded wait of the last call gave up).
  *   No allocation: it calls no cudaMalloc, cudaFree or allocating routine.
  *   Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and keeps it; make that
- *   first call before any stream capture on the device.
+ *   (cudaGetSymbolAddress, with that device current) and keeps it. Under
+ *   CUDA's default lazy module loading that first lookup also loads the
+ *   library's device code on the device, which reserves the array and can
+ *   synchronise: make one warm-up call outside any latency-critical loop, and
+ *   before any stream capture on the device. The address is kept for the
+ *   life of the process: do not use this entry point after cudaDeviceReset
+ *   (or in a different primary context) of a device it has already run on.
  *   Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents (the error word is cleared at the start of each call).
  *   Calls whose executions overlap on the GPU (different streams, or several
@@ -438,12 +446,31 @@ q3a_status q3a_gated_decode_device_pos(const q3a_bf16* qg, const q3a_bf16* k_new
                                        void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * q3a_selftest_bounded_wait — a diagnostic: one block of 32 threads waits on
+ * an mbarrier through the bounded-wait routine that every kernel of this
+ * library uses, with a wait limit of `limit_cycles` SM cycles
+ * (1 .. about 2 s of cycles). With arrive == 0 nothing arrives: the wait gives
+ * up, writes its timeout code into the error word at the start of `workspace`
+ * (>= 256 bytes, 16-byte aligned, device memory) and the kernel returns, so
+ * q3a_last_device_error(workspace) then reports Q3A_ETIMEOUT; with arrive != 0
+ * the barrier completes and the word stays zero. It lets a caller check, on
+ * its own GPU, that a device-side wait that runs out is reported as an error
+ * and leaves the context usable (the clear-error rule of "Chapter 20, Qwen3
+ * and Qwen3.5" §20.9), without faulting or hanging the device.
+ * Returns Q3A_EINVAL for a bad workspace or limit (nothing launched).
+ * ------------------------------------------------------------------------- */
+q3a_status q3a_selftest_bounded_wait(void* workspace, size_t ws_bytes, long long limit_cycles,
+                                     int arrive, void* stream);
+
+/* ---------------------------------------------------------------------------
  * q3a_last_device_error — reads, synchronously on `stream`, the error word
  * that the kernels of the last call which used `workspace` left in its first
  * bytes (prefill and decode workspaces both keep it at offset 0).
+ * With workspace == NULL it reads the error word of q3a_decode_noalloc (in
+ * that entry point's static array) on the current device.
  * Returns Q3A_OK when the word is zero, Q3A_ERANGE when the device-side
  * position check of q3a_decode_device_pos failed, Q3A_ETIMEOUT when a bounded
- * device wait gave up, Q3A_EINVAL for a NULL workspace or when a chunk's
+ * device wait gave up, Q3A_EINVAL when a chunk's
  * cached keys broke their norm precondition so far that a softmax sum
  * overflowed, Q3A_ECUDA if the read failed. The prologue of each prefill or
  * chunk call clears the word.

@@ -27,7 +27,7 @@ EXPORTED = ["q3a_status_string", "q3a_qknorm_rope", "q3a_prefill_workspace_size"
             "q3a_gated_decode_workspace_size", "q3a_gated_decode",
             "q3a_gated_decode_device_pos", "q3a_gated_prefill_fill_workspace_size",
             "q3a_gated_prefill_fill", "q3a_gated_prefill_chunk_workspace_size",
-            "q3a_gated_prefill_chunk"]
+            "q3a_gated_prefill_chunk", "q3a_selftest_bounded_wait"]
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +84,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_decode_noalloc.restype = i
         lib.q3a_last_device_error.argtypes = [vp, vp]
         lib.q3a_last_device_error.restype = i
+        lib.q3a_selftest_bounded_wait.argtypes = [vp, sz, ctypes.c_longlong, i, vp]
+        lib.q3a_selftest_bounded_wait.restype = i
         lib.q3a_gated_prefill_workspace_size.argtypes = [i] * 5
         lib.q3a_gated_prefill_workspace_size.restype = sz
         lib.q3a_gated_prefill.argtypes = [vp] * 6 + [i] * 6 + [d, f, vp, sz, vp]
@@ -320,9 +322,24 @@ def decode_device_pos(q, k_new, v_new, k_cache, v_cache, start_pos, q_gamma, k_g
     return out
 
 
-def last_device_error(workspace: torch.Tensor) -> int:
-    """Status from the error word a call left in its workspace (synchronises)."""
+def last_device_error(workspace: torch.Tensor | None) -> int:
+    """Status from the error word a call left in its workspace (synchronises).
+    ``None`` reads the error word of q3a_decode_noalloc on the current device."""
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        return int(load().q3a_last_device_error(None, _stream(dev)))
     return int(load().q3a_last_device_error(workspace.data_ptr(), _stream(workspace.device)))
+
+
+def selftest_bounded_wait(workspace: torch.Tensor, limit_cycles: int, arrive: bool) -> None:
+    """Launches the bounded-wait self-test (one block waiting on an mbarrier
+    that completes only if ``arrive``); read the outcome with
+    ``last_device_error(workspace)``."""
+    _check(workspace, "workspace", dtype=torch.uint8)
+    st = load().q3a_selftest_bounded_wait(workspace.data_ptr(), workspace.numel(),
+                                          int(limit_cycles), int(bool(arrive)),
+                                          _stream(workspace.device))
+    _raise(st, "q3a_selftest_bounded_wait")
 
 
 # ---------------------------------------------------------------------------

@@ -865,7 +865,11 @@ q3a_status q3a_gated_decode_device_pos(const q3a_bf16* qg, const q3a_bf16* k_new
 }
 
 q3a_status q3a_last_device_error(const void* workspace, void* stream) {
-  if (!workspace) return Q3A_EINVAL;
+  if (!workspace) {  // q3a_decode_noalloc's error word on the current device
+    void* p = nullptr;
+    if (noalloc_error_word(&p) != cudaSuccess) return Q3A_ECUDA;
+    workspace = p;
+  }
   uint32_t word = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)

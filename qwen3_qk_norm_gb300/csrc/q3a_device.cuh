@@ -23,6 +23,7 @@ enum DeviceError : uint32_t {
   kDevTimeoutSoftmax = 0x103,
   kDevTimeoutEpilogue = 0x104,
   kDevTimeoutDecode = 0x105,
+  kDevTimeoutSelftest = 0x106,  // the bounded-wait self-test below its limit
 };
 
 // about two seconds at the GB300's SM clocks
@@ -93,21 +94,23 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 constexpr uint32_t kSuspendHintNs = 20000;
 
 // Wait until the phase with the given parity has completed. Returns false
-// (and records `code`) if it did not complete within kWaitLimitCycles, or if
-// another thread of the CTA already gave up (*abort set). kSleep: the thread
-// sleeps in hardware between checks (for warps that share a scheduler with
-// busy ones); otherwise it polls, which reacts faster (for a latency-critical
-// single thread such as an MMA issuer).
+// (and records `code`) if it did not complete within `limit` SM cycles
+// (kWaitLimitCycles unless a caller passes a shorter one), or if another
+// thread of the CTA already gave up (*abort set). kSleep: the thread sleeps in
+// hardware between checks (for warps that share a scheduler with busy ones);
+// otherwise it polls, which reacts faster (for a latency-critical single
+// thread such as an MMA issuer).
 template <bool kSleep = true>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
-                                          uint32_t code, volatile int* abort) {
+                                          uint32_t code, volatile int* abort,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (kSleep ? mbar_try_wait_sleep(bar, parity, kSuspendHintNs) : mbar_try_wait(bar, parity))
       return true;
     if (abort && *abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       record_error(err, code);
       if (abort) *abort = 1;
       return false;
@@ -471,7 +474,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// packed fp32 pairs (Blackwell f32x2 pipes): d = a * b + c, d = a + b
+// packed fp32 pairs (Blackwell f32x2 pipes): d = a * b + c, a * b, a - b, a + b
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -483,6 +486,16 @@ __device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {

@@ -124,6 +124,8 @@ constexpr uint32_t kErrWordRange = 0x201;
 constexpr uint32_t kErrWordBound = 0x301;
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);        // d = 128
+// device address of q3a_decode_noalloc's error word on the current device
+cudaError_t noalloc_error_word(void** out);
 cudaError_t launch_gated_decode(const DecodeArgs& a, cudaStream_t stream);  // d = 256
 
 // ----- K5/K6: gated global attention of Qwen3-Next / Qwen3.5 (d = 256) ------

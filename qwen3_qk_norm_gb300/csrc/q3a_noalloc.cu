@@ -55,6 +55,11 @@ cudaError_t scratch_address(void** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// The error word of q3a_decode_noalloc on the current device (offset 0 of the
+// scratch array), for q3a_last_device_error(NULL, stream).
+cudaError_t noalloc_error_word(void** out) { return scratch_address(out); }
+
 }  // namespace q3a
 
 using namespace q3a;

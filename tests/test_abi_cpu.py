@@ -277,3 +277,11 @@ def test_gated_prefill_chunk_host_checks(lib):
     assert call(sp=()) == binding.Q3A_OK
     assert (lib.q3a_gated_prefill_chunk_workspace_size(2, 100, 16, 2, 256)
             == lib.q3a_gated_prefill_fill_workspace_size(2, 100, 16, 2, 256))
+
+
+def test_selftest_validates_before_launching(lib):
+    assert lib.q3a_selftest_bounded_wait(None, 256, 1000, 0, None) == binding.Q3A_EINVAL
+    assert lib.q3a_selftest_bounded_wait(FAKE, 128, 1000, 0, None) == binding.Q3A_EINVAL
+    assert lib.q3a_selftest_bounded_wait(FAKE + 4, 256, 1000, 0, None) == binding.Q3A_EINVAL
+    assert lib.q3a_selftest_bounded_wait(FAKE, 256, 0, 0, None) == binding.Q3A_EINVAL
+    assert lib.q3a_selftest_bounded_wait(FAKE, 256, 1 << 62, 0, None) == binding.Q3A_EINVAL
