@@ -41,6 +41,9 @@ CHUNK_WORKLOAD = "qwen3-8b-chunk-b4-t1024-at3072"
 GATED_WORKLOAD = "qwen3-next-80b-gated-b4-t4096"
 GATED_DECODE_WORKLOAD = "qwen3-next-80b-gated-decode-b64"
 GATED_CHUNK_WORKLOAD = "qwen3-next-80b-gated-chunk-b4-t1024-at3072"
+# the prefill workloads reported beside the headline one
+EXTRA_PREFILL_WORKLOADS = ["qwen3-0.6b-prefill-b1-t128", "qwen3-32b-prefill-b2-t8192",
+                           "qwen3-30b-a3b-prefill-b1-t32768"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2 ** 20
 
@@ -620,6 +623,23 @@ def run_ours(args) -> None:
     k1_bytes = (w.B * w.T * (w.Hq + w.Hkv) * w.d * 2) * 2 + 2 * w.d * 2
     traffic = ncu_traffic("prefill_attention_kernel")
 
+    # the other prefill workloads, each timed as the headline one (K1 and K2 by
+    # events within every step)
+    extra = {}
+    if not args.no_prefill_configs:
+        with ClockSampler(device) as clk2:
+            for name in EXTRA_PREFILL_WORKLOADS:
+                if name == w.name:
+                    continue
+                ew, ex, e_step, e_k1, e_k2 = bench_prefill(binding, device, args.steps,
+                                                           args.warmup, world, name)
+                del ex
+                torch.cuda.empty_cache()
+                extra[name] = (ew, max_over_ranks(e_step, world, device),
+                               max_over_ranks(e_k1, world, device),
+                               max_over_ranks(e_k2, world, device))
+        extra_clocks = clk2.summary()
+
     e2e_steps = max(1, min(args.steps, 10))
     e2e_dt, h2d, d2h = bench_prefill_e2e(binding, device, w, e2e_steps)
     e2e_dt = max_over_ranks(e2e_dt, world, device)
@@ -667,6 +687,35 @@ def run_ours(args) -> None:
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
+    line["step_frac_of_peak"] = round(value / world / peaks["bf16_tflops"], 4)
+    if extra:
+        cfgs = {}
+        for name, (ew, e_step, e_k1, e_k2) in extra.items():
+            ef = accounting.prefill_flops(ew.B, ew.T, ew.Hq, ew.d)
+            e_bytes = ew.B * ew.T * (3 * ew.Hq + 3 * ew.Hkv) * ew.d * 2
+            k2_rate = ef / (e_k2 / 1e3) / 1e12
+            cfgs[name] = {
+                "value": round(whole_job_rate(ef, world, e_step / 1e3) / 1e12, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(e_step, 4),
+                "us_per_step": round(e_step * 1e3, 1),
+                "step_frac_of_peak": round(ef / (e_step / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                "config": {"B": ew.B, "T": ew.T, "Hq": ew.Hq, "Hkv": ew.Hkv, "d": ew.d,
+                           "theta": ew.theta, "flops_per_step": ef,
+                           "l2": (f"inputs {'larger' if e_bytes > L2_BYTES else 'SMALLER'} than L2"
+                                  f" (no flush): {e_bytes / 2**20:.1f} MiB per step")},
+                "roofline": {"bound": "tensor", "kernel": "prefill_attention_kernel",
+                             "achieved": round(k2_rate, 2), "peak": peaks["bf16_tflops"],
+                             "unit": "TFLOP/s", "frac": round(k2_rate / peaks["bf16_tflops"], 4),
+                             "peak_source": f"{peak_src} bf16 dense burst",
+                             "frac_of_sustained": round(k2_rate / peaks.get(
+                                 "bf16_tflops_sustained", peaks["bf16_tflops"]), 4),
+                             "ms_per_launch": round(e_k2, 4)},
+                "prologue_ms_per_launch": round(e_k1, 4),
+                "gpu_launches": 2 * args.steps,
+            }
+        line["prefill_configs"] = {"workloads": cfgs, "clocks": extra_clocks,
+                                   "api": "q3a_prefill_prologue + q3a_prefill_attention, "
+                                          "timed as the headline step"}
     if dec_ms is not None:
         dbytes = accounting.decode_bytes(start_pos.tolist(), dw.Hq, dw.Hkv, dw.d)
         dec_ms_max = max_over_ranks(dec_ms, world, device)
@@ -838,6 +887,8 @@ def main(argv=None) -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunk", action="store_true")
     ap.add_argument("--no-gated", action="store_true")
+    ap.add_argument("--no-prefill-configs", action="store_true",
+                    help="skip the other prefill workloads (tiny, 32B-shaped, 30B-A3B-shaped)")
     ap.add_argument("--prefill-workload", default=PREFILL_WORKLOAD,
                     choices=[n for n, w in WORKLOADS.items() if w.kind == "prefill"],
                     help="prefill workload of the step (the default is the headline one)")
