@@ -216,27 +216,34 @@ def bench_prefill(binding, device, steps: int, warmup: int, world: int,
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        binding.prefill_prologue(x["q"], x["k"], x["q_gamma"], x["k_gamma"], w.theta, w.eps, ws)
+        binding.prefill_prologue(x["k"], x["q_gamma"], x["k_gamma"], w.Hq, w.theta, w.eps, ws)
         if ev is not None:
             ev[1].record(stream)
-        binding.prefill_attention(x["v"], out, w.Hq, ws)
+        binding.prefill_attention(x["q"], x["v"], x["q_gamma"], out, w.eps, ws)
         if ev is not None:
             ev[2].record(stream)
 
     for _ in range(warmup):
         step()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    # the step: back-to-back steps with events only around them (the kernels
+    # of consecutive launches may overlap their start and end)
     barrier(world, device)
     synchronize_all(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(steps):
-        step(evs[i])
+        step()
     t1.record(stream)
     synchronize_all(device)
     barrier(world, device)
     total_ms = t0.elapsed_time(t1)
+    # each kernel alone: events between the two launches of every step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    synchronize_all(device)
+    for i in range(steps):
+        step(evs[i])
+    synchronize_all(device)
     k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
     k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
     status = binding.last_device_error(ws)
@@ -620,7 +627,9 @@ def run_ours(args) -> None:
     k1_ms_max = max_over_ranks(k1_ms, world, device)
     value = whole_job_rate(flops, world, step_ms_max / 1e3) / 1e12
     k2_tflops = flops / (k2_ms_max / 1e3) / 1e12
-    k1_bytes = (w.B * w.T * (w.Hq + w.Hkv) * w.d * 2) * 2 + 2 * w.d * 2
+    # the prologue normalises the keys (read + write) and writes the table of
+    # RoPE cos/sin per position; the query tiles are normalised inside K2
+    k1_bytes = (w.B * w.T * w.Hkv * w.d * 2) * 2 + w.T * 64 * 8 + 2 * w.d * 2
     traffic = ncu_traffic("prefill_attention_kernel")
 
     # the other prefill workloads, each timed as the headline one (K1 and K2 by

@@ -90,8 +90,11 @@ q3a_status q3a_qknorm_rope(const q3a_bf16* x, const q3a_bf16* gamma, q3a_bf16* y
  *   Softmax scale is fixed to 1/sqrt(d).
  *   workspace: device scratch of at least q3a_prefill_workspace_size() bytes,
  *           256-byte aligned, owned by the caller, contents need not be
- *           initialised; it holds the normalised+rotated Q and K and an error
- *           word. It must not be shared by two calls that run concurrently.
+ *           initialised; it holds the normalised+rotated K, a table of the
+ *           RoPE cos/sin of positions 0..T-1 and an error word (the query
+ *           tiles are normalised and rotated in shared memory by the attention
+ *           kernel itself). It must not be shared by two calls that run
+ *           concurrently.
  *   B == 0 or T == 0: returns Q3A_OK and launches nothing.
  *   Limits: B*T*Hq <= 2^31 - 1 rows; Hq + Hkv <= 512.
  * ------------------------------------------------------------------------- */
@@ -110,24 +113,30 @@ q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
  * q3a_prefill_prologue(...) followed by q3a_prefill_attention(...) on the
  * same stream and workspace.
  *
- * q3a_prefill_prologue — steps 1-2: normalises and rotates q and k (positions
- *   0..T-1) into `workspace`, and clears the workspace's error word. Same
- *   argument rules as q3a_prefill.
- * q3a_prefill_attention — step 3: causal GQA attention of the normalised,
- *   rotated Q and K that the last q3a_prefill_prologue with the same B, T, Hq,
- *   Hkv left in `workspace`, against v, into out. The workspace contents are
- *   only read. Calling it on a workspace that no prologue of these shapes has
- *   filled computes on whatever bytes are there (no fault, meaningless output).
+ * q3a_prefill_prologue — steps 1-2 for the keys: normalises and rotates k
+ *   (positions 0..T-1) into `workspace`, writes there the logit bound that
+ *   QK-Norm implies (from q_gamma and k_gamma) and clears the workspace's
+ *   error word. Same argument rules as q3a_prefill.
+ * q3a_prefill_attention — steps 1-2 for the queries and step 3: the kernel
+ *   loads each tile of q, normalises and rotates it in shared memory (q_gamma
+ *   and eps as for q3a_prefill; the RoPE angles of each position come from a
+ *   table the prologue leaves in the workspace), and computes the causal GQA
+ *   attention against the keys that the last q3a_prefill_prologue with the
+ *   same B, T, Hq, Hkv left in `workspace` and against v, into out. The
+ *   workspace contents are only read. Calling it on a workspace that no
+ *   prologue of these shapes has filled computes on whatever bytes are there
+ *   (no fault, meaningless output).
  * Sources: as q3a_prefill.
  * ------------------------------------------------------------------------- */
-q3a_status q3a_prefill_prologue(const q3a_bf16* q, const q3a_bf16* k,
+q3a_status q3a_prefill_prologue(const q3a_bf16* k,
                                 const q3a_bf16* q_gamma, const q3a_bf16* k_gamma,
                                 int B, int T, int Hq, int Hkv, int d,
                                 double theta, float eps,
                                 void* workspace, size_t ws_bytes, void* stream);
 
-q3a_status q3a_prefill_attention(const q3a_bf16* v, q3a_bf16* out,
-                                 int B, int T, int Hq, int Hkv, int d,
+q3a_status q3a_prefill_attention(const q3a_bf16* q, const q3a_bf16* v,
+                                 const q3a_bf16* q_gamma, q3a_bf16* out,
+                                 int B, int T, int Hq, int Hkv, int d, float eps,
                                  void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------

@@ -66,9 +66,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q3a_prefill_workspace_size.restype = sz
         lib.q3a_prefill.argtypes = [vp] * 6 + [i] * 5 + [d, f, vp, sz, vp]
         lib.q3a_prefill.restype = i
-        lib.q3a_prefill_prologue.argtypes = [vp] * 4 + [i] * 5 + [d, f, vp, sz, vp]
+        lib.q3a_prefill_prologue.argtypes = [vp] * 3 + [i] * 5 + [d, f, vp, sz, vp]
         lib.q3a_prefill_prologue.restype = i
-        lib.q3a_prefill_attention.argtypes = [vp] * 2 + [i] * 5 + [vp, sz, vp]
+        lib.q3a_prefill_attention.argtypes = [vp] * 4 + [i] * 5 + [f, vp, sz, vp]
         lib.q3a_prefill_attention.restype = i
         lib.q3a_prefill_chunk_workspace_size.argtypes = [i] * 5
         lib.q3a_prefill_chunk_workspace_size.restype = sz
@@ -178,31 +178,33 @@ def prefill(q, k, v, q_gamma, k_gamma, theta: float, eps: float, out=None,
     return out
 
 
-def prefill_prologue(q, k, q_gamma, k_gamma, theta: float, eps: float,
+def prefill_prologue(k, q_gamma, k_gamma, Hq: int, theta: float, eps: float,
                      workspace: torch.Tensor) -> None:
-    """Steps 1-2 of prefill into ``workspace`` (see q3a_prefill_prologue)."""
-    B, T, Hq, d = q.shape
-    Hkv = k.shape[2]
-    _check(q, "q")
-    _check(k, "k", (B, T, Hkv, d))
+    """Steps 1-2 of prefill for the keys into ``workspace`` (see q3a_prefill_prologue)."""
+    B, T, Hkv, d = k.shape
+    _check(k, "k")
     _check(q_gamma, "q_gamma", (d,))
     _check(k_gamma, "k_gamma", (d,))
     _check(workspace, "workspace", dtype=torch.uint8)
-    st = load().q3a_prefill_prologue(q.data_ptr(), k.data_ptr(), q_gamma.data_ptr(),
-                                     k_gamma.data_ptr(), B, T, Hq, Hkv, d, float(theta),
-                                     float(eps), workspace.data_ptr(), workspace.numel(),
-                                     _stream(q.device))
+    st = load().q3a_prefill_prologue(k.data_ptr(), q_gamma.data_ptr(), k_gamma.data_ptr(), B, T,
+                                     Hq, Hkv, d, float(theta), float(eps), workspace.data_ptr(),
+                                     workspace.numel(), _stream(k.device))
     _raise(st, "q3a_prefill_prologue")
 
 
-def prefill_attention(v, out, Hq: int, workspace: torch.Tensor) -> torch.Tensor:
-    """Step 3 of prefill from ``workspace`` (see q3a_prefill_attention)."""
-    B, T, Hkv, d = v.shape
-    _check(v, "v")
+def prefill_attention(q, v, q_gamma, out, eps: float, workspace: torch.Tensor) -> torch.Tensor:
+    """The query norm and attention of prefill, with the keys from ``workspace``
+    (see q3a_prefill_attention)."""
+    B, T, Hq, d = q.shape
+    Hkv = v.shape[2]
+    _check(q, "q")
+    _check(v, "v", (B, T, Hkv, d))
+    _check(q_gamma, "q_gamma", (d,))
     _check(out, "out", (B, T, Hq, d))
     _check(workspace, "workspace", dtype=torch.uint8)
-    st = load().q3a_prefill_attention(v.data_ptr(), out.data_ptr(), B, T, Hq, Hkv, d,
-                                      workspace.data_ptr(), workspace.numel(), _stream(v.device))
+    st = load().q3a_prefill_attention(q.data_ptr(), v.data_ptr(), q_gamma.data_ptr(),
+                                      out.data_ptr(), B, T, Hq, Hkv, d, float(eps),
+                                      workspace.data_ptr(), workspace.numel(), _stream(q.device))
     _raise(st, "q3a_prefill_attention")
     return out
 

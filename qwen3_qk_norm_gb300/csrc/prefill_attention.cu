@@ -97,8 +97,10 @@ constexpr uint32_t OFF_BAR = OFF_RING + kSlots * kTile;
 // row-half exchange: tile maxima [2 tiles][2 halves][2 parities][128] fp32,
 // then partial sums [2 item parities][2 tiles][2 halves][128] fp32
 constexpr uint32_t OFF_XCHG = OFF_BAR + 256;
-constexpr uint32_t kSmemBytes =
-    OFF_XCHG + (kQTiles * 2 * 2 * 128 + 2 * kQTiles * 2 * 128) * 4 + 1024;
+// plain prefill's query norm: gamma_q as fp32 [128], then the row sums of
+// squares [2 tiles][2 halves][128]
+constexpr uint32_t OFF_QNORM = OFF_XCHG + (kQTiles * 2 * 2 * 128 + 2 * kQTiles * 2 * 128) * 4;
+constexpr uint32_t kSmemBytes = OFF_QNORM + 128 * 4 + kQTiles * 2 * 128 * 4 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kScaleLog2 = 0.12751743074380046f;  // log2(e) / sqrt(128)
 constexpr float kRescaleThreshold = 8.0f;
@@ -109,6 +111,7 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct Bars {
   uint64_t q_full, q_empty;  // Q pair landed / free again (the item's last QK^T completed)
+  uint64_t q_ready[kQTiles];  // plain prefill: tile t normalised and rotated in place
   uint64_t slot_full[kSlots], slot_empty[kSlots];
   uint64_t s_full[kQTiles], p_full[kQTiles], o_final[kQTiles];
   uint64_t o_free[kQTiles];  // the item's epilogue has read O_t
@@ -144,6 +147,75 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_s, uint6
   for (int kk = 1; kk < 8; ++kk)
     mma_bf16_ts(tmem_o, tmem_s + (kk >> 2) * 64 + (kk & 3) * 8, v_desc + (uint64_t)(kk * 2048 >> 4),
                 idesc, 1u);
+}
+
+// Q-Norm + RoPE of the query tiles of the plain prefill, in shared memory.
+// Thread (r, hc) of a tile's two softmax warpgroups owns row r and the rotate-
+// half pairs i = 32hc .. 32hc+31: elements i (chunks 4hc.. of the first 64-
+// column half, 128-byte swizzle: chunk c of row r sits at c ^ (r & 7)) and
+// i + 64 (the same chunks of the second half). The row's sum of squares meets
+// its partner's through `xss` and the tile's named barrier; then
+//   y = x / sqrt(mean(x^2) + eps) * gamma,  y'_i = y_i c - y_{i+64} s,
+//   y'_{i+64} = y_{i+64} c + y_i s,  a_i = pos * theta^(-2i/128),
+// one bf16 rounding, written back in place ("7.2 Qwen3 full-scale
+// implementation", §7.2.1 RMSNorm then apply_rope; norm before RoPE). cs points
+// at (cos a_i, sin a_i, cos a_{i+1}, sin a_{i+1}) for i = 32hc + 2m, m = 0..15,
+// in the prologue's table row of the row's position.
+__device__ __forceinline__ void qnorm_rope_half_row(uint8_t* tile, int r, int hc,
+                                                    const float4* cs, const float* gam,
+                                                    float eps, float* xss, uint32_t bar_id) {
+  const uint32_t sw = (uint32_t)(r & 7);
+  uint64_t ss2 = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t off = (uint32_t)r * 128u + ((((uint32_t)(4 * hc + (j & 3))) ^ sw) << 4);
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + (j >> 2) * kHalf + off);
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint64_t x2 = f2_pack(bf16_lo(v[m]), bf16_hi(v[m]));
+      ss2 = f2_fma(x2, x2, ss2);
+    }
+  }
+  float s_lo, s_hi;
+  f2_unpack(ss2, s_lo, s_hi);
+  float ss = s_lo + s_hi;
+  xss[hc * 128 + r] = ss;
+  named_barrier_sync(bar_id, 256);
+  ss += xss[(hc ^ 1) * 128 + r];
+  const float inv_rms = rsqrtf(ss * (1.0f / 128.0f) + eps);
+  const uint64_t inv2 = f2_pack(inv_rms, inv_rms);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    // the chunk is read again after the barrier rather than kept in registers
+    const uint32_t off = (uint32_t)r * 128u + ((((uint32_t)(4 * hc + j)) ^ sw) << 4);
+    const uint4 wl = *reinterpret_cast<const uint4*>(tile + off);
+    const uint4 wh = *reinterpret_cast<const uint4*>(tile + kHalf + off);
+    const uint32_t lo[4] = {wl.x, wl.y, wl.z, wl.w};
+    const uint32_t hi[4] = {wh.x, wh.y, wh.z, wh.w};
+    uint32_t ol[4], oh[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int i0 = 8 * (4 * hc + j) + 2 * m;  // pairs i0, i0 + 1
+      const float2 gl = *reinterpret_cast<const float2*>(gam + i0);
+      const float2 gh = *reinterpret_cast<const float2*>(gam + 64 + i0);
+      const float4 t4 = __ldg(cs + 4 * j + m);
+      const uint64_t C2 = f2_pack(t4.x, t4.z), S2 = f2_pack(t4.y, t4.w);
+      const uint64_t A = f2_mul(f2_mul(f2_pack(bf16_lo(lo[m]), bf16_hi(lo[m])), f2_pack(gl.x, gl.y)),
+                                inv2);  // y_i
+      const uint64_t Bv = f2_mul(
+          f2_mul(f2_pack(bf16_lo(hi[m]), bf16_hi(hi[m])), f2_pack(gh.x, gh.y)), inv2);  // y_{i+64}
+      const uint64_t OL = f2_sub(f2_mul(A, C2), f2_mul(Bv, S2));
+      const uint64_t OH = f2_fma(A, S2, f2_mul(Bv, C2));
+      float o0, o1;
+      f2_unpack(OL, o0, o1);
+      ol[m] = pack_bf16x2(o0, o1);
+      f2_unpack(OH, o0, o1);
+      oh[m] = pack_bf16x2(o0, o1);
+    }
+    *reinterpret_cast<uint4*>(tile + off) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+    *reinterpret_cast<uint4*>(tile + kHalf + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+  }
 }
 
 // The plain prefill and the chunk against the caches are two instantiations,
@@ -201,9 +273,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     return it;
   };
 
+  constexpr bool kFuseQ = !kChunk;  // the plain prefill normalises its query tiles itself
+  float* qn_gamma = reinterpret_cast<float*>(smem + OFF_QNORM);
+  float* qn_ss = reinterpret_cast<float*>(smem + OFF_QNORM + 512);
+  if (kFuseQ && threadIdx.x < 128)
+    qn_gamma[threadIdx.x] = __uint_as_float((uint32_t)a.q_gamma[threadIdx.x] << 16);
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
+    for (int t = 0; t < kQTiles; ++t) mbar_init(&bars->q_ready[t], 256);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->slot_full[s], 1);
       mbar_init(&bars->slot_empty[s], kQTiles);  // one arrive per Q tile's softmax
@@ -349,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           return mbar_wait3(&bars->slot_full[iv % kSlots], (iv / kSlots) & 1, second, second_par,
                             &bars->p_full[0], (S + j) & 1, a.err, kDevTimeoutMma, abort);
         };
-        ok = mbar_wait(&bars->q_full, k & 1, a.err, kDevTimeoutMma, abort) &&
+        // the Q pair has landed (chunk: Qhat) or each tile has been normalised
+        // and rotated in place by its softmax warpgroups (plain prefill)
+        ok = mbar_wait(kFuseQ ? &bars->q_ready[0] : &bars->q_full, k & 1, a.err, kDevTimeoutMma,
+                       abort) &&
              mbar_wait(&bars->slot_full[L % kSlots], (L / kSlots) & 1, a.err, kDevTimeoutMma,
                        abort);
         if (!ok) break;
@@ -357,6 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_qk(tmem, q_desc0, k_desc0);
         mma_commit(&bars->s_full[0]);
+        if (kFuseQ) {
+          // tile 1's warpgroups finish their previous epilogue later than
+          // tile 0's: this wait is longer than the commit above takes to resolve
+          ok = mbar_wait(&bars->q_ready[1], k & 1, a.err, kDevTimeoutMma, abort);
+          if (!ok) break;
+          tc_fence_after();
+        }
         issue_qk(tmem + 128, q_desc1, k_desc0);
         // PV0_0 overwrites O0: the previous item's tile-0 epilogue must have
         // read it
@@ -428,10 +516,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok = it.t0 + t * tile_tok + r / g;
         tok_pos = it.p0 + (kChunk ? min(tok, a.T - 1) : tok);
       }
+      bool ok = true;
+      if (kFuseQ) {
+        // Q-Norm + RoPE of this tile's rows once the raw Q pair has landed.
+        // The row's cos/sin come from the prologue's table (L2), loaded before
+        // the wait. After an abort every wait returns at once and only the
+        // named barrier inside is kept, so both halves meet it once per item.
+        const float4* trow =
+            reinterpret_cast<const float4*>(a.rope_table + (size_t)min(tok_pos, a.T - 1) * 128) +
+            16 * hc;
+        // the row's 256 table bytes (two cache lines) into L1 while Q lands
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(trow));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(trow + 8));
+        ok = __all_sync(kFull, mbar_wait(&bars->q_full, k & 1, a.err, kDevTimeoutSoftmax, abort));
+        if (ok) {
+          qnorm_rope_half_row(smem + OFF_Q + t * kTile, r, hc, trow, qn_gamma, a.eps,
+                              qn_ss + t * 256, bar_id);
+          fence_proxy_async_smem();  // the tensor core reads the rows next
+        } else {
+          named_barrier_sync(bar_id, 256);
+        }
+        mbar_arrive(&bars->q_ready[t]);
+      }
       float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
       float l = 0.f;
-      bool ok = true;
-      for (int j = 0; j < n_tiles; ++j) {
+      for (int j = 0; ok && j < n_tiles; ++j) {
         const uint32_t step = S + (uint32_t)j;
         ok = __all_sync(kFull,
                         mbar_wait(&bars->s_full[t], step & 1, a.err, kDevTimeoutSoftmax, abort));

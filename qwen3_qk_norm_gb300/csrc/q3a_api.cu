@@ -122,9 +122,10 @@ q3a_status q3a_qknorm_rope(const q3a_bf16* x, const q3a_bf16* gamma, q3a_bf16* y
   return from_cuda(launch_qknorm_rope(a, static_cast<cudaStream_t>(stream)));
 }
 
+// prefill workspace: header, Khat, then the RoPE table [T][64] (cos, sin)
 size_t q3a_prefill_workspace_size(int B, int T, int Hq, int Hkv, int d) {
   if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || d != 128) return 0;
-  return kHeader + align256(prefill_q_bytes(B, T, Hq)) + align256(prefill_k_bytes(B, T, Hkv));
+  return kHeader + align256(prefill_k_bytes(B, T, Hkv)) + align256((size_t)T * 64 * 8);
 }
 
 static q3a_status prefill_check(const void* const* ptrs, int nptrs, int B, int T, int Hq,
@@ -144,33 +145,39 @@ static q3a_status prefill_check(const void* const* ptrs, int nptrs, int B, int T
   return Q3A_OK;
 }
 
+// chunk workspace: header, then Qhat; prefill workspace: header, Khat, RoPE table
 static uint16_t* ws_qhat(void* ws) { return reinterpret_cast<uint16_t*>((uint8_t*)ws + kHeader); }
-static uint16_t* ws_khat(void* ws, int B, int T, int Hq) {
-  return reinterpret_cast<uint16_t*>((uint8_t*)ws + kHeader + align256(prefill_q_bytes(B, T, Hq)));
+static uint16_t* ws_khat(void* ws) { return reinterpret_cast<uint16_t*>((uint8_t*)ws + kHeader); }
+static float* ws_rope_table(void* ws, int B, int T, int Hkv) {
+  return reinterpret_cast<float*>((uint8_t*)ws + kHeader + align256(prefill_k_bytes(B, T, Hkv)));
 }
 
-static void prologue_args(RopeArgs& ra, const q3a_bf16* q, const q3a_bf16* k,
-                          const q3a_bf16* q_gamma, const q3a_bf16* k_gamma, int B, int T, int Hq,
-                          int Hkv, double theta, float eps, void* workspace) {
+// Prefill prologue: K -> Khat (QK-Norm + RoPE at positions 0..T-1) in the
+// head-major layout [B, Hkv, T] (a 128-key tile of one group is contiguous),
+// plus the logit bound and the cleared error word. The query tiles are
+// normalised and rotated by the attention kernel itself.
+static void prologue_args(RopeArgs& ra, const q3a_bf16* k, const q3a_bf16* q_gamma,
+                          const q3a_bf16* k_gamma, int B, int T, int Hkv, double theta, float eps,
+                          void* workspace) {
   memset(&ra, 0, sizeof ra);
-  uint16_t* qhat = ws_qhat(workspace);
-  uint16_t* khat = ws_khat(workspace, B, T, Hq);
-  // Q -> Qhat, same [B, T, Hq] row order
-  ra.t[0] = RopeTensor{q, q_gamma, qhat, Hq, (long long)T * Hq, Hq, 1, (long long)T * Hq, Hq, 1};
-  // K [B, T, Hkv] -> Khat [B, Hkv, T] so that a 128-key tile of one group is contiguous
-  ra.t[1] = RopeTensor{k, k_gamma, khat, Hkv, (long long)T * Hkv, Hkv, 1, (long long)Hkv * T, 1, T};
-  ra.ntensors = 2;
+  ra.t[0] = RopeTensor{k, k_gamma, ws_khat(workspace), Hkv, (long long)T * Hkv, Hkv, 1,
+                       (long long)Hkv * T, 1, T};
+  ra.ntensors = 1;
   ra.B = B;
   ra.T = T;
   ra.pos0 = 0;
   ra.eps = eps;
   ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
   ra.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
+  ra.bound_gamma[0] = q_gamma;
+  ra.bound_gamma[1] = k_gamma;
+  ra.rope_table = ws_rope_table(workspace, B, T, Hkv);
   fill_turn_freq(theta, 128, ra.turn_freq);
 }
 
-static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* out, int B, int T,
-                                 int Hq, int Hkv, void* workspace) {
+static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* q, const q3a_bf16* v,
+                                 const q3a_bf16* q_gamma, q3a_bf16* out, int B, int T, int Hq,
+                                 int Hkv, float eps, void* workspace) {
   memset(&pa, 0, sizeof pa);
   const int g = Hq / Hkv;
   const uint64_t dq[4] = {128, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
@@ -182,10 +189,13 @@ static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* o
   const uint64_t dv[4] = {128, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
   const uint64_t sv[3] = {256, (uint64_t)Hkv * 256, (uint64_t)T * Hkv * 256};
   const uint32_t bv[4] = {64, 1, 128, 1};
-  if (encode_tensor_map(&pa.tm_q, ws_qhat(workspace), 4, dq, sq, bq) != CUDA_SUCCESS ||
-      encode_tensor_map(&pa.tm_k, ws_khat(workspace, B, T, Hq), 3, dk, sk, bk) != CUDA_SUCCESS ||
+  if (encode_tensor_map(&pa.tm_q, q, 4, dq, sq, bq) != CUDA_SUCCESS ||
+      encode_tensor_map(&pa.tm_k, ws_khat(workspace), 3, dk, sk, bk) != CUDA_SUCCESS ||
       encode_tensor_map(&pa.tm_v, v, 4, dv, sv, bv) != CUDA_SUCCESS)
     return Q3A_ECUDA;
+  pa.q_gamma = q_gamma;
+  pa.eps = eps;
+  pa.rope_table = ws_rope_table(workspace, B, T, Hkv);
   pa.out = out;
   pa.err = reinterpret_cast<uint32_t*>(workspace);
   pa.logit_bound = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + 8);
@@ -199,28 +209,30 @@ static q3a_status attention_args(PrefillArgs& pa, const q3a_bf16* v, q3a_bf16* o
   return Q3A_OK;
 }
 
-q3a_status q3a_prefill_prologue(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* q_gamma,
+q3a_status q3a_prefill_prologue(const q3a_bf16* k, const q3a_bf16* q_gamma,
                                 const q3a_bf16* k_gamma, int B, int T, int Hq, int Hkv, int d,
                                 double theta, float eps, void* workspace, size_t ws_bytes,
                                 void* stream) {
   if (!scalars_ok(theta, eps)) return Q3A_EINVAL;
-  const void* ptrs[] = {q, k, q_gamma, k_gamma};
+  const void* ptrs[] = {k, q_gamma, k_gamma};
   bool empty;
-  q3a_status s = prefill_check(ptrs, 4, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
+  q3a_status s = prefill_check(ptrs, 3, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
   if (s != Q3A_OK || empty) return s;
   RopeArgs ra;
-  prologue_args(ra, q, k, q_gamma, k_gamma, B, T, Hq, Hkv, theta, eps, workspace);
+  prologue_args(ra, k, q_gamma, k_gamma, B, T, Hkv, theta, eps, workspace);
   return from_cuda(launch_qknorm_rope(ra, static_cast<cudaStream_t>(stream)));
 }
 
-q3a_status q3a_prefill_attention(const q3a_bf16* v, q3a_bf16* out, int B, int T, int Hq, int Hkv,
-                                 int d, void* workspace, size_t ws_bytes, void* stream) {
-  const void* ptrs[] = {v, out};
+q3a_status q3a_prefill_attention(const q3a_bf16* q, const q3a_bf16* v, const q3a_bf16* q_gamma,
+                                 q3a_bf16* out, int B, int T, int Hq, int Hkv, int d, float eps,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+  if (!scalars_ok(2.0, eps)) return Q3A_EINVAL;
+  const void* ptrs[] = {q, v, q_gamma, out};
   bool empty;
-  q3a_status s = prefill_check(ptrs, 2, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
+  q3a_status s = prefill_check(ptrs, 4, B, T, Hq, Hkv, d, workspace, ws_bytes, &empty);
   if (s != Q3A_OK || empty) return s;
   PrefillArgs pa;
-  s = attention_args(pa, v, out, B, T, Hq, Hkv, workspace);
+  s = attention_args(pa, q, v, q_gamma, out, B, T, Hq, Hkv, eps, workspace);
   if (s != Q3A_OK) return s;
   return from_cuda(launch_prefill_attention(pa, static_cast<cudaStream_t>(stream)));
 }
@@ -236,10 +248,10 @@ q3a_status q3a_prefill(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf16* v,
   if (s != Q3A_OK || empty) return s;
   // tensor maps first: a failure there launches nothing
   PrefillArgs pa;
-  s = attention_args(pa, v, out, B, T, Hq, Hkv, workspace);
+  s = attention_args(pa, q, v, q_gamma, out, B, T, Hq, Hkv, eps, workspace);
   if (s != Q3A_OK) return s;
   RopeArgs ra;
-  prologue_args(ra, q, k, q_gamma, k_gamma, B, T, Hq, Hkv, theta, eps, workspace);
+  prologue_args(ra, k, q_gamma, k_gamma, B, T, Hkv, theta, eps, workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_qknorm_rope(ra, st);
   if (e == cudaSuccess) e = launch_prefill_attention(pa, st);
@@ -327,6 +339,8 @@ q3a_status q3a_prefill_chunk(const q3a_bf16* q, const q3a_bf16* k, const q3a_bf1
   ra.eps = eps;
   ra.err_clear = reinterpret_cast<uint32_t*>(workspace);
   ra.logit_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 8);
+  ra.bound_gamma[0] = q_gamma;
+  ra.bound_gamma[1] = k_gamma;
   fill_turn_freq(theta, 128, ra.turn_freq);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

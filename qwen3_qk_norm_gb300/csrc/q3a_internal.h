@@ -39,9 +39,13 @@ struct RopeArgs {
   int tok_per_cta;      // set by launch_qknorm_rope
   uint32_t* err_clear;  // if non-null, block 0 zeroes this error word
   // if non-null, block 0 writes here the bound on |q.k| / sqrt(128) * log2(e)
-  // that QK-Norm guarantees: sqrt(128) * max|gamma_q| * max|gamma_k| * log2(e)
-  // (tensor 0 is Q, tensor 1 is K)
+  // that QK-Norm guarantees: sqrt(128) * max|gamma_q| * max|gamma_k| * log2(e),
+  // from bound_gamma[0] (gamma_q) and bound_gamma[1] (gamma_k)
   float* logit_bound;
+  const uint16_t* bound_gamma[2];
+  // if non-null: the (cos, sin) of every angle i < 64 at positions 0..T-1,
+  // [T][64] float2, written by the CTAs of sequence 0 (plain prefill only)
+  float* rope_table;
   unsigned long long turn_freq[64];  // theta^(-2i/128) / (2 pi), 0.64 fixed point
 };
 
@@ -54,7 +58,9 @@ cudaError_t launch_qknorm_rope(const RopeArgs& a, cudaStream_t stream);
 
 // ----- K2: causal GQA prefill attention (tcgen05) ---------------------------
 struct PrefillArgs {
-  CUtensorMap tm_q;  // Qhat [B, T, Hq, 128] bf16, box {64, g, 128/g, 1}
+  // plain prefill: raw q [B, T, Hq, 128], normalised and rotated in shared
+  // memory by the kernel itself; chunk: Qhat from the prologue. Box {64, g, 128/g, 1}
+  CUtensorMap tm_q;
   CUtensorMap tm_k;  // Khat [B*Hkv, rows, 128] bf16, box {64, 128, 1} (workspace or cache)
   CUtensorMap tm_v;  // V [B, T, Hkv, 128], box {64, 1, 128, 1}; or, for a chunk,
                      // [B*Hkv, S_max, 128] (the cache), box {64, 128, 1}
@@ -63,6 +69,10 @@ struct PrefillArgs {
   const float* logit_bound;  // written by the prologue (see RopeArgs)
   int B, T, Hq, Hkv, g;
   int n_mtiles;      // ceil(T / prefill_tokens_per_cta(g))
+  // the plain prefill's Q-Norm + RoPE of the query tiles (unused by a chunk)
+  const uint16_t* q_gamma;   // [128]
+  float eps;
+  const float* rope_table;   // [T][64] (cos, sin) pairs, written by the prologue
 };
 
 // A chunk against the caches: keys and values are read from the head-major

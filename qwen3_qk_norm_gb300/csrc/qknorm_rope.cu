@@ -34,12 +34,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kHalfWarps = kThreads / 16;
-constexpr int kMaxTok = 8;
+constexpr int kMaxTok = 32;
 
 __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_constant__ RopeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(16) float cos_s[kMaxTok][64];
-  __shared__ __align__(16) float sin_s[kMaxTok][64];
   __shared__ uint64_t bar;
   const int tid = threadIdx.x;
   const int tok_per_cta = a.tok_per_cta;
@@ -53,6 +51,9 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
   uint16_t* rows0 = reinterpret_cast<uint16_t*>(smem);
   uint16_t* rows1 = reinterpret_cast<uint16_t*>(smem + (size_t)tok_per_cta * H0 * 256);
   uint16_t* rows2 = reinterpret_cast<uint16_t*>(smem + (size_t)tok_per_cta * (H0 + H1) * 256);
+  // the CTA's tokens' cos and sin [tok][64] each, after the staged rows
+  float* cos_s = reinterpret_cast<float*>(smem + (size_t)tok_per_cta * (H0 + H1 + H2) * 256);
+  float* sin_s = cos_s + tok_per_cta * 64;
 
   if (tid == 0) {
     mbar_init(&bar, 1);
@@ -65,13 +66,13 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
   if (blockIdx.x == 0 && tid >= 32 && tid < 64) {
     const int l = tid - 32;
     if (a.err_clear && l == 0) *a.err_clear = 0u;
-    if (a.logit_bound && a.ntensors >= 2) {
+    if (a.logit_bound) {
       // QK-Norm bounds every logit: |qhat| <= sqrt(128) max|gamma_q| and the
       // same for khat, so |qhat . khat| / sqrt(128) <= sqrt(128) gq gk
       float gq = 0.f, gk = 0.f;
       for (int i = l; i < 128; i += 32) {
-        gq = fmaxf(gq, fabsf(__uint_as_float((uint32_t)a.t[0].gamma[i] << 16)));
-        gk = fmaxf(gk, fabsf(__uint_as_float((uint32_t)a.t[1].gamma[i] << 16)));
+        gq = fmaxf(gq, fabsf(__uint_as_float((uint32_t)a.bound_gamma[0][i] << 16)));
+        gk = fmaxf(gk, fabsf(__uint_as_float((uint32_t)a.bound_gamma[1][i] << 16)));
       }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
@@ -92,54 +93,103 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
     token_bt(b_first, t_first, tt, a.T, b, t);
     const long long pos = (a.per_b_pos ? (long long)a.pos_b[b] : a.pos0) + t;
     const float2 c_s = rope_cos_sin(pos, a.turn_freq[i]);
-    cos_s[tt][i] = c_s.x;
-    sin_s[tt][i] = c_s.y;
+    cos_s[tt * 64 + i] = c_s.x;
+    sin_s[tt * 64 + i] = c_s.y;
+    // the prefill's table of (cos, sin) per position, for the query tiles that
+    // the attention kernel normalises itself: written by sequence 0's tokens
+    if (a.rope_table && b == 0) reinterpret_cast<float2*>(a.rope_table)[t * 64 + i] = c_s;
   }
   const int lane16 = tid & 15;
   const int hw = tid >> 4;
-  float gl[2][4], gh[2][4];
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const uint16_t* gp = s ? a.t[1].gamma : a.t[0].gamma;
-    if (s < a.ntensors && !a.t[s].copy_only) {
-      unpack4(reinterpret_cast<const uint2*>(gp)[lane16], gl[s]);
-      unpack4(reinterpret_cast<const uint2*>(gp + 64)[lane16], gh[s]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) gl[s][j] = gh[s][j] = 0.f;
-    }
-  }
   __syncthreads();  // barrier initialised, table written
   mbar_wait(&bar, 0, nullptr, 0, nullptr);
 
-  const int R0 = a.t[0].copy_only ? 0 : tok_here * H0;
-  const int R1 = (a.ntensors > 1 && !a.t[1].copy_only) ? tok_here * H1 : 0;
-  const int rows = R0 + R1;
-  const int rows_even = (rows + 1) & ~1;  // whole warps, so the shuffles stay converged
-  for (int q = hw; q < rows_even; q += kHalfWarps) {
-    const bool live = q < rows;
-    const int qq = live ? q : rows - 1;
-    const int s = qq < R0 ? 0 : 1;
-    const int rr = s ? qq - R0 : qq;
-    const int tt = rr / (s ? H1 : H0);
-    uint16_t* row = (s ? rows1 : rows0) + (size_t)rr * 128;
-    float xl[4], xh[4], ol[4], oh[4];
-    unpack4(reinterpret_cast<const uint2*>(row)[lane16], xl);
-    unpack4(reinterpret_cast<const uint2*>(row + 64)[lane16], xh);
-    const float4 c4 = reinterpret_cast<const float4*>(cos_s[tt])[lane16];
-    const float4 s4 = reinterpret_cast<const float4*>(sin_s[tt])[lane16];
-    const float2 c_s[4] = {make_float2(c4.x, s4.x), make_float2(c4.y, s4.y),
-                           make_float2(c4.z, s4.z), make_float2(c4.w, s4.w)};
-    float gls[4], ghs[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      gls[j] = s ? gl[1][j] : gl[0][j];
-      ghs[j] = s ? gh[1][j] : gh[0][j];
+  // Normalised rows whose output is not in the input's layout (head-major
+  // Khat, cache rows) go straight from registers to global memory: a half-warp
+  // writes one 256-byte row, instead of a bulk store per row afterwards.
+  auto contiguous_out = [&](int s, int H) {
+    const RopeTensor& ts = a.t[s];
+    return !ts.y_at_position && ts.ysh == 1 && ts.yst == H && ts.ysb == (long long)a.T * H;
+  };
+#pragma unroll 1
+  for (int s = 0; s < 2; ++s) {
+    if (s >= a.ntensors || a.t[s].copy_only) break;  // tensors that normalise come first
+    const RopeTensor& ts = a.t[s];
+    const int H = s ? H1 : H0;
+    const int R = tok_here * H;
+    uint16_t* base = s ? rows1 : rows0;
+    const bool direct = !contiguous_out(s, H);
+    // this lane's gamma (elements 4L..4L+3 and 64+4L..) as packed fp32 pairs
+    uint64_t GL[2], GH[2];
+    {
+      const uint2 gl = reinterpret_cast<const uint2*>(ts.gamma)[lane16];
+      const uint2 gh = reinterpret_cast<const uint2*>(ts.gamma + 64)[lane16];
+      GL[0] = f2_pack(bf16_lo(gl.x), bf16_hi(gl.x));
+      GL[1] = f2_pack(bf16_lo(gl.y), bf16_hi(gl.y));
+      GH[0] = f2_pack(bf16_lo(gh.x), bf16_hi(gh.x));
+      GH[1] = f2_pack(bf16_lo(gh.y), bf16_hi(gh.y));
     }
-    qknorm_rope_halfwarp(xl, xh, gls, ghs, c_s, a.eps, ol, oh);
-    if (live) {
-      reinterpret_cast<uint2*>(row)[lane16] = pack4(ol);
-      reinterpret_cast<uint2*>(row + 64)[lane16] = pack4(oh);
+    // token of row r: floor(r / H) = umulhi(r, ceil(2^32 / H)), exact for r * H < 2^32
+    // (H = 1, whose multiplier does not fit 32 bits, is r itself)
+    const uint32_t magic = H > 1 ? 0xFFFFFFFFu / (uint32_t)H + 1u : 0u;
+    const int R_even = (R + 1) & ~1;  // whole warps, so the shuffles stay converged
+#pragma unroll 1
+    for (int q = hw; q < R_even; q += kHalfWarps) {
+      const bool live = q < R;
+      const int rr = live ? q : R - 1;
+      const int tt = H > 1 ? (int)__umulhi((uint32_t)rr, magic) : rr;
+      uint16_t* row = base + (size_t)rr * 128;
+      const uint2 wl = reinterpret_cast<const uint2*>(row)[lane16];
+      const uint2 wh = reinterpret_cast<const uint2*>(row + 64)[lane16];
+      const uint64_t XL0 = f2_pack(bf16_lo(wl.x), bf16_hi(wl.x));
+      const uint64_t XL1 = f2_pack(bf16_lo(wl.y), bf16_hi(wl.y));
+      const uint64_t XH0 = f2_pack(bf16_lo(wh.x), bf16_hi(wh.x));
+      const uint64_t XH1 = f2_pack(bf16_lo(wh.y), bf16_hi(wh.y));
+      uint64_t ss2 = f2_mul(XL0, XL0);
+      ss2 = f2_fma(XL1, XL1, ss2);
+      ss2 = f2_fma(XH0, XH0, ss2);
+      ss2 = f2_fma(XH1, XH1, ss2);
+      float s0, s1;
+      f2_unpack(ss2, s0, s1);
+      float ss = s0 + s1;
+      ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      const float inv_rms = rsqrtf(ss * (1.0f / 128.0f) + a.eps);
+      const uint64_t INV2 = f2_pack(inv_rms, inv_rms);
+      const float4 c4 = reinterpret_cast<const float4*>(cos_s + tt * 64)[lane16];
+      const float4 s4 = reinterpret_cast<const float4*>(sin_s + tt * 64)[lane16];
+      const uint64_t C2[2] = {f2_pack(c4.x, c4.y), f2_pack(c4.z, c4.w)};
+      const uint64_t S2[2] = {f2_pack(s4.x, s4.y), f2_pack(s4.z, s4.w)};
+      const uint64_t XL[2] = {XL0, XL1}, XH[2] = {XH0, XH1};
+      uint32_t ol[2], oh[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        // y = x * gamma / rms; y'_i = y_i c - y_{i+64} s; y'_{i+64} = y_{i+64} c + y_i s
+        const uint64_t A = f2_mul(f2_mul(XL[j], GL[j]), INV2);
+        const uint64_t Bv = f2_mul(f2_mul(XH[j], GH[j]), INV2);
+        const uint64_t OL = f2_sub(f2_mul(A, C2[j]), f2_mul(Bv, S2[j]));
+        const uint64_t OH = f2_fma(A, S2[j], f2_mul(Bv, C2[j]));
+        float o0, o1;
+        f2_unpack(OL, o0, o1);
+        ol[j] = pack_bf16x2(o0, o1);
+        f2_unpack(OH, o0, o1);
+        oh[j] = pack_bf16x2(o0, o1);
+      }
+      if (live) {
+        uint16_t* dst = row;
+        if (direct) {
+          const int h = rr - tt * H;
+          long long b;
+          int t_in;
+          token_bt(b_first, t_first, tt, a.T, b, t_in);
+          const long long t = t_in + (ts.y_at_position ? (long long)a.pos_b[b] : 0);
+          dst = ts.y + (b * ts.ysb + t * ts.yst + (long long)h * ts.ysh) * 128;
+        }
+        reinterpret_cast<uint2*>(dst)[lane16] = make_uint2(ol[0], ol[1]);
+        reinterpret_cast<uint2*>(dst + 64)[lane16] = make_uint2(oh[0], oh[1]);
+      }
     }
   }
   fence_proxy_async_smem();  // the bulk stores below read what was just written
@@ -158,6 +208,7 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
     const long long ysb = ts.ysb, yst = ts.yst, ysh = ts.ysh;
     const int at_pos = ts.y_at_position;
     const bool contiguous = !at_pos && ysh == 1 && yst == H && ysb == (long long)a.T * H;
+    if (!ts.copy_only && !contiguous) continue;  // written from registers above
     if (contiguous) {
       const uint32_t bytes = s == 2 ? bytes2 : (s ? bytes1 : bytes0);
       if (tid == 0 && bytes) {
@@ -230,14 +281,14 @@ cudaError_t launch_qknorm_rope(const RopeArgs& a_in, cudaStream_t stream) {
   int tok = (40 * 1024) / (rows_per_tok * 256);
   tok = tok < 1 ? 1 : (tok > kMaxTok ? kMaxTok : tok);
   a.tok_per_cta = tok;
-  const size_t smem = (size_t)tok * rows_per_tok * 256;
+  const size_t smem = (size_t)tok * rows_per_tok * 256 + (size_t)tok * 64 * 2 * 4;
   static unsigned long long attr_mask = 0;  // per-device dynamic smem opt-in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(attr_mask & (1ull << dev))) {
     e = cudaFuncSetAttribute(qknorm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             512 * 256);
+                             512 * 256 + kMaxTok * 64 * 2 * 4);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_mask |= 1ull << dev;
   }

@@ -69,15 +69,20 @@ def test_chunk_cache_ends_exactly_at_s_max(cuda_lib):
 
 def test_chunk_at_position_zero_is_prefill(cuda_lib):
     """With every start_pos = 0 a chunk is a plain prefill that also fills
-    the caches: same output bits as q3a_prefill, and the cache holds what
-    q3a_qknorm_rope writes for K."""
+    the caches: both outputs match the oracle's prefill (the chunk takes its
+    query rows from the prologue, the plain prefill normalises them inside the
+    attention kernel, so the two may differ in the last bit), and the cache
+    holds what q3a_qknorm_rope writes for K."""
     B, T, Hq, Hkv, S = 2, 333, 32, 8, 512
     x = chunk_inputs(B, T, Hq, Hkv, S, [0, 0], seed=41)
     out, d = run_chunk(x)
     full = binding.prefill(d["q"], d["k"], d["v"], d["q_gamma"], d["k_gamma"], 1e6, 1e-6)
     khat = binding.qknorm_rope(d["k"], d["k_gamma"], 1e6, 1e-6)
     torch.cuda.synchronize()
-    assert torch.equal(out, full)
+    ref = oracle.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    assert_close_attention(out, ref, "chunk at position 0")
+    assert_close_attention(full, ref, "prefill")
+    assert float((out.float() - full.float()).abs().max()) <= 2e-2
     assert torch.equal(d["k_cache"][:, :, :T], khat.transpose(1, 2))
     assert torch.equal(d["v_cache"][:, :, :T], d["v"].transpose(1, 2))
 
@@ -127,8 +132,6 @@ def test_chunks_in_sequence_equal_one_prefill(cuda_lib, T, cuts):
     got = torch.cat(parts, 1)
     assert_close_attention(got, ref, f"chunks {cuts}")
     assert_close_attention(got, full.cpu().double(), f"chunks {cuts} against one prefill")
-    # the first chunk starts at 0 and so is bit-identical to the prefill's rows
-    assert torch.equal(parts[0], full[:, :cuts[1]])
     assert torch.equal(kc[:, :, :T], khat.transpose(1, 2))
     assert torch.equal(vc[:, :, :T], x["v"].transpose(1, 2))
     assert torch.isnan(kc[:, :, T:].float()).all()

@@ -98,6 +98,21 @@ def test_prefill_row0_is_v_row0(cuda_lib):
         assert_within_one_ulp(out[:, 0, h], x["v"][:, 0, h // 4].double(), "row 0")
 
 
+def test_prefill_halves_equal_the_whole_call(cuda_lib):
+    """q3a_prefill_prologue (keys) then q3a_prefill_attention (query norm and
+    attention) on one workspace give q3a_prefill's bits."""
+    B, T, Hq, Hkv = 2, 333, 16, 4
+    x = {k: t.cuda() for k, t in inputs.prefill_inputs(B, T, Hq, Hkv, seed=16).items()}
+    whole = binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    ws = torch.empty(binding.prefill_workspace_size(B, T, Hq, Hkv), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(x["q"])
+    binding.prefill_prologue(x["k"], x["q_gamma"], x["k_gamma"], Hq, 1e6, 1e-6, ws)
+    binding.prefill_attention(x["q"], x["v"], x["q_gamma"], out, 1e-6, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, whole)
+
+
 def test_prefill_is_deterministic(cuda_lib):
     x = inputs.prefill_inputs(1, 300, 32, 8, seed=13)
     assert torch.equal(run_prefill(x, 1e6), run_prefill(x, 1e6))
