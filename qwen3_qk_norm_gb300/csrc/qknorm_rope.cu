@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
   // the CTA's tokens' cos and sin [tok][64] each, after the staged rows
   float* cos_s = reinterpret_cast<float*>(smem + (size_t)tok_per_cta * (H0 + H1 + H2) * 256);
   float* sin_s = cos_s + tok_per_cta * 64;
+  // per normalised tensor and token: the output row (in rows of 128) of head 0
+  long long* obase_s = reinterpret_cast<long long*>(sin_s + tok_per_cta * 64);
 
   if (tid == 0) {
     mbar_init(&bar, 1);
@@ -99,9 +101,19 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
     // the attention kernel normalises itself: written by sequence 0's tokens
     if (a.rope_table && b == 0) reinterpret_cast<float2*>(a.rope_table)[t * 64 + i] = c_s;
   }
+  for (int e = tid; e < 2 * tok_here; e += kThreads) {
+    const int s = e >= tok_here ? 1 : 0, tt = e - s * tok_here;
+    if (s >= a.ntensors) continue;
+    const RopeTensor& ts = a.t[s];
+    long long b;
+    int t;
+    token_bt(b_first, t_first, tt, a.T, b, t);
+    obase_s[s * tok_per_cta + tt] =
+        b * ts.ysb + (t + (ts.y_at_position ? (long long)a.pos_b[b] : 0)) * ts.yst;
+  }
   const int lane16 = tid & 15;
   const int hw = tid >> 4;
-  __syncthreads();  // barrier initialised, table written
+  __syncthreads();  // barrier initialised, tables written
   mbar_wait(&bar, 0, nullptr, 0, nullptr);
 
   // Normalised rows whose output is not in the input's layout (head-major
@@ -181,11 +193,7 @@ __global__ void __launch_bounds__(kThreads) qknorm_rope_kernel(const __grid_cons
         uint16_t* dst = row;
         if (direct) {
           const int h = rr - tt * H;
-          long long b;
-          int t_in;
-          token_bt(b_first, t_first, tt, a.T, b, t_in);
-          const long long t = t_in + (ts.y_at_position ? (long long)a.pos_b[b] : 0);
-          dst = ts.y + (b * ts.ysb + t * ts.yst + (long long)h * ts.ysh) * 128;
+          dst = ts.y + (obase_s[s * tok_per_cta + tt] + (long long)h * ts.ysh) * 128;
         }
         reinterpret_cast<uint2*>(dst)[lane16] = make_uint2(ol[0], ol[1]);
         reinterpret_cast<uint2*>(dst + 64)[lane16] = make_uint2(oh[0], oh[1]);
@@ -281,14 +289,14 @@ cudaError_t launch_qknorm_rope(const RopeArgs& a_in, cudaStream_t stream) {
   int tok = (40 * 1024) / (rows_per_tok * 256);
   tok = tok < 1 ? 1 : (tok > kMaxTok ? kMaxTok : tok);
   a.tok_per_cta = tok;
-  const size_t smem = (size_t)tok * rows_per_tok * 256 + (size_t)tok * 64 * 2 * 4;
+  const size_t smem = (size_t)tok * rows_per_tok * 256 + (size_t)tok * 64 * 2 * 4 + (size_t)tok * 2 * 8;
   static unsigned long long attr_mask = 0;  // per-device dynamic smem opt-in
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(attr_mask & (1ull << dev))) {
     e = cudaFuncSetAttribute(qknorm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             512 * 256 + kMaxTok * 64 * 2 * 4);
+                             512 * 256 + kMaxTok * (64 * 2 * 4 + 2 * 8));
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_mask |= 1ull << dev;
   }
