@@ -647,22 +647,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t o[32];
           tmem_ld32_wait(tmem + kTmemO + cq * 64 + cc * 32 + lane_off, o);
           if (store) {
+            // 32-byte stores fill whole sectors of the row (out is 16-byte
+            // aligned by contract; 16-byte stores serve the other case)
+            const bool wide = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const uint4 g4 = grow[cc * 4 + q4];
-              const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
-              uint32_t zw[4];
+            for (int q8 = 0; q8 < 2; ++q8) {
+              uint32_t zw[8];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                // sigmoid(x) = 1 / (1 + 2^(-x log2 e))
-                const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
-                const float sg0 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g0));
-                const float sg1 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g1));
-                zw[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l * sg0,
-                                    __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l * sg1);
+              for (int h4 = 0; h4 < 2; ++h4) {
+                const int q4 = 2 * q8 + h4;
+                const uint4 g4 = grow[cc * 4 + q4];
+                const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  // sigmoid(x) = 1 / (1 + 2^(-x log2 e))
+                  const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
+                  const float sg0 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g0));
+                  const float sg1 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g1));
+                  zw[h4 * 4 + e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l * sg0,
+                                               __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l * sg1);
+                }
               }
-              reinterpret_cast<uint4*>(orow + cc * 32)[q4] =
-                  make_uint4(zw[0], zw[1], zw[2], zw[3]);
+              uint16_t* dst = orow + cc * 32 + q8 * 16;
+              if (wide) {
+                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst),
+                             "r"(zw[0]), "r"(zw[1]), "r"(zw[2]), "r"(zw[3]), "r"(zw[4]), "r"(zw[5]),
+                             "r"(zw[6]), "r"(zw[7]) : "memory");
+              } else {
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(zw[0], zw[1], zw[2], zw[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(zw[4], zw[5], zw[6], zw[7]);
+              }
             }
           }
         }

@@ -428,10 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             &bars->p_full[0], (S + j) & 1, a.err, kDevTimeoutMma, abort);
         };
         // the Q pair has landed (chunk: Qhat) or each tile has been normalised
-        // and rotated in place by its softmax warpgroups (plain prefill)
-        ok = mbar_wait(kFuseQ ? &bars->q_ready[0] : &bars->q_full, k & 1, a.err, kDevTimeoutMma,
+        // and rotated in place by its softmax warpgroups (plain prefill);
+        // polled, as the tensor pipe is idle until this wait returns
+        ok = mbar_poll(kFuseQ ? &bars->q_ready[0] : &bars->q_full, k & 1, a.err, kDevTimeoutMma,
                        abort) &&
-             mbar_wait(&bars->slot_full[L % kSlots], (L / kSlots) & 1, a.err, kDevTimeoutMma,
+             mbar_poll(&bars->slot_full[L % kSlots], (L / kSlots) & 1, a.err, kDevTimeoutMma,
                        abort);
         if (!ok) break;
         const uint64_t k_desc0 = slot_k0 + (uint64_t)(L % kSlots) * kSlotStep;
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kFuseQ) {
           // tile 1's warpgroups finish their previous epilogue later than
           // tile 0's: this wait is longer than the commit above takes to resolve
-          ok = mbar_wait(&bars->q_ready[1], k & 1, a.err, kDevTimeoutMma, abort);
+          ok = mbar_poll(&bars->q_ready[1], k & 1, a.err, kDevTimeoutMma, abort);
           if (!ok) break;
           tc_fence_after();
         }
@@ -657,7 +658,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                          hc * 64;
         uint32_t o[64];
         tmem_ld64_wait(tmem_o, o);  // all 64 columns, one wait
-        if (store) {
+        if (store && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) {
+          // a thread owns 64 columns (128 bytes) of its row: 32-byte stores
+          // fill whole sectors, which the memory system takes far faster
+          // than 16-byte halves of them (out is 16-byte aligned by contract;
+          // the 16-byte path below serves the other case)
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t wv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              wv[e] = pack_bf16x2(__uint_as_float(o[q4 * 16 + 2 * e]) * inv_l,
+                                  __uint_as_float(o[q4 * 16 + 2 * e + 1]) * inv_l);
+            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + q4 * 16),
+                         "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3]), "r"(wv[4]), "r"(wv[5]),
+                         "r"(wv[6]), "r"(wv[7]) : "memory");
+          }
+        } else if (store) {
 #pragma unroll
           for (int q8 = 0; q8 < 8; ++q8) {
             uint4 w;

@@ -356,3 +356,17 @@ def test_gated_rotary_widths(cuda_lib, d_r):
     r2, _ = oracle.gated_decode(y["qg"], y["k_new"], y["v_new"], y["k_cache"], y["v_cache"],
                                 y["start_pos"], y["q_w"], y["k_w"], d_r, 1e7, 1e-6)
     assert_close_attention(o2, r2, f"gated decode d_r {d_r}")
+
+
+def test_gated_output_only_16_byte_aligned(cuda_lib):
+    """32-byte stores when the output allows them, 16-byte ones otherwise: an
+    output that starts 16 bytes into a buffer gets the same bits."""
+    B, T, Hq, Hkv = 1, 150, 16, 2
+    x = {k: t.cuda() for k, t in inputs.gated_inputs(B, T, Hq, Hkv, seed=19).items()}
+    full = binding.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6)
+    buf = torch.empty(B * T * Hq * D + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(B, T, Hq, D)
+    assert out.data_ptr() % 32 == 16
+    binding.gated_prefill(x["qg"], x["k"], x["v"], x["q_w"], x["k_w"], 64, 1e7, 1e-6, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, full)

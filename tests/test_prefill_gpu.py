@@ -113,6 +113,21 @@ def test_prefill_halves_equal_the_whole_call(cuda_lib):
     assert torch.equal(out, whole)
 
 
+def test_prefill_output_only_16_byte_aligned(cuda_lib):
+    """The contract asks for 16-byte aligned tensors; the kernel writes 32-byte
+    pieces of each output row when it can and 16-byte ones otherwise: an
+    output that starts 16 bytes into a buffer gets the same bits."""
+    B, T, Hq, Hkv = 1, 200, 16, 4
+    x = {k: t.cuda() for k, t in inputs.prefill_inputs(B, T, Hq, Hkv, seed=17).items()}
+    full = binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6)
+    buf = torch.empty(B * T * Hq * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(B, T, Hq, 128)
+    assert out.data_ptr() % 32 == 16
+    binding.prefill(x["q"], x["k"], x["v"], x["q_gamma"], x["k_gamma"], 1e6, 1e-6, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, full)
+
+
 def test_prefill_is_deterministic(cuda_lib):
     x = inputs.prefill_inputs(1, 300, 32, 8, seed=13)
     assert torch.equal(run_prefill(x, 1e6), run_prefill(x, 1e6))
