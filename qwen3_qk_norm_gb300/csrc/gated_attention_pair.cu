@@ -653,11 +653,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q8 = 0; q8 < 2; ++q8) {
               uint32_t zw[8];
+              // the gate's 16 values of this piece: one 32-byte load when aligned
+              uint32_t g8[8];
+              if (wide && (reinterpret_cast<uintptr_t>(a.qg) & 31u) == 0) {
+                asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                             : "=r"(g8[0]), "=r"(g8[1]), "=r"(g8[2]), "=r"(g8[3]), "=r"(g8[4]),
+                               "=r"(g8[5]), "=r"(g8[6]), "=r"(g8[7])
+                             : "l"(grow + cc * 4 + 2 * q8));
+              } else {
+                const uint4 ga = grow[cc * 4 + 2 * q8], gb = grow[cc * 4 + 2 * q8 + 1];
+                g8[0] = ga.x; g8[1] = ga.y; g8[2] = ga.z; g8[3] = ga.w;
+                g8[4] = gb.x; g8[5] = gb.y; g8[6] = gb.z; g8[7] = gb.w;
+              }
 #pragma unroll
               for (int h4 = 0; h4 < 2; ++h4) {
                 const int q4 = 2 * q8 + h4;
-                const uint4 g4 = grow[cc * 4 + q4];
-                const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+                const uint32_t gw[4] = {g8[h4 * 4], g8[h4 * 4 + 1], g8[h4 * 4 + 2], g8[h4 * 4 + 3]};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   // sigmoid(x) = 1 / (1 + 2^(-x log2 e))
