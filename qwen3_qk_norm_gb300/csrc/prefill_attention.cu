@@ -318,6 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&a.tm_k);
         tma_prefetch_desc(&a.tm_v);
       }
+      // K/V tiles are read again by the group's other items (kept in L2
+      // ahead of the query tiles, which are read once)
+      const uint64_t pol_last = l2_evict_last_policy(), pol_first = l2_evict_first_policy();
       uint32_t L = 0;       // first load index of the current item
       uint32_t issued = 0;  // loads issued (lane 0)
       uint32_t n_q = 0;     // Q pairs issued (lane 0)
@@ -332,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < kQTiles; ++t) {
               uint8_t* qd = smem + OFF_Q + t * kTile;
               const int tq = it.t0 + t * tile_tok;
-              tma_load_4d(qd, &a.tm_q, &bars->q_full, 0, it.kv * g, tq, it.b);
-              tma_load_4d(qd + kHalf, &a.tm_q, &bars->q_full, 64, it.kv * g, tq, it.b);
+              tma_load_4d_hint(qd, &a.tm_q, &bars->q_full, 0, it.kv * g, tq, it.b, pol_first);
+              tma_load_4d_hint(qd + kHalf, &a.tm_q, &bars->q_full, 64, it.kv * g, tq, it.b,
+                               pol_first);
             }
             ++n_q;
           }
@@ -350,14 +354,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* dst = smem + OFF_RING + s * kTile;
             const int j = i >> 1;
             if ((i & 1) == 0) {
-              tma_load_3d(dst, &a.tm_k, &bars->slot_full[s], 0, j * BN, row3);
-              tma_load_3d(dst + kHalf, &a.tm_k, &bars->slot_full[s], 64, j * BN, row3);
+              tma_load_3d_hint(dst, &a.tm_k, &bars->slot_full[s], 0, j * BN, row3, pol_last);
+              tma_load_3d_hint(dst + kHalf, &a.tm_k, &bars->slot_full[s], 64, j * BN, row3,
+                               pol_last);
             } else if (kChunk) {
-              tma_load_3d(dst, &a.tm_v, &bars->slot_full[s], 0, j * BN, row3);
-              tma_load_3d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, j * BN, row3);
+              tma_load_3d_hint(dst, &a.tm_v, &bars->slot_full[s], 0, j * BN, row3, pol_last);
+              tma_load_3d_hint(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, j * BN, row3,
+                               pol_last);
             } else {
-              tma_load_4d(dst, &a.tm_v, &bars->slot_full[s], 0, it.kv, j * BN, it.b);
-              tma_load_4d(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, it.kv, j * BN, it.b);
+              tma_load_4d_hint(dst, &a.tm_v, &bars->slot_full[s], 0, it.kv, j * BN, it.b,
+                               pol_last);
+              tma_load_4d_hint(dst + kHalf, &a.tm_v, &bars->slot_full[s], 64, it.kv, j * BN, it.b,
+                               pol_last);
             }
             issued = li + 1;
           }
@@ -658,6 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          hc * 64;
         uint32_t o[64];
         tmem_ld64_wait(tmem_o, o);  // all 64 columns, one wait
+        const uint64_t opol = l2_evict_first_policy();  // outputs are not read again here
         if (store && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) {
           // a thread owns 64 columns (128 bytes) of its row: 32-byte stores
           // fill whole sectors, which the memory system takes far faster
@@ -670,9 +679,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e)
               wv[e] = pack_bf16x2(__uint_as_float(o[q4 * 16 + 2 * e]) * inv_l,
                                   __uint_as_float(o[q4 * 16 + 2 * e + 1]) * inv_l);
-            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + q4 * 16),
-                         "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3]), "r"(wv[4]), "r"(wv[5]),
-                         "r"(wv[6]), "r"(wv[7]) : "memory");
+            asm volatile(
+                "st.global.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(
+                    orow + q4 * 16),
+                "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3]), "r"(wv[4]), "r"(wv[5]), "r"(wv[6]),
+                "r"(wv[7]), "l"(opol)
+                : "memory");
           }
         } else if (store) {
 #pragma unroll

@@ -172,6 +172,41 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+
+// L2 eviction priorities (createpolicy): operands that many CTAs read again
+// (K/V tiles) are kept ahead of streamed ones (query tiles, outputs).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// The tiled loads above with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const void* tmap, uint64_t* bar,
+                                                 int c0, int c1, int c2, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+      "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const void* tmap, uint64_t* bar,
+                                                 int c0, int c1, int c2, int c3, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // Untiled bulk copies (cp.async.bulk): both addresses 16-byte aligned, size a
 // multiple of 16 bytes. Loads complete on an mbarrier (complete_tx); stores
 // are tracked per thread in bulk groups.
