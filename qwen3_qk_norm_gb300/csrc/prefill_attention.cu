@@ -74,6 +74,10 @@
 // Every mbarrier wait is bounded (q3a_device.cuh); a timeout sets the error
 // word, all roles unwind, in-flight copies and MMAs are drained and TMEM is
 // freed before the CTA exits.
+#include <algorithm>
+#include <type_traits>
+#include <vector>
+
 #include "q3a_device.cuh"
 #include "q3a_internal.h"
 
@@ -84,6 +88,26 @@ namespace {
 constexpr int BM = 128;  // query rows per Q tile
 constexpr int BN = 128;  // keys per KV tile
 constexpr int kQTiles = 2;
+
+// Work items. Item i is a pair of Q tiles (m-tile mt) of one (b, kv) group.
+// The groups are split into equal sets of `per` groups taken one after
+// another; within a set items go longest first (mt descending), the set's
+// groups interleaved. With one set every group is in flight at once; with
+// more, fewer groups are, so more CTAs read each group's K/V prefix at about
+// the same time and fewer K/V bytes have to stay in L2 between their reads.
+struct ItemIndex {
+  int bk, mt;
+};
+__host__ __device__ __forceinline__ ItemIndex item_index(int i, int n_mtiles, int per) {
+  const int set = i / (per * n_mtiles), j = i - set * per * n_mtiles;
+  return ItemIndex{set * per + j % per, n_mtiles - 1 - j / per};
+}
+// KV tiles of an item: its last token t_last sits at position p0 + t_last
+__host__ __device__ __forceinline__ int item_kv_tiles(int mt, int tile_tok, int T, int p0) {
+  const int t0 = mt * kQTiles * tile_tok;
+  const int t_last = (t0 + kQTiles * tile_tok < T ? t0 + kQTiles * tile_tok : T) - 1;
+  return (p0 + t_last) / BN + 1;
+}
 constexpr int kSoftmaxWGs = 4;  // two column halves per Q tile
 constexpr int kSlots = 4;       // K/V ring slots
 // four softmax warpgroups, then the producer warp and the MMA warp (576
@@ -244,10 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work items ------------------------------------------------------------
-  // Item i (longest first): Q tile pair mt = n_mtiles - 1 - i / (B * Hkv) of
-  // group (b, kv) = i % (B * Hkv). A CTA takes items in rounds of gridDim.x,
-  // in snake order (forward in even rounds, backward in odd ones), so the
-  // long and short items of consecutive rounds pair up across CTAs.
+  // Item i as item_index orders them (longest first within each set of
+  // groups). A CTA takes items in rounds of gridDim.x, in snake order (forward
+  // in even rounds, backward in odd ones), so the long and short items of
+  // consecutive rounds pair up across CTAs.
   const int bk_count = a.B * a.Hkv;
   const int n_items = a.n_mtiles * bk_count;
   const int g = a.g;
@@ -259,16 +283,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto item_at = [&](int i) {
     Item it;
-    const int mt = a.n_mtiles - 1 - i / bk_count;
-    const int bk = i % bk_count;
-    it.b = bk / a.Hkv;
-    it.kv = bk % a.Hkv;
-    it.t0 = mt * kQTiles * tile_tok;
-    const int t_last = min(it.t0 + kQTiles * tile_tok, a.T) - 1;
+    ItemIndex ix;
+    if (kChunk) {
+      // group_sets: a power of two dividing the group count
+      ix = item_index(i, a.n_mtiles, bk_count >> (31 - __clz(a.group_sets)));
+    } else {
+      ix = ItemIndex{i % bk_count, a.n_mtiles - 1 - i / bk_count};  // one set
+    }
+    it.b = ix.bk / a.Hkv;
+    it.kv = ix.bk % a.Hkv;
+    it.t0 = ix.mt * kQTiles * tile_tok;
     // token t of the sequence sits at position p0 + t (p0 = 0 for a plain
     // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
     it.p0 = chunk_start(args, it.b);
-    it.n_tiles = (it.p0 + t_last) / BN + 1;
+    it.n_tiles = item_kv_tiles(ix.mt, tile_tok, a.T, it.p0);
     it.n_keys = it.p0 + a.T;
     return it;
   };
@@ -725,13 +753,55 @@ int prefill_tokens_per_cta(int g) { return kQTiles * (BM / g); }
 
 static const PrefillArgs& base_args_host(const PrefillArgs& a) { return a; }
 static const PrefillArgs& base_args_host(const PrefillChunkArgs& a) { return a.base; }
+static PrefillArgs& base_args_host(PrefillArgs& a) { return a; }
+static PrefillArgs& base_args_host(PrefillChunkArgs& a) { return a.base; }
+static int chunk_start_host(const PrefillArgs&, int) { return 0; }
+static int chunk_start_host(const PrefillChunkArgs& a, int b) { return a.pos_b[b]; }
+
+// The number of group sets (see item_index) for a launch of `grid` CTAs: the
+// schedule is replayed on the host for 1, 2, 4 and 8 sets (those dividing the
+// group count; the kernel relies on a power of two), each item costing its KV tiles plus a fixed boundary cost of
+// about four tiles (the last PV, the epilogue and the next item's first QK^T
+// measured at an item boundary), and the count with the smallest busiest-CTA
+// total is kept; on a tie the larger count (fewer groups in flight).
+template <class Args>
+static int choose_group_sets(const Args& args, int grid) {
+  constexpr int kItemCost = 4;
+  constexpr long long kMaxReplay = 1 << 16;  // beyond this many items: one set
+  const PrefillArgs& a = base_args_host(args);
+  const int bk_count = a.B * a.Hkv;
+  const long long n_items = (long long)a.n_mtiles * bk_count;
+  if (n_items > kMaxReplay) return 1;
+  const int tile_tok = BM / a.g;
+  std::vector<long long> load((size_t)grid);
+  int best = 1;
+  long long best_max = -1;
+  for (int sets = 1; sets <= 8; sets *= 2) {
+    if (bk_count % sets) break;
+    std::fill(load.begin(), load.end(), 0LL);
+    for (long long i = 0; i < n_items; ++i) {
+      const long long r = i / grid, k = i % grid;
+      const int cta = (int)((r & 1) ? grid - 1 - k : k);
+      const ItemIndex ix = item_index((int)i, a.n_mtiles, bk_count / sets);
+      load[(size_t)cta] +=
+          item_kv_tiles(ix.mt, tile_tok, a.T, chunk_start_host(args, ix.bk / a.Hkv)) + kItemCost;
+    }
+    const long long mx = *std::max_element(load.begin(), load.end());
+    if (best_max < 0 || mx <= best_max) {
+      best = sets;
+      best_max = mx;
+    }
+  }
+  return best;
+}
 
 template <class Args>
-static cudaError_t launch(const Args& args, cudaStream_t stream) {
+static cudaError_t launch(const Args& args_in, cudaStream_t stream) {
   // per-device set-up: the dynamic shared memory limit is a per-device
   // attribute of each instantiation
   static unsigned long long done_mask = 0;
-  const PrefillArgs& a = base_args_host(args);
+  Args args = args_in;
+  PrefillArgs& a = base_args_host(args);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -753,6 +823,10 @@ static cudaError_t launch(const Args& args, cudaStream_t stream) {
     if (dev < 64) sm_count[dev] = n_sm;
   }
   const long long grid = items < n_sm ? items : (long long)n_sm;
+  // a plain prefill's items of one group run from 1 to n_mtiles KV tiles,
+  // and longest first over all groups balances them best: one set (the
+  // kernel's plain instantiation does not read the field)
+  a.group_sets = std::is_same<Args, PrefillChunkArgs>::value ? choose_group_sets(args, (int)grid) : 1;
   prefill_attention_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();
 }

@@ -69,6 +69,9 @@ struct PrefillArgs {
   const float* logit_bound;  // written by the prologue (see RopeArgs)
   int B, T, Hq, Hkv, g;
   int n_mtiles;      // ceil(T / prefill_tokens_per_cta(g))
+  int group_sets;    // chunk: the (b, kv) groups' work items in this many
+                     // sets, one after another (a power of two dividing
+                     // B * Hkv, set by the launcher)
   // the plain prefill's Q-Norm + RoPE of the query tiles (unused by a chunk)
   const uint16_t* q_gamma;   // [128]
   float eps;
