@@ -49,9 +49,11 @@
 //            read them complete: K_j's when S_j completes, V_j's when PV_j
 //            does (an arrive on "PV done" follows every PV).
 // TMEM per CTA: S0 | S1 (128 fp32 columns each, double-buffered) | O (256).
-// "P ready" is the even CTA's barrier: its own softmax warps arrive with CTA
-// scope, the odd CTA's with cluster scope (the wider release costs each of
-// those warps a memory barrier, so the even CTA's do not pay it).
+// "P ready" and "O free" are the even CTA's barriers: its own softmax warps
+// arrive with CTA scope, the odd CTA's with cluster scope, all relaxed (the
+// payload is tensor memory the warp has finished with, so nothing needs
+// releasing, and a release would make each warp wait for its earlier global
+// stores: the odd CTA's on every tile, both CTAs' after the epilogue).
 // P goes back as bf16 pairs over the first half of each thread's own S
 // columns and PV reads it from there. MMA stream: S_0, S_1, then per KV tile
 // j: PV_j, S_{j+2}. Commits arrive on the barriers of both CTAs.
@@ -528,6 +530,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // last key this row sees: padding rows of a chunk stop at the last
         // valid key, so they never read rows past the valid keys either
         key_last = kChunk ? it.p0 + min(tok, a.T - 1) : tok;
+        // the row's 64 gate values (one 128-byte line) into L2 now, so that
+        // the epilogue, on the item boundary, finds them there
+        if (tok < a.T) {
+          const long long grow_idx = ((long long)it.b * a.T + tok) * a.Hq + (it.kv * g + (r % g));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(a.qg + grow_idx * (2 * D) + D + cq * 64));
+        }
       }
       float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
       float l = 0.f;
@@ -607,14 +615,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         f2_unpack(sum2[1], b0, b1);
         l += (a0 + a1) + (b0 + b1);
         // the warp's tcgen05.st has completed (wait::st above, warp-collective):
-        // one arrive per warp, on the even CTA's barrier, publishes its 32 rows
+        // one arrive per warp, on the even CTA's barrier, publishes its 32 rows.
+        // P is the signal's only payload, so the arrive releases nothing
+        // (relaxed): the odd CTA's warps then pay no cluster-scope fence
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           if (rank == 0)
-            mbar_arrive(&bars->p_full[s & 1]);  // the issuer's own CTA: CTA scope suffices
+            mbar_arrive_relaxed(&bars->p_full[s & 1]);
           else
-            mbar_arrive_cluster(p_full_even[s & 1]);
+            mbar_arrive_cluster_relaxed(p_full_even[s & 1]);
         }
       }
       // ---- epilogue: the row's four partial sums, then O / l * sigmoid(gate)
@@ -671,10 +681,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t gw[4] = {g8[h4 * 4], g8[h4 * 4 + 1], g8[h4 * 4 + 2], g8[h4 * 4 + 3]};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  // sigmoid(x) = 1 / (1 + 2^(-x log2 e))
+                  // sigmoid(x) = 1 / (1 + 2^(-x log2 e)), the quotient by the
+                  // reciprocal-based fast division (a few fp32 ulps, far
+                  // below the bf16 rounding of z; 1 + 2^y past 2^126 gives 0,
+                  // the limit): an IEEE division per element cost the
+                  // epilogue, which sits on the item boundary, ~3 % of K6
                   const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
-                  const float sg0 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g0));
-                  const float sg1 = 1.0f / (1.0f + ex2(-1.4426950408889634f * g1));
+                  const float sg0 = __fdividef(1.0f, 1.0f + ex2(-1.4426950408889634f * g0));
+                  const float sg1 = __fdividef(1.0f, 1.0f + ex2(-1.4426950408889634f * g1));
                   zw[h4 * 4 + e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l * sg0,
                                                __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l * sg1);
                 }
@@ -693,14 +707,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       // O has been read: the next item's first PV may overwrite it (one
-      // arrive per warp of both CTAs, on the even CTA's barrier)
+      // arrive per warp of both CTAs, on the even CTA's barrier). Relaxed: the
+      // epilogue's output stores need not drain before the signal (with a
+      // release the arrive waited for them, on the item boundary)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if (rank == 0)
-          mbar_arrive(&bars->o_free);
+          mbar_arrive_relaxed(&bars->o_free);
         else
-          mbar_arrive_cluster(o_free_even);
+          mbar_arrive_cluster_relaxed(o_free_even);
       }
       S += (uint32_t)n_tiles;
     }

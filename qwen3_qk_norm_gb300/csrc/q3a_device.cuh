@@ -55,6 +55,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// An arrive that orders nothing but itself (no release of earlier writes).
+// For signals whose only payload is tensor memory the thread has already
+// finished with (a tcgen05.st or tcgen05.ld followed by its wait and by
+// tcgen05.fence::before_thread_sync): the waiting side's acquire and
+// tcgen05.fence::after_thread_sync order its next MMA after them, and the
+// thread's outstanding global stores need not drain first.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
