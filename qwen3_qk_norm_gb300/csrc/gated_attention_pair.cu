@@ -76,6 +76,8 @@
 // Every mbarrier wait is bounded; a timeout sets the error word and every
 // role unwinds; the MMA issuer drains its MMAs and both CTAs meet at a cluster
 // barrier before freeing tensor memory.
+#include <type_traits>
+
 #include "q3a_internal.h"
 #include "q3a_pair.cuh"
 
@@ -170,6 +172,8 @@ __host__ __device__ __forceinline__ const GatedAttnArgs& base_args(const GatedAt
 __host__ __device__ __forceinline__ const GatedAttnArgs& base_args(const GatedAttnChunkArgs& a) {
   return a.base;
 }
+static GatedAttnArgs& base_args_mut(GatedAttnArgs& a) { return a; }
+static GatedAttnArgs& base_args_mut(GatedAttnChunkArgs& a) { return a.base; }
 __device__ __forceinline__ int chunk_start(const GatedAttnArgs&, int) { return 0; }
 __device__ __forceinline__ int chunk_start(const GatedAttnChunkArgs& a, int b) {
   return a.pos_b[b];
@@ -194,8 +198,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- work items ------------------------------------------------------------
   // Item i (longest first): pair tile pm = n_mtiles - 1 - i / (B * Hkv) of
-  // group (b, kv) = i % (B * Hkv). A pair takes items in rounds of the number
-  // of pairs, in snake order (forward in even rounds, backward in odd ones).
+  // group (b, kv) = i % (B * Hkv); a chunk's as item_index orders them
+  // (longest first within each set of groups). A pair takes items in rounds
+  // of the number of pairs, in snake order (forward in even rounds, backward
+  // in odd ones).
   const int bk_count = a.B * a.Hkv;
   const int n_items = a.n_mtiles * bk_count;
   const int g = a.g;
@@ -207,8 +213,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   };
   auto item_at = [&](int i) {
     Item it;
-    const int pm = a.n_mtiles - 1 - i / bk_count;
-    const int bk = i % bk_count;
+    int pm, bk;
+    if (kChunk) {
+      // group_sets: a power of two dividing the group count
+      const ItemIndex ix = item_index(i, a.n_mtiles, bk_count >> (31 - __clz(a.group_sets)));
+      pm = ix.mt;
+      bk = ix.bk;
+    } else {
+      pm = a.n_mtiles - 1 - i / bk_count;
+      bk = i % bk_count;
+    }
     it.b = bk / a.Hkv;
     it.kv = bk % a.Hkv;
     it.t0_pair = pm * 2 * tile_tok;
@@ -734,8 +748,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 template <class Args>
-cudaError_t launch(const Args& args, cudaStream_t stream) {
-  const GatedAttnArgs& a = base_args(args);
+cudaError_t launch(const Args& args_in, cudaStream_t stream) {
+  Args args = args_in;
+  GatedAttnArgs& a = base_args_mut(args);
   static unsigned long long done_mask = 0;  // per-device dynamic smem opt-in, per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -759,6 +774,13 @@ cudaError_t launch(const Args& args, cudaStream_t stream) {
   }
   const long long pairs = items < n_sm / 2 ? items : (long long)(n_sm / 2);
   const long long grid = 2 * pairs;
+  // a plain prefill keeps one set (its items of one group run from 1 to n
+  // KV tiles; longest first over all groups balances them best)
+  if constexpr (std::is_same<Args, GatedAttnChunkArgs>::value)
+    a.group_sets = choose_group_sets(a.n_mtiles, a.B, a.Hkv, 2 * (BM / a.g), a.T, args.pos_b, BN,
+                                     (int)pairs);
+  else
+    a.group_sets = 1;
   gated_attention_pair_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();
 }

@@ -88,26 +88,6 @@ namespace {
 constexpr int BM = 128;  // query rows per Q tile
 constexpr int BN = 128;  // keys per KV tile
 constexpr int kQTiles = 2;
-
-// Work items. Item i is a pair of Q tiles (m-tile mt) of one (b, kv) group.
-// The groups are split into equal sets of `per` groups taken one after
-// another; within a set items go longest first (mt descending), the set's
-// groups interleaved. With one set every group is in flight at once; with
-// more, fewer groups are, so more CTAs read each group's K/V prefix at about
-// the same time and fewer K/V bytes have to stay in L2 between their reads.
-struct ItemIndex {
-  int bk, mt;
-};
-__host__ __device__ __forceinline__ ItemIndex item_index(int i, int n_mtiles, int per) {
-  const int set = i / (per * n_mtiles), j = i - set * per * n_mtiles;
-  return ItemIndex{set * per + j % per, n_mtiles - 1 - j / per};
-}
-// KV tiles of an item: its last token t_last sits at position p0 + t_last
-__host__ __device__ __forceinline__ int item_kv_tiles(int mt, int tile_tok, int T, int p0) {
-  const int t0 = mt * kQTiles * tile_tok;
-  const int t_last = (t0 + kQTiles * tile_tok < T ? t0 + kQTiles * tile_tok : T) - 1;
-  return (p0 + t_last) / BN + 1;
-}
 constexpr int kSoftmaxWGs = 4;  // two column halves per Q tile
 constexpr int kSlots = 4;       // K/V ring slots
 // four softmax warpgroups, then the producer warp and the MMA warp (576
@@ -296,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // token t of the sequence sits at position p0 + t (p0 = 0 for a plain
     // prefill) and sees keys 0..p0+t; keys p0+T.. are not valid
     it.p0 = chunk_start(args, it.b);
-    it.n_tiles = item_kv_tiles(ix.mt, tile_tok, a.T, it.p0);
+    it.n_tiles = item_kv_tiles(it.t0, kQTiles * tile_tok, a.T, it.p0, BN);
     it.n_keys = it.p0 + a.T;
     return it;
   };
@@ -751,40 +731,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int prefill_tokens_per_cta(int g) { return kQTiles * (BM / g); }
 
-static const PrefillArgs& base_args_host(const PrefillArgs& a) { return a; }
-static const PrefillArgs& base_args_host(const PrefillChunkArgs& a) { return a.base; }
 static PrefillArgs& base_args_host(PrefillArgs& a) { return a; }
 static PrefillArgs& base_args_host(PrefillChunkArgs& a) { return a.base; }
-static int chunk_start_host(const PrefillArgs&, int) { return 0; }
-static int chunk_start_host(const PrefillChunkArgs& a, int b) { return a.pos_b[b]; }
 
-// The number of group sets (see item_index) for a launch of `grid` CTAs: the
-// schedule is replayed on the host for 1, 2, 4 and 8 sets (those dividing the
-// group count; the kernel relies on a power of two), each item costing its KV tiles plus a fixed boundary cost of
-// about four tiles (the last PV, the epilogue and the next item's first QK^T
-// measured at an item boundary), and the count with the smallest busiest-CTA
-// total is kept; on a tie the larger count (fewer groups in flight).
-template <class Args>
-static int choose_group_sets(const Args& args, int grid) {
+int choose_group_sets(int n_mtiles, int B, int Hkv, int tokens_per_item, int T,
+                      const int* p0_b, int keys_per_tile, int workers) {
   constexpr int kItemCost = 4;
   constexpr long long kMaxReplay = 1 << 16;  // beyond this many items: one set
-  const PrefillArgs& a = base_args_host(args);
-  const int bk_count = a.B * a.Hkv;
-  const long long n_items = (long long)a.n_mtiles * bk_count;
-  if (n_items > kMaxReplay) return 1;
-  const int tile_tok = BM / a.g;
-  std::vector<long long> load((size_t)grid);
+  const int bk_count = B * Hkv;
+  const long long n_items = (long long)n_mtiles * bk_count;
+  if (n_items > kMaxReplay || workers <= 0) return 1;
+  std::vector<long long> load((size_t)workers);
   int best = 1;
   long long best_max = -1;
   for (int sets = 1; sets <= 8; sets *= 2) {
     if (bk_count % sets) break;
     std::fill(load.begin(), load.end(), 0LL);
     for (long long i = 0; i < n_items; ++i) {
-      const long long r = i / grid, k = i % grid;
-      const int cta = (int)((r & 1) ? grid - 1 - k : k);
-      const ItemIndex ix = item_index((int)i, a.n_mtiles, bk_count / sets);
-      load[(size_t)cta] +=
-          item_kv_tiles(ix.mt, tile_tok, a.T, chunk_start_host(args, ix.bk / a.Hkv)) + kItemCost;
+      const long long r = i / workers, k = i % workers;
+      const int w = (int)((r & 1) ? workers - 1 - k : k);
+      const ItemIndex ix = item_index((int)i, n_mtiles, bk_count / sets);
+      const int p0 = p0_b ? p0_b[ix.bk / Hkv] : 0;
+      load[(size_t)w] +=
+          item_kv_tiles(ix.mt * tokens_per_item, tokens_per_item, T, p0, keys_per_tile) + kItemCost;
     }
     const long long mx = *std::max_element(load.begin(), load.end());
     if (best_max < 0 || mx <= best_max) {
@@ -826,7 +795,11 @@ static cudaError_t launch(const Args& args_in, cudaStream_t stream) {
   // a plain prefill's items of one group run from 1 to n_mtiles KV tiles,
   // and longest first over all groups balances them best: one set (the
   // kernel's plain instantiation does not read the field)
-  a.group_sets = std::is_same<Args, PrefillChunkArgs>::value ? choose_group_sets(args, (int)grid) : 1;
+  if constexpr (std::is_same<Args, PrefillChunkArgs>::value)
+    a.group_sets = choose_group_sets(a.n_mtiles, a.B, a.Hkv, kQTiles * (BM / a.g), a.T,
+                                     args.pos_b, BN, (int)grid);
+  else
+    a.group_sets = 1;
   prefill_attention_kernel<Args><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(args);
   return cudaGetLastError();
 }

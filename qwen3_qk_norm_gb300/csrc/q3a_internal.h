@@ -86,6 +86,38 @@ struct PrefillChunkArgs {
   int pos_b[kMaxBatch];
 };
 
+// Work items of the persistent attention kernels (K2, K6). Item i is a pair
+// of Q tiles (m-tile mt) of one (b, kv) group. The groups are split into
+// equal sets of `per` groups taken one after another; within a set items go
+// longest first (mt descending), the set's groups interleaved. With one set
+// every group is in flight at once; with more, fewer groups are, so more
+// workers read each group's K/V prefix at about the same time and fewer K/V
+// bytes have to stay in L2 between their reads.
+struct ItemIndex {
+  int bk, mt;
+};
+__host__ __device__ __forceinline__ ItemIndex item_index(int i, int n_mtiles, int per) {
+  const int set = i / (per * n_mtiles), j = i - set * per * n_mtiles;
+  return ItemIndex{set * per + j % per, n_mtiles - 1 - j / per};
+}
+// KV tiles of `keys_per_tile` keys that an item of tokens_per_item tokens
+// from token t0 reaches: its last token t_last sits at position p0 + t_last
+__host__ __device__ __forceinline__ int item_kv_tiles(int t0, int tokens_per_item, int T, int p0,
+                                                      int keys_per_tile) {
+  const int t_last = (t0 + tokens_per_item < T ? t0 + tokens_per_item : T) - 1;
+  return (p0 + t_last) / keys_per_tile + 1;
+}
+// The number of group sets (1, 2, 4 or 8, a power of two dividing B * Hkv)
+// for `workers` persistent workers taking items in snake order over rounds:
+// the schedule is replayed on the host for each count, an item costing its KV
+// tiles plus a fixed boundary cost of about four tiles (the last PV, the
+// epilogue and the next item's first QK^T, measured at an item boundary), and
+// the count with the smallest busiest-worker total is kept; on a tie the
+// larger count (fewer groups in flight). p0_b: each sequence's first position
+// (null: 0).
+int choose_group_sets(int n_mtiles, int B, int Hkv, int tokens_per_item, int T,
+                      const int* p0_b, int keys_per_tile, int workers);
+
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_attention(const PrefillChunkArgs& a, cudaStream_t stream);
 // tokens of one KV group that one attention CTA covers (n_mtiles = ceil(T / this))
@@ -192,6 +224,9 @@ struct GatedAttnArgs {
   int B, T, Hq, Hkv, g;
   int n_mtiles;  // pair tiles: ceil(T / gated_tokens_per_cta(g))
   int v_head_major;
+  int group_sets;  // chunk: the (b, kv) groups' work items in this many sets,
+                   // one after another (a power of two dividing B * Hkv,
+                   // set by the launcher)
 };
 // A chunk against the caches: K and V come from the head-major caches (maps
 // over all S_max rows, v_head_major set) and token t of sequence b sits at
