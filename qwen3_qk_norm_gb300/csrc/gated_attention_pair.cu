@@ -650,6 +650,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const long long row = ((long long)it.b * a.T + tok) * a.Hq + (it.kv * g + (r % g));
       // the partial sums go to a slot double-buffered by item; every thread of
       // the four warpgroups reaches this barrier once per item
+      // the row's first 32-byte gate piece is requested now, so that its
+      // latency runs under the partial-sum barrier and the wait for O (the
+      // other three follow inside the epilogue: holding them all across the
+      // wait spills at the register cap)
+      const bool g_wide =
+          ((reinterpret_cast<uintptr_t>(a.out) | reinterpret_cast<uintptr_t>(a.qg)) & 31u) == 0;
+      uint32_t g_first[8];
+      if (store && g_wide)
+        asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(g_first[0]), "=r"(g_first[1]), "=r"(g_first[2]), "=r"(g_first[3]),
+              "=r"(g_first[4]), "=r"(g_first[5]), "=r"(g_first[6]), "=r"(g_first[7])
+            : "l"(a.qg + row * (2 * D) + D + cq * 64));
       float* lsum = xchg + 2 * 4 * 128 + (k & 1) * 4 * 128;  // [quarter][128]
       lsum[cq * 128 + r] = l;
       named_barrier_sync(1, kSoftmaxWGs * 128);
@@ -679,7 +691,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               uint32_t zw[8];
               // the gate's 16 values of this piece: one 32-byte load when aligned
               uint32_t g8[8];
-              if (wide && (reinterpret_cast<uintptr_t>(a.qg) & 31u) == 0) {
+              if (cc == 0 && q8 == 0 && g_wide) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) g8[e] = g_first[e];
+              } else if (wide && (reinterpret_cast<uintptr_t>(a.qg) & 31u) == 0) {
                 asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                              : "=r"(g8[0]), "=r"(g8[1]), "=r"(g8[2]), "=r"(g8[3]), "=r"(g8[4]),
                                "=r"(g8[5]), "=r"(g8[6]), "=r"(g8[7])
