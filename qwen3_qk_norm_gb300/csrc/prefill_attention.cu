@@ -74,9 +74,7 @@
 // Every mbarrier wait is bounded (q3a_device.cuh); a timeout sets the error
 // word, all roles unwind, in-flight copies and MMAs are drained and TMEM is
 // freed before the CTA exits.
-#include <algorithm>
 #include <type_traits>
-#include <vector>
 
 #include "q3a_device.cuh"
 #include "q3a_internal.h"
@@ -733,36 +731,6 @@ int prefill_tokens_per_cta(int g) { return kQTiles * (BM / g); }
 
 static PrefillArgs& base_args_host(PrefillArgs& a) { return a; }
 static PrefillArgs& base_args_host(PrefillChunkArgs& a) { return a.base; }
-
-int choose_group_sets(int n_mtiles, int B, int Hkv, int tokens_per_item, int T,
-                      const int* p0_b, int keys_per_tile, int workers) {
-  constexpr int kItemCost = 4;
-  constexpr long long kMaxReplay = 1 << 16;  // beyond this many items: one set
-  const int bk_count = B * Hkv;
-  const long long n_items = (long long)n_mtiles * bk_count;
-  if (n_items > kMaxReplay || workers <= 0) return 1;
-  std::vector<long long> load((size_t)workers);
-  int best = 1;
-  long long best_max = -1;
-  for (int sets = 1; sets <= 8; sets *= 2) {
-    if (bk_count % sets) break;
-    std::fill(load.begin(), load.end(), 0LL);
-    for (long long i = 0; i < n_items; ++i) {
-      const long long r = i / workers, k = i % workers;
-      const int w = (int)((r & 1) ? workers - 1 - k : k);
-      const ItemIndex ix = item_index((int)i, n_mtiles, bk_count / sets);
-      const int p0 = p0_b ? p0_b[ix.bk / Hkv] : 0;
-      load[(size_t)w] +=
-          item_kv_tiles(ix.mt * tokens_per_item, tokens_per_item, T, p0, keys_per_tile) + kItemCost;
-    }
-    const long long mx = *std::max_element(load.begin(), load.end());
-    if (best_max < 0 || mx <= best_max) {
-      best = sets;
-      best_max = mx;
-    }
-  }
-  return best;
-}
 
 template <class Args>
 static cudaError_t launch(const Args& args_in, cudaStream_t stream) {

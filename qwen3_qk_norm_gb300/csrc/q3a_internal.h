@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <vector>
+
 namespace q3a {
 
 // ----- K1: QK-Norm + RoPE prologue ------------------------------------------
@@ -115,8 +118,35 @@ __host__ __device__ __forceinline__ int item_kv_tiles(int t0, int tokens_per_ite
 // the count with the smallest busiest-worker total is kept; on a tie the
 // larger count (fewer groups in flight). p0_b: each sequence's first position
 // (null: 0).
-int choose_group_sets(int n_mtiles, int B, int Hkv, int tokens_per_item, int T,
-                      const int* p0_b, int keys_per_tile, int workers);
+inline int choose_group_sets(int n_mtiles, int B, int Hkv, int tokens_per_item, int T,
+                             const int* p0_b, int keys_per_tile, int workers) {
+  constexpr int kItemCost = 4;
+  constexpr long long kMaxReplay = 1 << 16;  // beyond this many items: one set
+  const int bk_count = B * Hkv;
+  const long long n_items = (long long)n_mtiles * bk_count;
+  if (n_items <= 0 || n_items > kMaxReplay || workers <= 0) return 1;
+  std::vector<long long> load((size_t)workers);
+  int best = 1;
+  long long best_max = -1;
+  for (int sets = 1; sets <= 8; sets *= 2) {
+    if (bk_count % sets) break;
+    std::fill(load.begin(), load.end(), 0LL);
+    for (long long i = 0; i < n_items; ++i) {
+      const long long r = i / workers, k = i % workers;
+      const int w = (int)((r & 1) ? workers - 1 - k : k);
+      const ItemIndex ix = item_index((int)i, n_mtiles, bk_count / sets);
+      const int p0 = p0_b ? p0_b[ix.bk / Hkv] : 0;
+      load[(size_t)w] +=
+          item_kv_tiles(ix.mt * tokens_per_item, tokens_per_item, T, p0, keys_per_tile) + kItemCost;
+    }
+    const long long mx = *std::max_element(load.begin(), load.end());
+    if (best_max < 0 || mx <= best_max) {
+      best = sets;
+      best_max = mx;
+    }
+  }
+  return best;
+}
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_attention(const PrefillChunkArgs& a, cudaStream_t stream);
