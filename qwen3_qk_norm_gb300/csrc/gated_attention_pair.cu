@@ -547,8 +547,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the row's 64 gate values (one 128-byte line) into L2 now, so that
         // the epilogue, on the item boundary, finds them there
         if (tok < a.T) {
-          const long long grow_idx = ((long long)it.b * a.T + tok) * a.Hq + (it.kv * g + (r % g));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(a.qg + grow_idx * (2 * D) + D + cq * 64));
+          const long long gate_row = ((long long)it.b * a.T + tok) * a.Hq + (it.kv * g + (r % g));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(a.qg + gate_row * (2 * D) + D + cq * 64));
         }
       }
       float m = fixed_max ? bound * 1.01f + 0.5f : -INFINITY;
@@ -648,8 +648,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // whole token when g does not divide 128, are padding
       const bool store = ok && tok < a.T && r < g * tile_tok;
       const long long row = ((long long)it.b * a.T + tok) * a.Hq + (it.kv * g + (r % g));
-      // the partial sums go to a slot double-buffered by item; every thread of
-      // the four warpgroups reaches this barrier once per item
       // the row's first 32-byte gate piece is requested now, so that its
       // latency runs under the partial-sum barrier and the wait for O (the
       // other three follow inside the epilogue: holding them all across the
@@ -662,6 +660,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             : "=r"(g_first[0]), "=r"(g_first[1]), "=r"(g_first[2]), "=r"(g_first[3]),
               "=r"(g_first[4]), "=r"(g_first[5]), "=r"(g_first[6]), "=r"(g_first[7])
             : "l"(a.qg + row * (2 * D) + D + cq * 64));
+      // the partial sums go to a slot double-buffered by item; every thread of
+      // the four warpgroups reaches this barrier once per item
       float* lsum = xchg + 2 * 4 * 128 + (k & 1) * 4 * 128;  // [quarter][128]
       lsum[cq * 128 + r] = l;
       named_barrier_sync(1, kSoftmaxWGs * 128);
