@@ -14,8 +14,15 @@
 // so each K/V byte is read once per 256/g tokens. KV tiles above the causal
 // diagonal are never loaded; diagonal tiles are masked per element.
 //
+// Query tiles. A chunk's Q tiles arrive normalised and rotated (Qhat from the
+// prologue); the plain prefill loads the raw q rows and the tile's two softmax
+// warpgroups apply Q-Norm + RoPE to them in shared memory at the start of each
+// item (qnorm_rope_half_row), releasing the tile to the MMA thread on its
+// "Q ready" barrier, so Qhat never makes a round trip through HBM.
+//
 // Work items and persistence. An item is one pair of Q tiles of one KV group
-// (longest items first). The plain prefill runs one CTA per SM, each walking
+// (longest items first; a chunk's longest first within sets of KV groups, as
+// item_index orders them). The plain prefill runs one CTA per SM, each walking
 // its items in rounds of gridDim.x in snake order (forward in even rounds,
 // backward in odd ones, so long and short items pair up across CTAs); the
 // tensor pipe does not drain between items: the next item's Q pair is loaded
@@ -89,7 +96,8 @@ constexpr int kQTiles = 2;
 constexpr int kSoftmaxWGs = 4;  // two column halves per Q tile
 constexpr int kSlots = 4;       // K/V ring slots
 // four softmax warpgroups, then the producer warp and the MMA warp (576
-// threads: the register file then allows 112 registers per thread)
+// threads, 18 warps: a scheduler holding five of them caps a thread at 96
+// registers)
 constexpr int kThreads = kSoftmaxWGs * 128 + 64;
 constexpr uint32_t kHalf = 16384;      // 128 rows x 128 bytes
 constexpr uint32_t kTile = 2 * kHalf;  // 128 rows x 128 bf16

@@ -13,8 +13,9 @@
 // and the head rows of those tokens are contiguous in the [tokens, H, 128]
 // inputs, so one bulk copy per tensor (cp.async.bulk, completion on an
 // mbarrier) brings them all into shared memory. While that copy is in flight
-// the CTA forms the rotation angles of its tokens (p * w_i and its reduction
-// modulo 2 pi in fp64, then fp32 cos/sin). A half-warp then owns one row:
+// the CTA forms the rotation angles of its tokens (p * w_i as an exact 64-bit
+// fixed-point count of turns, then sincospif: rope_cos_sin in q3a_rope.cuh)
+// and their fp32 cos/sin. A half-warp then owns one row:
 // lane L holds elements 4L..4L+3 and their rotate-half partners 64+4L..,
 // so the rotation needs no data exchange and the RMS needs a 4-step shuffle
 // reduction. Results overwrite the staged rows, and bulk stores write them
